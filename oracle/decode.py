@@ -1,0 +1,241 @@
+"""Oracle decoding loops: vanilla greedy and one EAGLE step (test infrastructure only).
+
+Vanilla greedy ("Speculative Decoding with EAGLE", section "Deep dive": normal
+generation runs one full forward per token): the lossless reference the
+speculative loop must reproduce token for token (same section: the output is
+identical to what the target produces alone; "yuhuili": consistency with
+vanilla decoding).
+
+One EAGLE step, in the pages' order:
+
+1. Draft. Catch-up rows for the positions committed by the previous step run
+   the head on [f_i ; E(t_{i+1})] at position i; the last of them predicts the
+   feature at the root's position, whose draft distribution gives the root's
+   children. Tree nodes are expanded (static rank paths, or the EAGLE-2
+   dynamic rule) by further head rows: a depth-t node's row takes its parent's
+   predicted feature and its own token, sits at position L + t - 1 and attends
+   to the committed draft prefix, its expanded ancestors and itself.
+2. Verify. The target runs all N+1 tree rows in one pass: row j has position
+   L + depth(j), writes its K/V to slot L + j and attends to the prefix slots
+   [0, L) and the slots of its root-to-node path.
+3. Accept. Greedy longest accepted path plus the bonus token.
+4. Compact. The accepted nodes' K/V move from slot L + j_t to slot L + t in
+   every layer (positions are already L + t, so no re-rotation); the features
+   of the root and the accepted nodes become the next step's catch-up inputs.
+
+Committed-token count (reading): the prefill's first token counts as the first
+new token; the stream is trimmed to ``max_new``.
+
+Pins (tests/test_oracle_decode.py): speculative output equals vanilla greedy
+output on the tiny model (64 tokens) and on a reduced 8B-width model; trees
+with the vanilla continuation planted at a chosen depth are accepted to
+exactly that depth; after a commit the KV cache equals the one vanilla
+decoding builds for the same tokens.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import fixtures as FX
+
+from .core import F32, argmax, topk
+from .model import KVCache, Model, causal_visible, draft_logp, draft_rows, logits_of, target_rows
+from .tree import Pool, Tree, accept, rerank, select_frontier, static_layout, static_paths
+
+
+@dataclasses.dataclass
+class SeqState:
+    L: int                       # committed KV length (slots 0..L-1 valid)
+    root: int                    # x_L: committed, not yet in the KV
+    pend_feats: np.ndarray       # [c, d] target features f_{L-c} .. f_{L-1}
+    pend_tokens: np.ndarray      # [c] t_{L-c+1} .. t_L (the last is the root)
+    out: list[int]               # committed new tokens
+    kv: KVCache
+    dkv: KVCache
+    accepted: list[int] = dataclasses.field(default_factory=list)
+    n_flagged: int = 0
+
+
+def prefill(m: Model, prompt: np.ndarray, cap: int) -> SeqState:
+    """Target over the prompt (causal), first new token, and the head over prompt rows 0..P-2."""
+    s = m.shape
+    P = len(prompt)
+    kv = KVCache(s.n_layers, cap, s.n_kv_heads, s.head_dim)
+    dkv = KVCache(1, cap, s.n_kv_heads, s.head_dim)
+    pos = np.arange(P)
+    feats = target_rows(m, kv, prompt, pos, pos, causal_visible(0, P))
+    root = int(argmax(logits_of(m, feats[-1:]))[0])
+    if P > 1:
+        draft_rows(m, dkv, feats[:P - 1], prompt[1:], pos[:P - 1], pos[:P - 1], causal_visible(0, P - 1))
+    return SeqState(L=P, root=root, pend_feats=feats[P - 1:], pend_tokens=np.array([root], np.int32),
+                    out=[root], kv=kv, dkv=dkv)
+
+
+def draft_catchup(m: Model, st: SeqState) -> tuple[np.ndarray, np.ndarray]:
+    """Head rows for the newly committed positions; returns (f^ at the root position, its draft log-probs)."""
+    c = len(st.pend_tokens)
+    start = st.L - c
+    pos = np.arange(start, st.L)
+    fhat = draft_rows(m, st.dkv, st.pend_feats, st.pend_tokens, pos, pos, causal_visible(start, c))
+    return fhat[-1], draft_logp(m, fhat[-1:])[0]
+
+
+class _Scratch:
+    """Draft rows of tree nodes live in draft-cache slots L, L+1, ... in creation order."""
+
+    def __init__(self, L: int):
+        self.L, self.used = L, 0
+
+    def take(self, n: int) -> np.ndarray:
+        s = np.arange(self.L + self.used, self.L + self.used + n)
+        self.used += n
+        return s
+
+
+def draft_static(m: Model, st: SeqState, kind: str) -> Tree:
+    """Static-tree draft: each non-leaf node's draft row supplies its children by rank."""
+    paths = static_paths(kind)
+    parent, rank, depth = static_layout(paths)
+    n = len(paths)
+    k = int(rank.max()) + 1
+    fhat_root, logp_root = draft_catchup(m, st)
+    tokens = np.zeros(n + 1, np.int32)
+    tokens[0] = st.root
+    kids_of = {0: topk(logp_root, k)[0]}
+    fhat_of = {0: fhat_root}
+    slot_of: dict[int, int] = {}
+    scratch = _Scratch(st.L)
+    has_kids = set(int(p) for p in parent[1:])
+    for t in range(1, int(depth.max()) + 1):
+        level = [j for j in range(1, n + 1) if depth[j] == t]
+        for j in level:
+            tokens[j] = kids_of[int(parent[j])][rank[j]]
+        grow = [j for j in level if j in has_kids]
+        if not grow:
+            continue
+        slots = scratch.take(len(grow))
+        for j, sl in zip(grow, slots):
+            slot_of[j] = int(sl)
+        vis = []
+        for j in grow:
+            anc = [slot_of[a] for a in _ancestors(parent, j)]
+            vis.append(np.concatenate([np.arange(st.L), np.array(anc + [slot_of[j]])]))
+        fh = draft_rows(m, st.dkv, np.stack([fhat_of[int(parent[j])] for j in grow]), tokens[grow],
+                        np.full(len(grow), st.L + t - 1), slots, vis)
+        lp = draft_logp(m, fh)
+        for i, j in enumerate(grow):
+            fhat_of[j] = fh[i]
+            kids_of[j] = topk(lp[i], k)[0]
+    return Tree(tokens=tokens, parent=parent.copy(), depth=depth.copy())
+
+
+def _ancestors(parent: np.ndarray, j: int) -> list[int]:
+    """Non-root strict ancestors of node j, root side first."""
+    a = []
+    p = int(parent[j])
+    while p > 0:
+        a.append(p)
+        p = int(parent[p])
+    return a[::-1]
+
+
+def draft_dynamic(m: Model, st: SeqState, k: int, depth: int, n_nodes: int, tau: float) -> tuple[Tree, Pool]:
+    """EAGLE-2 dynamic draft tree: expand the top-k by cumulative confidence, prune below tau, rerank top-N."""
+    ln_tau = np.float32(np.log(tau))
+    fhat_root, logp_root = draft_catchup(m, st)
+    pool = Pool()
+    idx, val = topk(logp_root, k)
+    for r in range(k):
+        pool.add(val[r], idx[r], -1, 1, (1, 0, r))
+    fhat_of: dict[int, np.ndarray] = {}
+    slot_of: dict[int, int] = {}
+    scratch = _Scratch(st.L)
+    for t in range(2, depth + 1):
+        front = select_frontier(pool, t - 1, k, ln_tau)
+        slots = scratch.take(len(front))
+        for i, sl in zip(front, slots):
+            slot_of[i] = int(sl)
+        vis, feats = [], []
+        for i in front:
+            anc, p = [], pool.parent[i]
+            while p >= 0:
+                anc.append(slot_of[p])
+                p = pool.parent[p]
+            vis.append(np.concatenate([np.arange(st.L), np.array(anc[::-1] + [slot_of[i]])]))
+            feats.append(fhat_root if pool.parent[i] < 0 else fhat_of[pool.parent[i]])
+        fh = draft_rows(m, st.dkv, np.stack(feats), np.array([pool.token[i] for i in front], np.int32),
+                        np.full(len(front), st.L + t - 2), slots, vis)
+        lp = draft_logp(m, fh)
+        for fr, i in enumerate(front):
+            fhat_of[i] = fh[fr]
+            cidx, cval = topk(lp[fr], k)
+            for r in range(k):
+                pool.add(np.float32(pool.score[i] + cval[r]), cidx[r], i, t, (t, fr, r))
+    tree, _ = rerank(pool, n_nodes, st.root)
+    return tree, pool
+
+
+def verify(m: Model, st: SeqState, tree: Tree):
+    """Target forward over every tree row in one pass; returns (argmax [N+1], features, logits)."""
+    L = st.L
+    slots = L + np.arange(tree.n + 1)
+    pos = L + tree.depth
+    prefix = np.arange(L)
+    vis = [np.concatenate([prefix, L + np.array(tree.path(j))]) for j in range(tree.n + 1)]
+    feats = target_rows(m, st.kv, tree.tokens, pos, slots, vis)
+    logits = logits_of(m, feats)
+    return argmax(logits), feats, logits
+
+
+def accept_commit(st: SeqState, tree: Tree, amax: np.ndarray, feats: np.ndarray) -> int:
+    """Greedy accept, compact the accepted KV and features, commit tokens; returns the accepted length."""
+    path, bonus = accept(tree, amax)
+    a = len(path) - 1
+    L = st.L
+    if a:
+        st.kv.move([L + j for j in path[1:]], [L + t for t in range(1, a + 1)])
+    new = [int(tree.tokens[j]) for j in path[1:]] + [bonus]
+    st.pend_feats = feats[path].copy()
+    st.pend_tokens = np.array(new, np.int32)
+    st.out.extend(new)
+    st.L = L + a + 1
+    st.root = bonus
+    st.accepted.append(a)
+    return a
+
+
+def draft_tree(m: Model, st: SeqState, w: FX.Workload) -> Tree:
+    if w.tree == "static":
+        return draft_static(m, st, w.static_tree)
+    return draft_dynamic(m, st, w.top_k, w.depth, w.n_nodes, w.tau)[0]
+
+
+def speculative_generate(m: Model, prompt: np.ndarray, w: FX.Workload, max_new: int | None = None,
+                         cap: int | None = None) -> SeqState:
+    max_new = w.max_new if max_new is None else max_new
+    st = prefill(m, prompt, cap or FX.kv_capacity(w))
+    while len(st.out) < max_new:
+        tree = draft_tree(m, st, w)
+        amax, feats, _ = verify(m, st, tree)
+        accept_commit(st, tree, amax, feats)
+    st.out = st.out[:max_new]
+    return st
+
+
+def vanilla_greedy(m: Model, prompt: np.ndarray, max_new: int, cap: int) -> list[int]:
+    """One target forward per token, argmax each time."""
+    s = m.shape
+    P = len(prompt)
+    kv = KVCache(s.n_layers, cap, s.n_kv_heads, s.head_dim)
+    pos = np.arange(P)
+    feats = target_rows(m, kv, prompt, pos, pos, causal_visible(0, P))
+    x = int(argmax(logits_of(m, feats[-1:]))[0])
+    out, L = [x], P
+    while len(out) < max_new:
+        f = target_rows(m, kv, np.array([x], np.int32), np.array([L]), np.array([L]), [np.arange(L + 1)])
+        x = int(argmax(logits_of(m, f))[0])
+        out.append(x)
+        L += 1
+    return out

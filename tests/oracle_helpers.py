@@ -1,0 +1,50 @@
+"""Small models and trees for oracle and parity tests (test-side helpers)."""
+import dataclasses
+
+import numpy as np
+
+import fixtures as FX
+from oracle import model as OM
+from oracle import tree as OT
+
+# A grouped-query bf16 model small enough for CPU tests: 8 query heads over 2 KV heads of dim 64.
+GQA_SMALL = FX.ModelShape(n_layers=2, d=512, n_heads=8, n_kv_heads=2, head_dim=64, ffn=1024, vocab=2048,
+                          rope_theta=5e5, bf16=True, lm_head_std=0.08, seed=11)
+
+_models = {}
+
+
+def model(shape: FX.ModelShape, max_pos: int = 512) -> OM.Model:
+    key = (shape, max_pos)
+    if key not in _models:
+        _models[key] = OM.build_model(shape, max_pos)
+    return _models[key]
+
+
+def workload(base: str, **kw) -> FX.Workload:
+    return dataclasses.replace(FX.WORKLOADS[base], **kw)
+
+
+def random_tree(rng, n: int, vocab: int, max_depth: int = 6, shape: str = "random") -> OT.Tree:
+    """BFS-ordered tree with n nodes (root excluded); shape: random | chain | star | binary."""
+    parent, depth = [-1], [0]
+    for j in range(1, n + 1):
+        if shape == "chain":
+            p = j - 1
+        elif shape == "star":
+            p = 0
+        elif shape == "binary":
+            p = (j - 1) // 2
+        else:
+            cands = [i for i in range(j) if depth[i] < max_depth and depth[i] >= depth[-1] - 1]
+            p = int(rng.choice(cands))
+        parent.append(p)
+        depth.append(depth[p] + 1)
+    order = sorted(range(1, n + 1), key=lambda j: (depth[j], j))
+    where = {0: 0}
+    for i, j in enumerate(order):
+        where[j] = i + 1
+    par = [-1] + [where[parent[j]] for j in order]
+    dep = [0] + [depth[j] for j in order]
+    tokens = rng.integers(0, vocab, n + 1).astype(np.int32)
+    return OT.Tree(tokens=tokens, parent=np.array(par, np.int32), depth=np.array(dep, np.int32))
