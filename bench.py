@@ -1,0 +1,332 @@
+"""Benchmark of one EAGLE speculative-decoding step on GB300 (one JSON line on rank 0).
+
+Default workload: the Llama-3-8B-shaped bf16 target with its one-layer EAGLE
+head, EAGLE-2 dynamic tree (top-10 per depth, 6 depths, tau 0.3, 60 verified
+nodes), batch 1, 1024-token random prompt. A step is one full pass of the hot
+path: draft (catch-up + 5 frontier expansions + rerank), verify (61 tree rows
+through 32 layers and the LM head), accept and compact. Steps are replayed
+from a captured CUDA graph; K steps are timed with CUDA events on the
+library's stream, bracketed by a barrier and device synchronisation.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl eagle|reference]
+
+--impl reference times the CPU oracle (fp32 numpy) on the host cores instead.
+With N > 1 (torchrun) every rank decodes its own batch (replicas, weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s bs1 8B-shape EAGLE-2 tree; verify-step HBM GB/s vs 8 TB/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def verify_bytes(m, batch: int, L: int, rows: int) -> int:
+    """Algorithmic HBM bytes of one verify pass: every weight once, the KV prefix read once per layer,
+    the new K/V rows written (bf16)."""
+    per_layer = (m.q_dim + 2 * m.kv_dim) * m.d + m.d * m.q_dim + 2 * m.ffn * m.d + m.d * m.ffn
+    weights = m.n_layers * per_layer * 2 + m.vocab * m.d * 2
+    kv_read = m.n_layers * batch * L * 2 * m.kv_dim * 2
+    kv_write = m.n_layers * batch * rows * 2 * m.kv_dim * 2
+    return weights + kv_read + kv_write
+
+
+def gemm_roofline(eng, m, rows: int, reps: int = 2):
+    """The verify GEMM kernel (tcgen05) at the verify shapes, on the layers' own weights, timed per launch."""
+    import torch
+    from eagle_speculative_decoding_02_gb300.engine import op_gemm, op_gemm_scratch
+    dev = eng.device
+    shapes = {"qkv": (m.q_dim + 2 * m.kv_dim, m.d), "o": (m.d, m.q_dim), "gu": (2 * m.ffn, m.d),
+              "down": (m.d, m.ffn), "lm_head": (m.vocab, m.d)}
+    xs = {k: (torch.randn(rows, K, device=dev) * 0.5).to(torch.bfloat16) for k, (N, K) in shapes.items()}
+    ys = {k: torch.empty(rows, N, device=dev) for k, (N, K) in shapes.items()}
+    scr = op_gemm_scratch(rows, m.vocab, m.ffn, torch.bfloat16, dev)
+    launches = []
+    for lw in eng.weights.layers:
+        launches += [("qkv", lw.wqkv), ("o", lw.wo), ("gu", lw.wgu), ("down", lw.wd)]
+    launches.append(("lm_head", eng.weights.lm_head))
+    op_gemm(xs["qkv"], launches[0][1], ys["qkv"], scr)
+    torch.cuda.synchronize()
+    nbytes = 0
+    for k, w in launches:
+        N, K = shapes[k]
+        nbytes += N * K * 2 + rows * K * 2 + rows * N * 4
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        for k, w in launches:
+            op_gemm(xs[k], w, ys[k], scr)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return nbytes / len(launches), ms / len(launches), len(launches)
+
+
+def cpu_baseline(w, prompt_len: int, budget_s: float):
+    """The oracle as it stands, on the host cores: full-depth model, shorter prompt, whole speculative steps."""
+    import numpy as np
+
+    import fixtures as FX
+    from oracle import decode as OD
+    from oracle import model as OM
+    wl = __import__("dataclasses").replace(w, prompt_len=prompt_len)
+    cap = prompt_len + 64 + 2 * (w.depth + 1) + w.n_nodes_max + 1
+    t0 = time.time()
+    m = OM.build_model(w.model, cap)
+    prompt = FX.prompts(w.model, 1, prompt_len)[0]
+    st = OD.prefill(m, prompt, cap)
+    t_setup = time.time() - t0
+    steps, toks, t_steps = 0, 0, 0.0
+    while steps < 1 or t_steps < budget_s:
+        n0 = len(st.out)
+        t1 = time.perf_counter()
+        tree = OD.draft_tree(m, st, wl)
+        amax, feats, _ = OD.verify(m, st, tree)
+        OD.accept_commit(st, tree, amax, feats)
+        t_steps += time.perf_counter() - t1
+        toks += len(st.out) - n0
+        steps += 1
+    return {"value": toks / t_steps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{steps} speculative steps (draft+verify+accept) of the full-depth model on one sequence "
+                      f"after a {prompt_len}-token prompt instead of {w.prompt_len} (oracle setup {t_setup:.0f} s "
+                      f"excluded)", "s_per_step": t_steps / steps}, steps, toks, t_steps
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import dataclasses
+
+    import fixtures as FX
+    from oracle import decode as OD
+    from oracle import model as OM
+    P = 64
+    wl = dataclasses.replace(w, prompt_len=P)
+    cap = P + (args.steps + args.warmup + 2) * (w.depth + 1) + w.n_nodes_max + 8
+    m = OM.build_model(w.model, cap)
+    prompt = FX.prompts(w.model, 1, P)[0]
+    st = OD.prefill(m, prompt, cap)
+    for _ in range(args.warmup):
+        tree = OD.draft_tree(m, st, wl)
+        amax, feats, _ = OD.verify(m, st, tree)
+        OD.accept_commit(st, tree, amax, feats)
+    n0 = len(st.out)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tree = OD.draft_tree(m, st, wl)
+        amax, feats, _ = OD.verify(m, st, tree)
+        OD.accept_commit(st, tree, amax, feats)
+    dt = time.perf_counter() - t0
+    v = (len(st.out) - n0) / dt
+    sample = (f"each step one oracle speculative step (draft+verify+accept) of the full-depth model, one sequence, "
+              f"{P}-token prompt instead of {w.prompt_len}")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "oracle_prompt": P},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="eagle", choices=["eagle", "reference"])
+    ap.add_argument("--workload", default="8b_eagle2")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle steps for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import fixtures as FX
+    w = FX.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+    from eagle_speculative_decoding_02_gb300 import build as B
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    B.build()
+
+    m = w.model
+    D1 = w.depth + 1
+    max_new = max(w.max_new, (args.steps + args.warmup + 2) * D1 + 1)
+    eng = S.make_engine(w, max_new=max_new)
+    prompt = S.prompts(w)
+    eng.prefill(prompt)
+    eng.step(args.warmup, use_graph=True)
+    torch.cuda.synchronize()
+    n_launch = eng.step_kernel_count()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    c0 = eng.committed_counts().sum().item()
+    clocks = Clocks(local)
+    clocks.start()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(eng.stream)
+    eng.step(args.steps, use_graph=True)
+    e1.record(eng.stream)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    toks = eng.committed_counts().sum().item() - c0
+    eng.sync_status()
+    if world > 1:
+        t = torch.tensor([ms, float(toks)], device="cuda")
+        ms_all = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(ms_all, t)
+        ms = max(float(x[0]) for x in ms_all)
+        toks = sum(float(x[1]) for x in ms_all)
+    value = toks / (ms / 1e3)
+
+    # verify pass alone: HBM bytes per verify / its device time
+    hbm, tflops, peak_kind = _peaks()
+    vms = []
+    for _ in range(4):
+        tree = eng.draft_tree()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(eng.stream)
+        eng.verify(tree)
+        b.record(eng.stream)
+        eng.accept_commit()
+        torch.cuda.synchronize()
+        vms.append(a.elapsed_time(b))
+    L_now = int(eng.committed_counts().max().item()) + w.prompt_len
+    vb = verify_bytes(m, w.batch, L_now, w.n_nodes + 1)
+    v_ms = statistics.median(vms)
+    verify = {"ms": v_ms, "gbs": vb / v_ms / 1e6, "frac": vb / v_ms / 1e6 / hbm, "bytes": vb}
+
+    # dominant kernel: the tcgen05 weight-streaming GEMM at the verify shapes
+    bpl, mspl, nl = gemm_roofline(eng, m, w.batch * (w.n_nodes + 1))
+    ach = bpl / mspl / 1e6
+    roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "kernel": "gemm_tc_kernel", "launch_ms": mspl, "bytes_per_launch": bpl,
+            "peak_kind": f"{peak_kind} (hbm_gbs)"}
+
+    # end to end through the public API: pinned host prompt -> device, generate, tokens -> host
+    e2e = None
+    if rank == 0 or world > 1:
+        n_new = w.max_new
+        host_prompt = prompt.cpu().pin_memory()
+        host_out = torch.empty((w.batch, n_new), dtype=torch.int32).pin_memory()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dprompt = host_prompt.to("cuda", non_blocking=True)
+        out, stats = eng.generate(dprompt, n_new, use_graph=True)
+        host_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        e2e = {"value": w.batch * n_new / dt, "unit": "tokens/s", "h2d_bytes_per_step": host_prompt.numel() * 4,
+               "d2h_bytes_per_step": host_out.numel() * 4,
+               "step": f"one eagle_generate call ({w.prompt_len}-token prompt, {n_new} new tokens, prefill included)",
+               "steps_in_call": stats["steps"], "prefill_ms": stats["prefill_ms"],
+               "decode_ms": stats["decode_ms"], "mean_accept": stats["mean_accept"]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        del eng
+        torch.cuda.empty_cache()
+        cpu, *_ = cpu_baseline(w, 64, args.cpu_budget)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, "
+                "uniform random prompt tokens)",
+                "config": {"workload": w.name, "batch": w.batch, "prompt": w.prompt_len,
+                           "tree": f"{w.tree} top_k={w.top_k} depth={w.depth} tau={w.tau} nodes={w.n_nodes}",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                           "l2": "no flush: every step streams ~16 GB of weights, far above the 129 MB L2"},
+                "tokens_timed": toks, "tokens_per_step": toks / args.steps / max(world, 1) / w.batch,
+                "verify": verify, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": n_launch * args.steps if n_launch > 0 else None,
+                "gpu_launches_per_step": n_launch, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,124 @@
+// Shared definitions of the EAGLE step kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace eg {
+
+using bf16 = __nv_bfloat16;
+
+// GEMM output tile width: weight rows per tile, and the column width of the
+// per-row sum-of-squares partials that feed the next RMSNorm.
+constexpr int kTileN = 128;
+constexpr int kMaxTreeRows = 121;
+constexpr int kMaxDepth = 8;
+constexpr int kMaxTopK = 16;
+
+// Device status word values (mirror eagle_status).
+enum : int { kStOk = 0, kStCapacity = 4, kStTimeout = 6 };
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, kStOk, code);
+}
+
+// Per-row metadata of one forward phase (verify, catch-up, draft depth, prefill chunk).
+struct Rows {
+  int* seq;        // [M] sequence index
+  int* pos;        // [M] RoPE position
+  int* slot;       // [M] KV slot to write, -1 = none (padding row)
+  int* grp;        // [M] attention group
+  uint64_t* mask;  // [M][2] visibility over the group's tree block
+  int* tok;        // [M] input token (embedding row)
+  int* fsrc;       // [M] feature row feeding the draft head's FC (draft phases)
+};
+
+// Rows of one sequence that share a fully visible prefix [0, prefix) and a
+// tree block of slots [prefix, prefix + block_len) seen through per-row masks.
+struct Group {
+  int seq, row0, nrows, prefix, block_len;
+};
+
+enum EpiKind : int {
+  kEpiStore = 0,   // y_f32[m][n] = acc * r_m
+  kEpiQkv = 1,     // RoPE on q/k, q -> out, k/v -> KV cache slots
+  kEpiSwiglu = 2,  // silu(gate) * up over interleaved 64-row blocks -> out
+  kEpiResid = 3,   // h += acc; hb = h * gain_next; per-tile sum of squares of h
+  kEpiFc = 4,      // h = acc; hb = h * gain_next; per-tile sum of squares
+  kEpiLmHead = 5,  // per-row top-k, max and sum-exp per vocab tile (+ optional logits)
+};
+
+struct EpiParams {
+  int kind = kEpiStore;
+  int M = 0, N = 0;
+  // Row scale of RMSNorm applied after the product: r_m = 1/sqrt(sum_j ssq_in[j][m] / d_in + eps).
+  const float* ssq_in = nullptr;
+  int n_ssq_in = 0;
+  float inv_d_in = 0.f;
+  float eps = 0.f;
+  float* y = nullptr;       // kEpiStore output; kEpiLmHead optional logits [M][N]
+  void* out = nullptr;      // q (kEpiQkv) [M][q_dim] or act (kEpiSwiglu) [M][ffn]
+  // kEpiQkv
+  int q_dim = 0, kv_dim = 0, head_dim = 0, n_kv = 0, cap = 0;
+  const float* rope_cos = nullptr;  // [positions][head_dim/2]
+  const float* rope_sin = nullptr;
+  void* kc = nullptr;       // layer cache base [B][n_kv][cap][head_dim]
+  void* vc = nullptr;
+  Rows rows{};
+  // kEpiSwiglu
+  int ffn = 0;
+  // kEpiResid / kEpiFc
+  float* h = nullptr;       // [M][N] float32 residual stream
+  void* hb = nullptr;       // [M][N] next GEMM input (h * gain_next)
+  float* ssq_out = nullptr; // [N/128][M]
+  const float* gain = nullptr;
+  // kEpiLmHead
+  int topk = 1;
+  float* rec_val = nullptr; // [ntiles][M][topk]
+  int* rec_idx = nullptr;
+  float* rec_max = nullptr; // [ntiles][M]
+  float* rec_sum = nullptr; // [ntiles][M] sum exp(logit - tile max)
+};
+
+// Barriers for code shared by whole-block and warp-specialised kernels.
+struct BlockSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+// Named barrier 1 over the 128 epilogue threads of a warp-specialised kernel.
+struct EpilogueSync {
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+};
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.f + __expf(-x)); }
+
+// Warp arg-max on (value desc, index asc).
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace eg

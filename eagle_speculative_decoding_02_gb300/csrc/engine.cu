@@ -1,0 +1,883 @@
+// Host orchestration of the EAGLE step and the C ABI declared in include/eagle.h.
+//
+// The context carves one caller-owned workspace into the KV caches, the
+// per-phase row buffers and the device-resident decoding state, then enqueues
+// each phase as a fixed sequence of kernels on the caller's stream:
+//   prefill   target layers over the prompt (chunked), first token, head catch-up
+//   draft     head rows for the newly committed positions, then tree expansion
+//   verify    target layers over the tree rows, LM-head argmax per row
+//   accept    greedy walk, commit, in-place KV compaction
+// Shapes never depend on device values, so a step can be captured in a CUDA
+// graph and replayed.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/eagle.h"
+#include "kernels.h"
+#include "step.h"
+
+namespace eg {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+struct LayerPtrs {
+  const void* wqkv;
+  const void* wo;
+  const void* wgu;
+  const void* wd;
+  const float* attn_norm;
+  const float* ffn_norm;
+};
+
+// Host-derived sizes of a configuration.
+struct Dims {
+  int B, d, Hq, Hkv, hd, ffn, V, Lyr, cap, cap_d, P_max, out_cap;
+  int qd, kvd, nqkv;
+  int mode, NR, D, D1, k, S, n_nodes;
+  std::vector<int> level_rows;  // rows per sequence of the depth-t draft forward, t = 1..D-1 (index t)
+  std::vector<int> level_base;  // absolute first row of level t in the draft buffers (index t)
+  int R_d;                      // total draft rows
+  int CL;                       // prefill chunk length per sequence
+  int M_tgt, M_dft, M_max, M_lm, n_groups_max, ntV, pool_cap;
+  bool bf16;
+  // static topology (host)
+  std::vector<int> s_parent, s_rank, s_depth, s_lrow, s_sidx, s_level_nodes, s_level_count;
+  std::vector<uint64_t> s_smask, s_anc;
+};
+
+struct Layout {
+  size_t total = 0;
+  size_t take(size_t bytes) {
+    const size_t at = total;
+    total += align_up(bytes);
+    return at;
+  }
+};
+
+}  // namespace
+}  // namespace eg
+
+struct eagle_ctx {
+  eagle_config cfg{};
+  eg::Dims dm;
+  cudaStream_t stream = nullptr;
+  std::vector<eg::LayerPtrs> layers;
+  eg::LayerPtrs head{};
+  const void* embed = nullptr;
+  const void* lm_head = nullptr;
+  const float* final_norm = nullptr;
+  const void* fc = nullptr;
+  std::string err;
+  bool failed = false;
+  int phase = 0;  // 0 fresh, 1 prefilled, 2 drafted, 3 verified
+  // buffers
+  eg::Rows rows{};
+  eg::Group* groups = nullptr;
+  float* h_tgt = nullptr;
+  float* h_dft = nullptr;
+  void* hb = nullptr;
+  float* ssq_a = nullptr;
+  float* ssq_b = nullptr;
+  void* q = nullptr;
+  void* attn = nullptr;
+  void* act = nullptr;
+  void* xfc = nullptr;
+  void* lm_hb = nullptr;
+  float* lm_ssq = nullptr;
+  int* lm_src = nullptr;
+  float* rec_val = nullptr;
+  int* rec_idx = nullptr;
+  float* rec_max = nullptr;
+  float* rec_sum = nullptr;
+  int* dtopk_idx = nullptr;
+  float* dtopk_val = nullptr;
+  float* dlse = nullptr;
+  int* vargmax = nullptr;
+  int* root_idx = nullptr;
+  eg::TreeOut tree{};
+  eg::TreeOut vtree{};  // one-row tree of vanilla decoding
+  eg::TreeOut last_tree{};
+  eg::State st{};
+  eg::Pool pool{};
+  eg::StaticTopo topo{};
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  void* kc = nullptr;
+  void* vc = nullptr;
+  void* kc_d = nullptr;
+  void* vc_d = nullptr;
+  void* gemm_scratch = nullptr;
+  size_t gemm_scratch_bytes = 0;
+  float* attn_part = nullptr;
+  cudaGraphExec_t graph_exec[2] = {nullptr, nullptr};  // captured step: [0] speculative, [1] vanilla
+  int graph_kernels[2] = {-1, -1};                       // kernel nodes in each captured step
+};
+
+namespace eg {
+namespace {
+
+eagle_status fail(eagle_ctx* c, eagle_status s, const std::string& msg) {
+  if (c) {
+    c->err = msg;
+    if (s != EAGLE_ERR_INVALID_ARG) c->failed = true;
+  }
+  return s;
+}
+
+#define EG_CK(call)                                                                             \
+  do {                                                                                          \
+    cudaError_t e_ = (call);                                                                    \
+    if (e_ != cudaSuccess)                                                                      \
+      return fail(c, EAGLE_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_));      \
+  } while (0)
+
+#define EG_TRY(call)                   \
+  do {                                 \
+    eagle_status s_ = (call);          \
+    if (s_ != EAGLE_OK) return s_;     \
+  } while (0)
+
+bool gemm_tc_ok(const Dims& dm, int N, int K) {
+  return dm.bf16 && N % kTileN == 0 && K % 64 == 0;
+}
+
+eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
+  auto bad = [&](const char* m) { why = m; return EAGLE_ERR_INVALID_ARG; };
+  if (cfg.n_layers <= 0 || cfg.d <= 0 || cfg.n_heads <= 0 || cfg.n_kv_heads <= 0 || cfg.ffn <= 0 ||
+      cfg.vocab <= 0 || cfg.batch <= 0 || cfg.kv_cap <= 0 || cfg.max_prompt <= 0 || cfg.max_new <= 0)
+    return bad("non-positive dimension");
+  if (cfg.dtype != EAGLE_DTYPE_F32 && cfg.dtype != EAGLE_DTYPE_BF16) return bad("dtype");
+  if (cfg.d % kTileN) { why = "d must be a multiple of 128"; return EAGLE_ERR_UNSUPPORTED; }
+  if (cfg.head_dim != 64 && cfg.head_dim != 128) { why = "head_dim must be 64 or 128"; return EAGLE_ERR_UNSUPPORTED; }
+  if (cfg.n_heads % cfg.n_kv_heads) return bad("n_kv_heads must divide n_heads");
+  if (!(cfg.rms_eps > 0.f) || !(cfg.rope_theta > 0.f)) return bad("rms_eps / rope_theta");
+  dm.B = cfg.batch; dm.d = cfg.d; dm.Hq = cfg.n_heads; dm.Hkv = cfg.n_kv_heads; dm.hd = cfg.head_dim;
+  dm.ffn = cfg.ffn; dm.V = cfg.vocab; dm.Lyr = cfg.n_layers; dm.cap = cfg.kv_cap; dm.P_max = cfg.max_prompt;
+  dm.qd = dm.Hq * dm.hd; dm.kvd = dm.Hkv * dm.hd; dm.nqkv = dm.qd + 2 * dm.kvd;
+  dm.bf16 = cfg.dtype == EAGLE_DTYPE_BF16;
+  if (dm.bf16 && (dm.ffn % 64)) { why = "bf16 models need ffn % 64 == 0"; return EAGLE_ERR_UNSUPPORTED; }
+  dm.mode = cfg.tree_mode;
+  dm.n_nodes = cfg.n_nodes;
+  if (cfg.n_nodes < 1 || cfg.n_nodes + 1 > kMaxTreeRows) return bad("n_nodes must be in 1..120");
+  dm.NR = cfg.n_nodes + 1;
+  dm.level_rows.assign(kMaxDepth + 1, 0);
+  dm.level_base.assign(kMaxDepth + 1, 0);
+  if (cfg.tree_mode == EAGLE_TREE_STATIC) {
+    if (!cfg.static_parent || !cfg.static_rank) return bad("static tree arrays missing");
+    const int NR = dm.NR;
+    dm.s_parent.assign(cfg.static_parent, cfg.static_parent + NR);
+    dm.s_rank.assign(cfg.static_rank, cfg.static_rank + NR);
+    if (dm.s_parent[0] != -1) return bad("static_parent[0] must be -1");
+    dm.s_depth.assign(NR, 0);
+    int kmax = 0, D = 0;
+    for (int j = 1; j < NR; ++j) {
+      const int p = dm.s_parent[j];
+      if (p < 0 || p >= j) return bad("static tree must be in BFS order (0 <= parent[j] < j)");
+      if (dm.s_rank[j] < 0 || dm.s_rank[j] >= kMaxTopK) return bad("static rank out of range");
+      dm.s_depth[j] = dm.s_depth[p] + 1;
+      if (j > 1 && dm.s_depth[j] < dm.s_depth[j - 1]) return bad("static tree must be in BFS order (depth)");
+      for (int i = 1; i < j; ++i)
+        if (dm.s_parent[i] == p && dm.s_rank[i] == dm.s_rank[j]) return bad("duplicate sibling rank");
+      kmax = std::max(kmax, dm.s_rank[j] + 1);
+      D = std::max(D, dm.s_depth[j]);
+    }
+    if (D > kMaxDepth) return bad("static tree deeper than 8");
+    dm.D = D; dm.k = kmax;
+    std::vector<int> has_kids(NR, 0);
+    for (int j = 1; j < NR; ++j) has_kids[dm.s_parent[j]] = 1;
+    dm.s_lrow.assign(NR, -1); dm.s_sidx.assign(NR, -1); dm.s_smask.assign(NR, 0);
+    dm.s_level_nodes.assign((size_t)(D + 1) * NR, 0); dm.s_level_count.assign(D + 1, 0);
+    int S = 0;
+    for (int j = 1; j < NR; ++j) {
+      if (!has_kids[j]) continue;
+      const int t = dm.s_depth[j];
+      dm.s_lrow[j] = dm.s_level_count[t];
+      dm.s_level_nodes[(size_t)t * NR + dm.s_level_count[t]] = j;
+      dm.s_level_count[t]++;
+      dm.s_sidx[j] = S++;
+    }
+    if (S > 64) return bad("static tree has more than 64 expanded nodes");
+    for (int j = 1; j < NR; ++j) {
+      if (!has_kids[j]) continue;
+      uint64_t m = 0;
+      for (int a = j; a > 0; a = dm.s_parent[a]) m |= 1ull << dm.s_sidx[a];
+      dm.s_smask[j] = m;
+    }
+    dm.S = S;
+    for (int t = 1; t < D; ++t) dm.level_rows[t] = dm.s_level_count[t];
+    dm.s_anc.assign((size_t)NR * 2, 0);
+    for (int j = 0; j < NR; ++j)
+      for (int a = j; a >= 0; a = a ? dm.s_parent[a] : -1) {
+        dm.s_anc[2 * j + a / 64] |= 1ull << (a % 64);
+        if (a == 0) break;
+      }
+  } else if (cfg.tree_mode == EAGLE_TREE_DYNAMIC) {
+    if (cfg.top_k < 1 || cfg.top_k > 11) return bad("top_k must be in 1..11");
+    if (cfg.depth < 1 || cfg.depth > kMaxDepth) return bad("depth must be in 1..8");
+    if (!(cfg.tau > 0.f) || cfg.tau > 1.f) return bad("tau must be in (0, 1]");
+    dm.D = cfg.depth; dm.k = cfg.top_k;
+    dm.S = (dm.D - 1) * dm.k;
+    if (dm.S > 64) return bad("(depth-1)*top_k must be <= 64");
+    for (int t = 1; t < dm.D; ++t) dm.level_rows[t] = dm.k;
+    dm.pool_cap = dm.k + (dm.D - 1) * dm.k * dm.k;
+    if (dm.pool_cap > 1024) return bad("pool larger than 1024");
+    if (dm.pool_cap < dm.n_nodes) return bad("n_nodes exceeds the candidate pool");
+  } else {
+    return bad("tree_mode");
+  }
+  dm.D1 = dm.D + 1;
+  int base = dm.B * dm.D1;
+  for (int t = 1; t < dm.D; ++t) {
+    dm.level_base[t] = base;
+    base += dm.B * dm.level_rows[t];
+  }
+  dm.R_d = base;
+  dm.cap_d = (dm.cap + dm.S + 7) / 8 * 8;
+  dm.out_cap = cfg.max_new + dm.D1 + 1;
+  const int rows_budget = 8192;
+  int CL = std::max(128, rows_budget / dm.B / 128 * 128);
+  dm.CL = std::min(dm.P_max, CL);
+  const int M_pf = dm.B * dm.CL;
+  dm.M_tgt = std::max(dm.B * kMaxTreeRows, M_pf);
+  dm.M_dft = std::max(dm.R_d, M_pf);
+  dm.M_max = std::max(dm.M_tgt, dm.M_dft);
+  int lvl_max = dm.D1;
+  for (int t = 1; t < dm.D; ++t) lvl_max = std::max(lvl_max, dm.level_rows[t]);
+  dm.M_lm = std::max(dm.B * kMaxTreeRows, dm.B * lvl_max);
+  dm.n_groups_max = std::max(dm.B * ((dm.CL + 127) / 128), dm.B);
+  dm.ntV = (dm.V + kTileN - 1) / kTileN;
+  if (dm.P_max + cfg.max_new + dm.D1 + dm.NR > dm.cap) {
+    why = "kv_cap too small for max_prompt + max_new + tree";
+    return EAGLE_ERR_INVALID_ARG;
+  }
+  return EAGLE_OK;
+}
+
+struct Offsets {
+  size_t rows_seq, rows_pos, rows_slot, rows_grp, rows_tok, rows_fsrc, rows_mask, groups;
+  size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, attn, act, xfc, lm_hb, lm_ssq, lm_src;
+  size_t rec_val, rec_idx, rec_max, rec_sum, dtopk_idx, dtopk_val, dlse, vargmax, root_idx;
+  size_t t_tok, t_par, t_dep, t_anc, vt_tok, vt_par, vt_dep, vt_anc;
+  size_t L, c, root, pend_tok, pend_feat, n_out, out, acc_len, acc_path, L_prev, hist, status;
+  size_t p_score, p_token, p_parent, p_depth, p_cid, p_frow, p_smask, p_count, p_front, p_nfront;
+  size_t s_parent, s_rank, s_depth, s_lrow, s_sidx, s_smask, s_lnodes, s_lcount;
+  size_t rope_cos, rope_sin, kc, vc, kc_d, vc_d, gemm, attn_part;
+  size_t gemm_bytes;
+  size_t total;
+};
+
+Offsets plan(const Dims& dm) {
+  Offsets o{};
+  Layout L;
+  const size_t es = dm.bf16 ? 2 : 4;
+  const size_t M = dm.M_max;
+  const int nt_d = dm.d / kTileN;
+  o.rows_seq = L.take(M * 4); o.rows_pos = L.take(M * 4); o.rows_slot = L.take(M * 4);
+  o.rows_grp = L.take(M * 4); o.rows_tok = L.take(M * 4); o.rows_fsrc = L.take(M * 4);
+  o.rows_mask = L.take(M * 16); o.groups = L.take((size_t)dm.n_groups_max * sizeof(Group));
+  o.h_tgt = L.take((size_t)dm.M_tgt * dm.d * 4);
+  o.h_dft = L.take((size_t)dm.M_dft * dm.d * 4);
+  o.hb = L.take(M * dm.d * es);
+  o.ssq_a = L.take(M * nt_d * 4); o.ssq_b = L.take(M * nt_d * 4);
+  o.q = L.take(M * dm.qd * es); o.attn = L.take(M * dm.qd * es);
+  o.act = L.take(M * dm.ffn * es); o.xfc = L.take(M * 2 * dm.d * es);
+  o.lm_hb = L.take((size_t)dm.B * dm.d * es); o.lm_ssq = L.take((size_t)dm.B * nt_d * 4);
+  o.lm_src = L.take((size_t)dm.B * 4);
+  const size_t nrec = (size_t)dm.ntV * dm.M_lm;
+  const int krec = std::max(dm.k, 1);
+  o.rec_val = L.take(nrec * krec * 4); o.rec_idx = L.take(nrec * krec * 4);
+  o.rec_max = L.take(nrec * 4); o.rec_sum = L.take(nrec * 4);
+  o.dtopk_idx = L.take((size_t)dm.R_d * krec * 4); o.dtopk_val = L.take((size_t)dm.R_d * krec * 4);
+  o.dlse = L.take((size_t)dm.R_d * 4);
+  o.vargmax = L.take((size_t)dm.B * kMaxTreeRows * 4); o.root_idx = L.take((size_t)dm.B * 4);
+  const size_t tn = (size_t)dm.B * kMaxTreeRows;
+  o.t_tok = L.take(tn * 4); o.t_par = L.take(tn * 4); o.t_dep = L.take(tn * 4); o.t_anc = L.take(tn * 16);
+  o.vt_tok = L.take(dm.B * 4); o.vt_par = L.take(dm.B * 4); o.vt_dep = L.take(dm.B * 4); o.vt_anc = L.take(dm.B * 16);
+  const size_t B = dm.B;
+  o.L = L.take(B * 4); o.c = L.take(B * 4); o.root = L.take(B * 4);
+  o.pend_tok = L.take(B * dm.D1 * 4); o.pend_feat = L.take(B * dm.D1 * dm.d * 4);
+  o.n_out = L.take(B * 4); o.out = L.take(B * dm.out_cap * 4); o.acc_len = L.take(B * 4);
+  o.acc_path = L.take(B * dm.D1 * 4); o.L_prev = L.take(B * 4);
+  o.hist = L.take((kMaxDepth + 1) * 8); o.status = L.take(4);
+  const size_t pc = (size_t)std::max(dm.pool_cap, 1) * B;
+  o.p_score = L.take(pc * 4); o.p_token = L.take(pc * 4); o.p_parent = L.take(pc * 4); o.p_depth = L.take(pc * 4);
+  o.p_cid = L.take(pc * 4); o.p_frow = L.take(pc * 4); o.p_smask = L.take(pc * 8);
+  o.p_count = L.take(B * 4); o.p_front = L.take(B * std::max(dm.k, 1) * 4); o.p_nfront = L.take(B * 4);
+  const size_t NR = dm.NR;
+  o.s_parent = L.take(NR * 4); o.s_rank = L.take(NR * 4); o.s_depth = L.take(NR * 4); o.s_lrow = L.take(NR * 4);
+  o.s_sidx = L.take(NR * 4); o.s_smask = L.take(NR * 8); o.s_lnodes = L.take((dm.D + 1) * NR * 4);
+  o.s_lcount = L.take((dm.D + 1) * 4);
+  o.rope_cos = L.take((size_t)dm.cap_d * (dm.hd / 2) * 4); o.rope_sin = L.take((size_t)dm.cap_d * (dm.hd / 2) * 4);
+  const size_t kvl = B * dm.Hkv * (size_t)dm.cap * dm.hd * es;
+  o.kc = L.take(kvl * dm.Lyr); o.vc = L.take(kvl * dm.Lyr);
+  const size_t kvd = B * dm.Hkv * (size_t)dm.cap_d * dm.hd * es;
+  o.kc_d = L.take(kvd); o.vc_d = L.take(kvd);
+  size_t g = 0;
+  if (dm.bf16) {
+    const int Ns[] = {dm.nqkv, dm.d, 2 * dm.ffn, dm.d, dm.V};
+    const int Ks[] = {dm.d, dm.qd, dm.d, dm.ffn, dm.d};
+    for (int i = 0; i < 5; ++i) g = std::max(g, gemm_tc_scratch_bytes((int)M, Ns[i], Ks[i]));
+    g = std::max(g, gemm_tc_scratch_bytes((int)M, dm.d, 2 * dm.d));
+  }
+  o.gemm_bytes = g;
+  o.gemm = L.take(std::max<size_t>(g, 256));
+  o.attn_part = L.take(std::max<size_t>(dm.bf16 ? attention_tc_scratch_bytes((int)M, dm.Hq, dm.hd, dm.cap_d) : 0, 256));
+  o.total = L.total;
+  return o;
+}
+
+template <typename T>
+struct Eng {
+  static eagle_status gemm(eagle_ctx* c, const void* X, const void* W, int M, int N, int K, const EpiParams& ep) {
+    if (M <= 0) return EAGLE_OK;
+    if constexpr (sizeof(T) == 2) {
+      if (gemm_tc_ok(c->dm, N, K)) {
+        EG_CK(gemm_tc((const bf16*)X, (const bf16*)W, M, N, K, ep, c->gemm_scratch, c->st.status, c->stream));
+        return EAGLE_OK;
+      }
+    }
+    EG_CK(gemm_simt<T>((const T*)X, (const T*)W, M, N, K, ep, c->stream));
+    return EAGLE_OK;
+  }
+
+  static eagle_status attention(eagle_ctx* c, const AttnArgs& a) {
+    if constexpr (sizeof(T) == 2) {
+      EG_CK(attention_tc(a, c->stream));
+    } else {
+      EG_CK(attention_simt<T>(a, c->stream));
+    }
+    return EAGLE_OK;
+  }
+
+  static EpiParams epi(eagle_ctx* c, int kind, int M, int N) {
+    EpiParams e;
+    e.kind = kind;
+    e.M = M;
+    e.N = N;
+    e.eps = c->cfg.rms_eps;
+    return e;
+  }
+
+  // One pre-norm decoder layer over M rows whose (hb, ssq_b) hold the layer input.
+  static eagle_status layer(eagle_ctx* c, const LayerPtrs& lw, void* kc, void* vc, int cap, int M, int n_groups,
+                            float* h, const float* gain_next) {
+    const Dims& dm = c->dm;
+    EpiParams e = epi(c, kEpiQkv, M, dm.nqkv);
+    e.ssq_in = c->ssq_b; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d;
+    e.out = c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
+    e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = c->rows;
+    EG_TRY(gemm(c, c->hb, lw.wqkv, M, dm.nqkv, dm.d, e));
+
+    AttnArgs a{};
+    a.q = c->q; a.kc = kc; a.vc = vc; a.o = c->attn; a.groups = c->groups; a.n_groups = n_groups;
+    a.mask = c->rows.mask; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap;
+    a.max_prefix = cap; a.scale = 1.f / std::sqrt((float)dm.hd); a.part = c->attn_part; a.status = c->st.status;
+    EG_TRY(attention(c, a));
+
+    e = epi(c, kEpiResid, M, dm.d);
+    e.h = h; e.hb = c->hb; e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
+    EG_TRY(gemm(c, c->attn, lw.wo, M, dm.d, dm.qd, e));
+
+    e = epi(c, kEpiSwiglu, M, 2 * dm.ffn);
+    e.ssq_in = c->ssq_a; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.out = c->act; e.ffn = dm.ffn;
+    EG_TRY(gemm(c, c->hb, lw.wgu, M, 2 * dm.ffn, dm.d, e));
+
+    e = epi(c, kEpiResid, M, dm.d);
+    e.h = h; e.hb = c->hb; e.ssq_out = c->ssq_b; e.gain = gain_next;
+    EG_TRY(gemm(c, c->act, lw.wd, M, dm.d, dm.ffn, e));
+    return EAGLE_OK;
+  }
+
+  static eagle_status lm_head(eagle_ctx* c, const void* X, const float* ssq, int M, int k, int* idx, float* val,
+                              float* lse, float* logits) {
+    const Dims& dm = c->dm;
+    EpiParams e = epi(c, kEpiLmHead, M, dm.V);
+    e.ssq_in = ssq; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.topk = k; e.y = logits;
+    e.rec_val = c->rec_val; e.rec_idx = c->rec_idx; e.rec_max = c->rec_max; e.rec_sum = c->rec_sum;
+    EG_TRY(gemm(c, X, c->lm_head, M, dm.V, dm.d, e));
+    EG_CK(topk_merge(c->rec_val, c->rec_idx, c->rec_max, c->rec_sum, dm.ntV, M, k, idx, val, lse, c->stream));
+    return EAGLE_OK;
+  }
+
+  static eagle_status target_stack(eagle_ctx* c, int M, int n_groups) {
+    const Dims& dm = c->dm;
+    const size_t es = sizeof(T);
+    const size_t kvl = (size_t)dm.B * dm.Hkv * dm.cap * dm.hd;
+    EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok, M, dm.d, c->layers[0].attn_norm, c->h_tgt, (T*)c->hb,
+                        c->ssq_b, c->stream));
+    for (int l = 0; l < dm.Lyr; ++l) {
+      const float* gn = l + 1 < dm.Lyr ? c->layers[l + 1].attn_norm : c->final_norm;
+      EG_TRY(layer(c, c->layers[l], (char*)c->kc + l * kvl * es, (char*)c->vc + l * kvl * es, dm.cap, M, n_groups,
+                   c->h_tgt, gn));
+    }
+    return EAGLE_OK;
+  }
+
+  // Draft head over the phase's rows: FC([feature ; E(token)]) then the head layer, then (k > 0) LM-head top-k.
+  static eagle_status draft_forward(eagle_ctx* c, const float* feat, int M, int n_groups, int hbase, int k) {
+    const Dims& dm = c->dm;
+    float* h = c->h_dft + (size_t)hbase * dm.d;
+    EG_CK(fc_input<T>(feat, c->rows.fsrc, (const T*)c->embed, c->rows.tok, M, dm.d, (T*)c->xfc, c->stream));
+    EpiParams e = epi(c, kEpiFc, M, dm.d);
+    e.h = h; e.hb = c->hb; e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
+    EG_TRY(gemm(c, c->xfc, c->fc, M, dm.d, 2 * dm.d, e));
+    EG_TRY(layer(c, c->head, c->kc_d, c->vc_d, dm.cap_d, M, n_groups, h, c->final_norm));
+    if (k > 0)
+      EG_TRY(lm_head(c, c->hb, c->ssq_b, M, k, c->dtopk_idx + (size_t)hbase * k, c->dtopk_val + (size_t)hbase * k,
+                     c->dlse + hbase, nullptr));
+    return EAGLE_OK;
+  }
+
+  static eagle_status prefill(eagle_ctx* c, const int* d_tokens, int P, int* root_out) {
+    const Dims& dm = c->dm;
+    for (int c0 = 0; c0 < P; c0 += dm.CL) {
+      const int cl = std::min(dm.CL, P - c0);
+      const int M = dm.B * cl, G = dm.B * ((cl + 127) / 128);
+      EG_CK(setup_prefill_rows(d_tokens, P, c0, cl, dm.B, false, c->rows, c->groups, c->stream));
+      EG_TRY(target_stack(c, M, G));
+      if (c0 + cl == P) {
+        std::vector<int> src(dm.B);
+        for (int b = 0; b < dm.B; ++b) src[b] = b * cl + cl - 1;
+        EG_CK(cudaMemcpyAsync(c->lm_src, src.data(), dm.B * sizeof(int), cudaMemcpyHostToDevice, c->stream));
+        EG_CK(gather_rows<T>((const T*)c->hb, c->ssq_b, M, c->lm_src, dm.B, dm.d, (T*)c->lm_hb, c->lm_ssq, c->stream));
+        EG_TRY(lm_head(c, c->lm_hb, c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr));
+        EG_CK(prefill_finish(c->st, c->root_idx, c->h_tgt, cl, P, root_out, c->stream));
+        EG_CK(cudaStreamSynchronize(c->stream));  // src is a host temporary
+      }
+      EG_CK(setup_prefill_rows(d_tokens, P, c0, cl, dm.B, true, c->rows, c->groups, c->stream));
+      EG_TRY(draft_forward(c, c->h_tgt, M, G, 0, 0));
+    }
+    return EAGLE_OK;
+  }
+
+  static eagle_status draft(eagle_ctx* c) {
+    const Dims& dm = c->dm;
+    const Level catchup{0, dm.D1};
+    EG_CK(setup_catchup_rows(c->st, c->rows, c->groups, c->stream));
+    EG_TRY(draft_forward(c, c->st.pend_feat, dm.B * dm.D1, dm.B, 0, dm.k));
+    for (int t = 1; t <= dm.D; ++t) {
+      const Level prev = t > 1 ? Level{dm.level_base[t - 1], dm.level_rows[t - 1]} : Level{0, 0};
+      const Level next = t < dm.D ? Level{dm.level_base[t], dm.level_rows[t]} : Level{0, 0};
+      if (dm.mode == EAGLE_TREE_STATIC) {
+        EG_CK(static_level(c->st, c->topo, t, c->dtopk_idx, catchup, prev, next, c->tree, c->rows, c->groups, dm.S,
+                           c->stream));
+      } else {
+        const float ln_tau = (float)std::log((double)c->cfg.tau);
+        EG_CK(eagle2_level(c->st, c->pool, t, dm.D, dm.k, ln_tau, c->dtopk_idx, c->dtopk_val, c->dlse, catchup,
+                           prev, next, c->rows, c->groups, dm.S, c->stream));
+      }
+      if (next.per_seq > 0)
+        EG_TRY(draft_forward(c, c->h_dft, dm.B * next.per_seq, dm.B, next.base, dm.k));
+    }
+    if (dm.mode == EAGLE_TREE_DYNAMIC) EG_CK(eagle2_final(c->st, c->pool, dm.n_nodes, c->tree, c->stream));
+    return EAGLE_OK;
+  }
+
+  static eagle_status verify(eagle_ctx* c, const TreeOut& tree, int* d_argmax, float* d_logits) {
+    const Dims& dm = c->dm;
+    const int M = dm.B * tree.n_rows;
+    EG_CK(setup_verify_rows(c->st, tree, c->rows, c->groups, c->stream));
+    EG_TRY(target_stack(c, M, dm.B));
+    EG_TRY(lm_head(c, c->hb, c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits));
+    if (d_argmax)
+      EG_CK(cudaMemcpyAsync(d_argmax, c->vargmax, (size_t)M * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+    return EAGLE_OK;
+  }
+
+  static eagle_status accept(eagle_ctx* c, int* acc_out, int* tok_out) {
+    const Dims& dm = c->dm;
+    EG_CK(accept_commit(c->st, c->last_tree, c->vargmax, c->h_tgt, acc_out, tok_out, c->stream));
+    EG_CK(compact_kv<T>(c->st, (T*)c->kc, (T*)c->vc, dm.Lyr, dm.Hkv, dm.hd, c->stream));
+    return EAGLE_OK;
+  }
+};
+
+template <typename F>
+eagle_status dispatch(eagle_ctx* c, F&& f) {
+  if (c->dm.bf16) return f(Eng<bf16>{});
+  return f(Eng<float>{});
+}
+
+eagle_status check_ready(eagle_ctx* c) {
+  if (!c) return EAGLE_ERR_INVALID_ARG;
+  if (c->failed) return EAGLE_ERR_STATE;
+  return EAGLE_OK;
+}
+
+eagle_status read_status(eagle_ctx* c) {
+  int s = 0;
+  EG_CK(cudaStreamSynchronize(c->stream));
+  EG_CK(cudaMemcpy(&s, c->st.status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (s == kStCapacity) return fail(c, EAGLE_ERR_CAPACITY, "device: KV cache capacity exceeded");
+  if (s == kStTimeout) return fail(c, EAGLE_ERR_TIMEOUT, "device: bounded wait timed out");
+  if (s != 0) return fail(c, EAGLE_ERR_CUDA, "device: status " + std::to_string(s));
+  return EAGLE_OK;
+}
+
+}  // namespace
+}  // namespace eg
+
+using namespace eg;
+
+extern "C" {
+
+eagle_status eagle_workspace_size(const eagle_config* cfg, size_t* bytes) {
+  if (!cfg || !bytes) return EAGLE_ERR_INVALID_ARG;
+  Dims dm;
+  std::string why;
+  eagle_status s = derive(*cfg, dm, why);
+  if (s != EAGLE_OK) return s;
+  *bytes = plan(dm).total;
+  return EAGLE_OK;
+}
+
+eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d_ws, size_t ws_bytes, void* stream,
+                        eagle_ctx** out) {
+  if (!cfg || !w || !out) return EAGLE_ERR_INVALID_ARG;
+  *out = nullptr;
+  eagle_ctx* c = new eagle_ctx();
+  c->cfg = *cfg;
+  std::string why;
+  eagle_status s = derive(*cfg, c->dm, why);
+  if (s != EAGLE_OK) {
+    delete c;
+    return s;
+  }
+  const Dims& dm = c->dm;
+  if (!w->embed || !w->lm_head || !w->final_norm || !w->layers || !w->fc) {
+    delete c;
+    return EAGLE_ERR_INVALID_ARG;
+  }
+  auto lp = [](const eagle_layer_weights& l) {
+    return LayerPtrs{l.wqkv, l.wo, l.wgu, l.wd, l.attn_norm, l.ffn_norm};
+  };
+  for (int l = 0; l < dm.Lyr; ++l) c->layers.push_back(lp(w->layers[l]));
+  c->head = lp(w->head);
+  for (const LayerPtrs& l : c->layers)
+    if (!l.wqkv || !l.wo || !l.wgu || !l.wd || !l.attn_norm || !l.ffn_norm) { delete c; return EAGLE_ERR_INVALID_ARG; }
+  if (!c->head.wqkv || !c->head.wo || !c->head.wgu || !c->head.wd || !c->head.attn_norm || !c->head.ffn_norm) {
+    delete c;
+    return EAGLE_ERR_INVALID_ARG;
+  }
+  c->embed = w->embed; c->lm_head = w->lm_head; c->final_norm = w->final_norm; c->fc = w->fc;
+  const Offsets o = plan(dm);
+  if (!d_ws || ws_bytes < o.total || (reinterpret_cast<uintptr_t>(d_ws) % kAlign)) {
+    delete c;
+    return EAGLE_ERR_WORKSPACE;
+  }
+  c->stream = (cudaStream_t)stream;
+  char* base = (char*)d_ws;
+  auto P = [&](size_t off) { return (void*)(base + off); };
+  c->rows = Rows{(int*)P(o.rows_seq), (int*)P(o.rows_pos), (int*)P(o.rows_slot), (int*)P(o.rows_grp),
+                 (uint64_t*)P(o.rows_mask), (int*)P(o.rows_tok), (int*)P(o.rows_fsrc)};
+  c->groups = (Group*)P(o.groups);
+  c->h_tgt = (float*)P(o.h_tgt); c->h_dft = (float*)P(o.h_dft); c->hb = P(o.hb);
+  c->ssq_a = (float*)P(o.ssq_a); c->ssq_b = (float*)P(o.ssq_b);
+  c->q = P(o.q); c->attn = P(o.attn); c->act = P(o.act); c->xfc = P(o.xfc);
+  c->lm_hb = P(o.lm_hb); c->lm_ssq = (float*)P(o.lm_ssq); c->lm_src = (int*)P(o.lm_src);
+  c->rec_val = (float*)P(o.rec_val); c->rec_idx = (int*)P(o.rec_idx);
+  c->rec_max = (float*)P(o.rec_max); c->rec_sum = (float*)P(o.rec_sum);
+  c->dtopk_idx = (int*)P(o.dtopk_idx); c->dtopk_val = (float*)P(o.dtopk_val); c->dlse = (float*)P(o.dlse);
+  c->vargmax = (int*)P(o.vargmax); c->root_idx = (int*)P(o.root_idx);
+  c->tree = TreeOut{dm.NR, (int*)P(o.t_tok), (int*)P(o.t_par), (int*)P(o.t_dep), (uint64_t*)P(o.t_anc)};
+  c->vtree = TreeOut{1, (int*)P(o.vt_tok), (int*)P(o.vt_par), (int*)P(o.vt_dep), (uint64_t*)P(o.vt_anc)};
+  State& st = c->st;
+  st.L = (int*)P(o.L); st.c = (int*)P(o.c); st.root = (int*)P(o.root); st.pend_tok = (int*)P(o.pend_tok);
+  st.pend_feat = (float*)P(o.pend_feat); st.n_out = (int*)P(o.n_out); st.out = (int*)P(o.out);
+  st.acc_len = (int*)P(o.acc_len); st.acc_path = (int*)P(o.acc_path); st.L_prev = (int*)P(o.L_prev);
+  st.hist = (unsigned long long*)P(o.hist); st.status = (int*)P(o.status);
+  st.B = dm.B; st.D1 = dm.D1; st.d = dm.d; st.cap = dm.cap; st.cap_d = dm.cap_d; st.out_cap = dm.out_cap;
+  st.V = dm.V;
+  Pool& pl = c->pool;
+  pl.score = (float*)P(o.p_score); pl.token = (int*)P(o.p_token); pl.parent = (int*)P(o.p_parent);
+  pl.depth = (int*)P(o.p_depth); pl.cid = (int*)P(o.p_cid); pl.frow = (int*)P(o.p_frow);
+  pl.smask = (uint64_t*)P(o.p_smask); pl.count = (int*)P(o.p_count); pl.front = (int*)P(o.p_front);
+  pl.nfront = (int*)P(o.p_nfront); pl.cap = dm.pool_cap;
+  StaticTopo& tp = c->topo;
+  tp.n_rows = dm.NR; tp.depth_max = dm.D; tp.k = dm.k;
+  tp.parent = (int*)P(o.s_parent); tp.rank = (int*)P(o.s_rank); tp.depth = (int*)P(o.s_depth);
+  tp.lrow = (int*)P(o.s_lrow); tp.sidx = (int*)P(o.s_sidx); tp.smask = (uint64_t*)P(o.s_smask);
+  tp.level_nodes = (int*)P(o.s_lnodes); tp.level_count = (int*)P(o.s_lcount);
+  c->rope_cos = (float*)P(o.rope_cos); c->rope_sin = (float*)P(o.rope_sin);
+  c->kc = P(o.kc); c->vc = P(o.vc); c->kc_d = P(o.kc_d); c->vc_d = P(o.vc_d);
+  c->gemm_scratch = P(o.gemm); c->gemm_scratch_bytes = o.gemm_bytes; c->attn_part = (float*)P(o.attn_part);
+
+  // Zero the workspace (tile counters, status, caches), then upload the tables.
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, o.total, c->stream);
+  // RoPE table: angle pos * theta^(-2i/hd), in double, rounded to float.
+  const int half = dm.hd / 2;
+  std::vector<float> cs((size_t)dm.cap_d * half), sn((size_t)dm.cap_d * half);
+  for (int p = 0; p < dm.cap_d; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow((double)cfg->rope_theta, -2.0 * i / dm.hd);
+      const double ang = (double)p * inv;
+      cs[(size_t)p * half + i] = (float)std::cos(ang);
+      sn[(size_t)p * half + i] = (float)std::sin(ang);
+    }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice, c->stream);
+  std::vector<int> tpar, tdep;
+  std::vector<uint64_t> tanc;
+  if (e == cudaSuccess && dm.mode == EAGLE_TREE_STATIC) {
+    const size_t NR = dm.NR;
+    e = cudaMemcpyAsync((void*)tp.parent, dm.s_parent.data(), NR * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)tp.rank, dm.s_rank.data(), NR * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)tp.depth, dm.s_depth.data(), NR * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)tp.lrow, dm.s_lrow.data(), NR * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)tp.sidx, dm.s_sidx.data(), NR * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)tp.smask, dm.s_smask.data(), NR * 8, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync((void*)tp.level_nodes, dm.s_level_nodes.data(), dm.s_level_nodes.size() * 4,
+                          cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync((void*)tp.level_count, dm.s_level_count.data(), dm.s_level_count.size() * 4,
+                          cudaMemcpyHostToDevice, c->stream);
+    for (int b = 0; b < dm.B; ++b) {
+      tpar.insert(tpar.end(), dm.s_parent.begin(), dm.s_parent.end());
+      tdep.insert(tdep.end(), dm.s_depth.begin(), dm.s_depth.end());
+      tanc.insert(tanc.end(), dm.s_anc.begin(), dm.s_anc.end());
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->tree.parent, tpar.data(), tpar.size() * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->tree.depth, tdep.data(), tdep.size() * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->tree.anc, tanc.data(), tanc.size() * 8, cudaMemcpyHostToDevice, c->stream);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) {
+    delete c;
+    return EAGLE_ERR_CUDA;
+  }
+  *out = c;
+  return EAGLE_OK;
+}
+
+eagle_status eagle_prefill(eagle_ctx* c, const int32_t* d_tokens, int32_t P, int32_t* d_root_out) {
+  EG_TRY(check_ready(c));
+  if (!d_tokens || P < 1 || P > c->dm.P_max) return fail(c, EAGLE_ERR_INVALID_ARG, "prompt_len out of range");
+  EG_TRY(dispatch(c, [&](auto E) { return decltype(E)::prefill(c, d_tokens, P, d_root_out); }));
+  c->phase = 1;
+  return EAGLE_OK;
+}
+
+eagle_status eagle_draft_tree(eagle_ctx* c, eagle_tree* out) {
+  EG_TRY(check_ready(c));
+  if (c->phase < 1) return fail(c, EAGLE_ERR_INVALID_ARG, "draft before prefill");
+  if (c->phase == 2 || c->phase == 3) return fail(c, EAGLE_ERR_INVALID_ARG, "draft twice without accept");
+  EG_TRY(dispatch(c, [&](auto E) { return decltype(E)::draft(c); }));
+  if (out && out->tokens) {
+    if (!out->parent || !out->depth || !out->anc || out->n_rows < c->tree.n_rows)
+      return fail(c, EAGLE_ERR_INVALID_ARG, "draft_tree: caller arrays too small");
+    const size_t n = (size_t)c->dm.B * c->tree.n_rows;
+    // caller arrays use the same [batch][n_rows] packing as the workspace tree
+    EG_CK(cudaMemcpyAsync(out->tokens, c->tree.tokens, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    EG_CK(cudaMemcpyAsync(out->parent, c->tree.parent, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    EG_CK(cudaMemcpyAsync(out->depth, c->tree.depth, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    EG_CK(cudaMemcpyAsync(out->anc, c->tree.anc, n * 16, cudaMemcpyDeviceToDevice, c->stream));
+    out->n_rows = c->tree.n_rows;
+  } else if (out) {
+    *out = eagle_tree{c->tree.n_rows, c->tree.tokens, c->tree.parent, c->tree.depth, c->tree.anc};
+  }
+  c->phase = 2;
+  return EAGLE_OK;
+}
+
+eagle_status eagle_verify(eagle_ctx* c, const eagle_tree* tree, int32_t* d_argmax, float* d_logits) {
+  EG_TRY(check_ready(c));
+  if (c->phase < 1) return fail(c, EAGLE_ERR_INVALID_ARG, "verify before prefill");
+  if (!tree || tree->n_rows < 1 || tree->n_rows > EAGLE_MAX_TREE_ROWS || !tree->tokens || !tree->parent ||
+      !tree->depth || !tree->anc)
+    return fail(c, EAGLE_ERR_INVALID_ARG, "bad tree");
+  TreeOut t{tree->n_rows, tree->tokens, tree->parent, tree->depth, tree->anc};
+  c->last_tree = t;
+  EG_TRY(dispatch(c, [&](auto E) { return decltype(E)::verify(c, t, d_argmax, d_logits); }));
+  c->phase = 3;
+  return EAGLE_OK;
+}
+
+eagle_status eagle_accept_commit(eagle_ctx* c, int32_t* d_accept_len, int32_t* d_tokens_out) {
+  EG_TRY(check_ready(c));
+  if (c->phase != 3) return fail(c, EAGLE_ERR_INVALID_ARG, "accept without verify");
+  EG_TRY(dispatch(c, [&](auto E) { return decltype(E)::accept(c, d_accept_len, d_tokens_out); }));
+  c->phase = 1;
+  return EAGLE_OK;
+}
+
+static eagle_status step_once(eagle_ctx* c, bool vanilla) {
+  return dispatch(c, [&](auto E) -> eagle_status {
+    using En = decltype(E);
+    if (vanilla) {
+      const TreeOut t = c->vtree;
+      EG_CK(set_root_tree(c->st, t, c->stream));
+      c->last_tree = t;
+      EG_TRY(En::verify(c, t, nullptr, nullptr));
+    } else {
+      EG_TRY(En::draft(c));
+      c->last_tree = c->tree;
+      EG_TRY(En::verify(c, c->tree, nullptr, nullptr));
+    }
+    return En::accept(c, nullptr, nullptr);
+  });
+}
+
+// The captured step of this context (captured on first use). A legacy-default
+// (NULL) stream cannot be captured: *exec stays NULL and the caller runs eagerly.
+static eagle_status step_graph(eagle_ctx* c, bool vanilla, cudaGraphExec_t* exec) {
+  *exec = nullptr;
+  if (c->stream == nullptr) return EAGLE_OK;
+  cudaGraphExec_t& slot = c->graph_exec[vanilla ? 1 : 0];
+  if (!slot) {
+    cudaGraph_t graph = nullptr;
+    EG_CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+    eagle_status s = step_once(c, vanilla);
+    cudaError_t ce = cudaStreamEndCapture(c->stream, &graph);
+    if (s != EAGLE_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return s;
+    }
+    if (ce != cudaSuccess) return fail(c, EAGLE_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(ce));
+    size_t n_nodes = 0;
+    EG_CK(cudaGraphGetNodes(graph, nullptr, &n_nodes));
+    std::vector<cudaGraphNode_t> nodes(n_nodes);
+    EG_CK(cudaGraphGetNodes(graph, nodes.data(), &n_nodes));
+    int kernels = 0;
+    for (cudaGraphNode_t nd : nodes) {
+      cudaGraphNodeType ty;
+      EG_CK(cudaGraphNodeGetType(nd, &ty));
+      kernels += ty == cudaGraphNodeTypeKernel;
+    }
+    c->graph_kernels[vanilla ? 1 : 0] = kernels;
+    cudaError_t ie = cudaGraphInstantiate(&slot, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) return fail(c, EAGLE_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
+  }
+  *exec = slot;
+  return EAGLE_OK;
+}
+
+static eagle_status run_steps(eagle_ctx* c, int n, bool vanilla, cudaGraphExec_t exec) {
+  for (int i = 0; i < n; ++i) {
+    if (exec) {
+      EG_CK(cudaGraphLaunch(exec, c->stream));
+    } else {
+      EG_TRY(step_once(c, vanilla));
+    }
+  }
+  return EAGLE_OK;
+}
+
+static eagle_status generate(eagle_ctx* c, const int32_t* d_prompt, int32_t P, int32_t max_new, int32_t use_graph,
+                             int32_t* d_out, eagle_stats* h_stats, bool vanilla) {
+  EG_TRY(check_ready(c));
+  const Dims& dm = c->dm;
+  if (!d_prompt || !d_out || P < 1 || P > dm.P_max || max_new < 1 || max_new > c->cfg.max_new)
+    return fail(c, EAGLE_ERR_INVALID_ARG, "generate: bad arguments");
+  cudaEvent_t e0, e1, e2;
+  EG_CK(cudaEventCreate(&e0));
+  EG_CK(cudaEventCreate(&e1));
+  EG_CK(cudaEventCreate(&e2));
+  EG_CK(cudaMemsetAsync(c->st.hist, 0, (kMaxDepth + 1) * 8, c->stream));
+  EG_CK(cudaEventRecord(e0, c->stream));
+  EG_TRY(dispatch(c, [&](auto E) { return decltype(E)::prefill(c, d_prompt, P, nullptr); }));
+  c->phase = 1;
+  EG_CK(cudaEventRecord(e1, c->stream));
+  cudaGraphExec_t exec = nullptr;
+  if (use_graph) EG_TRY(step_graph(c, vanilla, &exec));
+  std::vector<int> nout(dm.B);
+  int64_t steps = 0;
+  double tps = 1.0;
+  for (;;) {
+    EG_CK(cudaMemcpyAsync(nout.data(), c->st.n_out, dm.B * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    EG_CK(cudaStreamSynchronize(c->stream));
+    int mn = nout[0];
+    long long tot = 0;
+    for (int b = 0; b < dm.B; ++b) { mn = std::min(mn, nout[b]); tot += nout[b]; }
+    if (mn >= max_new) break;
+    if (steps > 0) tps = std::max(1.0, (double)(tot - dm.B) / (double)(steps * dm.B));
+    const int remaining = max_new - mn;
+    int run = std::max(1, (int)std::floor(remaining / tps));
+    if (steps == 0) run = std::min(run, 8);
+    EG_TRY(run_steps(c, run, vanilla, exec));
+    steps += run;
+    if (steps > (int64_t)max_new * 2 + 16) return fail(c, EAGLE_ERR_STATE, "generate: no progress");
+  }
+  EG_CK(cudaEventRecord(e2, c->stream));
+  EG_CK(copy_out(c->st, max_new, d_out, c->stream));
+  eagle_status s = read_status(c);
+  if (s != EAGLE_OK) return s;
+  if (h_stats) {
+    std::memset(h_stats, 0, sizeof(*h_stats));
+    unsigned long long hist[kMaxDepth + 1];
+    EG_CK(cudaMemcpy(hist, c->st.hist, sizeof(hist), cudaMemcpyDeviceToHost));
+    int64_t n = 0, acc = 0;
+    for (int i = 0; i <= kMaxDepth; ++i) {
+      h_stats->accept_hist[i] = (int64_t)hist[i];
+      n += (int64_t)hist[i];
+      acc += (int64_t)hist[i] * i;
+    }
+    h_stats->steps = steps;
+    h_stats->mean_accept = n ? (double)acc / n : 0.0;
+    EG_CK(cudaMemcpy(nout.data(), c->st.n_out, dm.B * sizeof(int), cudaMemcpyDeviceToHost));
+    for (int b = 0; b < dm.B; ++b) h_stats->committed += nout[b];
+    float ms = 0.f;
+    EG_CK(cudaEventElapsedTime(&ms, e0, e1));
+    h_stats->prefill_ms = ms;
+    EG_CK(cudaEventElapsedTime(&ms, e1, e2));
+    h_stats->decode_ms = ms;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaEventDestroy(e2);
+  return EAGLE_OK;
+}
+
+eagle_status eagle_generate(eagle_ctx* c, const int32_t* d_prompt, int32_t P, int32_t max_new, int32_t use_graph,
+                            int32_t* d_out, eagle_stats* h_stats) {
+  return generate(c, d_prompt, P, max_new, use_graph, d_out, h_stats, false);
+}
+
+eagle_status eagle_generate_vanilla(eagle_ctx* c, const int32_t* d_prompt, int32_t P, int32_t max_new,
+                                    int32_t use_graph, int32_t* d_out, eagle_stats* h_stats) {
+  return generate(c, d_prompt, P, max_new, use_graph, d_out, h_stats, true);
+}
+
+eagle_status eagle_step(eagle_ctx* c, int32_t n_steps, int32_t vanilla, int32_t use_graph) {
+  EG_TRY(check_ready(c));
+  if (c->phase != 1) return fail(c, EAGLE_ERR_INVALID_ARG, "step: needs a prefilled context between steps");
+  if (n_steps < 0) return fail(c, EAGLE_ERR_INVALID_ARG, "step: n_steps < 0");
+  cudaGraphExec_t exec = nullptr;
+  if (use_graph) EG_TRY(step_graph(c, vanilla != 0, &exec));
+  return run_steps(c, n_steps, vanilla != 0, exec);
+}
+
+int32_t eagle_step_kernel_count(const eagle_ctx* c, int32_t vanilla) {
+  return c ? c->graph_kernels[vanilla ? 1 : 0] : -1;
+}
+
+eagle_status eagle_sync_status(eagle_ctx* c) {
+  if (!c) return EAGLE_ERR_INVALID_ARG;
+  if (c->failed) return EAGLE_ERR_STATE;
+  return read_status(c);
+}
+
+eagle_status eagle_committed_counts(eagle_ctx* c, int32_t* d_counts) {
+  if (!c || !d_counts) return EAGLE_ERR_INVALID_ARG;
+  EG_CK(cudaMemcpyAsync(d_counts, c->st.n_out, c->dm.B * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+  return EAGLE_OK;
+}
+
+eagle_status eagle_destroy(eagle_ctx* c) {
+  if (!c) return EAGLE_ERR_INVALID_ARG;
+  for (cudaGraphExec_t& g : c->graph_exec)
+    if (g) cudaGraphExecDestroy(g);
+  delete c;
+  return EAGLE_OK;
+}
+
+const char* eagle_last_error(const eagle_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+// GEMM epilogues shared by the SIMT and the tcgen05 GEMM.
+//
+// Both GEMMs finish an output tile of up to 128 weight rows (columns n of Y)
+// by `msub` token rows (rows m of Y) as float32 in shared memory,
+// tile[m * ldt + c] = sum_k X[m0+m][k] W[n0+c][k], and call run_epilogue with
+// 128 threads. The epilogue applies the RMSNorm row scale of the GEMM input
+// and the op that follows the projection in a Llama decoder layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace eg {
+
+// rscale must hold msub floats of shared memory. Run by 128 threads with
+// ranks tid = 0..127; sync() must be a barrier over exactly those threads.
+template <typename T, typename Sync>
+__device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, int msub, int n0,
+                             float* rscale, int tid, Sync sync) {
+  const int ncols = min(kTileN, p.N - n0);
+  for (int m = tid; m < msub; m += 128) {
+    float r = 1.f;
+    if (p.ssq_in) {
+      float s = 0.f;
+      for (int j = 0; j < p.n_ssq_in; ++j) s += p.ssq_in[(size_t)j * p.M + m0 + m];
+      r = rsqrtf(s * p.inv_d_in + p.eps);
+    }
+    rscale[m] = r;
+  }
+  sync();
+
+  switch (p.kind) {
+    case kEpiStore: {
+      for (int m = 0; m < msub; ++m)
+        if (tid < ncols) p.y[(size_t)(m0 + m) * p.N + n0 + tid] = tile[m * ldt + tid] * rscale[m];
+      break;
+    }
+    case kEpiQkv: {
+      const int c = tid;
+      if (c < ncols) {
+        const int n = n0 + c;
+        const int hd = p.head_dim, half = hd >> 1;
+        const int i = n % hd;
+        const int region = n < p.q_dim ? 0 : (n < p.q_dim + p.kv_dim ? 1 : 2);
+        const int partner = i < half ? c + half : c - half;
+        const int fi = i < half ? i : i - half;
+        for (int m = 0; m < msub; ++m) {
+          const int row = m0 + m;
+          float v = tile[m * ldt + c] * rscale[m];
+          if (region < 2) {
+            const float pv = tile[m * ldt + partner] * rscale[m];
+            const int pos = p.rows.pos[row];
+            const float cs = p.rope_cos[(size_t)pos * half + fi];
+            const float sn = p.rope_sin[(size_t)pos * half + fi];
+            v = i < half ? v * cs - pv * sn : v * cs + pv * sn;
+          }
+          if (region == 0) {
+            reinterpret_cast<T*>(p.out)[(size_t)row * p.q_dim + n] = from_f<T>(v);
+          } else {
+            const int slot = p.rows.slot[row];
+            if (slot >= 0) {
+              const int nn = n - p.q_dim - (region == 2 ? p.kv_dim : 0);
+              const int kvh = nn / hd;
+              const size_t at = (((size_t)p.rows.seq[row] * p.n_kv + kvh) * p.cap + slot) * hd + i;
+              reinterpret_cast<T*>(region == 1 ? p.kc : p.vc)[at] = from_f<T>(v);
+            }
+          }
+        }
+      }
+      break;
+    }
+    case kEpiSwiglu: {
+      const int blk = n0 / kTileN;
+      const int rr = min(64, p.ffn - blk * 64);
+      const int c = tid;
+      if (c < rr) {
+        for (int m = 0; m < msub; ++m) {
+          const float g = tile[m * ldt + c] * rscale[m];
+          const float u = tile[m * ldt + rr + c] * rscale[m];
+          reinterpret_cast<T*>(p.out)[(size_t)(m0 + m) * p.ffn + blk * 64 + c] = from_f<T>(silu_f(g) * u);
+        }
+      }
+      break;
+    }
+    case kEpiResid:
+    case kEpiFc: {
+      const int c = tid;
+      if (c < ncols) {
+        const int n = n0 + c;
+        const float gn = p.gain[n];
+        for (int m = 0; m < msub; ++m) {
+          const size_t at = (size_t)(m0 + m) * p.N + n;
+          const float hn = (p.kind == kEpiResid ? p.h[at] : 0.f) + tile[m * ldt + c] * rscale[m];
+          p.h[at] = hn;
+          reinterpret_cast<T*>(p.hb)[at] = from_f<T>(hn * gn);
+          tile[m * ldt + c] = hn * hn;
+        }
+      } else {
+        for (int m = 0; m < msub; ++m) tile[m * ldt + c] = 0.f;
+      }
+      sync();
+      const int warp = tid >> 5, lane = tid & 31;
+      for (int m = warp; m < msub; m += 4) {
+        float s = tile[m * ldt + lane] + tile[m * ldt + lane + 32] + tile[m * ldt + lane + 64] +
+                  tile[m * ldt + lane + 96];
+        s = warp_sum(s);
+        if (lane == 0) p.ssq_out[(size_t)(n0 / kTileN) * p.M + m0 + m] = s;
+      }
+      break;
+    }
+    case kEpiLmHead: {
+      const int warp = tid >> 5, lane = tid & 31;
+      const int ti = n0 / kTileN;
+      for (int m = warp; m < msub; m += 4) {
+        float v[4];
+        int idx[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = lane + 32 * j;
+          idx[j] = n0 + c;
+          v[j] = c < ncols ? tile[m * ldt + c] * rscale[m] : -INFINITY;
+          if (p.y && c < ncols) p.y[(size_t)(m0 + m) * p.N + n0 + c] = v[j];
+        }
+        float mx = warp_max(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+        float se = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) se += (lane + 32 * j < ncols) ? __expf(v[j] - mx) : 0.f;
+        se = warp_sum(se);
+        const size_t rec = (size_t)ti * p.M + m0 + m;
+        if (lane == 0) {
+          p.rec_max[rec] = mx;
+          p.rec_sum[rec] = se;
+        }
+        for (int k = 0; k < p.topk; ++k) {
+          float bv = v[0];
+          int bi = idx[0], bj = 0;
+#pragma unroll
+          for (int j = 1; j < 4; ++j)
+            if (v[j] > bv || (v[j] == bv && idx[j] < bi)) { bv = v[j]; bi = idx[j]; bj = j; }
+          float wv = bv;
+          int wi = bi;
+          warp_argmax(wv, wi);
+          if (bi == wi && bv == wv) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j == bj) v[j] = -INFINITY;
+          }
+          if (lane == 0) {
+            p.rec_val[rec * p.topk + k] = wv;
+            p.rec_idx[rec * p.topk + k] = wi < p.N ? wi : -1;
+          }
+        }
+      }
+      break;
+    }
+  }
+  sync();
+}
+
+}  // namespace eg

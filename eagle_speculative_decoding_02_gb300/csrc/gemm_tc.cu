@@ -1,0 +1,487 @@
+// Weight-streaming GEMM Y = X W^T on the sm_103a tensor cores (tcgen05 + TMA).
+//
+// The verify pass multiplies a few dozen token rows by every weight matrix of
+// the target, so it is bound by streaming the weights from HBM. Swap-AB: a
+// 128-row weight tile is the UMMA M operand (A, K-major, 128B-swizzled, loaded
+// by TMA), the token rows are the UMMA N operand (B, N = 32..256), and the
+// fp32 accumulator lives in tensor memory. The (tile, 64-wide k-block) units of
+// a GEMM are split evenly over the SMs (stream-K); a tile cut between CTAs is
+// summed by the CTA that finishes it last, over the CTAs in ascending order,
+// so every output is summed in an order that depends only on (N, K) and the SM
+// count, never on M or on timing.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer (one lane): W box [128 x 64] + X box [MT x 64] per stage
+//   warp 1     TMEM allocator and MMA issuer (one lane): 4 x tcgen05.mma (K = 16) per stage
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//              32 (w % 4) ..), fixup, then the shared epilogue on 32-row sub-tiles
+// Every mbarrier wait is bounded (2 s of %globaltimer); a timeout sets the
+// device status word and an abort flag that the other roles observe, and the
+// kernel drains and frees its tensor memory before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace eg {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBK = 64;                       // K elements per stage: one 128-byte swizzle row
+constexpr int kWBytes = kTileN * kBK * 2;     // 16 KB weight box
+constexpr int kSub = 32;                      // epilogue rows per sub-tile
+constexpr int kLdt = kTileN + 1;
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 232448;           // 227 KB opt-in per block
+constexpr int kNsmSizing = 160;               // SM count bound used for scratch sizing
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+struct TcArgs {
+  int M, MT, m_chunks, n_tiles, kbt, G, stages;
+  long long T;
+  uint32_t tmem_cols;
+  int* counters;   // [m_chunks][n_tiles], zero on entry and on exit
+  float* partial;  // [m_chunks][G][2][MT][128]
+  int* status;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false on timeout (status set, abort raised) or when another role aborted.
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        set_status(status, kStTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+// Barrier over the 128 epilogue threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, 1, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major tile of 128-byte rows, 128B swizzle,
+// 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                     // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset
+  d |= (uint64_t)1 << 46;                     // descriptor version
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ schedule
+__device__ __forceinline__ long long unit_start(const TcArgs& a, int c) { return (long long)c * a.T / a.G; }
+__device__ __forceinline__ int cta_of(const TcArgs& a, long long u) {
+  return (int)(((u + 1) * a.G - 1) / a.T);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
+                   EpiParams ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.stages, MT = a.MT;
+  const int xbytes = MT * kBK * 2;
+  const int stage_bytes = kWBytes + xbytes;
+  uint8_t* stage_base = smem;
+  float* tile = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
+  float* rscale = tile + kSub * kLdt;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rscale + kSub);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* afull = bars + 2 * S;
+  uint64_t* aempty = bars + 2 * S + 2;
+  uint64_t* drain = bars + 2 * S + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x / a.m_chunks, mc = blockIdx.x % a.m_chunks;
+  const int m0 = mc * MT;
+  const long long u0 = unit_start(a, c), u1 = unit_start(a, c + 1);
+  const int kbt = a.kbt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+      int it = 0;
+      bool ok = true;
+      for (long long u = u0; u < u1 && ok;) {
+        const int t = (int)(u / kbt);
+        const int kb0 = (int)(u - (long long)t * kbt);
+        const int kb1 = (int)min((long long)kbt, u1 - (long long)t * kbt);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % S;
+          if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw = stage_base + (size_t)s * stage_bytes;
+          mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
+          tma_load_2d(sw, &tmW, &full[s], kb * kBK, t * kTileN);
+          tma_load_2d(sw + kWBytes, &tmX, &full[s], kb * kBK, m0);
+        }
+        u = (long long)(t + 1) * kbt;
+      }
+      if (!ok) {
+        // drain: wait (bounded) for every load still in flight before the CTA exits
+        for (int j = max(0, it - S); j < it; ++j) {
+          const int s = j % S;
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(&full[s], (j / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_bf16(MT);
+      int it = 0, f = 0;
+      bool ok = true;
+      for (long long u = u0; u < u1 && ok;) {
+        const int t = (int)(u / kbt);
+        const int kb0 = (int)(u - (long long)t * kbt);
+        const int kb1 = (int)min((long long)kbt, u1 - (long long)t * kbt);
+        const int buf = f & 1;
+        if (f >= 2 && !mbar_wait(&aempty[buf], ((f >> 1) - 1) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * MT);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(&full[s], (it / S) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sw = smem_u32(stage_base + (size_t)s * stage_bytes);
+          const uint32_t sx = sw + kWBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma(d, sw128_desc(sw + k * 32), sw128_desc(sx + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&afull[buf]);
+        ++f;
+        u = (long long)(t + 1) * kbt;
+      }
+      // no MMA may still be writing tensor memory when it is freed
+      umma_commit(drain);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (128 threads)
+    const int etid = threadIdx.x - 64;
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int col = q * 32 + lane;        // weight row within the tile = output column
+    const int rows_valid = min(MT, a.M - m0);
+    const int t_first = (int)(u0 / kbt);
+    int f = 0;
+    for (long long u = u0; u < u1;) {
+      const int t = (int)(u / kbt);
+      const int kb0 = (int)(u - (long long)t * kbt);
+      const int kb1 = (int)min((long long)kbt, u1 - (long long)t * kbt);
+      const bool whole = kb0 == 0 && kb1 == kbt;
+      const int buf = f & 1;
+      const bool ok = epi_all(mbar_wait(&afull[buf], (f >> 1) & 1, abort_flag, a.status));
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MT);
+      const int n0 = t * kTileN;
+      if (whole) {
+        for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+          float v[32];
+          tmem_ld32(tb + r0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tile[j * kLdt + col] = ok ? v[j] : 0.f;
+          EpilogueSync{}();
+          if (ok) run_epilogue<bf16>(ep, tile, kLdt, m0 + r0, min(kSub, rows_valid - r0), n0, rscale, etid,
+                                     EpilogueSync{});
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[buf]);
+      } else {
+        float* slot = a.partial + (((size_t)mc * a.G + c) * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
+        for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+          float v[32];
+          tmem_ld32(tb + r0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (r0 + j < rows_valid) slot[(size_t)(r0 + j) * kTileN + col] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[buf]);
+        __threadfence();
+        EpilogueSync{}();
+        const long long tu0 = (long long)t * kbt, tu1 = (long long)(t + 1) * kbt - 1;
+        const int c0 = cta_of(a, tu0), c1 = cta_of(a, tu1);
+        if (etid == 0) {
+          int* cnt = a.counters + (size_t)mc * a.n_tiles + t;
+          const int prev = atomicAdd(cnt, 1);
+          const int last = prev == (c1 - c0);
+          if (last) *cnt = 0;
+          *last_flag = last;
+        }
+        EpilogueSync{}();
+        if (*last_flag && ok) {
+          __threadfence();
+          for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+            for (int j = 0; j < kSub; ++j) {
+              float s = 0.f;
+              if (r0 + j < rows_valid) {
+                for (int cc = c0; cc <= c1; ++cc) {
+                  const int tf = (int)(unit_start(a, cc) / kbt);
+                  const float* sl =
+                      a.partial + (((size_t)mc * a.G + cc) * 2 + (t != tf ? 1 : 0)) * (size_t)MT * kTileN;
+                  s += __ldcg(sl + (size_t)(r0 + j) * kTileN + col);
+                }
+              }
+              tile[j * kLdt + col] = s;
+            }
+            EpilogueSync{}();
+            run_epilogue<bf16>(ep, tile, kLdt, m0 + r0, min(kSub, rows_valid - r0), n0, rscale, etid,
+                               EpilogueSync{});
+          }
+        }
+      }
+      ++f;
+      u = (long long)(t + 1) * kbt;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+    if (n > kNsmSizing) n = kNsmSizing;
+  }
+  return n;
+}
+
+struct Plan {
+  int MT, m_chunks, n_tiles, kbt, G, stages;
+  long long T;
+  uint32_t tmem_cols;
+  size_t smem, counters_bytes, partial_bytes;
+};
+
+Plan plan(int M, int N, int K, int nsm) {
+  Plan p{};
+  p.MT = M > 256 ? 256 : ((M + 31) / 32) * 32;
+  if (p.MT < 32) p.MT = 32;
+  p.m_chunks = (M + p.MT - 1) / p.MT;
+  p.n_tiles = N / kTileN;
+  p.kbt = K / kBK;
+  p.T = (long long)p.n_tiles * p.kbt;
+  const bool split = (long long)p.m_chunks * p.n_tiles < 2LL * nsm;
+  p.G = split ? (int)std::min<long long>(nsm, p.T) : p.n_tiles;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * p.MT)) cols <<= 1;
+  p.tmem_cols = cols;
+  const size_t stage = kWBytes + (size_t)p.MT * kBK * 2;
+  const size_t fixed = (size_t)kSub * kLdt * 4 + kSub * 4 + (2 * kMaxStages + 5) * 8 + 16 + 1024;
+  int st = (int)((kSmemBudget - fixed) / stage);
+  p.stages = std::max(2, std::min(kMaxStages, st));
+  p.smem = (size_t)p.stages * stage + fixed;
+  p.counters_bytes = ((size_t)p.m_chunks * p.n_tiles * 4 + 255) / 256 * 256;
+  p.partial_bytes = split ? (size_t)p.m_chunks * p.G * 2 * p.MT * kTileN * 4 : 0;
+  return p;
+}
+
+}  // namespace
+
+size_t gemm_tc_scratch_bytes(int M, int N, int K) {
+  // enough for any M' <= M on up to kNsmSizing SMs
+  size_t best = 256;
+  const int chunks = (M + 255) / 256;
+  for (int mc = 1; mc <= chunks; ++mc) {
+    const int Mp = mc == 1 ? std::min(M, 256) : mc * 256;
+    const Plan p = plan(Mp, N, K, kNsmSizing);
+    best = std::max(best, p.counters_bytes + p.partial_bytes);
+  }
+  return best;
+}
+
+cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const EpiParams& ep, void* scratch,
+                    int* status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  if (N % kTileN || K % kBK || !scratch) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
+  const Plan p = plan(M, N, K, num_sms());
+  CUtensorMap tmW, tmX;
+  if (!make_map(&tmW, W, N, K, kTileN) || !make_map(&tmX, X, M, K, p.MT)) return cudaErrorInvalidValue;
+  static std::once_flag attr;
+  std::call_once(attr, [] {
+    cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  });
+  TcArgs a{};
+  a.M = M;
+  a.MT = p.MT;
+  a.m_chunks = p.m_chunks;
+  a.n_tiles = p.n_tiles;
+  a.kbt = p.kbt;
+  a.G = p.G;
+  a.stages = p.stages;
+  a.T = p.T;
+  a.tmem_cols = p.tmem_cols;
+  a.counters = reinterpret_cast<int*>(scratch);
+  a.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + p.counters_bytes);
+  a.status = status;
+  gemm_tc_kernel<<<p.G * p.m_chunks, kThreads, p.smem, s>>>(tmW, tmX, a, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace eg

@@ -1,0 +1,55 @@
+// Host-side launchers of the EAGLE step kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace eg {
+
+// ---- GEMM: Y = X W^T with a fused epilogue ------------------------------------------------------
+template <typename T>
+cudaError_t gemm_simt(const T* X, const T* W, int M, int N, int K, const EpiParams& ep, cudaStream_t s);
+
+// tcgen05 + TMA weight-streaming GEMM (bf16). `scratch` holds split-K partials
+// and per-tile arrival counters (counters must start at zero; the kernel
+// leaves them at zero). Returns cudaErrorInvalidValue for unsupported shapes.
+size_t gemm_tc_scratch_bytes(int M, int N, int K);
+cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const EpiParams& ep, void* scratch,
+                    int* status, cudaStream_t s);
+
+// ---- attention ---------------------------------------------------------------------------------
+struct AttnArgs {
+  const void* q;      // [M][Hq][hd] (RoPE applied)
+  const void* kc;     // [B][Hkv][cap][hd]
+  const void* vc;
+  void* o;            // [M][Hq * hd]
+  const Group* groups;
+  int n_groups;
+  const uint64_t* mask;  // [M][2]
+  int M, Hq, Hkv, hd, cap;
+  int max_prefix;     // upper bound on any group's prefix (sizes the split grid)
+  float scale;        // 1/sqrt(hd)
+  float* part;        // split partials (tensor-core path)
+  int* status;
+};
+template <typename T>
+cudaError_t attention_simt(const AttnArgs& a, cudaStream_t s);
+size_t attention_tc_scratch_bytes(int M, int Hq, int hd, int max_prefix);
+cudaError_t attention_tc(const AttnArgs& a, cudaStream_t s);
+
+// ---- rows, embeddings, FC input ----------------------------------------------------------------
+template <typename T>
+cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, float* ssq,
+                       cudaStream_t s);
+template <typename T>
+cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x,
+                     cudaStream_t s);
+// Copy rows src[i] of (hb, ssq) to rows i of (hb_dst, ssq_dst).
+template <typename T>
+cudaError_t gather_rows(const T* hb, const float* ssq, int M_src, const int* src, int n, int d, T* hb_dst,
+                        float* ssq_dst, cudaStream_t s);
+
+// ---- LM-head top-k merge over vocab tiles ------------------------------------------------------
+cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* rec_max, const float* rec_sum,
+                       int ntiles, int M, int k, int* idx, float* val, float* lse, cudaStream_t s);
+
+}  // namespace eg

@@ -1,0 +1,165 @@
+// Row-wise kernels: embedding gather, draft-head FC input, row gather and the
+// LM-head top-k merge across vocab tiles.
+#include "kernels.h"
+
+namespace eg {
+namespace {
+
+// Block sum over 128 threads in a fixed order (warp tree, then warps 0..3).
+__device__ float block_sum128(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  return ((red[0] + red[1]) + red[2]) + red[3];
+}
+
+// h = E[tok]; hb = h * gain; ssq[j][m] = sum of h^2 over column tile j.
+template <typename T>
+__global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ E, const int* __restrict__ tok, int M,
+                                                    int d, const float* __restrict__ gain, float* h, T* hb,
+                                                    float* ssq) {
+  __shared__ float red[4];
+  const int m = blockIdx.x;
+  const int t = tok[m];
+  for (int j = 0; j * kTileN < d; ++j) {
+    const int n = j * kTileN + threadIdx.x;
+    float v = 0.f;
+    if (n < d) {
+      v = to_f(E[(size_t)t * d + n]);
+      h[(size_t)m * d + n] = v;
+      hb[(size_t)m * d + n] = from_f<T>(v * gain[n]);
+    }
+    const float s = block_sum128(v * v, red);
+    if (threadIdx.x == 0) ssq[(size_t)j * M + m] = s;
+  }
+}
+
+// x[m] = [ T(feat[fsrc[m]]) ; E[tok[m]] ]  (length 2d).
+template <typename T>
+__global__ void fc_input_kernel(const float* __restrict__ feat, const int* __restrict__ fsrc,
+                                const T* __restrict__ E, const int* __restrict__ tok, int d, T* x) {
+  const int m = blockIdx.x;
+  const float* f = feat + (size_t)fsrc[m] * d;
+  const T* e = E + (size_t)tok[m] * d;
+  T* xr = x + (size_t)m * 2 * d;
+  for (int n = threadIdx.x; n < d; n += blockDim.x) {
+    xr[n] = from_f<T>(f[n]);
+    xr[d + n] = e[n];
+  }
+}
+
+template <typename T>
+__global__ void gather_rows_kernel(const T* __restrict__ hb, const float* __restrict__ ssq, int M_src,
+                                   const int* __restrict__ src, int n_rows, int d, T* hb_dst, float* ssq_dst) {
+  const int i = blockIdx.x;
+  const int r = src[i];
+  for (int n = threadIdx.x; n < d; n += blockDim.x) hb_dst[(size_t)i * d + n] = hb[(size_t)r * d + n];
+  for (int j = threadIdx.x; j * kTileN < d; j += blockDim.x) ssq_dst[(size_t)j * n_rows + i] = ssq[(size_t)j * M_src + r];
+}
+
+// One block per row: log-sum-exp over all vocab tiles (fixed order) and the k
+// best (value desc, index asc) of the per-tile candidates.
+__global__ void __launch_bounds__(128) topk_merge_kernel(const float* __restrict__ rec_val,
+                                                         const int* __restrict__ rec_idx,
+                                                         const float* __restrict__ rec_max,
+                                                         const float* __restrict__ rec_sum, int ntiles, int M, int k,
+                                                         int* out_idx, float* out_val, float* out_lse) {
+  __shared__ float red[4];
+  __shared__ float sv[4];
+  __shared__ int si[4];
+  const int m = blockIdx.x, tid = threadIdx.x;
+  float mx = -INFINITY;
+  for (int t = tid; t < ntiles; t += 128) mx = fmaxf(mx, rec_max[(size_t)t * M + m]);
+  mx = warp_max(mx);
+  __syncthreads();
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  const float gmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float se = 0.f;
+  for (int t = tid; t < ntiles; t += 128) {
+    const size_t r = (size_t)t * M + m;
+    se += rec_sum[r] * __expf(rec_max[r] - gmax);
+  }
+  se = block_sum128(se, red);
+  if (tid == 0 && out_lse) out_lse[m] = gmax + __logf(se);
+
+  // k rounds: the best candidate strictly after the previous winner in (value desc, index asc).
+  float pv = INFINITY;
+  int pi = -1;
+  const int nc = ntiles * k;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = tid; c < nc; c += 128) {
+      const int t = c / k, j = c % k;
+      const size_t rr = ((size_t)t * M + m) * k + j;
+      const float v = rec_val[rr];
+      const int ix = rec_idx[rr];
+      if (ix < 0) continue;
+      const bool after = (v < pv) || (v == pv && ix > pi);
+      if (after && (v > bv || (v == bv && ix < bi))) { bv = v; bi = ix; }
+    }
+    warp_argmax(bv, bi);
+    __syncthreads();
+    if ((tid & 31) == 0) { sv[tid >> 5] = bv; si[tid >> 5] = bi; }
+    __syncthreads();
+    bv = sv[0];
+    bi = si[0];
+    for (int w = 1; w < 4; ++w)
+      if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
+    if (tid == 0) {
+      out_idx[(size_t)m * k + r] = bi;
+      if (out_val) out_val[(size_t)m * k + r] = bv;
+    }
+    pv = bv;
+    pi = bi;
+  }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, float* ssq,
+                       cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  embed_kernel<T><<<M, 128, 0, s>>>(E, tok, M, d, gain, h, hb, ssq);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x,
+                     cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  fc_input_kernel<T><<<M, 256, 0, s>>>(feat, fsrc, E, tok, d, x);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t gather_rows(const T* hb, const float* ssq, int M_src, const int* src, int n, int d, T* hb_dst,
+                        float* ssq_dst, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  gather_rows_kernel<T><<<n, 256, 0, s>>>(hb, ssq, M_src, src, n, d, hb_dst, ssq_dst);
+  return cudaGetLastError();
+}
+
+cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* rec_max, const float* rec_sum,
+                       int ntiles, int M, int k, int* idx, float* val, float* lse, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  topk_merge_kernel<<<M, 128, 0, s>>>(rec_val, rec_idx, rec_max, rec_sum, ntiles, M, k, idx, val, lse);
+  return cudaGetLastError();
+}
+
+#define EG_INST(T)                                                                                      \
+  template cudaError_t embed_rows<T>(const T*, const int*, int, int, const float*, float*, T*, float*,  \
+                                     cudaStream_t);                                                     \
+  template cudaError_t fc_input<T>(const float*, const int*, const T*, const int*, int, int, T*,        \
+                                   cudaStream_t);                                                       \
+  template cudaError_t gather_rows<T>(const T*, const float*, int, const int*, int, int, T*, float*,    \
+                                      cudaStream_t);
+EG_INST(float)
+EG_INST(bf16)
+#undef EG_INST
+
+}  // namespace eg

@@ -102,15 +102,32 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 _CHUNK = 1 << 22
+_HOST_LIB = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfixtures_cpu.so")
+_host = None
 
 
 def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def normal(key: int, count: int, std: float, start: int = 0, bf16: bool = False,
-           noise_key: int | None = None, noise_std: float = 0.0) -> np.ndarray:
-    """Elements [start, start+count) of a generated tensor as float32."""
+def _host_lib():
+    """The C/OpenMP implementation of the same recipe (fixtures/gen_cpu.c), if built."""
+    global _host
+    if _host is None:
+        _host = False
+        if os.path.exists(_HOST_LIB):
+            import ctypes as C
+            lib = C.CDLL(_HOST_LIB)
+            lib.fx_fill_normal_host.restype = None
+            lib.fx_fill_normal_host.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_uint64, C.c_double,
+                                                C.c_uint64, C.c_double, C.c_int, C.c_int]
+            _host = lib
+    return _host
+
+
+def normal_numpy(key: int, count: int, std: float, start: int = 0, bf16: bool = False,
+                 noise_key: int | None = None, noise_std: float = 0.0) -> np.ndarray:
+    """The recipe written out in numpy (reference form of ``normal``)."""
     out = np.empty(count, dtype=np.float32)
 
     def job(c0: int) -> None:
@@ -128,6 +145,18 @@ def normal(key: int, count: int, std: float, start: int = 0, bf16: bool = False,
         for c0 in starts:
             job(c0)
     return round_bf16(out) if bf16 else out
+
+
+def normal(key: int, count: int, std: float, start: int = 0, bf16: bool = False,
+           noise_key: int | None = None, noise_std: float = 0.0) -> np.ndarray:
+    """Elements [start, start+count) of a generated tensor as float32 (bf16-rounded when asked)."""
+    lib = _host_lib() if count >= (1 << 16) else None
+    if not lib:
+        return normal_numpy(key, count, std, start, bf16, noise_key, noise_std)
+    out = np.empty(count, dtype=np.float32)
+    lib.fx_fill_normal_host(out.ctypes.data, count, start, key, std, noise_key or 0, noise_std,
+                            int(noise_key is not None), int(bf16))
+    return out
 
 
 def tokens(seed: int, b: int, count: int, vocab: int) -> np.ndarray:

@@ -1,0 +1,88 @@
+"""Device-side fixture generation: the same seeded tensors as ``fixtures``, filled on the GPU.
+
+``libfixtures_gen.so`` (built from fixtures/gen.cu) implements the generator
+definition of ``fixtures/__init__.py``; these helpers return plain logical
+tensors (wq, wk, ..., embed, lm_head) as torch CUDA tensors. Packing them into
+a consumer's layout is left to the caller (a ``pack_layer`` callback).
+"""
+from __future__ import annotations
+
+import ctypes as C
+from pathlib import Path
+
+import torch
+
+import fixtures as FX
+
+_LIB = Path(__file__).resolve().parent / "libfixtures_gen.so"
+_lib = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        if not _LIB.exists():
+            raise RuntimeError(f"{_LIB} is not built; run __graft_entry__.build() first")
+        _lib = C.CDLL(str(_LIB))
+        _lib.fx_fill_normal.restype = C.c_int
+        _lib.fx_fill_normal.argtypes = [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_uint64, C.c_double,
+                                        C.c_uint64, C.c_double, C.c_int, C.c_void_p]
+    return _lib
+
+
+def fill_normal(out: torch.Tensor, key: int, std: float, start: int = 0, noise_key: int | None = None,
+                noise_std: float = 0.0) -> torch.Tensor:
+    assert out.is_cuda and out.is_contiguous() and out.dtype in (torch.float32, torch.bfloat16)
+    s = torch.cuda.current_stream(out.device).cuda_stream
+    rc = lib().fx_fill_normal(out.data_ptr(), int(out.dtype == torch.bfloat16), out.numel(), start, key, std,
+                              noise_key or 0, noise_std, int(noise_key is not None), s)
+    if rc != 0:
+        raise RuntimeError(f"fx_fill_normal failed: {rc}")
+    return out
+
+
+def _dt(m: FX.ModelShape):
+    return torch.bfloat16 if m.bf16 else torch.float32
+
+
+def target_tensor(m: FX.ModelShape, name: str, layer: int = -1, device="cuda") -> torch.Tensor:
+    if name in ("embed", "lm_head"):
+        shape = (m.vocab, m.d)
+        key = FX.stream_key(m.seed, FX.CODE_EMBED if name == "embed" else FX.CODE_LM_HEAD)
+        std = m.init_std if name == "embed" else m.lm_head_std
+    else:
+        shape = FX.layer_shapes(m)[name]
+        key, std = FX.layer_key(m, layer, name), m.init_std
+    return fill_normal(torch.empty(shape, dtype=_dt(m), device=device), key, std)
+
+
+def head_tensor(m: FX.ModelShape, name: str, device="cuda") -> torch.Tensor:
+    if name == "fc":
+        fc = torch.zeros((m.d, 2 * m.d), dtype=_dt(m), device=device)
+        fc[:, : m.d] = torch.eye(m.d, dtype=_dt(m), device=device)
+        return fc
+    shape = FX.layer_shapes(m)[name]
+    return fill_normal(torch.empty(shape, dtype=_dt(m), device=device), FX.layer_key(m, m.n_layers - 1, name),
+                       m.init_std, noise_key=FX.stream_key(m.seed, FX.CODE_HEAD_NOISE + FX.KIND[name]),
+                       noise_std=0.1 * m.init_std)
+
+
+def generate_model(m: FX.ModelShape, pack_layer, device="cuda"):
+    """Yield (kind, value): ("embed"|"lm_head"|"final_norm"|"fc", tensor), ("layer", l, packed), ("head", packed).
+
+    Layers are generated and packed one at a time, so the peak extra memory is one layer.
+    """
+    ones = torch.ones(m.d, dtype=torch.float32, device=device)
+    out = {"embed": target_tensor(m, "embed", device=device), "lm_head": target_tensor(m, "lm_head", device=device),
+           "final_norm": ones.clone(), "fc": head_tensor(m, "fc", device=device), "layers": []}
+    for l in range(m.n_layers):
+        t = {k: target_tensor(m, k, l, device=device) for k in FX.layer_shapes(m)}
+        out["layers"].append(pack_layer(**t, attn_norm=ones.clone(), ffn_norm=ones.clone()))
+        del t
+    h = {k: head_tensor(m, k, device=device) for k in FX.layer_shapes(m)}
+    out["head"] = pack_layer(**h, attn_norm=ones.clone(), ffn_norm=ones.clone())
+    return out
+
+
+def prompts(m: FX.ModelShape, batch: int, length: int, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(FX.prompts(m, batch, length)).to(device)

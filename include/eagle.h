@@ -1,0 +1,253 @@
+/*
+ * eagle.h - C ABI of the GB300 EAGLE speculative-decoding step.
+ *
+ * One speculative-decoding step of a Llama-style target model on one GPU:
+ *   draft  (feature-level head + static or EAGLE-2 dynamic tree),
+ *   verify (one tree-masked target pass over the KV cache),
+ *   accept (greedy longest accepted root-to-leaf path),
+ *   commit (compact the accepted K/V and features in place).
+ *
+ * Method sources (web pages on EAGLE speculative decoding):
+ *   [SDE]  "Speculative Decoding with EAGLE" (aiunderstanding.org), sections
+ *          "Deep dive" and "Technical insight".
+ *   [LPD]  "EAGLE (LLM decoding)" (jisaku.com/glossary/llm-parallel-decoding-eagle),
+ *          sections "How EAGLE works", "EAGLE vs EAGLE-2", FAQ Q3.
+ *   [YHL]  "yuhuili" (llmyourway.com/authors/yuhuili).
+ *
+ * Conventions for every entry point:
+ *   - All functions are `extern "C"`, never throw, and return eagle_status.
+ *   - "d_" pointers are device pointers, "h_" pointers host pointers.
+ *   - Work is enqueued asynchronously on the stream given to eagle_init
+ *     (a cudaStream_t passed as void*; NULL selects the legacy default stream).
+ *     Only eagle_generate, eagle_sync_status and eagle_op_* timing helpers
+ *     synchronise that stream.
+ *   - The library never allocates device memory: the caller owns the weights,
+ *     the workspace (size from eagle_workspace_size) and all outputs, and keeps
+ *     them alive until eagle_destroy.
+ *   - Argument errors are detected on the host and returned synchronously.
+ *     Errors found on the device (KV capacity, bounded-wait timeout) are
+ *     written to a status word in the workspace and returned by the next
+ *     eagle_sync_status / eagle_generate. After any error the context refuses
+ *     further work with EAGLE_ERR_STATE until destroyed; eagle_last_error
+ *     gives a one-line description.
+ *
+ * Data types: EAGLE_DTYPE_F32 models keep weights, activations and the KV
+ * cache in float32 (SIMT kernels); EAGLE_DTYPE_BF16 models keep them in
+ * bfloat16 with float32 accumulation, float32 residual stream and float32
+ * features (tcgen05 tensor-core GEMMs, mma tensor-core attention).
+ */
+#ifndef EAGLE_H
+#define EAGLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID_ARG = 1,   /* bad pointer, size or shape (host-detected) */
+  EAGLE_ERR_UNSUPPORTED = 2,   /* shape the kernels do not support */
+  EAGLE_ERR_WORKSPACE = 3,     /* workspace too small or misaligned */
+  EAGLE_ERR_CAPACITY = 4,      /* KV cache or output capacity exceeded (device-detected) */
+  EAGLE_ERR_CUDA = 5,          /* a CUDA runtime or driver call failed */
+  EAGLE_ERR_TIMEOUT = 6,       /* a bounded device wait gave up */
+  EAGLE_ERR_STATE = 7          /* call out of order, or context already failed */
+} eagle_status;
+
+typedef enum { EAGLE_DTYPE_F32 = 0, EAGLE_DTYPE_BF16 = 1 } eagle_dtype;
+typedef enum { EAGLE_TREE_STATIC = 0, EAGLE_TREE_DYNAMIC = 1 } eagle_tree_mode;
+
+/* Largest verified tree: 120 draft nodes plus the root ([LPD] "EAGLE vs
+ * EAGLE-2": EAGLE-2 adapts between 40 and 120 nodes). Ancestor sets are
+ * 128-bit masks. */
+#define EAGLE_MAX_TREE_ROWS 121
+#define EAGLE_MAX_DEPTH 8
+#define EAGLE_MAX_TOPK 16
+
+/* Model and decoding configuration. */
+typedef struct {
+  int32_t n_layers;      /* target decoder layers */
+  int32_t d;             /* hidden size; multiple of 128 */
+  int32_t n_heads;       /* query heads */
+  int32_t n_kv_heads;    /* KV heads (grouped-query attention); divides n_heads */
+  int32_t head_dim;      /* 64 or 128 */
+  int32_t ffn;           /* SwiGLU inner size */
+  int32_t vocab;         /* vocabulary size */
+  float rope_theta;      /* RoPE base */
+  float rms_eps;         /* RMSNorm epsilon */
+  int32_t dtype;         /* eagle_dtype */
+  int32_t batch;         /* independent sequences decoded together */
+  int32_t kv_cap;        /* KV slots per sequence (prompt + generated + tree) */
+  int32_t max_prompt;    /* longest prompt eagle_prefill will see */
+  int32_t max_new;       /* capacity of the per-sequence committed-token buffer */
+  int32_t tree_mode;     /* eagle_tree_mode */
+  int32_t n_nodes;       /* verified draft nodes per step, root excluded (<= 120) */
+  /* EAGLE_TREE_STATIC: BFS-ordered topology, host arrays of n_nodes+1 entries,
+   * copied at eagle_init. static_parent[0] = -1 (root); static_rank[j] = r
+   * makes node j the r-th most likely draft token of its parent. */
+  const int32_t* static_parent;
+  const int32_t* static_rank;
+  /* EAGLE_TREE_DYNAMIC ([LPD] "EAGLE vs EAGLE-2", FAQ Q3): expand the top_k
+   * nodes per depth by cumulative draft confidence, children top_k per node,
+   * depth levels, prune expansion below confidence tau. */
+  int32_t top_k;
+  int32_t depth;
+  float tau;
+} eagle_config;
+
+/* Device pointers of one decoder layer. Matrices are row-major [out, in]
+ * (y = x W^T), element type = config dtype; norm gains are float32 [d]. */
+typedef struct {
+  const void* wqkv;        /* [(n_heads + 2 n_kv_heads) head_dim, d]: q rows, then k, then v */
+  const void* wo;          /* [d, n_heads head_dim] */
+  const void* wgu;         /* [2 ffn, d]: gate and up rows interleaved in blocks of 64:
+                              block b holds gate rows 64b.. then up rows 64b.. (the last
+                              block may hold r < 64 of each) */
+  const void* wd;          /* [d, ffn] */
+  const float* attn_norm;  /* [d] */
+  const float* ffn_norm;   /* [d] */
+} eagle_layer_weights;
+
+typedef struct {
+  const void* embed;                   /* [vocab, d] token embedding E */
+  const void* lm_head;                 /* [vocab, d] */
+  const float* final_norm;             /* [d] */
+  const eagle_layer_weights* layers;   /* host array of n_layers entries */
+  const void* fc;                      /* draft head FC [d, 2d] over [feature ; E(next token)] */
+  eagle_layer_weights head;            /* draft head decoder layer */
+} eagle_weights;
+
+/* A draft tree per sequence, BFS order, row 0 = root. Device arrays. */
+typedef struct {
+  int32_t n_rows;          /* N + 1, same for every sequence */
+  int32_t* tokens;         /* [batch][n_rows] */
+  int32_t* parent;         /* [batch][n_rows], -1 at the root */
+  int32_t* depth;          /* [batch][n_rows] */
+  uint64_t* anc;           /* [batch][n_rows][2]: bit i set when row i is on the root-to-row path (self included) */
+} eagle_tree;
+
+typedef struct {
+  int64_t steps;               /* speculative steps run by eagle_generate */
+  int64_t committed;           /* tokens committed over all sequences (before trimming) */
+  int64_t accept_hist[EAGLE_MAX_DEPTH + 1]; /* accepted draft length per (step, sequence) */
+  double mean_accept;          /* mean accepted draft tokens per step and sequence */
+  double prefill_ms;           /* wall time of the prefill */
+  double decode_ms;            /* wall time of the step loop */
+} eagle_stats;
+
+typedef struct eagle_ctx eagle_ctx;
+
+/* Bytes of device workspace eagle_init needs for this configuration. Host-only; no CUDA call. */
+eagle_status eagle_workspace_size(const eagle_config* cfg, size_t* bytes);
+
+/* Validate the configuration, carve the workspace (256-byte aligned, owned by
+ * the caller, contents overwritten) and bind the weights. Returns the context
+ * through *out. The device current at this call must be the one holding all pointers. */
+eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d_workspace,
+                        size_t workspace_bytes, void* stream, eagle_ctx** out);
+
+/* Target prefill of batch prompts of equal length prompt_len (d_tokens [batch][prompt_len]),
+ * the head's catch-up over prompt rows 0..prompt_len-2, and the first new token
+ * (greedy) per sequence, written to d_root_out [batch] when not NULL. Resets all
+ * per-sequence state. */
+eagle_status eagle_prefill(eagle_ctx* ctx, const int32_t* d_tokens, int32_t prompt_len,
+                           int32_t* d_root_out);
+
+/* Draft step ([SDE] "Technical insight"; [LPD] "How EAGLE works", "EAGLE vs
+ * EAGLE-2"): head rows for the positions committed last, then tree expansion
+ * (static rank paths or EAGLE-2). If out->tokens is NULL on entry, *out
+ * receives device views of the tree inside the workspace, valid until the
+ * next eagle_draft_tree; otherwise the tree is copied (on the stream) into
+ * the caller's four arrays, which must hold batch * n_nodes+1 rows. */
+eagle_status eagle_draft_tree(eagle_ctx* ctx, eagle_tree* out);
+
+/* Verify ([LPD] "How EAGLE works": tree attention scores every node in one
+ * forward pass): target pass over tree->n_rows rows per sequence at positions
+ * L + depth, K/V written to slots L + row. d_argmax [batch][n_rows] receives the
+ * greedy token after each row; d_logits [batch][n_rows][vocab] float32 receives
+ * the logits when not NULL (debug/parity path). The tree may be the one
+ * eagle_draft_tree returned or any caller-built tree (n_rows <= 121). */
+eagle_status eagle_verify(eagle_ctx* ctx, const eagle_tree* tree, int32_t* d_argmax, float* d_logits);
+
+/* Accept and commit ([SDE] "Deep dive": longest correct prefix): greedy walk
+ * over the last verified tree, compaction of the accepted K/V to contiguous
+ * slots, features kept for the next draft. d_accept_len [batch] (may be NULL)
+ * receives the accepted draft length a; d_tokens_out [batch][EAGLE_MAX_DEPTH+1]
+ * (may be NULL) the a+1 committed tokens (accepted nodes, then the bonus token),
+ * padded with -1. */
+eagle_status eagle_accept_commit(eagle_ctx* ctx, int32_t* d_accept_len, int32_t* d_tokens_out);
+
+/* Prefill, then draft/verify/accept steps until every sequence has at least
+ * max_new committed tokens (the prefill's first token counts); d_out
+ * [batch][max_new] receives exactly max_new tokens per sequence. With
+ * use_graph != 0 the step is captured once in a CUDA graph and replayed.
+ * h_stats (may be NULL) is filled after the final synchronisation. */
+eagle_status eagle_generate(eagle_ctx* ctx, const int32_t* d_prompt, int32_t prompt_len, int32_t max_new,
+                            int32_t use_graph, int32_t* d_out, eagle_stats* h_stats);
+
+/* Vanilla greedy decoding with the same kernels (one-row tree per step), the
+ * lossless reference ([SDE] "Deep dive"). Same arguments as eagle_generate. */
+eagle_status eagle_generate_vanilla(eagle_ctx* ctx, const int32_t* d_prompt, int32_t prompt_len,
+                                    int32_t max_new, int32_t use_graph, int32_t* d_out, eagle_stats* h_stats);
+
+/* Enqueue n_steps further steps (draft, verify, accept/commit; vanilla != 0:
+ * one-row trees, i.e. plain greedy decoding) on a prefilled context without
+ * any host synchronisation. With use_graph != 0 and a non-NULL stream, the
+ * step is captured once into a CUDA graph (cached in the context) and
+ * replayed. The caller keeps the KV capacity in mind: each step commits
+ * between 1 and depth+1 tokens per sequence. */
+eagle_status eagle_step(eagle_ctx* ctx, int32_t n_steps, int32_t vanilla, int32_t use_graph);
+
+/* Kernel launches in one captured step (the CUDA graph's kernel nodes), or -1
+ * before the first graph-captured eagle_step / eagle_generate. Host-only. */
+int32_t eagle_step_kernel_count(const eagle_ctx* ctx, int32_t vanilla);
+
+/* Synchronise the stream and return the device status word (EAGLE_OK if clean). */
+eagle_status eagle_sync_status(eagle_ctx* ctx);
+
+/* Copy the committed-token count per sequence (int32 [batch]) to device memory d_counts (on the stream). */
+eagle_status eagle_committed_counts(eagle_ctx* ctx, int32_t* d_counts);
+
+eagle_status eagle_destroy(eagle_ctx* ctx);
+const char* eagle_last_error(const eagle_ctx* ctx);
+
+/* ---------------------------------------------------------------------------
+ * Kernel-level entry points: one hot-path kernel on caller buffers, for unit
+ * parity tests and roofline timing. They run on `stream`, allocate nothing,
+ * and need no context.
+ * ------------------------------------------------------------------------- */
+
+/* Y[M,N] (float32, row-major) = X[M,K] W[N,K]^T with the verify-pass GEMM
+ * kernel for `dtype` (bf16: tcgen05 + TMA weight streaming; f32: SIMT).
+ * N multiple of 128 and K multiple of 64 for bf16. d_scratch must hold
+ * eagle_op_gemm_scratch_bytes(M,N,K,dtype) bytes (split-K partials and tile
+ * counters, zeroed by the caller once; the kernel leaves counters at zero). */
+size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtype);
+eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w,
+                           float* d_y, void* d_scratch, void* stream);
+
+/* LM head + per-row top-k: for each row m of X [M,K], the k largest logits of
+ * X W^T (W [N,K]) as (index, value) ordered by value desc then index asc, and
+ * the row's log-sum-exp. d_idx/d_val [M][k], d_lse [M]. */
+size_t eagle_op_lmhead_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t k, int32_t dtype);
+eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k, const void* d_x,
+                                  const void* d_w, int32_t* d_idx, float* d_val, float* d_lse, void* d_scratch,
+                                  void* stream);
+
+/* Tree attention for one sequence over a KV cache slice: queries Q [rows][n_heads][hd]
+ * (RoPE applied), keys/values K,V [n_kv_heads][cap][hd]; row r attends to slots
+ * [0, prefix) and to slot prefix + i of the tree block for each bit i set in
+ * mask[r] (two uint64 words). Output O [rows][n_heads][hd] (dtype elements). */
+size_t eagle_op_attention_scratch_bytes(int32_t rows, int32_t n_heads, int32_t hd, int32_t prefix);
+eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_heads, int32_t n_kv_heads,
+                                     int32_t hd, int32_t cap, int32_t prefix, const void* d_q, const void* d_k,
+                                     const void* d_v, const uint64_t* d_mask, void* d_o, void* d_scratch,
+                                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_H */

@@ -48,3 +48,21 @@ def random_tree(rng, n: int, vocab: int, max_depth: int = 6, shape: str = "rando
     dep = [0] + [depth[j] for j in order]
     tokens = rng.integers(0, vocab, n + 1).astype(np.int32)
     return OT.Tree(tokens=tokens, parent=np.array(par, np.int32), depth=np.array(dep, np.int32))
+
+# A bf16 model with the 8B head geometry (head_dim 128, 4 query heads per KV head), reduced width and depth.
+GQA128 = FX.ModelShape(n_layers=2, d=1024, n_heads=8, n_kv_heads=2, head_dim=128, ffn=2048, vocab=4096,
+                       rope_theta=5e5, bf16=True, lm_head_std=0.05, seed=13)
+
+
+def tree_to_torch(tree: OT.Tree, batch: int = 1, device="cuda"):
+    """An engine Tree (batch copies) from an oracle Tree."""
+    import torch
+    from eagle_speculative_decoding_02_gb300.engine import Tree
+    masks = tree.ancestor_masks().view(np.int64)
+    rep = lambda a: torch.from_numpy(np.ascontiguousarray(np.stack([a] * batch))).to(device)
+    return Tree(tree.n + 1, rep(tree.tokens.astype(np.int32)), rep(tree.parent.astype(np.int32)),
+                rep(tree.depth.astype(np.int32)), rep(masks))
+
+
+def tree_from_torch(t, b: int = 0) -> OT.Tree:
+    return OT.Tree(tokens=t.tokens[b].cpu().numpy(), parent=t.parent[b].cpu().numpy(), depth=t.depth[b].cpu().numpy())
