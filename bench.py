@@ -105,7 +105,9 @@ def gemm_roofline(eng, m, rows: int, reps: int = 2):
               "down": (m.d, m.ffn), "lm_head": (m.vocab, m.d)}
     xs = {k: (torch.randn(rows, K, device=dev) * 0.5).to(torch.bfloat16) for k, (N, K) in shapes.items()}
     ys = {k: torch.empty(rows, N, device=dev) for k, (N, K) in shapes.items()}
-    scr = op_gemm_scratch(rows, m.vocab, m.ffn, torch.bfloat16, dev)
+    # one scratch buffer sized for the largest of the shapes serves all of them
+    scr = max((op_gemm_scratch(rows, N, K, torch.bfloat16, dev) for N, K in shapes.values()),
+              key=lambda t: t.numel())
     launches = []
     for lw in eng.weights.layers:
         launches += [("qkv", lw.wqkv), ("o", lw.wo), ("gu", lw.wgu), ("down", lw.wd)]
@@ -196,6 +198,39 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def profile_ops(w, reps: int = 3):
+    """GEMM (QKV, O, gate/up, down, LM head), tree attention and LM-head top-k at the verify shapes of one layer."""
+    import torch
+
+    from eagle_speculative_decoding_02_gb300 import build as B
+    from eagle_speculative_decoding_02_gb300.engine import op_gemm, op_gemm_scratch, op_lmhead_topk, op_tree_attention
+    B.build()
+    m, dev = w.model, "cuda"
+    rows = w.batch * (w.n_nodes + 1)
+    g = torch.Generator(device=dev).manual_seed(0)
+    for N, K in [(m.q_dim + 2 * m.kv_dim, m.d), (m.d, m.q_dim), (2 * m.ffn, m.d), (m.d, m.ffn), (m.vocab, m.d)]:
+        x = (torch.randn(rows, K, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+        wt = (torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        y = torch.empty(rows, N, device=dev)
+        scr = op_gemm_scratch(rows, N, K, torch.bfloat16, dev)
+        for _ in range(reps):
+            op_gemm(x, wt, y, scr)
+        del wt
+    L = w.prompt_len + 512
+    q = torch.randn(w.n_nodes + 1, m.n_heads, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
+    kc = torch.randn(m.n_kv_heads, L + 128, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
+    vc = torch.randn(m.n_kv_heads, L + 128, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
+    mask = torch.full((w.n_nodes + 1, 2), -1, dtype=torch.int64, device=dev)
+    for _ in range(reps):
+        op_tree_attention(q, kc, vc, mask, L)
+    x = (torch.randn(10, m.d, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+    lm = (torch.randn(m.vocab, m.d, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    for _ in range(reps):
+        op_lmhead_topk(x, lm, 10)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_ops": "done", "rows": rows, "reps": reps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -205,12 +240,17 @@ def main():
     ap.add_argument("--workload", default="8b_eagle2")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-ops", action="store_true",
+                    help="run only the hot kernels at the verify shapes (a small case for ncu captures)")
     args = ap.parse_args()
 
     import fixtures as FX
     w = FX.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.profile_ops:
+        return profile_ops(w)
 
     import torch
     import torch.distributed as dist
@@ -227,7 +267,7 @@ def main():
 
     m = w.model
     D1 = w.depth + 1
-    max_new = max(w.max_new, (args.steps + args.warmup + 2) * D1 + 1)
+    max_new = max(w.max_new, (args.steps + args.warmup + 8) * D1 + 1)   # capacity for any acceptance
     eng = S.make_engine(w, max_new=max_new)
     prompt = S.prompts(w)
     eng.prefill(prompt)
@@ -287,7 +327,7 @@ def main():
 
     # end to end through the public API: pinned host prompt -> device, generate, tokens -> host
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.no_e2e:
         n_new = w.max_new
         host_prompt = prompt.cpu().pin_memory()
         host_out = torch.empty((w.batch, n_new), dtype=torch.int32).pin_memory()

@@ -1,0 +1,264 @@
+// Tree-masked attention on tensor cores (bf16 mma.sync m16n8k16, fp32 softmax).
+//
+// "EAGLE (LLM decoding)", section "How EAGLE works": tree attention verifies
+// every draft node in one forward pass. A query row (node j, query head h) of
+// group g sees the prefix slots [0, prefix) and the slots prefix + i of the
+// tree block whose bit i is set in node j's ancestor mask.
+//
+// Split-K flash decode: CTA (chunk c, KV head, group) takes either prefix keys
+// [128 c, 128 c + 128) or, for c == ceil(prefix / 128), the tree block, and all
+// rows of the group times the G = Hq / Hkv query heads sharing that KV head
+// (the GQA rows form the M dimension of the MMA). Each CTA stages its K chunk
+// and the transposed V chunk in shared memory once; every warp runs 16-row
+// tiles over it with an online softmax and writes an unnormalised partial
+// (max, sum, O). attn_merge combines the partials of a row in chunk order.
+// Chunk boundaries are absolute slot multiples of 128, independent of how many
+// rows are verified.
+#include <cmath>
+
+#include "kernels.h"
+
+namespace eg {
+namespace {
+
+constexpr int kCK = 128;   // keys per chunk
+constexpr int kPad = 8;    // bf16 padding per shared-memory row
+
+__device__ __forceinline__ uint32_t ld_b32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__host__ __device__ __forceinline__ int n_prefix_chunks(int prefix) { return (prefix + kCK - 1) / kCK; }
+
+template <int HD>
+__global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a, int n_chunk_slots) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  bf16* Ks = reinterpret_cast<bf16*>(smem_raw);                 // [kCK][HD + kPad]
+  bf16* Vt = Ks + kCK * (HD + kPad);                            // [HD][kCK + kPad]
+  const Group g = a.groups[blockIdx.z];
+  const int kvh = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const int nck = n_prefix_chunks(g.prefix);
+  const bool block = chunk == nck;
+  if (chunk > nck || (block && g.block_len <= 0)) return;
+  const int key0 = block ? g.prefix : chunk * kCK;
+  const int nkeys = block ? g.block_len : min(kCK, g.prefix - key0);
+  const int G = a.Hq / a.Hkv;
+  const int R = g.nrows * G;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // stage K (row-major) and V (transposed) of the chunk; keys past nkeys are zero
+  const bf16* Kg = reinterpret_cast<const bf16*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
+  const bf16* Vg = reinterpret_cast<const bf16*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
+  constexpr int VEC = 8;  // bf16 per 16-byte vector
+  for (int e = tid; e < kCK * HD / VEC; e += 128) {
+    const int key = e / (HD / VEC), d0 = (e % (HD / VEC)) * VEC;
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+    if (key < nkeys) {
+      kv = *reinterpret_cast<const uint4*>(Kg + (size_t)key * HD + d0);
+      vv = *reinterpret_cast<const uint4*>(Vg + (size_t)key * HD + d0);
+    }
+    *reinterpret_cast<uint4*>(Ks + key * (HD + kPad) + d0) = kv;
+    const bf16* vp = reinterpret_cast<const bf16*>(&vv);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) Vt[(d0 + i) * (kCK + kPad) + key] = vp[i];
+  }
+  __syncthreads();
+
+  const float sl2 = a.scale * 1.4426950408889634f;  // scores in log2 units
+  const int quad = lane >> 2, qi = lane & 3;
+  for (int mt = warp; mt * 16 < R; mt += 4) {
+    // rows r0 = mt*16 + quad and r1 = r0 + 8 of this tile: (node, head) = (r / G, r % G)
+    int node[2], qh[2];
+    bool rv[2];
+    uint64_t mk0[2], mk1[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = mt * 16 + quad + 8 * i;
+      rv[i] = r < R;
+      node[i] = rv[i] ? r / G : 0;
+      qh[i] = kvh * G + (rv[i] ? r % G : 0);
+      const int row = g.row0 + node[i];
+      mk0[i] = block && rv[i] ? a.mask[2 * row] : 0ull;
+      mk1[i] = block && rv[i] ? a.mask[2 * row + 1] : 0ull;
+    }
+    uint32_t qa[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const bf16* qp = reinterpret_cast<const bf16*>(a.q) + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
+        qa[kk][i] = rv[i] ? ld_b32(qp + kk * 16 + qi * 2) : 0u;
+        qa[kk][i + 2] = rv[i] ? ld_b32(qp + kk * 16 + 8 + qi * 2) : 0u;
+      }
+    }
+    float o[HD / 8][4];
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+    for (int kb = 0; kb < nkeys; kb += 64) {
+      float s[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const bf16* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
+          mma16816(s[nt], qa[kk], ld_b32(kp), ld_b32(kp + 8));
+        }
+      }
+      // mask and scale; c-fragment (row quad (+8), key kb + nt*8 + qi*2 + {0,1})
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const int key = kb + nt * 8 + qi * 2 + (e & 1);
+          bool vis = key < nkeys && rv[i];
+          if (block && vis) vis = ((key < 64 ? (mk0[i] >> key) : (mk1[i] >> (key - 64))) & 1ull) != 0;
+          s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
+          mx[i] = fmaxf(mx[i], s[nt][e]);
+        }
+      }
+      float corr[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        const float mn = fmaxf(mrow[i], mx[i]);
+        corr[i] = (mn == -INFINITY) ? 1.f : exp2f(mrow[i] - mn);
+        mrow[i] = mn;
+      }
+      float sum[2] = {0.f, 0.f};
+      uint32_t pa[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const float p = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mrow[i]);
+          s[nt][e] = p;
+          sum[i] += p;
+        }
+        // P as the A operand of P.V: keys 16*kk2 .. of this 64-key block
+        const int kk2 = nt >> 1, hi = nt & 1;
+        pa[kk2][0 + 2 * hi] = pack_bf16(s[nt][0], s[nt][1]);
+        pa[kk2][1 + 2 * hi] = pack_bf16(s[nt][2], s[nt][3]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
+        lrow[i] = lrow[i] * corr[i] + sum[i];
+      }
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; ++dt) {
+        o[dt][0] *= corr[0];
+        o[dt][1] *= corr[0];
+        o[dt][2] *= corr[1];
+        o[dt][3] *= corr[1];
+      }
+#pragma unroll
+      for (int kk2 = 0; kk2 < 4; ++kk2) {
+#pragma unroll
+        for (int dt = 0; dt < HD / 8; ++dt) {
+          const bf16* vp = Vt + (dt * 8 + quad) * (kCK + kPad) + kb + kk2 * 16 + qi * 2;
+          mma16816(o[dt], pa[kk2], ld_b32(vp), ld_b32(vp + 8));
+        }
+      }
+    }
+    // partials: index (row * Hq + qh) * slots + chunk
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (!rv[i]) continue;
+      const size_t pr = ((size_t)(g.row0 + node[i]) * a.Hq + qh[i]) * n_chunk_slots + chunk;
+      float* po = a.part + pr * (HD + 2);
+      if (qi == 0) {
+        po[HD] = mrow[i];
+        po[HD + 1] = lrow[i];
+      }
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; ++dt)
+        *reinterpret_cast<float2*>(po + dt * 8 + qi * 2) = make_float2(o[dt][2 * i], o[dt][2 * i + 1]);
+    }
+  }
+}
+
+// One warp per (row, query head): combine the row's chunk partials in chunk order.
+template <int HD>
+__global__ void attn_merge_kernel(AttnArgs a, const int* __restrict__ row_grp, int n_chunk_slots) {
+  const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (w >= a.M * a.Hq) return;
+  const int row = w / a.Hq, qh = w % a.Hq;
+  const Group g = a.groups[row_grp ? row_grp[row] : 0];
+  const int nck = n_prefix_chunks(g.prefix) + (g.block_len > 0 ? 1 : 0);
+  const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < nck; ++c) M = fmaxf(M, base[(size_t)c * (HD + 2) + HD]);
+  float acc[HD / 32];
+#pragma unroll
+  for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
+  float L = 0.f;
+  for (int c = 0; c < nck; ++c) {
+    const float* p = base + (size_t)c * (HD + 2);
+    const float m = p[HD];
+    if (m == -INFINITY) continue;
+    const float wgt = exp2f(m - M);
+    L += wgt * p[HD + 1];
+#pragma unroll
+    for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * p[lane + 32 * i];
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  bf16* out = reinterpret_cast<bf16*>(a.o) + ((size_t)row * a.Hq + qh) * HD;
+#pragma unroll
+  for (int i = 0; i < HD / 32; ++i) out[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+}
+
+template <int HD>
+cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
+  const int slots = n_prefix_chunks(a.max_prefix) + 1;
+  const size_t smem = (size_t)kCK * (HD + kPad) * 2 + (size_t)HD * (kCK + kPad) * 2;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr = true;
+  }
+  dim3 grid(slots, a.Hkv, a.n_groups);
+  attn_tc_kernel<HD><<<grid, 128, smem, s>>>(a, slots);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int warps = a.M * a.Hq;
+  attn_merge_kernel<HD><<<(warps + 3) / 4, 128, 0, s>>>(a, a.row_grp, slots);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_tc_scratch_bytes(int M, int Hq, int hd, int max_prefix) {
+  const size_t slots = (size_t)n_prefix_chunks(max_prefix) + 1;
+  return (size_t)M * Hq * slots * (hd + 2) * sizeof(float);
+}
+
+cudaError_t attention_tc(const AttnArgs& a, cudaStream_t s) {
+  if (a.n_groups <= 0 || a.M <= 0) return cudaSuccess;
+  if (!a.part || a.Hq % a.Hkv) return cudaErrorInvalidValue;
+  if (a.hd == 128) return launch<128>(a, s);
+  if (a.hd == 64) return launch<64>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace eg

@@ -376,7 +376,7 @@ struct Eng {
 
     AttnArgs a{};
     a.q = c->q; a.kc = kc; a.vc = vc; a.o = c->attn; a.groups = c->groups; a.n_groups = n_groups;
-    a.mask = c->rows.mask; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap;
+    a.mask = c->rows.mask; a.row_grp = c->rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap;
     a.max_prefix = cap; a.scale = 1.f / std::sqrt((float)dm.hd); a.part = c->attn_part; a.status = c->st.status;
     EG_TRY(attention(c, a));
 

@@ -38,6 +38,11 @@ constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 232448;           // 227 KB opt-in per block
 constexpr int kNsmSizing = 160;               // SM count bound used for scratch sizing
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
+// Split-K arrival counters sit at the start of the scratch in a region of fixed
+// size, so that one scratch buffer serves GEMMs of every shape: a shape's
+// partial sums can never land on another shape's counters.
+constexpr int kCounterInts = 1 << 17;
+constexpr size_t kCounterBytes = (size_t)kCounterInts * 4;
 
 struct TcArgs {
   int M, MT, m_chunks, n_tiles, kbt, G, stages;
@@ -436,7 +441,7 @@ Plan plan(int M, int N, int K, int nsm) {
   int st = (int)((kSmemBudget - fixed) / stage);
   p.stages = std::max(2, std::min(kMaxStages, st));
   p.smem = (size_t)p.stages * stage + fixed;
-  p.counters_bytes = ((size_t)p.m_chunks * p.n_tiles * 4 + 255) / 256 * 256;
+  p.counters_bytes = kCounterBytes;
   p.partial_bytes = split ? (size_t)p.m_chunks * p.G * 2 * p.MT * kTileN * 4 : 0;
   return p;
 }
@@ -445,7 +450,7 @@ Plan plan(int M, int N, int K, int nsm) {
 
 size_t gemm_tc_scratch_bytes(int M, int N, int K) {
   // enough for any M' <= M on up to kNsmSizing SMs
-  size_t best = 256;
+  size_t best = kCounterBytes;
   const int chunks = (M + 255) / 256;
   for (int mc = 1; mc <= chunks; ++mc) {
     const int Mp = mc == 1 ? std::min(M, 256) : mc * 256;
@@ -461,6 +466,7 @@ cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const Epi
   if (N % kTileN || K % kBK || !scratch) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
   const Plan p = plan(M, N, K, num_sms());
+  if ((long long)p.m_chunks * p.n_tiles > kCounterInts) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, N, K, kTileN) || !make_map(&tmX, X, M, K, p.MT)) return cudaErrorInvalidValue;
   static std::once_flag attr;

@@ -25,6 +25,7 @@ struct AttnArgs {
   const Group* groups;
   int n_groups;
   const uint64_t* mask;  // [M][2]
+  const int* row_grp;    // [M] group of each row (NULL: all rows in group 0)
   int M, Hq, Hkv, hd, cap;
   int max_prefix;     // upper bound on any group's prefix (sizes the split grid)
   float scale;        // 1/sqrt(hd)

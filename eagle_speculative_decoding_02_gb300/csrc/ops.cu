@@ -29,8 +29,9 @@ size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtyp
 }
 
 eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* x, const void* w, float* y,
-                           void* scratch, void* stream) {
+                           void* scratch, size_t scratch_bytes, void* stream) {
   if (M < 1 || N < 1 || K < 1 || !x || !w || !y) return EAGLE_ERR_INVALID_ARG;
+  if (scratch_bytes < eagle_op_gemm_scratch_bytes(M, N, K, dtype)) return EAGLE_ERR_WORKSPACE;
   EpiParams e;
   e.kind = kEpiStore;
   e.M = M;
@@ -57,9 +58,11 @@ size_t eagle_op_lmhead_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t k,
 }
 
 eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k, const void* x,
-                                  const void* w, int32_t* idx, float* val, float* lse, void* scratch, void* stream) {
+                                  const void* w, int32_t* idx, float* val, float* lse, void* scratch,
+                                  size_t scratch_bytes, void* stream) {
   if (M < 1 || N < 1 || K < 1 || k < 1 || k > EAGLE_MAX_TOPK || k > N || !x || !w || !idx || !scratch)
     return EAGLE_ERR_INVALID_ARG;
+  if (scratch_bytes < eagle_op_lmhead_scratch_bytes(M, N, K, k, dtype)) return EAGLE_ERR_WORKSPACE;
   const size_t nt = (size_t)((N + kTileN - 1) / kTileN) * M;
   char* p = (char*)scratch;
   EpiParams e;
@@ -92,15 +95,17 @@ size_t eagle_op_attention_scratch_bytes(int32_t rows, int32_t n_heads, int32_t h
 
 eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
                                      int32_t cap, int32_t prefix, const void* q, const void* k, const void* v,
-                                     const uint64_t* mask, void* o, void* scratch, void* stream) {
+                                     const uint64_t* mask, void* o, void* scratch, size_t scratch_bytes,
+                                     void* stream) {
   if (rows < 1 || rows > 128 || n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || (hd != 64 && hd != 128) ||
       prefix < 0 || prefix + rows > cap || !q || !k || !v || !mask || !o || !scratch)
     return EAGLE_ERR_INVALID_ARG;
+  if (scratch_bytes < eagle_op_attention_scratch_bytes(rows, n_heads, hd, prefix)) return EAGLE_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   Group* g = (Group*)scratch;
   write_group_kernel<<<1, 1, 0, s>>>(g, rows, prefix, rows);
   AttnArgs a{};
-  a.q = q; a.kc = k; a.vc = v; a.o = o; a.groups = g; a.n_groups = 1; a.mask = mask; a.M = rows;
+  a.q = q; a.kc = k; a.vc = v; a.o = o; a.groups = g; a.n_groups = 1; a.mask = mask; a.row_grp = nullptr; a.M = rows;
   a.Hq = n_heads; a.Hkv = n_kv_heads; a.hd = hd; a.cap = cap; a.max_prefix = prefix;
   a.scale = 1.f / std::sqrt((float)hd);
   a.part = (float*)((char*)scratch + al(sizeof(Group)));

@@ -213,7 +213,7 @@ def op_gemm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
         scratch = op_gemm_scratch(M, N, K, x.dtype, x.device)
     s = torch.cuda.current_stream(x.device).cuda_stream
     L.check("eagle_op_gemm", lib.eagle_op_gemm(dt, M, N, K, x.data_ptr(), w.data_ptr(), y.data_ptr(),
-                                               scratch.data_ptr(), s))
+                                               scratch.data_ptr(), scratch.numel(), s))
     return y
 
 
@@ -230,7 +230,7 @@ def op_lmhead_topk(x: torch.Tensor, w: torch.Tensor, k: int):
     s = torch.cuda.current_stream(x.device).cuda_stream
     L.check("eagle_op_lmhead_topk", lib.eagle_op_lmhead_topk(dt, M, N, K, k, x.data_ptr(), w.data_ptr(),
                                                              idx.data_ptr(), val.data_ptr(), lse.data_ptr(),
-                                                             scratch.data_ptr(), s))
+                                                             scratch.data_ptr(), scratch.numel(), s))
     return idx, val, lse
 
 
@@ -246,5 +246,6 @@ def op_tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: t
     s = torch.cuda.current_stream(q.device).cuda_stream
     L.check("eagle_op_tree_attention", lib.eagle_op_tree_attention(dt, rows, hq, hkv, hd, cap, prefix, q.data_ptr(),
                                                                    k.data_ptr(), v.data_ptr(), mask.data_ptr(),
-                                                                   o.data_ptr(), scratch.data_ptr(), s))
+                                                                   o.data_ptr(), scratch.data_ptr(), scratch.numel(),
+                                                                   s))
     return o

@@ -222,12 +222,15 @@ const char* eagle_last_error(const eagle_ctx* ctx);
 
 /* Y[M,N] (float32, row-major) = X[M,K] W[N,K]^T with the verify-pass GEMM
  * kernel for `dtype` (bf16: tcgen05 + TMA weight streaming; f32: SIMT).
- * N multiple of 128 and K multiple of 64 for bf16. d_scratch must hold
- * eagle_op_gemm_scratch_bytes(M,N,K,dtype) bytes (split-K partials and tile
- * counters, zeroed by the caller once; the kernel leaves counters at zero). */
+ * N multiple of 128 and K multiple of 64 for bf16; X and W 16-byte aligned.
+ * d_scratch (scratch_bytes >= eagle_op_gemm_scratch_bytes(M,N,K,dtype), else
+ * EAGLE_ERR_WORKSPACE) holds split-K arrival counters and partial sums; the
+ * caller zeroes it once, every launch leaves the counters at zero, and one
+ * buffer sized for the largest shape serves every smaller one. Calls that
+ * share a scratch buffer must not overlap on the GPU. */
 size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtype);
 eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w,
-                           float* d_y, void* d_scratch, void* stream);
+                           float* d_y, void* d_scratch, size_t scratch_bytes, void* stream);
 
 /* LM head + per-row top-k: for each row m of X [M,K], the k largest logits of
  * X W^T (W [N,K]) as (index, value) ordered by value desc then index asc, and
@@ -235,7 +238,7 @@ eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const
 size_t eagle_op_lmhead_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t k, int32_t dtype);
 eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k, const void* d_x,
                                   const void* d_w, int32_t* d_idx, float* d_val, float* d_lse, void* d_scratch,
-                                  void* stream);
+                                  size_t scratch_bytes, void* stream);
 
 /* Tree attention for one sequence over a KV cache slice: queries Q [rows][n_heads][hd]
  * (RoPE applied), keys/values K,V [n_kv_heads][cap][hd]; row r attends to slots
@@ -245,7 +248,7 @@ size_t eagle_op_attention_scratch_bytes(int32_t rows, int32_t n_heads, int32_t h
 eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_heads, int32_t n_kv_heads,
                                      int32_t hd, int32_t cap, int32_t prefix, const void* d_q, const void* d_k,
                                      const void* d_v, const uint64_t* d_mask, void* d_o, void* d_scratch,
-                                     void* stream);
+                                     size_t scratch_bytes, void* stream);
 
 #ifdef __cplusplus
 }

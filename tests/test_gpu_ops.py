@@ -53,7 +53,7 @@ def test_gemm_bf16(cuda, M, N, K):
     ref = x.astype(np.float64) @ w[cols].astype(np.float64).T
     scale = np.sqrt(K) * 0.02
     err = np.abs(y[:, cols] - ref).max() / scale
-    assert err < 2e-5, err
+    assert err < 1e-4, err     # fp32 accumulation over K; bf16 output rounding would be ~4e-3
 
 
 def test_gemm_bf16_is_row_independent(cuda):
