@@ -46,6 +46,9 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a, int n_chunk_sl
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* Ks = reinterpret_cast<bf16*>(smem_raw);                 // [kCK][HD + kPad]
   bf16* Vt = Ks + kCK * (HD + kPad);                            // [HD][kCK + kPad]
+  // programmatic dependent launch: every CTA waits for the producer of q / K / V before any read
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Group g = a.groups[blockIdx.z];
   const int kvh = blockIdx.y;
   const int chunk = blockIdx.x;
@@ -201,6 +204,8 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a, int n_chunk_sl
 // One warp per (row, query head): combine the row's chunk partials in chunk order.
 template <int HD>
 __global__ void attn_merge_kernel(AttnArgs a, const int* __restrict__ row_grp, int n_chunk_slots) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= a.M * a.Hq) return;
   const int row = w / a.Hq, qh = w % a.Hq;
@@ -232,18 +237,27 @@ template <int HD>
 cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   const int slots = n_prefix_chunks(a.max_prefix) + 1;
   const size_t smem = (size_t)kCK * (HD + kPad) * 2 + (size_t)HD * (kCK + kPad) * 2;
-  static bool attr = false;
-  if (!attr) {
+  static bool smem_set = false;
+  if (!smem_set) {
     cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
+    smem_set = true;
   }
-  dim3 grid(slots, a.Hkv, a.n_groups);
-  attn_tc_kernel<HD><<<grid, 128, smem, s>>>(a, slots);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(slots, a.Hkv, a.n_groups);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, a, slots);
   if (e != cudaSuccess) return e;
   const int warps = a.M * a.Hq;
-  attn_merge_kernel<HD><<<(warps + 3) / 4, 128, 0, s>>>(a, a.row_grp, slots);
-  return cudaGetLastError();
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, a, a.row_grp, slots);
 }
 
 }  // namespace

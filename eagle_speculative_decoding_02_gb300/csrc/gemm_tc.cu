@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+// Programmatic dependent launch: wait for the previous kernel's results / let the next kernel start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // Barrier over the 128 epilogue threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool epi_all(bool v) {
   uint32_t r;
@@ -216,15 +227,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch();  // the next kernel may start its own prologue on freed SMs
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-      int it = 0;
+      uint64_t pol_w, pol_x;  // weights are read once per GEMM; activations by every CTA
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+      // The weights do not depend on earlier kernels: request the weight boxes
+      // of the first S stages before waiting for the previous kernel
+      // (programmatic dependent launch), the activation boxes after it.
+      int pre_kb[kMaxStages];
+      int npre = 0;
+      for (long long u = u0; u < u1 && npre < S; ++u, ++npre) {
+        const int t = (int)(u / kbt);
+        const int kb = (int)(u - (long long)t * kbt);
+        mbar_expect_tx(&full[npre], (uint32_t)stage_bytes);
+        tma_load_2d_hint(stage_base + (size_t)npre * stage_bytes, &tmW, &full[npre], kb * kBK, t * kTileN, pol_w);
+        pre_kb[npre] = kb;
+      }
+      griddep_wait();
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d_hint(stage_base + (size_t)i * stage_bytes + kWBytes, &tmX, &full[i], pre_kb[i] * kBK, m0, pol_x);
+      int it = npre;
       bool ok = true;
-      for (long long u = u0; u < u1 && ok;) {
+      for (long long u = u0 + npre; u < u1 && ok;) {
         const int t = (int)(u / kbt);
         const int kb0 = (int)(u - (long long)t * kbt);
         const int kb1 = (int)min((long long)kbt, u1 - (long long)t * kbt);
@@ -236,8 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sw = stage_base + (size_t)s * stage_bytes;
           mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
-          tma_load_2d(sw, &tmW, &full[s], kb * kBK, t * kTileN);
-          tma_load_2d(sw + kWBytes, &tmX, &full[s], kb * kBK, m0);
+          tma_load_2d_hint(sw, &tmW, &full[s], kb * kBK, t * kTileN, pol_w);
+          tma_load_2d_hint(sw + kWBytes, &tmX, &full[s], kb * kBK, m0, pol_x);
         }
         u = (long long)(t + 1) * kbt;
       }
@@ -291,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue (128 threads)
+    griddep_wait();                       // epilogue inputs (h, norms, rows) come from earlier kernels
     const int etid = threadIdx.x - 64;
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int col = q * 32 + lane;        // weight row within the tile = output column
@@ -431,7 +462,9 @@ Plan plan(int M, int N, int K, int nsm) {
   p.n_tiles = N / kTileN;
   p.kbt = K / kBK;
   p.T = (long long)p.n_tiles * p.kbt;
-  const bool split = (long long)p.m_chunks * p.n_tiles < 2LL * nsm;
+  // Stream-K whenever the token rows fit in a few chunks (every weight-streaming
+  // case, including the LM head); plain one-tile-per-CTA for large prefills.
+  const bool split = p.m_chunks <= 4 || (long long)p.m_chunks * p.n_tiles < 2LL * nsm;
   p.G = split ? (int)std::min<long long>(nsm, p.T) : p.n_tiles;
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * p.MT)) cols <<= 1;
@@ -469,8 +502,8 @@ cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const Epi
   if ((long long)p.m_chunks * p.n_tiles > kCounterInts) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, N, K, kTileN) || !make_map(&tmX, X, M, K, p.MT)) return cudaErrorInvalidValue;
-  static std::once_flag attr;
-  std::call_once(attr, [] {
+  static std::once_flag smem_attr;
+  std::call_once(smem_attr, [] {
     cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   });
   TcArgs a{};
@@ -486,8 +519,17 @@ cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const Epi
   a.counters = reinterpret_cast<int*>(scratch);
   a.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + p.counters_bytes);
   a.status = status;
-  gemm_tc_kernel<<<p.G * p.m_chunks, kThreads, p.smem, s>>>(tmW, tmX, a, ep);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G * p.m_chunks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, a, ep);
 }
 
 }  // namespace eg
