@@ -23,6 +23,7 @@
 
 #include <mutex>
 
+#include "../../include/eagle.h"
 #include "epilogue.cuh"
 #include "kernels.h"
 
@@ -43,6 +44,10 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 // partial sums can never land on another shape's counters.
 constexpr int kCounterInts = 1 << 17;
 constexpr size_t kCounterBytes = (size_t)kCounterInts * 4;
+// Allocation-free variant (eagle_op_gemm_noalloc): token rows <= 64, so the
+// partial sums need at most kNsmSizing CTAs x 2 fragments x 64 rows x 128 columns.
+constexpr int kNoAllocMaxM = 64;
+constexpr size_t kNoAllocScratchBytes = kCounterBytes + (size_t)kNsmSizing * 2 * 64 * kTileN * 4;
 
 struct TcArgs {
   int M, MT, m_chunks, n_tiles, kbt, G, stages;
@@ -533,3 +538,54 @@ cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const Epi
 }
 
 }  // namespace eg
+
+// ------------------------------------------------------------------ allocation-free entry point
+//
+// Some callers of the GEMM cannot allocate device memory: code running inside
+// a CUDA graph that is being captured by someone else, plugins of a runtime
+// that owns the device allocator, and callers that must not touch the memory
+// budget at all. eagle_op_gemm_noalloc gives them the same tcgen05 kernel with
+// its split-K scratch (arrival counters, then partial sums) in the static
+// device array below instead of a caller buffer. The array is
+// g_noalloc_scratch_bytes = 512 KiB of counters + 10 MiB of partials (160 SMs
+// x 2 fragments x 64 rows x 128 columns x 4 bytes); every GPU that loads this
+// library reserves it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[eg::kNoAllocScratchBytes];
+
+namespace eg {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[256] = {};  // device address of g_noalloc_scratch, per device ordinal
+}  // namespace
+}  // namespace eg
+
+extern "C" eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w,
+                                              float* d_y, void* stream) {
+  using namespace eg;
+  if (M < 1 || N < 1 || K < 1 || !d_x || !d_w || !d_y) return EAGLE_ERR_INVALID_ARG;
+  if (M > kNoAllocMaxM || N % kTileN || K % kBK || N / kTileN > kCounterInts) return EAGLE_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return EAGLE_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // first call on a device: look up the array's device address (host code
+    // cannot use the symbol itself, which names a host-side shadow)
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return EAGLE_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // the array keeps the previous call's contents: the counters this shape uses must start at zero
+  if (cudaMemsetAsync(scratch, 0, (size_t)(N / kTileN) * sizeof(int), s) != cudaSuccess) return EAGLE_ERR_CUDA;
+  EpiParams e;
+  e.kind = kEpiStore;
+  e.M = M;
+  e.N = N;
+  e.y = d_y;
+  const cudaError_t err = gemm_tc((const bf16*)d_x, (const bf16*)d_w, M, N, K, e, scratch, nullptr, s);
+  return err == cudaSuccess ? EAGLE_OK : (err == cudaErrorInvalidValue ? EAGLE_ERR_UNSUPPORTED : EAGLE_ERR_CUDA);
+}

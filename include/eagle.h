@@ -232,6 +232,23 @@ size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtyp
 eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w,
                            float* d_y, void* d_scratch, size_t scratch_bytes, void* stream);
 
+/* The same bf16 GEMM for callers that cannot allocate device memory (for
+ * example code running while someone else captures a CUDA graph, or a plugin
+ * whose host owns the allocator): the split-K scratch lives in a static device
+ * array inside this library (10.5 MiB, reserved on every GPU that loads the
+ * library until the process exits), so the caller passes only X, W and Y.
+ * The pages have no counterpart; this is an interface convenience.
+ *   - M <= 64 token rows, N a multiple of 128, K a multiple of 64; larger
+ *     shapes return EAGLE_ERR_UNSUPPORTED (use eagle_op_gemm with a scratch).
+ *   - Calls no cudaMalloc/cudaFree or allocating routine. The first call on a
+ *     device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call shares the one array and clears the counters it uses before
+ *     launching; calls that overlap on the GPU (other streams, other threads)
+ *     race on it and must be serialised by the caller. */
+eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w, float* d_y,
+                                   void* stream);
+
 /* LM head + per-row top-k: for each row m of X [M,K], the k largest logits of
  * X W^T (W [N,K]) as (index, value) ordered by value desc then index asc, and
  * the row's log-sum-exp. d_idx/d_val [M][k], d_lse [M]. */
