@@ -8,10 +8,11 @@
 // Split-K flash decode: CTA (chunk c, KV head, group) takes either prefix keys
 // [128 c, 128 c + 128) or, for c == ceil(prefix / 128), the tree block, and all
 // rows of the group times the G = Hq / Hkv query heads sharing that KV head
-// (the GQA rows form the M dimension of the MMA). Each CTA stages its K chunk
-// and the transposed V chunk in shared memory once; every warp runs 16-row
-// tiles over it with an online softmax and writes an unnormalised partial
-// (max, sum, O). attn_merge combines the partials of a row in chunk order.
+// (the GQA rows form the M dimension of the MMA). Each CTA stages its K and V
+// chunks in shared memory once with cp.async (V fragments are read transposed
+// with ldmatrix.trans); each of 8 warps runs 16-row tiles over them with an
+// online softmax and writes an unnormalised partial (max, sum, O).
+// attn_merge combines the partials of a row in chunk order.
 // Chunk boundaries are absolute slot multiples of 128, independent of how many
 // rows are verified.
 #include <cmath>
@@ -22,7 +23,8 @@ namespace eg {
 namespace {
 
 constexpr int kCK = 128;   // keys per chunk
-constexpr int kPad = 8;    // bf16 padding per shared-memory row
+constexpr int kPad = 8;    // bf16 padding per shared-memory row (rows 16-byte aligned, conflict-free)
+constexpr int kAttnThreads = 256;
 
 __device__ __forceinline__ uint32_t ld_b32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
@@ -41,11 +43,25 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
 
 __host__ __device__ __forceinline__ int n_prefix_chunks(int prefix) { return (prefix + kCK - 1) / kCK; }
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+
+// Four 8x8 b16 matrices, transposed, from shared memory (one row address per lane).
+__device__ __forceinline__ void ldsm_x4_trans(const bf16* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
 template <int HD>
-__global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a, int n_chunk_slots) {
+__global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n_chunk_slots) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* Ks = reinterpret_cast<bf16*>(smem_raw);                 // [kCK][HD + kPad]
-  bf16* Vt = Ks + kCK * (HD + kPad);                            // [HD][kCK + kPad]
+  bf16* Vs = Ks + kCK * (HD + kPad);                            // [kCK][HD + kPad]
   // programmatic dependent launch: every CTA waits for the producer of q / K / V before any read
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -61,27 +77,24 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a, int n_chunk_sl
   const int R = g.nrows * G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // stage K (row-major) and V (transposed) of the chunk; keys past nkeys are zero
+  // stage K and V of the chunk (row-major) with asynchronous 16-byte copies, all
+  // in flight at once; keys past nkeys are zero-filled
   const bf16* Kg = reinterpret_cast<const bf16*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
   const bf16* Vg = reinterpret_cast<const bf16*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
   constexpr int VEC = 8;  // bf16 per 16-byte vector
-  for (int e = tid; e < kCK * HD / VEC; e += 128) {
+  for (int e = tid; e < kCK * HD / VEC; e += kAttnThreads) {
     const int key = e / (HD / VEC), d0 = (e % (HD / VEC)) * VEC;
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (key < nkeys) {
-      kv = *reinterpret_cast<const uint4*>(Kg + (size_t)key * HD + d0);
-      vv = *reinterpret_cast<const uint4*>(Vg + (size_t)key * HD + d0);
-    }
-    *reinterpret_cast<uint4*>(Ks + key * (HD + kPad) + d0) = kv;
-    const bf16* vp = reinterpret_cast<const bf16*>(&vv);
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) Vt[(d0 + i) * (kCK + kPad) + key] = vp[i];
+    const int n = key < nkeys ? 16 : 0;
+    const size_t go = (size_t)min(key, nkeys - 1) * HD + d0;
+    cp_async16(Ks + key * (HD + kPad) + d0, Kg + go, n);
+    cp_async16(Vs + key * (HD + kPad) + d0, Vg + go, n);
   }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   const float sl2 = a.scale * 1.4426950408889634f;  // scores in log2 units
   const int quad = lane >> 2, qi = lane & 3;
-  for (int mt = warp; mt * 16 < R; mt += 4) {
+  for (int mt = warp; mt * 16 < R; mt += kAttnThreads / 32) {
     // rows r0 = mt*16 + quad and r1 = r0 + 8 of this tile: (node, head) = (r / G, r % G)
     int node[2], qh[2];
     bool rv[2];
@@ -175,12 +188,18 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a, int n_chunk_sl
         o[dt][2] *= corr[1];
         o[dt][3] *= corr[1];
       }
+      // B fragments of V (k = key, n = dim) from the row-major V tile with ldmatrix.trans:
+      // lane l addresses row (key) kb + 16 kk2 + 8 ((l >> 3) & 1) + (l & 7) of dim tile dt + (l >> 4)
 #pragma unroll
       for (int kk2 = 0; kk2 < 4; ++kk2) {
 #pragma unroll
-        for (int dt = 0; dt < HD / 8; ++dt) {
-          const bf16* vp = Vt + (dt * 8 + quad) * (kCK + kPad) + kb + kk2 * 16 + qi * 2;
-          mma16816(o[dt], pa[kk2], ld_b32(vp), ld_b32(vp + 8));
+        for (int dt = 0; dt < HD / 8; dt += 2) {
+          const int key = kb + kk2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const bf16* vp = Vs + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(vp, b0, b1, b2, b3);
+          mma16816(o[dt], pa[kk2], b0, b1);
+          mma16816(o[dt + 1], pa[kk2], b2, b3);
         }
       }
     }
@@ -212,18 +231,25 @@ __global__ void attn_merge_kernel(AttnArgs a, const int* __restrict__ row_grp, i
   const Group g = a.groups[row_grp ? row_grp[row] : 0];
   const int nck = n_prefix_chunks(g.prefix) + (g.block_len > 0 ? 1 : 0);
   const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
+  // chunk maxima and sums: one load per lane and chunk, all lanes at once
   float M = -INFINITY;
-  for (int c = 0; c < nck; ++c) M = fmaxf(M, base[(size_t)c * (HD + 2) + HD]);
+  for (int c = lane; c < nck; c += 32) M = fmaxf(M, base[(size_t)c * (HD + 2) + HD]);
+  M = warp_max(M);
+  float L = 0.f;
+  for (int c = lane; c < nck; c += 32) {
+    const float m = base[(size_t)c * (HD + 2) + HD];
+    if (m != -INFINITY) L += exp2f(m - M) * base[(size_t)c * (HD + 2) + HD + 1];
+  }
+  L = warp_sum(L);
+  // weighted sum of the chunk outputs in chunk order (independent loads, unrolled)
   float acc[HD / 32];
 #pragma unroll
   for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
-  float L = 0.f;
+#pragma unroll 4
   for (int c = 0; c < nck; ++c) {
     const float* p = base + (size_t)c * (HD + 2);
     const float m = p[HD];
-    if (m == -INFINITY) continue;
-    const float wgt = exp2f(m - M);
-    L += wgt * p[HD + 1];
+    const float wgt = m == -INFINITY ? 0.f : exp2f(m - M);
 #pragma unroll
     for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * p[lane + 32 * i];
   }
@@ -236,7 +262,7 @@ __global__ void attn_merge_kernel(AttnArgs a, const int* __restrict__ row_grp, i
 template <int HD>
 cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   const int slots = n_prefix_chunks(a.max_prefix) + 1;
-  const size_t smem = (size_t)kCK * (HD + kPad) * 2 + (size_t)HD * (kCK + kPad) * 2;
+  const size_t smem = 2 * (size_t)kCK * (HD + kPad) * 2;
   static bool smem_set = false;
   if (!smem_set) {
     cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -247,7 +273,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(slots, a.Hkv, a.n_groups);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = pdl;
@@ -256,6 +282,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int warps = a.M * a.Hq;
   cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, a, a.row_grp, slots);
 }

@@ -383,18 +383,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*last_flag && ok) {
           __threadfence();
           for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
-            for (int j = 0; j < kSub; ++j) {
-              float s = 0.f;
-              if (r0 + j < rows_valid) {
-                for (int cc = c0; cc <= c1; ++cc) {
-                  const int tf = (int)(unit_start(a, cc) / kbt);
-                  const float* sl =
-                      a.partial + (((size_t)mc * a.G + cc) * 2 + (t != tf ? 1 : 0)) * (size_t)MT * kTileN;
-                  s += __ldcg(sl + (size_t)(r0 + j) * kTileN + col);
-                }
-              }
-              tile[j * kLdt + col] = s;
+            // fragments in ascending CTA order; the 32 rows of a fragment are loaded together
+            float acc[kSub];
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) acc[j] = 0.f;
+            for (int cc = c0; cc <= c1; ++cc) {
+              const int tf = (int)(unit_start(a, cc) / kbt);
+              const float* sl = a.partial + (((size_t)mc * a.G + cc) * 2 + (t != tf ? 1 : 0)) * (size_t)MT * kTileN +
+                                (size_t)r0 * kTileN + col;
+              float v[kSub];
+#pragma unroll
+              for (int j = 0; j < kSub; ++j) v[j] = (r0 + j < rows_valid) ? __ldcg(sl + (size_t)j * kTileN) : 0.f;
+#pragma unroll
+              for (int j = 0; j < kSub; ++j) acc[j] += v[j];
             }
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) tile[j * kLdt + col] = acc[j];
             EpilogueSync{}();
             run_epilogue<bf16>(ep, tile, kLdt, m0 + r0, min(kSub, rows_valid - r0), n0, rscale, etid,
                                EpilogueSync{});

@@ -44,6 +44,7 @@ __global__ void fc_input_kernel(const float* __restrict__ feat, const int* __res
   const float* f = feat + (size_t)fsrc[m] * d;
   const T* e = E + (size_t)tok[m] * d;
   T* xr = x + (size_t)m * 2 * d;
+#pragma unroll 4
   for (int n = threadIdx.x; n < d; n += blockDim.x) {
     xr[n] = from_f<T>(f[n]);
     xr[d + n] = e[n];
@@ -85,36 +86,67 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const float* __restrict
   se = block_sum128(se, red);
   if (tid == 0 && out_lse) out_lse[m] = gmax + __logf(se);
 
-  // k rounds: the best candidate strictly after the previous winner in (value desc, index asc).
-  float pv = INFINITY;
-  int pi = -1;
-  const int nc = ntiles * k;
+  // Each thread keeps the k best of its candidates (value desc, index asc), sorted, in registers.
+  float lv[kMaxTopK];
+  int li[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    lv[j] = -INFINITY;
+    li[j] = 0x7fffffff;
+  }
+  for (int t = tid; t < ntiles; t += 128) {
+    const size_t base = ((size_t)t * M + m) * k;
+    for (int j = 0; j < k; ++j) {
+      const float v = rec_val[base + j];
+      const int ix = rec_idx[base + j];
+      // candidates of one tile arrive sorted: once one misses the list, the rest of the tile does too
+      if (ix < 0 || !(v > lv[k - 1] || (v == lv[k - 1] && ix < li[k - 1]))) break;
+      float cv = v;
+      int ci = ix;
+#pragma unroll
+      for (int q = 0; q < kMaxTopK; ++q) {
+        if (q < k && (cv > lv[q] || (cv == lv[q] && ci < li[q]))) {
+          const float tv = lv[q];
+          const int ti = li[q];
+          lv[q] = cv;
+          li[q] = ci;
+          cv = tv;
+          ci = ti;
+        }
+      }
+    }
+  }
+  // k rounds of a block arg-max over the heads of the 128 sorted lists
+  int head = 0;
   for (int r = 0; r < k; ++r) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int c = tid; c < nc; c += 128) {
-      const int t = c / k, j = c % k;
-      const size_t rr = ((size_t)t * M + m) * k + j;
-      const float v = rec_val[rr];
-      const int ix = rec_idx[rr];
-      if (ix < 0) continue;
-      const bool after = (v < pv) || (v == pv && ix > pi);
-      if (after && (v > bv || (v == bv && ix < bi))) { bv = v; bi = ix; }
-    }
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q)
+      if (q == head) {
+        bv = lv[q];
+        bi = li[q];
+      }
+    const int mine = bi;
     warp_argmax(bv, bi);
     __syncthreads();
-    if ((tid & 31) == 0) { sv[tid >> 5] = bv; si[tid >> 5] = bi; }
+    if ((tid & 31) == 0) {
+      sv[tid >> 5] = bv;
+      si[tid >> 5] = bi;
+    }
     __syncthreads();
     bv = sv[0];
     bi = si[0];
     for (int w = 1; w < 4; ++w)
-      if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
+      if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) {
+        bv = sv[w];
+        bi = si[w];
+      }
+    if (mine == bi && head < k) ++head;  // indices are unique: exactly one list owns the winner
     if (tid == 0) {
-      out_idx[(size_t)m * k + r] = bi;
+      out_idx[(size_t)m * k + r] = bi == 0x7fffffff ? -1 : bi;
       if (out_val) out_val[(size_t)m * k + r] = bv;
     }
-    pv = bv;
-    pi = bi;
   }
 }
 
