@@ -73,6 +73,7 @@ SIGNATURES = {
                                 C.c_void_p, C.c_size_t, C.c_void_p]),
     "eagle_op_gemm_noalloc": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_void_p]),
+    "eagle_selftest_bounded_wait": (C.c_int, [C.c_void_p, C.c_void_p]),
     "eagle_op_lmhead_scratch_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "eagle_op_lmhead_topk": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,

@@ -5,13 +5,13 @@
 // group g sees the prefix slots [0, prefix) and the slots prefix + i of the
 // tree block whose bit i is set in node j's ancestor mask.
 //
-// Split-K flash decode: CTA (chunk c, KV head, group) takes either prefix keys
-// [128 c, 128 c + 128) or, for c == ceil(prefix / 128), the tree block, and all
-// rows of the group times the G = Hq / Hkv query heads sharing that KV head
-// (the GQA rows form the M dimension of the MMA). Each CTA stages its K and V
-// chunks in shared memory once with cp.async (V fragments are read transposed
-// with ldmatrix.trans); each of 8 warps runs 16-row tiles over them with an
-// online softmax and writes an unnormalised partial (max, sum, O).
+// Split-K flash decode: CTA (chunk c, KV head and 64-row block, group) takes
+// either prefix keys [128 c, 128 c + 128) or, for c == ceil(prefix / 128), the
+// tree block, and 64 of the group's rows x G = Hq / Hkv query heads sharing
+// that KV head (the GQA rows form the M dimension of the MMA). Each CTA stages
+// its K and V chunks in shared memory once with cp.async (V fragments are read
+// transposed with ldmatrix.trans); each of its 4 warps runs one 16-row tile with
+// an online softmax and writes an unnormalised partial (max, sum, O).
 // attn_merge combines the partials of a row in chunk order.
 // Chunk boundaries are absolute slot multiples of 128, independent of how many
 // rows are verified.
@@ -23,8 +23,10 @@ namespace eg {
 namespace {
 
 constexpr int kCK = 128;   // keys per chunk
+constexpr int kMaxGroupRows = 128;  // rows of one group (tree rows, or one 128-row prefill block)
 constexpr int kPad = 8;    // bf16 padding per shared-memory row (rows 16-byte aligned, conflict-free)
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 128;  // 4 warps, one 16-row tile each
+constexpr int kRowBlock = 64;      // GQA rows (node x query head) per CTA
 
 __device__ __forceinline__ uint32_t ld_b32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
@@ -66,11 +68,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Group g = a.groups[blockIdx.z];
-  const int kvh = blockIdx.y;
+  const int rb_count = (kMaxGroupRows * (a.Hq / a.Hkv) + kRowBlock - 1) / kRowBlock;
+  const int kvh = blockIdx.y / rb_count, rb = blockIdx.y % rb_count;
   const int chunk = blockIdx.x;
   const int nck = n_prefix_chunks(g.prefix);
   const bool block = chunk == nck;
-  if (chunk > nck || (block && g.block_len <= 0)) return;
+  if (chunk > nck || (block && g.block_len <= 0) || rb * kRowBlock >= g.nrows * (a.Hq / a.Hkv)) return;
   const int key0 = block ? g.prefix : chunk * kCK;
   const int nkeys = block ? g.block_len : min(kCK, g.prefix - key0);
   const int G = a.Hq / a.Hkv;
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
 
   const float sl2 = a.scale * 1.4426950408889634f;  // scores in log2 units
   const int quad = lane >> 2, qi = lane & 3;
-  for (int mt = warp; mt * 16 < R; mt += kAttnThreads / 32) {
+  for (int mt = rb * (kRowBlock / 16) + warp; mt * 16 < R && mt < (rb + 1) * (kRowBlock / 16); mt += kAttnThreads / 32) {
     // rows r0 = mt*16 + quad and r1 = r0 + 8 of this tile: (node, head) = (r / G, r % G)
     int node[2], qh[2];
     bool rv[2];
@@ -272,7 +275,8 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(slots, a.Hkv, a.n_groups);
+  const int rb_count = (kMaxGroupRows * (a.Hq / a.Hkv) + kRowBlock - 1) / kRowBlock;
+  cfg.gridDim = dim3(slots, a.Hkv * rb_count, a.n_groups);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -11,20 +11,50 @@
 
 namespace eg {
 
-// rscale must hold msub floats of shared memory. Run by 128 threads with
-// ranks tid = 0..127; sync() must be a barrier over exactly those threads.
+// Rows per epilogue call, and the shared-memory row staging it needs:
+// row scale, RoPE position, KV slot and sequence of each row.
+constexpr int kEpiRows = 32;
+constexpr int kEpiRowSmemFloats = 4 * kEpiRows;
+// Loads of one thread are batched this many rows at a time, ahead of any store,
+// so that their latencies overlap.
+constexpr int kEpiBatch = 8;
+
+// rowsm must hold kEpiRowSmemFloats words of shared memory; msub <= kEpiRows.
+// Run by 128 threads with ranks tid = 0..127; sync() must be a barrier over
+// exactly those threads.
 template <typename T, typename Sync>
 __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, int msub, int n0,
-                             float* rscale, int tid, Sync sync) {
+                             float* rowsm, int tid, Sync sync) {
   const int ncols = min(kTileN, p.N - n0);
-  for (int m = tid; m < msub; m += 128) {
+  float* rscale = rowsm;
+  int* rpos = reinterpret_cast<int*>(rowsm + kEpiRows);
+  int* rslot = rpos + kEpiRows;
+  int* rseq = rslot + kEpiRows;
+  if (tid < msub) {
+    const int m = tid;
     float r = 1.f;
     if (p.ssq_in) {
+      const float* s_in = p.ssq_in + m0 + m;
+      float part[kEpiBatch];
+#pragma unroll
+      for (int q = 0; q < kEpiBatch; ++q) part[q] = 0.f;
+      int j = 0;
+      for (; j + kEpiBatch <= p.n_ssq_in; j += kEpiBatch) {
+#pragma unroll
+        for (int q = 0; q < kEpiBatch; ++q) part[q] += s_in[(size_t)(j + q) * p.M];
+      }
+      for (; j < p.n_ssq_in; ++j) part[0] += s_in[(size_t)j * p.M];
       float s = 0.f;
-      for (int j = 0; j < p.n_ssq_in; ++j) s += p.ssq_in[(size_t)j * p.M + m0 + m];
+#pragma unroll
+      for (int q = 0; q < kEpiBatch; ++q) s += part[q];
       r = rsqrtf(s * p.inv_d_in + p.eps);
     }
     rscale[m] = r;
+    if (p.kind == kEpiQkv) {
+      rpos[m] = p.rows.pos[m0 + m];
+      rslot[m] = p.rows.slot[m0 + m];
+      rseq[m] = p.rows.seq[m0 + m];
+    }
   }
   sync();
 
@@ -43,24 +73,33 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
         const int region = n < p.q_dim ? 0 : (n < p.q_dim + p.kv_dim ? 1 : 2);
         const int partner = i < half ? c + half : c - half;
         const int fi = i < half ? i : i - half;
-        for (int m = 0; m < msub; ++m) {
-          const int row = m0 + m;
-          float v = tile[m * ldt + c] * rscale[m];
-          if (region < 2) {
-            const float pv = tile[m * ldt + partner] * rscale[m];
-            const int pos = p.rows.pos[row];
-            const float cs = p.rope_cos[(size_t)pos * half + fi];
-            const float sn = p.rope_sin[(size_t)pos * half + fi];
-            v = i < half ? v * cs - pv * sn : v * cs + pv * sn;
+        const int nn = n - p.q_dim - (region == 2 ? p.kv_dim : 0);
+        const int kvh = nn / hd;
+        for (int mb = 0; mb < msub; mb += kEpiBatch) {
+          float cs[kEpiBatch], sn[kEpiBatch];
+#pragma unroll
+          for (int q = 0; q < kEpiBatch; ++q) {  // the batch's table loads, all in flight together
+            cs[q] = 1.f;
+            sn[q] = 0.f;
+            if (region < 2 && mb + q < msub) {
+              const size_t at = (size_t)rpos[mb + q] * half + fi;
+              cs[q] = p.rope_cos[at];
+              sn[q] = p.rope_sin[at];
+            }
           }
-          if (region == 0) {
-            reinterpret_cast<T*>(p.out)[(size_t)row * p.q_dim + n] = from_f<T>(v);
-          } else {
-            const int slot = p.rows.slot[row];
-            if (slot >= 0) {
-              const int nn = n - p.q_dim - (region == 2 ? p.kv_dim : 0);
-              const int kvh = nn / hd;
-              const size_t at = (((size_t)p.rows.seq[row] * p.n_kv + kvh) * p.cap + slot) * hd + i;
+#pragma unroll
+          for (int q = 0; q < kEpiBatch; ++q) {
+            const int m = mb + q;
+            if (m >= msub) break;
+            float v = tile[m * ldt + c] * rscale[m];
+            if (region < 2) {
+              const float pv = tile[m * ldt + partner] * rscale[m];
+              v = i < half ? v * cs[q] - pv * sn[q] : v * cs[q] + pv * sn[q];
+            }
+            if (region == 0) {
+              reinterpret_cast<T*>(p.out)[(size_t)(m0 + m) * p.q_dim + n] = from_f<T>(v);
+            } else if (rslot[m] >= 0) {
+              const size_t at = (((size_t)rseq[m] * p.n_kv + kvh) * p.cap + rslot[m]) * hd + i;
               reinterpret_cast<T*>(region == 1 ? p.kc : p.vc)[at] = from_f<T>(v);
             }
           }
@@ -87,12 +126,21 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
       if (c < ncols) {
         const int n = n0 + c;
         const float gn = p.gain[n];
-        for (int m = 0; m < msub; ++m) {
-          const size_t at = (size_t)(m0 + m) * p.N + n;
-          const float hn = (p.kind == kEpiResid ? p.h[at] : 0.f) + tile[m * ldt + c] * rscale[m];
-          p.h[at] = hn;
-          reinterpret_cast<T*>(p.hb)[at] = from_f<T>(hn * gn);
-          tile[m * ldt + c] = hn * hn;
+        for (int mb = 0; mb < msub; mb += kEpiBatch) {
+          float hv[kEpiBatch];
+#pragma unroll
+          for (int q = 0; q < kEpiBatch; ++q)  // residual loads of the batch, ahead of its stores
+            hv[q] = (p.kind == kEpiResid && mb + q < msub) ? p.h[(size_t)(m0 + mb + q) * p.N + n] : 0.f;
+#pragma unroll
+          for (int q = 0; q < kEpiBatch; ++q) {
+            const int m = mb + q;
+            if (m >= msub) break;
+            const size_t at = (size_t)(m0 + m) * p.N + n;
+            const float hn = hv[q] + tile[m * ldt + c] * rscale[m];
+            p.h[at] = hn;
+            reinterpret_cast<T*>(p.hb)[at] = from_f<T>(hn * gn);
+            tile[m * ldt + c] = hn * hn;
+          }
         }
       } else {
         for (int m = 0; m < msub; ++m) tile[m * ldt + c] = 0.f;

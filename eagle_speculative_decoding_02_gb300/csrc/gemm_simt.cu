@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* __restrict__ X,
   __shared__ float ws[BK][kTileN + 4];
   __shared__ float xs[BK][BM + 1];
   __shared__ float tile[BM * LDT];
-  __shared__ float rscale[BM];
+  __shared__ float rscale[kEpiRowSmemFloats];
   const int tid = threadIdx.x;
   const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * BM;
   const int tn = tid & 31, tm = tid >> 5;  // thread computes cols tn+32i, rows tm*8+j

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stage_base = smem;
   float* tile = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
   float* rscale = tile + kSub * kLdt;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rscale + kSub);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rscale + kEpiRowSmemFloats);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* afull = bars + 2 * S;
@@ -417,6 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Failure-detection self-test: one thread waits, with the GEMM pipeline's
+// bounded wait, on an mbarrier that nothing ever arrives on. The wait must give
+// up after its time limit and report kStTimeout through the status word; the
+// kernel then returns normally, so the context stays usable.
+__global__ void bounded_wait_selftest_kernel(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (mbar_wait(&bar, 0, &abort_flag, status)) set_status(status, 1);  // would mean the wait saw a phase flip
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -479,7 +493,7 @@ Plan plan(int M, int N, int K, int nsm) {
   while (cols < (uint32_t)(2 * p.MT)) cols <<= 1;
   p.tmem_cols = cols;
   const size_t stage = kWBytes + (size_t)p.MT * kBK * 2;
-  const size_t fixed = (size_t)kSub * kLdt * 4 + kSub * 4 + (2 * kMaxStages + 5) * 8 + 16 + 1024;
+  const size_t fixed = (size_t)kSub * kLdt * 4 + kEpiRowSmemFloats * 4 + (2 * kMaxStages + 5) * 8 + 16 + 1024;
   int st = (int)((kSmemBudget - fixed) / stage);
   p.stages = std::max(2, std::min(kMaxStages, st));
   p.smem = (size_t)p.stages * stage + fixed;
@@ -592,4 +606,10 @@ extern "C" eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, c
   e.y = d_y;
   const cudaError_t err = gemm_tc((const bf16*)d_x, (const bf16*)d_w, M, N, K, e, scratch, nullptr, s);
   return err == cudaSuccess ? EAGLE_OK : (err == cudaErrorInvalidValue ? EAGLE_ERR_UNSUPPORTED : EAGLE_ERR_CUDA);
+}
+
+extern "C" eagle_status eagle_selftest_bounded_wait(int32_t* d_status, void* stream) {
+  if (!d_status) return EAGLE_ERR_INVALID_ARG;
+  eg::bounded_wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(d_status);
+  return cudaGetLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }

@@ -430,6 +430,18 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
   const int b = blockIdx.x, tid = threadIdx.x;
   const int NR = tree.n_rows;
   const int base = b * NR;
+  // After any device-detected error (capacity, timeout) the state stops
+  // advancing: nothing is committed and nothing is compacted, so no later
+  // kernel indexes a slot past the caches.
+  if (*(volatile int*)st.status != kStOk) {
+    if (tid == 0) {
+      st.acc_len[b] = 0;
+      if (acc_out) acc_out[b] = -1;
+      if (tok_out)
+        for (int t = 0; t <= kMaxDepth; ++t) tok_out[b * (kMaxDepth + 1) + t] = -1;
+    }
+    return;
+  }
   if (tid < 32) {
     int cur = 0, a = 0;
     if (tid == 0) path[0] = 0;

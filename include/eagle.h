@@ -267,6 +267,13 @@ eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_head
                                      const void* d_v, const uint64_t* d_mask, void* d_o, void* d_scratch,
                                      size_t scratch_bytes, void* stream);
 
+/* Failure-detection self-test (no counterpart in the pages): one GPU thread
+ * waits, with the same bounded wait as the GEMM pipeline's mbarrier waits, on
+ * a barrier that nothing arrives on. After the wait's time limit (2 s) it gives
+ * up, writes EAGLE_ERR_TIMEOUT to *d_status (if *d_status was EAGLE_OK) and the
+ * kernel returns; no trap, no fault, and the CUDA context stays usable. */
+eagle_status eagle_selftest_bounded_wait(int32_t* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -106,3 +106,21 @@ def test_product_topology_matches_oracle():
         p, r = T.named(k)
         op, orank, _ = OT.static_layout(OT.static_paths(k))
         assert p == list(op) and r == list(orank)
+
+
+def test_init_rejects_small_or_misaligned_workspace_before_any_cuda_call(lib):
+    cfg, keep = _cfg(FX.WORKLOADS["tiny_static"])
+    n = C.c_size_t(0)
+    assert lib.eagle_workspace_size(C.byref(cfg), C.byref(n)) == 0
+    lw = L.EagleLayerWeights(*([256] * 6))
+    layers = (L.EagleLayerWeights * 2)(lw, lw)
+    w = L.EagleWeights(256, 256, 256, layers, 256, lw)          # non-null dummies: never dereferenced
+    ctx = C.c_void_p()
+    assert lib.eagle_init(C.byref(cfg), C.byref(w), C.c_void_p(1 << 20), n.value - 256, None, C.byref(ctx)) == 3
+    assert lib.eagle_init(C.byref(cfg), C.byref(w), C.c_void_p((1 << 20) + 16), n.value, None, C.byref(ctx)) == 3
+    assert not ctx.value
+
+
+def test_no_alloc_and_selftest_symbols_reject_null_arguments_on_the_host(lib):
+    assert lib.eagle_op_gemm_noalloc(0, 128, 64, None, None, None, None) == 1
+    assert lib.eagle_selftest_bounded_wait(None, None) == 1

@@ -1,0 +1,93 @@
+"""Full-size checks at the Llama-3-8B shape, in the launch configuration the benchmark times.
+
+* 2 layers at full width, heads and vocabulary (d 4096, 32/8 heads of 128,
+  ffn 14336, V 128256) against the CPU oracle: verify logits within 0.05
+  max-abs and cosine >= 0.999, greedy tokens equal except at flagged near-ties
+  (oracle top-2 margin < 0.1), and the same accepted lengths.
+* The full 32-layer model (16 GB of weights), GPU only: the speculative output
+  equals vanilla greedy decoding token for token up to the first flagged
+  near-tie, and a chain tree carrying the vanilla continuation is verified in
+  one pass to exactly the vanilla tokens (tree verification = sequential
+  decoding), with margins taken from that same pass.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import fixtures as FX
+from oracle import decode as OD
+from oracle import model as OM
+from oracle import tree as OT
+from tests.oracle_helpers import tree_from_torch, tree_to_torch
+
+pytestmark = pytest.mark.gpu
+
+TWO_LAYER_8B = FX.LLAMA3_8B.reduced(n_layers=2)
+
+
+def _margins(logits):
+    s = np.sort(logits, -1)
+    return s[..., -1] - s[..., -2]
+
+
+def test_8b_width_two_layers_verify_parity(cuda):
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    w = dataclasses.replace(FX.WORKLOADS["8b_eagle2"], model=TWO_LAYER_8B, prompt_len=64, max_new=32)
+    cap = FX.kv_capacity(w)
+    m = OM.build_model(TWO_LAYER_8B, cap)
+    prompt = FX.prompts(TWO_LAYER_8B, 1, w.prompt_len)
+    eng = S.make_engine(w)
+    root = eng.prefill(torch.from_numpy(prompt).to(cuda)).cpu().numpy()
+    st = OD.prefill(m, prompt[0], cap)
+    flagged = 0
+    for step in range(3):
+        gtree = eng.draft_tree()
+        tree = tree_from_torch(gtree)
+        real = int((tree.tokens >= 0).sum())
+        am, lg = eng.verify(gtree, logits=True)
+        oam, ofeats, ologits = OD.verify(m, st, OT.Tree(tree.tokens[:real], tree.parent[:real], tree.depth[:real]))
+        got = lg[0, :real].cpu().numpy()
+        err = np.abs(got - ologits).max()
+        cos = float((got.ravel() @ ologits.ravel()) / (np.linalg.norm(got) * np.linalg.norm(ologits)))
+        assert err < 0.05 and cos >= 0.999, (step, err, cos)
+        g_am = am[0, :real].cpu().numpy()
+        bad = (g_am != oam) & (_margins(ologits) >= 0.1)
+        assert not bad.any(), step
+        flagged += int((g_am != oam).sum())
+        a, _ = eng.accept_commit()
+        oa = OD.accept_commit(st, OT.Tree(tree.tokens[:real], tree.parent[:real], tree.depth[:real]), g_am, ofeats)
+        assert int(a[0]) == oa
+    print("flagged near-ties:", flagged, "first root", root[0])
+
+
+def test_8b_full_speculative_equals_vanilla(cuda):
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    w = dataclasses.replace(FX.WORKLOADS["8b_eagle2"], prompt_len=256, max_new=24)
+    eng = S.make_engine(w)
+    prompt = S.prompts(w)
+    van, _ = eng.generate(prompt, w.max_new, use_graph=True, vanilla=True)
+    spec, stats = eng.generate(prompt, w.max_new, use_graph=True)
+    van, spec = van[0].cpu().numpy(), spec[0].cpu().numpy()
+    # one verify pass over a chain carrying the vanilla continuation: its greedy tokens and margins
+    n = w.max_new
+    chain = OT.Tree(tokens=van[:n].astype(np.int32), parent=np.arange(-1, n - 1, dtype=np.int32),
+                    depth=np.arange(n, dtype=np.int32))
+    eng.prefill(prompt)
+    am, lg = eng.verify(tree_to_torch(chain), logits=True)
+    am, lg = am[0].cpu().numpy(), lg[0].cpu().numpy()
+    margins = _margins(lg)
+    # tree verification equals sequential decoding: the chain's greedy tokens are vanilla's next tokens
+    for i in range(n - 1):
+        if margins[i] < 0.1:
+            break
+        assert am[i] == van[i + 1], i
+    # speculative output equals vanilla output up to the first flagged near-tie
+    for i in range(1, n):
+        if margins[i - 1] < 0.1:
+            print("flagged near-tie at", i)
+            break
+        assert spec[i] == van[i], (i, spec[:i + 1], van[:i + 1])
+    assert spec[0] == van[0]
+    print("steps", stats["steps"], "mean accepted", stats["mean_accept"])
