@@ -86,6 +86,16 @@ class Clocks:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def aggregate(ms: float, toks: float, device) -> tuple[float, float]:
+    """Whole-job numbers of replica ranks: the slowest rank's time and the sum of all ranks' tokens."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms), float(toks)], dtype=torch.float64, device=device)
+    parts = [torch.zeros_like(t) for _ in range(dist.get_world_size())]
+    dist.all_gather(parts, t)
+    return max(float(x[0]) for x in parts), sum(float(x[1]) for x in parts)
+
+
 def verify_bytes(m, batch: int, L: int, rows: int) -> int:
     """Algorithmic HBM bytes of one verify pass: every weight once, the KV prefix read once per layer,
     the new K/V rows written (bf16)."""
@@ -294,11 +304,7 @@ def main():
     toks = eng.committed_counts().sum().item() - c0
     eng.sync_status()
     if world > 1:
-        t = torch.tensor([ms, float(toks)], device="cuda")
-        ms_all = [torch.zeros_like(t) for _ in range(world)]
-        dist.all_gather(ms_all, t)
-        ms = max(float(x[0]) for x in ms_all)
-        toks = sum(float(x[1]) for x in ms_all)
+        ms, toks = aggregate(ms, toks, "cuda")
     value = toks / (ms / 1e3)
 
     # verify pass alone: HBM bytes per verify / its device time

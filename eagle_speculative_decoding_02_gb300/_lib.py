@@ -70,7 +70,7 @@ SIGNATURES = {
     "eagle_last_error": (C.c_char_p, [C.c_void_p]),
     "eagle_op_gemm_scratch_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "eagle_op_gemm": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
-                                C.c_void_p, C.c_size_t, C.c_void_p]),
+                                C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "eagle_op_gemm_noalloc": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_void_p]),
     "eagle_selftest_bounded_wait": (C.c_int, [C.c_void_p, C.c_void_p]),

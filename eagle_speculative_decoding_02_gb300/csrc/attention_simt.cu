@@ -24,8 +24,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   const int nkeys = g.prefix + g.block_len;
   for (int r = warp; r < g.nrows; r += 4) {
     const int row = g.row0 + r;
-    const T* qr = reinterpret_cast<const T*>(a.q) + ((size_t)row * a.Hq + h) * hd;
-    for (int dd = lane; dd < hd; dd += 32) q[dd] = to_f(qr[dd]);
+    const float* qr = a.q + ((size_t)row * a.Hq + h) * hd;
+    for (int dd = lane; dd < hd; dd += 32) q[dd] = qr[dd];
     __syncwarp();
     const uint64_t m0 = a.mask[2 * row], m1 = a.mask[2 * row + 1];
     float mrun = -INFINITY, l = 0.f;

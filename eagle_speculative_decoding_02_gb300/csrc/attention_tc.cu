@@ -30,17 +30,20 @@ constexpr int kRowBlock = 64;      // GQA rows (node x query head) per CTA
 
 __device__ __forceinline__ uint32_t ld_b32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) floats -> packed bf16x2 high parts and packed bf16x2 residuals.
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 __host__ __device__ __forceinline__ int n_prefix_chunks(int prefix) { return (prefix + kCK - 1) / kCK; }
@@ -112,14 +115,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
       mk0[i] = block && rv[i] ? a.mask[2 * row] : 0ull;
       mk1[i] = block && rv[i] ? a.mask[2 * row + 1] : 0ull;
     }
-    uint32_t qa[HD / 16][4];
+    // q (float32) as a hi/lo pair of bf16 A fragments: S = Q_hi K^T + Q_lo K^T
+    uint32_t qa[HD / 16][4], ql[HD / 16][4];
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const bf16* qp = reinterpret_cast<const bf16*>(a.q) + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
-        qa[kk][i] = rv[i] ? ld_b32(qp + kk * 16 + qi * 2) : 0u;
-        qa[kk][i + 2] = rv[i] ? ld_b32(qp + kk * 16 + 8 + qi * 2) : 0u;
+        const float* qp = a.q + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
+        const float2 x0 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + qi * 2) : make_float2(0.f, 0.f);
+        const float2 x1 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + 8 + qi * 2) : make_float2(0.f, 0.f);
+        split_bf16x2(x0.x, x0.y, qa[kk][i], ql[kk][i]);
+        split_bf16x2(x1.x, x1.y, qa[kk][i + 2], ql[kk][i + 2]);
       }
     }
     float o[HD / 8][4];
@@ -136,7 +142,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           const bf16* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
-          mma16816(s[nt], qa[kk], ld_b32(kp), ld_b32(kp + 8));
+          const uint32_t k0 = ld_b32(kp), k1 = ld_b32(kp + 8);
+          mma16816(s[nt], qa[kk], k0, k1);
+          mma16816(s[nt], ql[kk], k0, k1);
         }
       }
       // mask and scale; c-fragment (row quad (+8), key kb + nt*8 + qi*2 + {0,1})
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
         mrow[i] = mn;
       }
       float sum[2] = {0.f, 0.f};
-      uint32_t pa[4][4];
+      uint32_t pa[4][4], pl[4][4];  // P as a hi/lo pair of bf16 A fragments
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
@@ -175,8 +183,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
         }
         // P as the A operand of P.V: keys 16*kk2 .. of this 64-key block
         const int kk2 = nt >> 1, hi = nt & 1;
-        pa[kk2][0 + 2 * hi] = pack_bf16(s[nt][0], s[nt][1]);
-        pa[kk2][1 + 2 * hi] = pack_bf16(s[nt][2], s[nt][3]);
+        split_bf16x2(s[nt][0], s[nt][1], pa[kk2][0 + 2 * hi], pl[kk2][0 + 2 * hi]);
+        split_bf16x2(s[nt][2], s[nt][3], pa[kk2][1 + 2 * hi], pl[kk2][1 + 2 * hi]);
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -202,7 +210,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
           uint32_t b0, b1, b2, b3;
           ldsm_x4_trans(vp, b0, b1, b2, b3);
           mma16816(o[dt], pa[kk2], b0, b1);
+          mma16816(o[dt], pl[kk2], b0, b1);
           mma16816(o[dt + 1], pa[kk2], b2, b3);
+          mma16816(o[dt + 1], pl[kk2], b2, b3);
         }
       }
     }
@@ -257,9 +267,9 @@ __global__ void attn_merge_kernel(AttnArgs a, const int* __restrict__ row_grp, i
     for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * p[lane + 32 * i];
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  bf16* out = reinterpret_cast<bf16*>(a.o) + ((size_t)row * a.Hq + qh) * HD;
+  const size_t ob = ((size_t)row * a.Hq + qh) * HD;
 #pragma unroll
-  for (int i = 0; i < HD / 32; ++i) out[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  for (int i = 0; i < HD / 32; ++i) store_hilo<bf16>(reinterpret_cast<bf16*>(a.o), a.o_lo, ob + lane + 32 * i, acc[i] * inv);
 }
 
 template <int HD>

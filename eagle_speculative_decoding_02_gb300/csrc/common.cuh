@@ -26,6 +26,15 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
 
+// Store v as a GEMM input: hi[at] = T(v) and, when lo is given (bf16 models),
+// lo[at] = bf16(v - hi), so that hi + lo carries v to about 16 mantissa bits.
+template <typename T>
+__device__ __forceinline__ void store_hilo(T* hi, bf16* lo, size_t at, float v) {
+  const T h = from_f<T>(v);
+  hi[at] = h;
+  if (lo) lo[at] = __float2bfloat16_rn(v - to_f(h));
+}
+
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, kStOk, code);
 }
@@ -65,7 +74,11 @@ struct EpiParams {
   float inv_d_in = 0.f;
   float eps = 0.f;
   float* y = nullptr;       // kEpiStore output; kEpiLmHead optional logits [M][N]
-  void* out = nullptr;      // q (kEpiQkv) [M][q_dim] or act (kEpiSwiglu) [M][ffn]
+  void* out = nullptr;      // q (kEpiQkv, float32) [M][q_dim] or act (kEpiSwiglu, T) [M][ffn]
+  // bf16 models carry GEMM inputs as hi/lo pairs (x = hi + lo): the low halves of
+  // act (kEpiSwiglu) and hb (kEpiResid / kEpiFc); NULL for float32 models.
+  bf16* out_lo = nullptr;
+  bf16* hb_lo = nullptr;
   // kEpiQkv
   int q_dim = 0, kv_dim = 0, head_dim = 0, n_kv = 0, cap = 0;
   const float* rope_cos = nullptr;  // [positions][head_dim/2]

@@ -82,6 +82,11 @@ struct eagle_ctx {
   float* h_tgt = nullptr;
   float* h_dft = nullptr;
   void* hb = nullptr;
+  eg::bf16* hb_lo = nullptr;   // bf16 models: GEMM inputs are hi/lo pairs (x = hb + hb_lo)
+  eg::bf16* act_lo = nullptr;
+  eg::bf16* attn_lo = nullptr;
+  eg::bf16* xfc_lo = nullptr;
+  eg::bf16* lm_hb_lo = nullptr;
   float* ssq_a = nullptr;
   float* ssq_b = nullptr;
   void* q = nullptr;
@@ -262,6 +267,7 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
 struct Offsets {
   size_t rows_seq, rows_pos, rows_slot, rows_grp, rows_tok, rows_fsrc, rows_mask, groups;
   size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, attn, act, xfc, lm_hb, lm_ssq, lm_src;
+  size_t hb_lo, act_lo, attn_lo, xfc_lo, lm_hb_lo;
   size_t rec_val, rec_idx, rec_max, rec_sum, dtopk_idx, dtopk_val, dlse, vargmax, root_idx;
   size_t t_tok, t_par, t_dep, t_anc, vt_tok, vt_par, vt_dep, vt_anc;
   size_t L, c, root, pend_tok, pend_feat, n_out, out, acc_len, acc_path, L_prev, hist, status;
@@ -285,9 +291,12 @@ Offsets plan(const Dims& dm) {
   o.h_dft = L.take((size_t)dm.M_dft * dm.d * 4);
   o.hb = L.take(M * dm.d * es);
   o.ssq_a = L.take(M * nt_d * 4); o.ssq_b = L.take(M * nt_d * 4);
-  o.q = L.take(M * dm.qd * es); o.attn = L.take(M * dm.qd * es);
+  o.q = L.take(M * dm.qd * 4); o.attn = L.take(M * dm.qd * es);
   o.act = L.take(M * dm.ffn * es); o.xfc = L.take(M * 2 * dm.d * es);
   o.lm_hb = L.take((size_t)dm.B * dm.d * es); o.lm_ssq = L.take((size_t)dm.B * nt_d * 4);
+  const size_t lo = dm.bf16 ? 2 : 0;  // low halves of the hi/lo GEMM inputs (bf16 models only)
+  o.hb_lo = L.take(M * dm.d * lo); o.act_lo = L.take(M * dm.ffn * lo); o.attn_lo = L.take(M * dm.qd * lo);
+  o.xfc_lo = L.take(M * 2 * dm.d * lo); o.lm_hb_lo = L.take((size_t)dm.B * dm.d * lo);
   o.lm_src = L.take((size_t)dm.B * 4);
   const size_t nrec = (size_t)dm.ntV * dm.M_lm;
   const int krec = std::max(dm.k, 1);
@@ -334,11 +343,12 @@ Offsets plan(const Dims& dm) {
 
 template <typename T>
 struct Eng {
-  static eagle_status gemm(eagle_ctx* c, const void* X, const void* W, int M, int N, int K, const EpiParams& ep) {
+  static eagle_status gemm(eagle_ctx* c, const void* X, const bf16* X_lo, const void* W, int M, int N, int K,
+                           const EpiParams& ep) {
     if (M <= 0) return EAGLE_OK;
     if constexpr (sizeof(T) == 2) {
       if (gemm_tc_ok(c->dm, N, K)) {
-        EG_CK(gemm_tc((const bf16*)X, (const bf16*)W, M, N, K, ep, c->gemm_scratch, c->st.status, c->stream));
+        EG_CK(gemm_tc((const bf16*)X, X_lo, (const bf16*)W, M, N, K, ep, c->gemm_scratch, c->st.status, c->stream));
         return EAGLE_OK;
       }
     }
@@ -354,6 +364,9 @@ struct Eng {
     }
     return EAGLE_OK;
   }
+
+  // low halves of the hi/lo activation pairs (bf16 models only)
+  static bf16* lo(bf16* p) { return sizeof(T) == 2 ? p : nullptr; }
 
   static EpiParams epi(eagle_ctx* c, int kind, int M, int N) {
     EpiParams e;
@@ -372,35 +385,36 @@ struct Eng {
     e.ssq_in = c->ssq_b; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d;
     e.out = c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
     e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = c->rows;
-    EG_TRY(gemm(c, c->hb, lw.wqkv, M, dm.nqkv, dm.d, e));
+    EG_TRY(gemm(c, c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e));
 
     AttnArgs a{};
-    a.q = c->q; a.kc = kc; a.vc = vc; a.o = c->attn; a.groups = c->groups; a.n_groups = n_groups;
+    a.q = (const float*)c->q; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo); a.groups = c->groups; a.n_groups = n_groups;
     a.mask = c->rows.mask; a.row_grp = c->rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap;
     a.max_prefix = cap; a.scale = 1.f / std::sqrt((float)dm.hd); a.part = c->attn_part; a.status = c->st.status;
     EG_TRY(attention(c, a));
 
     e = epi(c, kEpiResid, M, dm.d);
-    e.h = h; e.hb = c->hb; e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
-    EG_TRY(gemm(c, c->attn, lw.wo, M, dm.d, dm.qd, e));
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
+    EG_TRY(gemm(c, c->attn, lo(c->attn_lo), lw.wo, M, dm.d, dm.qd, e));
 
     e = epi(c, kEpiSwiglu, M, 2 * dm.ffn);
     e.ssq_in = c->ssq_a; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.out = c->act; e.ffn = dm.ffn;
-    EG_TRY(gemm(c, c->hb, lw.wgu, M, 2 * dm.ffn, dm.d, e));
+    e.out_lo = lo(c->act_lo);
+    EG_TRY(gemm(c, c->hb, lo(c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e));
 
     e = epi(c, kEpiResid, M, dm.d);
-    e.h = h; e.hb = c->hb; e.ssq_out = c->ssq_b; e.gain = gain_next;
-    EG_TRY(gemm(c, c->act, lw.wd, M, dm.d, dm.ffn, e));
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = gain_next;
+    EG_TRY(gemm(c, c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e));
     return EAGLE_OK;
   }
 
-  static eagle_status lm_head(eagle_ctx* c, const void* X, const float* ssq, int M, int k, int* idx, float* val,
-                              float* lse, float* logits) {
+  static eagle_status lm_head(eagle_ctx* c, const void* X, const bf16* X_lo, const float* ssq, int M, int k,
+                              int* idx, float* val, float* lse, float* logits) {
     const Dims& dm = c->dm;
     EpiParams e = epi(c, kEpiLmHead, M, dm.V);
     e.ssq_in = ssq; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.topk = k; e.y = logits;
     e.rec_val = c->rec_val; e.rec_idx = c->rec_idx; e.rec_max = c->rec_max; e.rec_sum = c->rec_sum;
-    EG_TRY(gemm(c, X, c->lm_head, M, dm.V, dm.d, e));
+    EG_TRY(gemm(c, X, X_lo, c->lm_head, M, dm.V, dm.d, e));
     EG_CK(topk_merge(c->rec_val, c->rec_idx, c->rec_max, c->rec_sum, dm.ntV, M, k, idx, val, lse, c->stream));
     return EAGLE_OK;
   }
@@ -410,7 +424,7 @@ struct Eng {
     const size_t es = sizeof(T);
     const size_t kvl = (size_t)dm.B * dm.Hkv * dm.cap * dm.hd;
     EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok, M, dm.d, c->layers[0].attn_norm, c->h_tgt, (T*)c->hb,
-                        c->ssq_b, c->stream));
+                        lo(c->hb_lo), c->ssq_b, c->stream));
     for (int l = 0; l < dm.Lyr; ++l) {
       const float* gn = l + 1 < dm.Lyr ? c->layers[l + 1].attn_norm : c->final_norm;
       EG_TRY(layer(c, c->layers[l], (char*)c->kc + l * kvl * es, (char*)c->vc + l * kvl * es, dm.cap, M, n_groups,
@@ -423,13 +437,15 @@ struct Eng {
   static eagle_status draft_forward(eagle_ctx* c, const float* feat, int M, int n_groups, int hbase, int k) {
     const Dims& dm = c->dm;
     float* h = c->h_dft + (size_t)hbase * dm.d;
-    EG_CK(fc_input<T>(feat, c->rows.fsrc, (const T*)c->embed, c->rows.tok, M, dm.d, (T*)c->xfc, c->stream));
+    EG_CK(fc_input<T>(feat, c->rows.fsrc, (const T*)c->embed, c->rows.tok, M, dm.d, (T*)c->xfc, lo(c->xfc_lo),
+                      c->stream));
     EpiParams e = epi(c, kEpiFc, M, dm.d);
-    e.h = h; e.hb = c->hb; e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
-    EG_TRY(gemm(c, c->xfc, c->fc, M, dm.d, 2 * dm.d, e));
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
+    EG_TRY(gemm(c, c->xfc, lo(c->xfc_lo), c->fc, M, dm.d, 2 * dm.d, e));
     EG_TRY(layer(c, c->head, c->kc_d, c->vc_d, dm.cap_d, M, n_groups, h, c->final_norm));
     if (k > 0)
-      EG_TRY(lm_head(c, c->hb, c->ssq_b, M, k, c->dtopk_idx + (size_t)hbase * k, c->dtopk_val + (size_t)hbase * k,
+      EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, k, c->dtopk_idx + (size_t)hbase * k,
+                     c->dtopk_val + (size_t)hbase * k,
                      c->dlse + hbase, nullptr));
     return EAGLE_OK;
   }
@@ -445,8 +461,9 @@ struct Eng {
         std::vector<int> src(dm.B);
         for (int b = 0; b < dm.B; ++b) src[b] = b * cl + cl - 1;
         EG_CK(cudaMemcpyAsync(c->lm_src, src.data(), dm.B * sizeof(int), cudaMemcpyHostToDevice, c->stream));
-        EG_CK(gather_rows<T>((const T*)c->hb, c->ssq_b, M, c->lm_src, dm.B, dm.d, (T*)c->lm_hb, c->lm_ssq, c->stream));
-        EG_TRY(lm_head(c, c->lm_hb, c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr));
+        EG_CK(gather_rows<T>((const T*)c->hb, lo(c->hb_lo), c->ssq_b, M, c->lm_src, dm.B, dm.d, (T*)c->lm_hb,
+                             lo(c->lm_hb_lo), c->lm_ssq, c->stream));
+        EG_TRY(lm_head(c, c->lm_hb, lo(c->lm_hb_lo), c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr));
         EG_CK(prefill_finish(c->st, c->root_idx, c->h_tgt, cl, P, root_out, c->stream));
         EG_CK(cudaStreamSynchronize(c->stream));  // src is a host temporary
       }
@@ -484,7 +501,7 @@ struct Eng {
     const int M = dm.B * tree.n_rows;
     EG_CK(setup_verify_rows(c->st, tree, c->rows, c->groups, c->stream));
     EG_TRY(target_stack(c, M, dm.B));
-    EG_TRY(lm_head(c, c->hb, c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits));
+    EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits));
     if (d_argmax)
       EG_CK(cudaMemcpyAsync(d_argmax, c->vargmax, (size_t)M * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
     return EAGLE_OK;
@@ -581,6 +598,8 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->ssq_a = (float*)P(o.ssq_a); c->ssq_b = (float*)P(o.ssq_b);
   c->q = P(o.q); c->attn = P(o.attn); c->act = P(o.act); c->xfc = P(o.xfc);
   c->lm_hb = P(o.lm_hb); c->lm_ssq = (float*)P(o.lm_ssq); c->lm_src = (int*)P(o.lm_src);
+  c->hb_lo = (bf16*)P(o.hb_lo); c->act_lo = (bf16*)P(o.act_lo); c->attn_lo = (bf16*)P(o.attn_lo);
+  c->xfc_lo = (bf16*)P(o.xfc_lo); c->lm_hb_lo = (bf16*)P(o.lm_hb_lo);
   c->rec_val = (float*)P(o.rec_val); c->rec_idx = (int*)P(o.rec_idx);
   c->rec_max = (float*)P(o.rec_max); c->rec_sum = (float*)P(o.rec_sum);
   c->dtopk_idx = (int*)P(o.dtopk_idx); c->dtopk_val = (float*)P(o.dtopk_val); c->dlse = (float*)P(o.dlse);

@@ -97,7 +97,7 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
               v = i < half ? v * cs[q] - pv * sn[q] : v * cs[q] + pv * sn[q];
             }
             if (region == 0) {
-              reinterpret_cast<T*>(p.out)[(size_t)(m0 + m) * p.q_dim + n] = from_f<T>(v);
+              reinterpret_cast<float*>(p.out)[(size_t)(m0 + m) * p.q_dim + n] = v;
             } else if (rslot[m] >= 0) {
               const size_t at = (((size_t)rseq[m] * p.n_kv + kvh) * p.cap + rslot[m]) * hd + i;
               reinterpret_cast<T*>(region == 1 ? p.kc : p.vc)[at] = from_f<T>(v);
@@ -115,7 +115,7 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
         for (int m = 0; m < msub; ++m) {
           const float g = tile[m * ldt + c] * rscale[m];
           const float u = tile[m * ldt + rr + c] * rscale[m];
-          reinterpret_cast<T*>(p.out)[(size_t)(m0 + m) * p.ffn + blk * 64 + c] = from_f<T>(silu_f(g) * u);
+          store_hilo<T>(reinterpret_cast<T*>(p.out), p.out_lo, (size_t)(m0 + m) * p.ffn + blk * 64 + c, silu_f(g) * u);
         }
       }
       break;
@@ -138,7 +138,7 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
             const size_t at = (size_t)(m0 + m) * p.N + n;
             const float hn = hv[q] + tile[m * ldt + c] * rscale[m];
             p.h[at] = hn;
-            reinterpret_cast<T*>(p.hb)[at] = from_f<T>(hn * gn);
+            store_hilo<T>(reinterpret_cast<T*>(p.hb), p.hb_lo, at, hn * gn);
             tile[m * ldt + c] = hn * hn;
           }
         }

@@ -51,6 +51,7 @@ constexpr size_t kNoAllocScratchBytes = kCounterBytes + (size_t)kNsmSizing * 2 *
 
 struct TcArgs {
   int M, MT, m_chunks, n_tiles, kbt, G, stages;
+  int has_lo;      // activations come as a hi/lo pair: a second X box per stage and a second MMA per k-step
   long long T;
   uint32_t tmem_cols;
   int* counters;   // [m_chunks][n_tiles], zero on entry and on exit
@@ -182,13 +183,13 @@ __device__ __forceinline__ int cta_of(const TcArgs& a, long long u) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
-                   EpiParams ep) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const __grid_constant__ CUtensorMap tmXlo, TcArgs a, EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages, MT = a.MT;
   const int xbytes = MT * kBK * 2;
-  const int stage_bytes = kWBytes + xbytes;
+  const int stage_bytes = kWBytes + xbytes * (a.has_lo ? 2 : 1);
   uint8_t* stage_base = smem;
   float* tile = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
   float* rscale = tile + kSub * kLdt;
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------------- TMA producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+      if (a.has_lo) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXlo)) : "memory");
       uint64_t pol_w, pol_x;  // weights are read once per GEMM; activations by every CTA
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
@@ -255,8 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pre_kb[npre] = kb;
       }
       griddep_wait();
-      for (int i = 0; i < npre; ++i)
-        tma_load_2d_hint(stage_base + (size_t)i * stage_bytes + kWBytes, &tmX, &full[i], pre_kb[i] * kBK, m0, pol_x);
+      for (int i = 0; i < npre; ++i) {
+        uint8_t* sx = stage_base + (size_t)i * stage_bytes + kWBytes;
+        tma_load_2d_hint(sx, &tmX, &full[i], pre_kb[i] * kBK, m0, pol_x);
+        if (a.has_lo) tma_load_2d_hint(sx + xbytes, &tmXlo, &full[i], pre_kb[i] * kBK, m0, pol_x);
+      }
       int it = npre;
       bool ok = true;
       for (long long u = u0 + npre; u < u1 && ok;) {
@@ -273,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
           tma_load_2d_hint(sw, &tmW, &full[s], kb * kBK, t * kTileN, pol_w);
           tma_load_2d_hint(sw + kWBytes, &tmX, &full[s], kb * kBK, m0, pol_x);
+          if (a.has_lo) tma_load_2d_hint(sw + kWBytes + xbytes, &tmXlo, &full[s], kb * kBK, m0, pol_x);
         }
         u = (long long)(t + 1) * kbt;
       }
@@ -310,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sw = smem_u32(stage_base + (size_t)s * stage_bytes);
           const uint32_t sx = sw + kWBytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
+          for (int k = 0; k < kBK / 16; ++k) {
             umma(d, sw128_desc(sw + k * 32), sw128_desc(sx + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            if (a.has_lo) umma(d, sw128_desc(sw + k * 32), sw128_desc(sx + xbytes + k * 32), idesc, 1u);
+          }
           umma_commit(&empty[s]);
         }
         umma_commit(&afull[buf]);
@@ -477,7 +485,7 @@ struct Plan {
   size_t smem, counters_bytes, partial_bytes;
 };
 
-Plan plan(int M, int N, int K, int nsm) {
+Plan plan(int M, int N, int K, int nsm, bool has_lo) {
   Plan p{};
   p.MT = M > 256 ? 256 : ((M + 31) / 32) * 32;
   if (p.MT < 32) p.MT = 32;
@@ -492,7 +500,7 @@ Plan plan(int M, int N, int K, int nsm) {
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * p.MT)) cols <<= 1;
   p.tmem_cols = cols;
-  const size_t stage = kWBytes + (size_t)p.MT * kBK * 2;
+  const size_t stage = kWBytes + (size_t)p.MT * kBK * 2 * (has_lo ? 2 : 1);
   const size_t fixed = (size_t)kSub * kLdt * 4 + kEpiRowSmemFloats * 4 + (2 * kMaxStages + 5) * 8 + 16 + 1024;
   int st = (int)((kSmemBudget - fixed) / stage);
   p.stages = std::max(2, std::min(kMaxStages, st));
@@ -510,21 +518,24 @@ size_t gemm_tc_scratch_bytes(int M, int N, int K) {
   const int chunks = (M + 255) / 256;
   for (int mc = 1; mc <= chunks; ++mc) {
     const int Mp = mc == 1 ? std::min(M, 256) : mc * 256;
-    const Plan p = plan(Mp, N, K, kNsmSizing);
+    const Plan p = plan(Mp, N, K, kNsmSizing, true);
     best = std::max(best, p.counters_bytes + p.partial_bytes);
   }
   return best;
 }
 
-cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const EpiParams& ep, void* scratch,
-                    int* status, cudaStream_t s) {
+cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N, int K, const EpiParams& ep,
+                    void* scratch, int* status, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (N % kTileN || K % kBK || !scratch) return cudaErrorInvalidValue;
-  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
-  const Plan p = plan(M, N, K, num_sms());
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(X_lo) | reinterpret_cast<uintptr_t>(W)) & 15)
+    return cudaErrorInvalidValue;
+  const Plan p = plan(M, N, K, num_sms(), X_lo != nullptr);
   if ((long long)p.m_chunks * p.n_tiles > kCounterInts) return cudaErrorInvalidValue;
-  CUtensorMap tmW, tmX;
+  CUtensorMap tmW, tmX, tmXlo;
   if (!make_map(&tmW, W, N, K, kTileN) || !make_map(&tmX, X, M, K, p.MT)) return cudaErrorInvalidValue;
+  if (X_lo && !make_map(&tmXlo, X_lo, M, K, p.MT)) return cudaErrorInvalidValue;
+  if (!X_lo) tmXlo = tmX;  // unused
   static std::once_flag smem_attr;
   std::call_once(smem_attr, [] {
     cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
@@ -539,6 +550,7 @@ cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const Epi
   a.stages = p.stages;
   a.T = p.T;
   a.tmem_cols = p.tmem_cols;
+  a.has_lo = X_lo != nullptr;
   a.counters = reinterpret_cast<int*>(scratch);
   a.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + p.counters_bytes);
   a.status = status;
@@ -552,7 +564,7 @@ cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const Epi
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, a, ep);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, tmXlo, a, ep);
 }
 
 }  // namespace eg
@@ -604,7 +616,7 @@ extern "C" eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, c
   e.M = M;
   e.N = N;
   e.y = d_y;
-  const cudaError_t err = gemm_tc((const bf16*)d_x, (const bf16*)d_w, M, N, K, e, scratch, nullptr, s);
+  const cudaError_t err = gemm_tc((const bf16*)d_x, nullptr, (const bf16*)d_w, M, N, K, e, scratch, nullptr, s);
   return err == cudaSuccess ? EAGLE_OK : (err == cudaErrorInvalidValue ? EAGLE_ERR_UNSUPPORTED : EAGLE_ERR_CUDA);
 }
 

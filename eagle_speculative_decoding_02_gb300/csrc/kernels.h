@@ -12,16 +12,18 @@ cudaError_t gemm_simt(const T* X, const T* W, int M, int N, int K, const EpiPara
 // tcgen05 + TMA weight-streaming GEMM (bf16). `scratch` holds split-K partials
 // and per-tile arrival counters (counters must start at zero; the kernel
 // leaves them at zero). Returns cudaErrorInvalidValue for unsupported shapes.
+// X_lo (may be NULL): low halves of a hi/lo activation pair, Y = (X + X_lo) W^T.
 size_t gemm_tc_scratch_bytes(int M, int N, int K);
-cudaError_t gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, const EpiParams& ep, void* scratch,
-                    int* status, cudaStream_t s);
+cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N, int K, const EpiParams& ep,
+                    void* scratch, int* status, cudaStream_t s);
 
 // ---- attention ---------------------------------------------------------------------------------
 struct AttnArgs {
-  const void* q;      // [M][Hq][hd] (RoPE applied)
+  const float* q;     // [M][Hq][hd] float32 (RoPE applied)
   const void* kc;     // [B][Hkv][cap][hd]
   const void* vc;
   void* o;            // [M][Hq * hd]
+  bf16* o_lo;         // low halves of o as a hi/lo pair (bf16 models; may be NULL)
   const Group* groups;
   int n_groups;
   const uint64_t* mask;  // [M][2]
@@ -39,15 +41,15 @@ cudaError_t attention_tc(const AttnArgs& a, cudaStream_t s);
 
 // ---- rows, embeddings, FC input ----------------------------------------------------------------
 template <typename T>
-cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, float* ssq,
-                       cudaStream_t s);
+cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, bf16* hb_lo,
+                       float* ssq, cudaStream_t s);
 template <typename T>
-cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x,
+cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x, bf16* x_lo,
                      cudaStream_t s);
-// Copy rows src[i] of (hb, ssq) to rows i of (hb_dst, ssq_dst).
+// Copy rows src[i] of (hb, hb_lo, ssq) to rows i of (hb_dst, lo_dst, ssq_dst); the lo pointers may be NULL.
 template <typename T>
-cudaError_t gather_rows(const T* hb, const float* ssq, int M_src, const int* src, int n, int d, T* hb_dst,
-                        float* ssq_dst, cudaStream_t s);
+cudaError_t gather_rows(const T* hb, const bf16* hb_lo, const float* ssq, int M_src, const int* src, int n, int d,
+                        T* hb_dst, bf16* lo_dst, float* ssq_dst, cudaStream_t s);
 
 // ---- LM-head top-k merge over vocab tiles ------------------------------------------------------
 cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* rec_max, const float* rec_sum,

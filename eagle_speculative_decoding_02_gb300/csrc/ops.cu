@@ -28,8 +28,8 @@ size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtyp
   return 256;
 }
 
-eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* x, const void* w, float* y,
-                           void* scratch, size_t scratch_bytes, void* stream) {
+eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* x, const void* x_lo,
+                           const void* w, float* y, void* scratch, size_t scratch_bytes, void* stream) {
   if (M < 1 || N < 1 || K < 1 || !x || !w || !y) return EAGLE_ERR_INVALID_ARG;
   if (scratch_bytes < eagle_op_gemm_scratch_bytes(M, N, K, dtype)) return EAGLE_ERR_WORKSPACE;
   EpiParams e;
@@ -41,7 +41,8 @@ eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const
   if (dtype == EAGLE_DTYPE_BF16) {
     if (N % kTileN || K % 64) return EAGLE_ERR_UNSUPPORTED;
     if (!scratch) return EAGLE_ERR_WORKSPACE;
-    err = gemm_tc((const bf16*)x, (const bf16*)w, M, N, K, e, scratch, nullptr, (cudaStream_t)stream);
+    err = gemm_tc((const bf16*)x, (const bf16*)x_lo, (const bf16*)w, M, N, K, e, scratch, nullptr,
+                  (cudaStream_t)stream);
   } else if (dtype == EAGLE_DTYPE_F32) {
     err = gemm_simt<float>((const float*)x, (const float*)w, M, N, K, e, (cudaStream_t)stream);
   } else {
@@ -78,7 +79,7 @@ eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K
   cudaError_t err;
   if (dtype == EAGLE_DTYPE_BF16) {
     if (N % kTileN || K % 64) return EAGLE_ERR_UNSUPPORTED;
-    err = gemm_tc((const bf16*)x, (const bf16*)w, M, N, K, e, p, nullptr, s);
+    err = gemm_tc((const bf16*)x, nullptr, (const bf16*)w, M, N, K, e, p, nullptr, s);
   } else if (dtype == EAGLE_DTYPE_F32) {
     err = gemm_simt<float>((const float*)x, (const float*)w, M, N, K, e, s);
   } else {
@@ -105,7 +106,7 @@ eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_head
   Group* g = (Group*)scratch;
   write_group_kernel<<<1, 1, 0, s>>>(g, rows, prefix, rows);
   AttnArgs a{};
-  a.q = q; a.kc = k; a.vc = v; a.o = o; a.groups = g; a.n_groups = 1; a.mask = mask; a.row_grp = nullptr; a.M = rows;
+  a.q = (const float*)q; a.o_lo = nullptr; a.kc = k; a.vc = v; a.o = o; a.groups = g; a.n_groups = 1; a.mask = mask; a.row_grp = nullptr; a.M = rows;
   a.Hq = n_heads; a.Hkv = n_kv_heads; a.hd = hd; a.cap = cap; a.max_prefix = prefix;
   a.scale = 1.f / std::sqrt((float)hd);
   a.part = (float*)((char*)scratch + al(sizeof(Group)));

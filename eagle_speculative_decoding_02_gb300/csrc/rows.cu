@@ -15,11 +15,11 @@ __device__ float block_sum128(float v, float* red) {
   return ((red[0] + red[1]) + red[2]) + red[3];
 }
 
-// h = E[tok]; hb = h * gain; ssq[j][m] = sum of h^2 over column tile j.
+// h = E[tok]; hb (+ hb_lo) = h * gain; ssq[j][m] = sum of h^2 over column tile j.
 template <typename T>
 __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ E, const int* __restrict__ tok, int M,
                                                     int d, const float* __restrict__ gain, float* h, T* hb,
-                                                    float* ssq) {
+                                                    bf16* hb_lo, float* ssq) {
   __shared__ float red[4];
   const int m = blockIdx.x;
   const int t = tok[m];
@@ -29,34 +29,40 @@ __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ E, con
     if (n < d) {
       v = to_f(E[(size_t)t * d + n]);
       h[(size_t)m * d + n] = v;
-      hb[(size_t)m * d + n] = from_f<T>(v * gain[n]);
+      store_hilo<T>(hb, hb_lo, (size_t)m * d + n, v * gain[n]);
     }
     const float s = block_sum128(v * v, red);
     if (threadIdx.x == 0) ssq[(size_t)j * M + m] = s;
   }
 }
 
-// x[m] = [ T(feat[fsrc[m]]) ; E[tok[m]] ]  (length 2d).
+// x[m] = [ feat[fsrc[m]] ; E[tok[m]] ] (length 2d); the float feature half is
+// stored as a hi/lo pair when x_lo is given, the embedding half is exact.
 template <typename T>
 __global__ void fc_input_kernel(const float* __restrict__ feat, const int* __restrict__ fsrc,
-                                const T* __restrict__ E, const int* __restrict__ tok, int d, T* x) {
+                                const T* __restrict__ E, const int* __restrict__ tok, int d, T* x, bf16* x_lo) {
   const int m = blockIdx.x;
   const float* f = feat + (size_t)fsrc[m] * d;
   const T* e = E + (size_t)tok[m] * d;
-  T* xr = x + (size_t)m * 2 * d;
+  const size_t row = (size_t)m * 2 * d;
 #pragma unroll 4
   for (int n = threadIdx.x; n < d; n += blockDim.x) {
-    xr[n] = from_f<T>(f[n]);
-    xr[d + n] = e[n];
+    store_hilo<T>(x, x_lo, row + n, f[n]);
+    x[row + d + n] = e[n];
+    if (x_lo) x_lo[row + d + n] = __float2bfloat16_rn(0.f);
   }
 }
 
 template <typename T>
-__global__ void gather_rows_kernel(const T* __restrict__ hb, const float* __restrict__ ssq, int M_src,
-                                   const int* __restrict__ src, int n_rows, int d, T* hb_dst, float* ssq_dst) {
+__global__ void gather_rows_kernel(const T* __restrict__ hb, const bf16* __restrict__ hb_lo,
+                                   const float* __restrict__ ssq, int M_src, const int* __restrict__ src, int n_rows,
+                                   int d, T* hb_dst, bf16* lo_dst, float* ssq_dst) {
   const int i = blockIdx.x;
   const int r = src[i];
-  for (int n = threadIdx.x; n < d; n += blockDim.x) hb_dst[(size_t)i * d + n] = hb[(size_t)r * d + n];
+  for (int n = threadIdx.x; n < d; n += blockDim.x) {
+    hb_dst[(size_t)i * d + n] = hb[(size_t)r * d + n];
+    if (lo_dst) lo_dst[(size_t)i * d + n] = hb_lo[(size_t)r * d + n];
+  }
   for (int j = threadIdx.x; j * kTileN < d; j += blockDim.x) ssq_dst[(size_t)j * n_rows + i] = ssq[(size_t)j * M_src + r];
 }
 
@@ -153,26 +159,26 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const float* __restrict
 }  // namespace
 
 template <typename T>
-cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, float* ssq,
-                       cudaStream_t s) {
+cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, bf16* hb_lo,
+                       float* ssq, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  embed_kernel<T><<<M, 128, 0, s>>>(E, tok, M, d, gain, h, hb, ssq);
+  embed_kernel<T><<<M, 128, 0, s>>>(E, tok, M, d, gain, h, hb, hb_lo, ssq);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x,
+cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x, bf16* x_lo,
                      cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  fc_input_kernel<T><<<M, 256, 0, s>>>(feat, fsrc, E, tok, d, x);
+  fc_input_kernel<T><<<M, 256, 0, s>>>(feat, fsrc, E, tok, d, x, x_lo);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t gather_rows(const T* hb, const float* ssq, int M_src, const int* src, int n, int d, T* hb_dst,
-                        float* ssq_dst, cudaStream_t s) {
+cudaError_t gather_rows(const T* hb, const bf16* hb_lo, const float* ssq, int M_src, const int* src, int n, int d,
+                        T* hb_dst, bf16* lo_dst, float* ssq_dst, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  gather_rows_kernel<T><<<n, 256, 0, s>>>(hb, ssq, M_src, src, n, d, hb_dst, ssq_dst);
+  gather_rows_kernel<T><<<n, 256, 0, s>>>(hb, hb_lo, ssq, M_src, src, n, d, hb_dst, lo_dst, ssq_dst);
   return cudaGetLastError();
 }
 
@@ -183,13 +189,13 @@ cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* re
   return cudaGetLastError();
 }
 
-#define EG_INST(T)                                                                                      \
-  template cudaError_t embed_rows<T>(const T*, const int*, int, int, const float*, float*, T*, float*,  \
-                                     cudaStream_t);                                                     \
-  template cudaError_t fc_input<T>(const float*, const int*, const T*, const int*, int, int, T*,        \
-                                   cudaStream_t);                                                       \
-  template cudaError_t gather_rows<T>(const T*, const float*, int, const int*, int, int, T*, float*,    \
-                                      cudaStream_t);
+#define EG_INST(T)                                                                                          \
+  template cudaError_t embed_rows<T>(const T*, const int*, int, int, const float*, float*, T*, bf16*, float*,  \
+                                     cudaStream_t);                                                         \
+  template cudaError_t fc_input<T>(const float*, const int*, const T*, const int*, int, int, T*, bf16*,      \
+                                   cudaStream_t);                                                           \
+  template cudaError_t gather_rows<T>(const T*, const bf16*, const float*, int, const int*, int, int, T*, bf16*, \
+                                      float*, cudaStream_t);
 EG_INST(float)
 EG_INST(bf16)
 #undef EG_INST

@@ -201,8 +201,8 @@ def op_gemm_scratch(M: int, N: int, K: int, dtype=torch.bfloat16, device="cuda")
 
 
 def op_gemm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
-            scratch: torch.Tensor | None = None) -> torch.Tensor:
-    """Y = X W^T through the library's GEMM kernel (bf16: tcgen05; f32: SIMT)."""
+            scratch: torch.Tensor | None = None, x_lo: torch.Tensor | None = None) -> torch.Tensor:
+    """Y = (X + X_lo) W^T through the library's GEMM kernel (bf16: tcgen05; f32: SIMT)."""
     lib = L.load()
     M, K = x.shape
     N = w.shape[0]
@@ -212,8 +212,8 @@ def op_gemm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
     if scratch is None:
         scratch = op_gemm_scratch(M, N, K, x.dtype, x.device)
     s = torch.cuda.current_stream(x.device).cuda_stream
-    L.check("eagle_op_gemm", lib.eagle_op_gemm(dt, M, N, K, x.data_ptr(), w.data_ptr(), y.data_ptr(),
-                                               scratch.data_ptr(), scratch.numel(), s))
+    L.check("eagle_op_gemm", lib.eagle_op_gemm(dt, M, N, K, x.data_ptr(), x_lo.data_ptr() if x_lo is not None else None,
+                                               w.data_ptr(), y.data_ptr(), scratch.data_ptr(), scratch.numel(), s))
     return y
 
 
@@ -235,12 +235,13 @@ def op_lmhead_topk(x: torch.Tensor, w: torch.Tensor, k: int):
 
 
 def op_tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor, prefix: int):
-    """q [rows, Hq, hd]; k, v [Hkv, cap, hd]; mask [rows, 2] int64. Returns o [rows, Hq, hd]."""
+    """q [rows, Hq, hd] float32; k, v [Hkv, cap, hd]; mask [rows, 2] int64. Returns o [rows, Hq, hd] (k's dtype)."""
     lib = L.load()
     rows, hq, hd = q.shape
     hkv, cap, _ = k.shape
-    dt = L.DTYPE_BF16 if q.dtype == torch.bfloat16 else L.DTYPE_F32
-    o = torch.empty_like(q)
+    dt = L.DTYPE_BF16 if k.dtype == torch.bfloat16 else L.DTYPE_F32
+    q = q.float().contiguous()
+    o = torch.empty(q.shape, dtype=k.dtype, device=q.device)
     nb = lib.eagle_op_attention_scratch_bytes(rows, hq, hd, prefix)
     scratch = torch.zeros(int(nb), dtype=torch.uint8, device=q.device)
     s = torch.cuda.current_stream(q.device).cuda_stream

@@ -32,9 +32,12 @@
  *     gives a one-line description.
  *
  * Data types: EAGLE_DTYPE_F32 models keep weights, activations and the KV
- * cache in float32 (SIMT kernels); EAGLE_DTYPE_BF16 models keep them in
- * bfloat16 with float32 accumulation, float32 residual stream and float32
- * features (tcgen05 tensor-core GEMMs, mma tensor-core attention).
+ * cache in float32 (SIMT kernels). EAGLE_DTYPE_BF16 models keep weights and
+ * the KV cache in bfloat16, the residual stream, features, queries and softmax
+ * statistics in float32, and feed every GEMM and attention product with
+ * activations split into hi/lo bfloat16 pairs (x = hi + lo, two tensor-core
+ * products accumulated in float32), so activations carry ~16 significant bits
+ * (tcgen05 tensor-core GEMMs, mma tensor-core attention).
  */
 #ifndef EAGLE_H
 #define EAGLE_H
@@ -220,8 +223,10 @@ const char* eagle_last_error(const eagle_ctx* ctx);
  * and need no context.
  * ------------------------------------------------------------------------- */
 
-/* Y[M,N] (float32, row-major) = X[M,K] W[N,K]^T with the verify-pass GEMM
- * kernel for `dtype` (bf16: tcgen05 + TMA weight streaming; f32: SIMT).
+/* Y[M,N] (float32, row-major) = (X + X_lo)[M,K] W[N,K]^T with the verify-pass
+ * GEMM kernel for `dtype` (bf16: tcgen05 + TMA weight streaming; f32: SIMT).
+ * d_x_lo (bf16 only, may be NULL) holds the low halves of activations carried
+ * as hi/lo bf16 pairs, as the step's GEMMs do.
  * N multiple of 128 and K multiple of 64 for bf16; X and W 16-byte aligned.
  * d_scratch (scratch_bytes >= eagle_op_gemm_scratch_bytes(M,N,K,dtype), else
  * EAGLE_ERR_WORKSPACE) holds split-K arrival counters and partial sums; the
@@ -229,8 +234,8 @@ const char* eagle_last_error(const eagle_ctx* ctx);
  * buffer sized for the largest shape serves every smaller one. Calls that
  * share a scratch buffer must not overlap on the GPU. */
 size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtype);
-eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w,
-                           float* d_y, void* d_scratch, size_t scratch_bytes, void* stream);
+eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_x_lo,
+                           const void* d_w, float* d_y, void* d_scratch, size_t scratch_bytes, void* stream);
 
 /* The same bf16 GEMM for callers that cannot allocate device memory (for
  * example code running while someone else captures a CUDA graph, or a plugin
@@ -258,7 +263,7 @@ eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K
                                   size_t scratch_bytes, void* stream);
 
 /* Tree attention for one sequence over a KV cache slice: queries Q [rows][n_heads][hd]
- * (RoPE applied), keys/values K,V [n_kv_heads][cap][hd]; row r attends to slots
+ * (float32, RoPE applied), keys/values K,V [n_kv_heads][cap][hd] (dtype); row r attends to slots
  * [0, prefix) and to slot prefix + i of the tree block for each bit i set in
  * mask[r] (two uint64 words). Output O [rows][n_heads][hd] (dtype elements). */
 size_t eagle_op_attention_scratch_bytes(int32_t rows, int32_t n_heads, int32_t hd, int32_t prefix);

@@ -91,3 +91,77 @@ def test_8b_full_speculative_equals_vanilla(cuda):
         assert spec[i] == van[i], (i, spec[:i + 1], van[:i + 1])
     assert spec[0] == van[0]
     print("steps", stats["steps"], "mean accepted", stats["mean_accept"])
+
+
+def _lossless(eng, prompt, n, b=0):
+    """Speculative == vanilla up to the first flagged near-tie, margins from a teacher-forced chain verify."""
+    van, _ = eng.generate(prompt, n, use_graph=True, vanilla=True)
+    spec, stats = eng.generate(prompt, n, use_graph=True)
+    van, spec = van[b].cpu().numpy(), spec[b].cpu().numpy()
+    chain = OT.Tree(tokens=van[:n].astype(np.int32), parent=np.arange(-1, n - 1, dtype=np.int32),
+                    depth=np.arange(n, dtype=np.int32))
+    eng.prefill(prompt)
+    am, lg = eng.verify(tree_to_torch(chain, batch=prompt.shape[0]), logits=True)
+    margins = _margins(lg[b].cpu().numpy())
+    assert spec[0] == van[0]
+    for i in range(1, n):
+        if margins[i - 1] < 0.1:
+            break
+        assert spec[i] == van[i], (i, spec[:i + 1], van[:i + 1])
+    return van, spec, stats
+
+
+def test_8b_static_tree_lossless(cuda):
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    w = dataclasses.replace(FX.WORKLOADS["8b_static"], prompt_len=128, max_new=24)
+    eng = S.make_engine(w)
+    _lossless(eng, S.prompts(w), w.max_new)
+
+
+def test_8b_batch4_sequences_match_batch1(cuda):
+    """Batch 4 (verify GEMMs with M = 244 rows): each sequence decodes like its batch-1 run."""
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    w = dataclasses.replace(FX.WORKLOADS["8b_static_bs4"], prompt_len=256, max_new=16, kv_cap=0)
+    e4 = S.make_engine(w)
+    p4 = S.prompts(w)
+    van4, spec4, _ = _lossless(e4, p4, w.max_new, b=2)
+    out4, _ = e4.generate(p4, w.max_new, use_graph=True)
+    e1 = S.make_engine(w, batch=1, weights=e4.weights)
+    for b in (0, 3):
+        out1, _ = e1.generate(p4[b:b + 1].contiguous(), w.max_new, use_graph=True)
+        assert out1[0].tolist() == out4[b].tolist(), b
+
+
+TWO_LAYER_70B = FX.LLAMA3_70B.reduced(n_layers=2)
+
+
+def test_70b_width_two_layers_verify_parity(cuda):
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    w = dataclasses.replace(FX.WORKLOADS["70b_eagle2"], model=TWO_LAYER_70B, prompt_len=48, max_new=16)
+    cap = FX.kv_capacity(w)
+    m = OM.build_model(TWO_LAYER_70B, cap)
+    prompt = FX.prompts(TWO_LAYER_70B, 1, w.prompt_len)
+    eng = S.make_engine(w)
+    eng.prefill(torch.from_numpy(prompt).to(cuda))
+    st = OD.prefill(m, prompt[0], cap)
+    gtree = eng.draft_tree()
+    tree = tree_from_torch(gtree)
+    real = int((tree.tokens >= 0).sum())
+    otree = OT.Tree(tree.tokens[:real], tree.parent[:real], tree.depth[:real])
+    am, lg = eng.verify(gtree, logits=True)
+    oam, ofeats, ologits = OD.verify(m, st, otree)
+    got = lg[0, :real].cpu().numpy()
+    err = np.abs(got - ologits).max()
+    cos = float((got.ravel() @ ologits.ravel()) / (np.linalg.norm(got) * np.linalg.norm(ologits)))
+    assert err < 0.05 and cos >= 0.999, (err, cos)
+    g_am = am[0, :real].cpu().numpy()
+    assert not ((g_am != oam) & (_margins(ologits) >= 0.1)).any()
+
+
+def test_70b_full_lossless(cuda):
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    w = dataclasses.replace(FX.WORKLOADS["70b_eagle2"], prompt_len=128, max_new=16)
+    eng = S.make_engine(w)
+    _lossless(eng, S.prompts(w), w.max_new)
+    del eng
+    torch.cuda.empty_cache()

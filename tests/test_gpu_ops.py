@@ -134,3 +134,22 @@ def test_tree_attention_f32_tiny_heads(cuda, prefix):
 def test_tree_attention_bf16_row_counts(cuda, rows):
     o, ref = _attn_case(cuda, "bf16", rows, 8, 2, 64, 300, "random")
     assert np.abs(o - ref).max() < 2e-2
+
+
+@pytest.mark.parametrize("M,N,K", [(61, 6144, 4096), (7, 4096, 14336), (244, 1024, 2048)])
+def test_gemm_bf16_hilo_pair_is_fp32_accurate(cuda, M, N, K):
+    """Activations as hi/lo bf16 pairs: the product matches fp64 of the float input to fp32 accumulation error."""
+    from eagle_speculative_decoding_02_gb300 import op_gemm
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    w = FX.round_bf16(rng.standard_normal((N, K)).astype(np.float32) * 0.02)
+    xt = torch.from_numpy(x).to(cuda)
+    hi = xt.bfloat16()
+    lo = (xt - hi.float()).bfloat16()
+    y = op_gemm(hi, _bf16(w).to(cuda), x_lo=lo).cpu().numpy()
+    cols = rng.choice(N, size=min(N, 256), replace=False)
+    ref = x.astype(np.float64) @ w[cols].astype(np.float64).T
+    err = np.abs(y[:, cols] - ref).max() / (np.sqrt(K) * 0.02)
+    assert err < 1e-4, err
+    y_hi = op_gemm(hi, _bf16(w).to(cuda)).cpu().numpy()            # without the low halves: bf16 input error
+    err_hi = np.abs(y_hi[:, cols] - ref).max() / (np.sqrt(K) * 0.02)
+    assert err_hi > 10 * err
