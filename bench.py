@@ -114,6 +114,7 @@ def gemm_roofline(eng, m, rows: int, reps: int = 2):
     shapes = {"qkv": (m.q_dim + 2 * m.kv_dim, m.d), "o": (m.d, m.q_dim), "gu": (2 * m.ffn, m.d),
               "down": (m.d, m.ffn), "lm_head": (m.vocab, m.d)}
     xs = {k: (torch.randn(rows, K, device=dev) * 0.5).to(torch.bfloat16) for k, (N, K) in shapes.items()}
+    los = {k: (x.float() * 1e-3).to(torch.bfloat16) for k, x in xs.items()}   # hi/lo activation pairs, as in the step
     ys = {k: torch.empty(rows, N, device=dev) for k, (N, K) in shapes.items()}
     # one scratch buffer sized for the largest of the shapes serves all of them
     scr = max((op_gemm_scratch(rows, N, K, torch.bfloat16, dev) for N, K in shapes.values()),
@@ -122,17 +123,17 @@ def gemm_roofline(eng, m, rows: int, reps: int = 2):
     for lw in eng.weights.layers:
         launches += [("qkv", lw.wqkv), ("o", lw.wo), ("gu", lw.wgu), ("down", lw.wd)]
     launches.append(("lm_head", eng.weights.lm_head))
-    op_gemm(xs["qkv"], launches[0][1], ys["qkv"], scr)
+    op_gemm(xs["qkv"], launches[0][1], ys["qkv"], scr, x_lo=los["qkv"])
     torch.cuda.synchronize()
     nbytes = 0
     for k, w in launches:
         N, K = shapes[k]
-        nbytes += N * K * 2 + rows * K * 2 + rows * N * 4
+        nbytes += N * K * 2 + 2 * rows * K * 2 + rows * N * 4
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(reps):
         for k, w in launches:
-            op_gemm(xs[k], w, ys[k], scr)
+            op_gemm(xs[k], w, ys[k], scr, x_lo=los[k])
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
@@ -220,11 +221,12 @@ def profile_ops(w, reps: int = 3):
     g = torch.Generator(device=dev).manual_seed(0)
     for N, K in [(m.q_dim + 2 * m.kv_dim, m.d), (m.d, m.q_dim), (2 * m.ffn, m.d), (m.d, m.ffn), (m.vocab, m.d)]:
         x = (torch.randn(rows, K, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+        xl = (x.float() * 1e-3).to(torch.bfloat16)
         wt = (torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16)
         y = torch.empty(rows, N, device=dev)
         scr = op_gemm_scratch(rows, N, K, torch.bfloat16, dev)
         for _ in range(reps):
-            op_gemm(x, wt, y, scr)
+            op_gemm(x, wt, y, scr, x_lo=xl)
         del wt
     L = w.prompt_len + 512
     q = torch.randn(w.n_nodes + 1, m.n_heads, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
