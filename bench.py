@@ -229,9 +229,9 @@ def profile_ops(w, reps: int = 3):
             op_gemm(x, wt, y, scr, x_lo=xl)
         del wt
     L = w.prompt_len + 512
-    q = torch.randn(w.n_nodes + 1, m.n_heads, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
-    kc = torch.randn(m.n_kv_heads, L + 128, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
-    vc = torch.randn(m.n_kv_heads, L + 128, m.head_dim, device=dev, generator=g).to(torch.bfloat16)
+    q = torch.randn(w.n_nodes + 1, m.n_heads, m.head_dim, device=dev, generator=g)
+    kc = torch.randn(m.n_kv_heads, L + 128, m.head_dim, device=dev, generator=g).to(torch.float16)
+    vc = torch.randn(m.n_kv_heads, L + 128, m.head_dim, device=dev, generator=g).to(torch.float16)
     mask = torch.full((w.n_nodes + 1, 2), -1, dtype=torch.int64, device=dev)
     for _ in range(reps):
         op_tree_attention(q, kc, vc, mask, L)

@@ -82,6 +82,5 @@ cudaError_t attention_simt(const AttnArgs& a, cudaStream_t s) {
 }
 
 template cudaError_t attention_simt<float>(const AttnArgs&, cudaStream_t);
-template cudaError_t attention_simt<bf16>(const AttnArgs&, cudaStream_t);
 
 }  // namespace eg

@@ -1,4 +1,4 @@
-// Tree-masked attention on tensor cores (bf16 mma.sync m16n8k16, fp32 softmax).
+// Tree-masked attention on tensor cores (f16 mma.sync m16n8k16, fp32 softmax).
 //
 // "EAGLE (LLM decoding)", section "How EAGLE works": tree attention verifies
 // every draft node in one forward pass. A query row (node j, query head h) of
@@ -12,6 +12,9 @@
 // its K and V chunks in shared memory once with cp.async (V fragments are read
 // transposed with ldmatrix.trans); each of its 4 warps runs one 16-row tile with
 // an online softmax and writes an unnormalised partial (max, sum, O).
+// The KV cache of a bf16 model holds IEEE half values; q (float32) and the
+// probabilities P enter the products rounded to half, so both MMAs are
+// f16 x f16 with fp32 accumulation.
 // attn_merge combines the partials of a row in chunk order.
 // Chunk boundaries are absolute slot multiples of 128, independent of how many
 // rows are verified.
@@ -24,26 +27,26 @@ namespace {
 
 constexpr int kCK = 128;   // keys per chunk
 constexpr int kMaxGroupRows = 128;  // rows of one group (tree rows, or one 128-row prefill block)
-constexpr int kPad = 8;    // bf16 padding per shared-memory row (rows 16-byte aligned, conflict-free)
+constexpr int kPad = 8;    // half padding per shared-memory row (rows 16-byte aligned, conflict-free)
 constexpr int kAttnThreads = 128;  // 4 warps, one 16-row tile each
 constexpr int kRowBlock = 64;      // GQA rows (node x query head) per CTA
 
-__device__ __forceinline__ uint32_t ld_b32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
+using half = __half;
+
+__device__ __forceinline__ uint32_t ld_b32(const half* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// (lo, hi) floats -> packed bf16x2 high parts and packed bf16x2 residuals.
-__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
+// Two floats -> packed half2 (x in the low half).
+__device__ __forceinline__ uint32_t pack_half2(float x, float y) {
+  const __half2 h = __floats2half2_rn(x, y);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __host__ __device__ __forceinline__ int n_prefix_chunks(int prefix) { return (prefix + kCK - 1) / kCK; }
@@ -56,7 +59,7 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src
 }
 
 // Four 8x8 b16 matrices, transposed, from shared memory (one row address per lane).
-__device__ __forceinline__ void ldsm_x4_trans(const bf16* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+__device__ __forceinline__ void ldsm_x4_trans(const half* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
@@ -65,8 +68,8 @@ __device__ __forceinline__ void ldsm_x4_trans(const bf16* p, uint32_t& r0, uint3
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n_chunk_slots) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  bf16* Ks = reinterpret_cast<bf16*>(smem_raw);                 // [kCK][HD + kPad]
-  bf16* Vs = Ks + kCK * (HD + kPad);                            // [kCK][HD + kPad]
+  half* Ks = reinterpret_cast<half*>(smem_raw);                 // [kCK][HD + kPad]
+  half* Vs = Ks + kCK * (HD + kPad);                            // [kCK][HD + kPad]
   // programmatic dependent launch: every CTA waits for the producer of q / K / V before any read
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -85,9 +88,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
 
   // stage K and V of the chunk (row-major) with asynchronous 16-byte copies, all
   // in flight at once; keys past nkeys are zero-filled
-  const bf16* Kg = reinterpret_cast<const bf16*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
-  const bf16* Vg = reinterpret_cast<const bf16*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
-  constexpr int VEC = 8;  // bf16 per 16-byte vector
+  const half* Kg = reinterpret_cast<const half*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
+  const half* Vg = reinterpret_cast<const half*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
+  constexpr int VEC = 8;  // halves per 16-byte vector
   for (int e = tid; e < kCK * HD / VEC; e += kAttnThreads) {
     const int key = e / (HD / VEC), d0 = (e % (HD / VEC)) * VEC;
     const int n = key < nkeys ? 16 : 0;
@@ -115,8 +118,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
       mk0[i] = block && rv[i] ? a.mask[2 * row] : 0ull;
       mk1[i] = block && rv[i] ? a.mask[2 * row + 1] : 0ull;
     }
-    // q (float32) as a hi/lo pair of bf16 A fragments: S = Q_hi K^T + Q_lo K^T
-    uint32_t qa[HD / 16][4], ql[HD / 16][4];
+    // q (float32) times the softmax scale in log2 units, rounded to half A fragments
+    uint32_t qa[HD / 16][4];
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
@@ -124,8 +127,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
         const float* qp = a.q + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
         const float2 x0 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + qi * 2) : make_float2(0.f, 0.f);
         const float2 x1 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + 8 + qi * 2) : make_float2(0.f, 0.f);
-        split_bf16x2(x0.x, x0.y, qa[kk][i], ql[kk][i]);
-        split_bf16x2(x1.x, x1.y, qa[kk][i + 2], ql[kk][i + 2]);
+        qa[kk][i] = pack_half2(x0.x * sl2, x0.y * sl2);
+        qa[kk][i + 2] = pack_half2(x1.x * sl2, x1.y * sl2);
       }
     }
     float o[HD / 8][4];
@@ -141,13 +144,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
       for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
-          const bf16* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
-          const uint32_t k0 = ld_b32(kp), k1 = ld_b32(kp + 8);
-          mma16816(s[nt], qa[kk], k0, k1);
-          mma16816(s[nt], ql[kk], k0, k1);
+          const half* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
+          mma16816(s[nt], qa[kk], ld_b32(kp), ld_b32(kp + 8));
         }
       }
-      // mask and scale; c-fragment (row quad (+8), key kb + nt*8 + qi*2 + {0,1})
+      // mask; c-fragment (row quad (+8), key kb + nt*8 + qi*2 + {0,1})
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
           const int key = kb + nt * 8 + qi * 2 + (e & 1);
           bool vis = key < nkeys && rv[i];
           if (block && vis) vis = ((key < 64 ? (mk0[i] >> key) : (mk1[i] >> (key - 64))) & 1ull) != 0;
-          s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
+          s[nt][e] = vis ? s[nt][e] : -INFINITY;
           mx[i] = fmaxf(mx[i], s[nt][e]);
         }
       }
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
         mrow[i] = mn;
       }
       float sum[2] = {0.f, 0.f};
-      uint32_t pa[4][4], pl[4][4];  // P as a hi/lo pair of bf16 A fragments
+      uint32_t pa[4][4];  // P as half A fragments
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
         }
         // P as the A operand of P.V: keys 16*kk2 .. of this 64-key block
         const int kk2 = nt >> 1, hi = nt & 1;
-        split_bf16x2(s[nt][0], s[nt][1], pa[kk2][0 + 2 * hi], pl[kk2][0 + 2 * hi]);
-        split_bf16x2(s[nt][2], s[nt][3], pa[kk2][1 + 2 * hi], pl[kk2][1 + 2 * hi]);
+        pa[kk2][0 + 2 * hi] = pack_half2(s[nt][0], s[nt][1]);
+        pa[kk2][1 + 2 * hi] = pack_half2(s[nt][2], s[nt][3]);
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -206,13 +207,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n
 #pragma unroll
         for (int dt = 0; dt < HD / 8; dt += 2) {
           const int key = kb + kk2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-          const bf16* vp = Vs + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
+          const half* vp = Vs + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4_trans(vp, b0, b1, b2, b3);
           mma16816(o[dt], pa[kk2], b0, b1);
-          mma16816(o[dt], pl[kk2], b0, b1);
           mma16816(o[dt + 1], pa[kk2], b2, b3);
-          mma16816(o[dt + 1], pl[kk2], b2, b3);
         }
       }
     }

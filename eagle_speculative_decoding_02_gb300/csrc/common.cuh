@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace eg {
@@ -33,6 +34,18 @@ __device__ __forceinline__ void store_hilo(T* hi, bf16* lo, size_t at, float v) 
   const T h = from_f<T>(v);
   hi[at] = h;
   if (lo) lo[at] = __float2bfloat16_rn(v - to_f(h));
+}
+
+// KV-cache element type: the model dtype for float32 models; IEEE half for bf16
+// models (11-bit significand, 8x finer than bf16, at the same two bytes; the
+// attention products then run as f16 MMAs). Stores saturate at the half range;
+// NaN passes through.
+template <typename T> struct KvOf { using type = T; };
+template <> struct KvOf<bf16> { using type = __half; };
+template <typename T> __device__ __forceinline__ typename KvOf<T>::type kv_from_f(float v);
+template <> __device__ __forceinline__ float kv_from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half kv_from_f<bf16>(float v) {
+  return __float2half_rn(v > 65504.f ? 65504.f : (v < -65504.f ? -65504.f : v));
 }
 
 __device__ __forceinline__ void set_status(int* status, int code) {
@@ -83,7 +96,7 @@ struct EpiParams {
   int q_dim = 0, kv_dim = 0, head_dim = 0, n_kv = 0, cap = 0;
   const float* rope_cos = nullptr;  // [positions][head_dim/2]
   const float* rope_sin = nullptr;
-  void* kc = nullptr;       // layer cache base [B][n_kv][cap][head_dim]
+  void* kc = nullptr;       // layer cache base [B][n_kv][cap][head_dim], KvOf<T> elements
   void* vc = nullptr;
   Rows rows{};
   // kEpiSwiglu
@@ -100,6 +113,30 @@ struct EpiParams {
   float* rec_max = nullptr; // [ntiles][M]
   float* rec_sum = nullptr; // [ntiles][M] sum exp(logit - tile max)
 };
+
+// Programmatic dependent launch. A kernel launched with launch_pdl may start
+// while its predecessor is still running; it must call pdl_wait() before it
+// reads or writes anything the predecessor touches (every kernel here does so
+// first thing), which makes ordering identical to a plain launch while the
+// launch latency overlaps the predecessor's tail.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Barriers for code shared by whole-block and warp-specialised kernels.
 struct BlockSync {

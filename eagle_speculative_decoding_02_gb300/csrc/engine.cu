@@ -37,15 +37,15 @@ struct LayerPtrs {
 
 // Host-derived sizes of a configuration.
 struct Dims {
-  int B, d, Hq, Hkv, hd, ffn, V, Lyr, cap, cap_d, P_max, out_cap;
-  int qd, kvd, nqkv;
-  int mode, NR, D, D1, k, S, n_nodes;
+  int B = 0, d = 0, Hq = 0, Hkv = 0, hd = 0, ffn = 0, V = 0, Lyr = 0, cap = 0, cap_d = 0, P_max = 0, out_cap = 0;
+  int qd = 0, kvd = 0, nqkv = 0;
+  int mode = 0, NR = 0, D = 0, D1 = 0, k = 0, S = 0, n_nodes = 0;
   std::vector<int> level_rows;  // rows per sequence of the depth-t draft forward, t = 1..D-1 (index t)
   std::vector<int> level_base;  // absolute first row of level t in the draft buffers (index t)
-  int R_d;                      // total draft rows
-  int CL;                       // prefill chunk length per sequence
-  int M_tgt, M_dft, M_max, M_lm, n_groups_max, ntV, pool_cap;
-  bool bf16;
+  int R_d = 0;                      // total draft rows
+  int CL = 0;                       // prefill chunk length per sequence
+  int M_tgt = 0, M_dft = 0, M_max = 0, M_lm = 0, n_groups_max = 0, ntV = 0, pool_cap = 0;
+  bool bf16 = false;
   // static topology (host)
   std::vector<int> s_parent, s_rank, s_depth, s_lrow, s_sidx, s_level_nodes, s_level_count;
   std::vector<uint64_t> s_smask, s_anc;
@@ -510,7 +510,8 @@ struct Eng {
   static eagle_status accept(eagle_ctx* c, int* acc_out, int* tok_out) {
     const Dims& dm = c->dm;
     EG_CK(accept_commit(c->st, c->last_tree, c->vargmax, c->h_tgt, acc_out, tok_out, c->stream));
-    EG_CK(compact_kv<T>(c->st, (T*)c->kc, (T*)c->vc, dm.Lyr, dm.Hkv, dm.hd, c->stream));
+    using KvT = typename KvOf<T>::type;
+    EG_CK(compact_kv<KvT>(c->st, (KvT*)c->kc, (KvT*)c->vc, dm.Lyr, dm.Hkv, dm.hd, c->stream));
     return EAGLE_OK;
   }
 };

@@ -100,7 +100,8 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
               reinterpret_cast<float*>(p.out)[(size_t)(m0 + m) * p.q_dim + n] = v;
             } else if (rslot[m] >= 0) {
               const size_t at = (((size_t)rseq[m] * p.n_kv + kvh) * p.cap + rslot[m]) * hd + i;
-              reinterpret_cast<T*>(region == 1 ? p.kc : p.vc)[at] = from_f<T>(v);
+              using KvT = typename KvOf<T>::type;
+              reinterpret_cast<KvT*>(region == 1 ? p.kc : p.vc)[at] = kv_from_f<T>(v);
             }
           }
         }

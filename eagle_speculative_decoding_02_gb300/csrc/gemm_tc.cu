@@ -417,6 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       u = (long long)(t + 1) * kbt;
     }
   }
+  // warps 0 and 1 ran their role on lane 0 only: reconverge each warp before the
+  // block barrier and the warp-wide (.sync.aligned) TMEM dealloc
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

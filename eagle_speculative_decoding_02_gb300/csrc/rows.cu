@@ -20,6 +20,8 @@ template <typename T>
 __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ E, const int* __restrict__ tok, int M,
                                                     int d, const float* __restrict__ gain, float* h, T* hb,
                                                     bf16* hb_lo, float* ssq) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[4];
   const int m = blockIdx.x;
   const int t = tok[m];
@@ -41,6 +43,8 @@ __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ E, con
 template <typename T>
 __global__ void fc_input_kernel(const float* __restrict__ feat, const int* __restrict__ fsrc,
                                 const T* __restrict__ E, const int* __restrict__ tok, int d, T* x, bf16* x_lo) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   const float* f = feat + (size_t)fsrc[m] * d;
   const T* e = E + (size_t)tok[m] * d;
@@ -57,6 +61,8 @@ template <typename T>
 __global__ void gather_rows_kernel(const T* __restrict__ hb, const bf16* __restrict__ hb_lo,
                                    const float* __restrict__ ssq, int M_src, const int* __restrict__ src, int n_rows,
                                    int d, T* hb_dst, bf16* lo_dst, float* ssq_dst) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const int r = src[i];
   for (int n = threadIdx.x; n < d; n += blockDim.x) {
@@ -73,6 +79,8 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const float* __restrict
                                                          const float* __restrict__ rec_max,
                                                          const float* __restrict__ rec_sum, int ntiles, int M, int k,
                                                          int* out_idx, float* out_val, float* out_lse) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[4];
   __shared__ float sv[4];
   __shared__ int si[4];
@@ -162,31 +170,27 @@ template <typename T>
 cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* gain, float* h, T* hb, bf16* hb_lo,
                        float* ssq, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  embed_kernel<T><<<M, 128, 0, s>>>(E, tok, M, d, gain, h, hb, hb_lo, ssq);
-  return cudaGetLastError();
+  return launch_pdl(embed_kernel<T>, dim3(M), dim3(128), 0, s, E, tok, M, d, gain, h, hb, hb_lo, ssq);
 }
 
 template <typename T>
 cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x, bf16* x_lo,
                      cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  fc_input_kernel<T><<<M, 256, 0, s>>>(feat, fsrc, E, tok, d, x, x_lo);
-  return cudaGetLastError();
+  return launch_pdl(fc_input_kernel<T>, dim3(M), dim3(256), 0, s, feat, fsrc, E, tok, d, x, x_lo);
 }
 
 template <typename T>
 cudaError_t gather_rows(const T* hb, const bf16* hb_lo, const float* ssq, int M_src, const int* src, int n, int d,
                         T* hb_dst, bf16* lo_dst, float* ssq_dst, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  gather_rows_kernel<T><<<n, 256, 0, s>>>(hb, hb_lo, ssq, M_src, src, n, d, hb_dst, lo_dst, ssq_dst);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel<T>, dim3(n), dim3(256), 0, s, hb, hb_lo, ssq, M_src, src, n, d, hb_dst, lo_dst, ssq_dst);
 }
 
 cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* rec_max, const float* rec_sum,
                        int ntiles, int M, int k, int* idx, float* val, float* lse, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  topk_merge_kernel<<<M, 128, 0, s>>>(rec_val, rec_idx, rec_max, rec_sum, ntiles, M, k, idx, val, lse);
-  return cudaGetLastError();
+  return launch_pdl(topk_merge_kernel, dim3(M), dim3(128), 0, s, rec_val, rec_idx, rec_max, rec_sum, ntiles, M, k, idx, val, lse);
 }
 
 #define EG_INST(T)                                                                                          \

@@ -22,6 +22,8 @@ __device__ __forceinline__ void causal_mask(int i, uint64_t* m) {
 // skip the last prompt position, whose next token is not known yet.
 __global__ void setup_prefill_kernel(const int* __restrict__ prompt, int P, int c0, int CL, int B, int draft,
                                      Rows rows, Group* groups) {
+  pdl_wait();
+  pdl_trigger();
   const int G = (CL + 127) / 128;
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m < B * CL) {
@@ -57,6 +59,8 @@ __global__ void setup_prefill_kernel(const int* __restrict__ prompt, int P, int 
 
 // Catch-up rows of the draft head: per sequence D1 rows, the first c valid.
 __global__ void setup_catchup_kernel(State st, Rows rows, Group* groups) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, i = threadIdx.x;
   const int L = st.L[b], c = st.c[b];
   if (i < st.D1) {
@@ -88,6 +92,8 @@ __global__ void setup_catchup_kernel(State st, Rows rows, Group* groups) {
 
 // Verify rows: tree row j of sequence b at position L + depth(j), KV slot L + j.
 __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* groups) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int NR = tree.n_rows;
   const int L = st.L[b];
@@ -119,6 +125,8 @@ __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* gr
 // After the last prefill chunk: first new token per sequence and the initial state.
 __global__ void prefill_finish_kernel(State st, const int* __restrict__ root_idx, const float* __restrict__ h_tgt,
                                       int CL, int P, int* root_out) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int root = root_idx[b];
   const float* f = h_tgt + ((size_t)b * CL + CL - 1) * st.d;
@@ -137,6 +145,8 @@ __global__ void prefill_finish_kernel(State st, const int* __restrict__ root_idx
 }
 
 __global__ void set_root_tree_kernel(State st, TreeOut tree) {
+  pdl_wait();
+  pdl_trigger();
   const int b = threadIdx.x;
   if (b < st.B) {
     const int m = b * tree.n_rows;
@@ -152,6 +162,8 @@ __global__ void set_root_tree_kernel(State st, TreeOut tree) {
 __global__ void static_level_kernel(State st, StaticTopo topo, int t, const int* __restrict__ topk_idx,
                                     Level catchup, Level prev, Level next, TreeOut tree, Rows rows,
                                     Group* groups, int S) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int NR = topo.n_rows;
   const int L = st.L[b], c = st.c[b];
@@ -236,6 +248,8 @@ __global__ void __launch_bounds__(256) eagle2_level_kernel(State st, Pool pool, 
                                                            const float* __restrict__ lse, Level catchup,
                                                            Level prev, Level next, Rows rows, Group* groups,
                                                            int S) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned long long key[128];
   __shared__ int val[128];
   __shared__ int s_first, s_n;
@@ -351,6 +365,8 @@ __global__ void __launch_bounds__(256) eagle2_level_kernel(State st, Pool pool, 
 }
 
 __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, int n_nodes, TreeOut tree) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned long long key[kPoolSort];
   __shared__ int val[kPoolSort];
   __shared__ int tpos[kPoolSort];  // pool index -> tree row (0 = not selected)
@@ -425,6 +441,8 @@ __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, 
 __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, const int* __restrict__ amax,
                                                      const float* __restrict__ h_verify, int* acc_out,
                                                      int* tok_out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int path[kMaxDepth + 1];
   __shared__ int s_a, s_bonus;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -496,6 +514,8 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
 // because a destination slot can be another accepted row's source.
 template <typename T>
 __global__ void compact_kernel(State st, T* kc, T* vc, int n_kv, int hd) {
+  pdl_wait();
+  pdl_trigger();
   const int l = blockIdx.x, b = blockIdx.y, kvh = blockIdx.z, i = threadIdx.x;
   const int a = st.acc_len[b];
   if (a == 0 || i >= hd) return;
@@ -521,6 +541,8 @@ __global__ void compact_kernel(State st, T* kc, T* vc, int n_kv, int hd) {
 }
 
 __global__ void copy_out_kernel(State st, int max_new, int* d_out) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < max_new; i += blockDim.x)
     d_out[(size_t)b * max_new + i] = i < st.n_out[b] ? st.out[(size_t)b * st.out_cap + i] : -1;
@@ -531,69 +553,58 @@ __global__ void copy_out_kernel(State st, int max_new, int* d_out) {
 cudaError_t setup_prefill_rows(const int* prompt, int P, int c0, int CL, int B, bool draft, Rows rows,
                                Group* groups, cudaStream_t s) {
   const int n = B * CL;
-  setup_prefill_kernel<<<(n + 127) / 128, 128, 0, s>>>(prompt, P, c0, CL, B, draft ? 1 : 0, rows, groups);
-  return cudaGetLastError();
+  return launch_pdl(setup_prefill_kernel, dim3((n + 127) / 128), dim3(128), 0, s, prompt, P, c0, CL, B, draft ? 1 : 0, rows, groups);
 }
 
 cudaError_t setup_catchup_rows(State st, Rows rows, Group* groups, cudaStream_t s) {
-  setup_catchup_kernel<<<st.B, 32, 0, s>>>(st, rows, groups);
-  return cudaGetLastError();
+  return launch_pdl(setup_catchup_kernel, dim3(st.B), dim3(32), 0, s, st, rows, groups);
 }
 
 cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, cudaStream_t s) {
-  setup_verify_kernel<<<st.B, 128, 0, s>>>(st, tree, rows, groups);
-  return cudaGetLastError();
+  return launch_pdl(setup_verify_kernel, dim3(st.B), dim3(128), 0, s, st, tree, rows, groups);
 }
 
 cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, int CL, int P, int* root_out,
                            cudaStream_t s) {
-  prefill_finish_kernel<<<st.B, 256, 0, s>>>(st, root_idx, h_tgt, CL, P, root_out);
-  return cudaGetLastError();
+  return launch_pdl(prefill_finish_kernel, dim3(st.B), dim3(256), 0, s, st, root_idx, h_tgt, CL, P, root_out);
 }
 
 cudaError_t set_root_tree(State st, TreeOut tree, cudaStream_t s) {
-  set_root_tree_kernel<<<1, 64, 0, s>>>(st, tree);
-  return cudaGetLastError();
+  return launch_pdl(set_root_tree_kernel, dim3(1), dim3(64), 0, s, st, tree);
 }
 
 cudaError_t static_level(State st, StaticTopo topo, int t, const int* topk_idx, Level catchup, Level prev,
                          Level next, TreeOut tree, Rows rows, Group* groups, int S, cudaStream_t s) {
-  static_level_kernel<<<st.B, 128, 0, s>>>(st, topo, t, topk_idx, catchup, prev, next, tree, rows, groups, S);
-  return cudaGetLastError();
+  return launch_pdl(static_level_kernel, dim3(st.B), dim3(128), 0, s, st, topo, t, topk_idx, catchup, prev, next, tree, rows, groups, S);
 }
 
 cudaError_t eagle2_level(State st, Pool pool, int t, int depth, int k, float ln_tau, const int* topk_idx,
                          const float* topk_val, const float* lse, Level catchup, Level prev, Level next,
                          Rows rows, Group* groups, int S, cudaStream_t s) {
   if (k > 11 || k < 1) return cudaErrorInvalidValue;
-  eagle2_level_kernel<<<st.B, 256, 0, s>>>(st, pool, t, depth, k, ln_tau, topk_idx, topk_val, lse, catchup, prev,
+  return launch_pdl(eagle2_level_kernel, dim3(st.B), dim3(256), 0, s, st, pool, t, depth, k, ln_tau, topk_idx, topk_val, lse, catchup, prev,
                                            next, rows, groups, S);
-  return cudaGetLastError();
 }
 
 cudaError_t eagle2_final(State st, Pool pool, int n_nodes, TreeOut tree, cudaStream_t s) {
-  eagle2_final_kernel<<<st.B, 256, 0, s>>>(st, pool, n_nodes, tree);
-  return cudaGetLastError();
+  return launch_pdl(eagle2_final_kernel, dim3(st.B), dim3(256), 0, s, st, pool, n_nodes, tree);
 }
 
 cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, int* acc_out,
                           int* tok_out, cudaStream_t s) {
-  accept_kernel<<<st.B, 256, 0, s>>>(st, tree, amax, h_verify, acc_out, tok_out);
-  return cudaGetLastError();
+  return launch_pdl(accept_kernel, dim3(st.B), dim3(256), 0, s, st, tree, amax, h_verify, acc_out, tok_out);
 }
 
 template <typename T>
 cudaError_t compact_kv(State st, T* kc, T* vc, int n_layers, int n_kv, int hd, cudaStream_t s) {
   dim3 grid(n_layers, st.B, n_kv);
-  compact_kernel<T><<<grid, hd, 0, s>>>(st, kc, vc, n_kv, hd);
-  return cudaGetLastError();
+  return launch_pdl(compact_kernel<T>, dim3(grid), dim3(hd), 0, s, st, kc, vc, n_kv, hd);
 }
 template cudaError_t compact_kv<float>(State, float*, float*, int, int, int, cudaStream_t);
-template cudaError_t compact_kv<bf16>(State, bf16*, bf16*, int, int, int, cudaStream_t);
+template cudaError_t compact_kv<__half>(State, __half*, __half*, int, int, int, cudaStream_t);
 
 cudaError_t copy_out(State st, int max_new, int* d_out, cudaStream_t s) {
-  copy_out_kernel<<<st.B, 256, 0, s>>>(st, max_new, d_out);
-  return cudaGetLastError();
+  return launch_pdl(copy_out_kernel, dim3(st.B), dim3(256), 0, s, st, max_new, d_out);
 }
 
 }  // namespace eg

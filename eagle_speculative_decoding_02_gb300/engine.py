@@ -235,13 +235,16 @@ def op_lmhead_topk(x: torch.Tensor, w: torch.Tensor, k: int):
 
 
 def op_tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor, prefix: int):
-    """q [rows, Hq, hd] float32; k, v [Hkv, cap, hd]; mask [rows, 2] int64. Returns o [rows, Hq, hd] (k's dtype)."""
+    """q [rows, Hq, hd] float32; k, v [Hkv, cap, hd] float16 (bf16 models' cache) or float32; mask [rows, 2]
+    int64. Returns o [rows, Hq, hd]: bfloat16 for a float16 cache, else float32."""
     lib = L.load()
     rows, hq, hd = q.shape
     hkv, cap, _ = k.shape
-    dt = L.DTYPE_BF16 if k.dtype == torch.bfloat16 else L.DTYPE_F32
+    if k.dtype != v.dtype or k.dtype not in (torch.float16, torch.float32):
+        raise TypeError("k and v must both be float16 (bf16 model) or float32")
+    dt = L.DTYPE_BF16 if k.dtype == torch.float16 else L.DTYPE_F32
     q = q.float().contiguous()
-    o = torch.empty(q.shape, dtype=k.dtype, device=q.device)
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if dt == L.DTYPE_BF16 else torch.float32, device=q.device)
     nb = lib.eagle_op_attention_scratch_bytes(rows, hq, hd, prefix)
     scratch = torch.zeros(int(nb), dtype=torch.uint8, device=q.device)
     s = torch.cuda.current_stream(q.device).cuda_stream

@@ -32,12 +32,14 @@
  *     gives a one-line description.
  *
  * Data types: EAGLE_DTYPE_F32 models keep weights, activations and the KV
- * cache in float32 (SIMT kernels). EAGLE_DTYPE_BF16 models keep weights and
- * the KV cache in bfloat16, the residual stream, features, queries and softmax
- * statistics in float32, and feed every GEMM and attention product with
- * activations split into hi/lo bfloat16 pairs (x = hi + lo, two tensor-core
- * products accumulated in float32), so activations carry ~16 significant bits
- * (tcgen05 tensor-core GEMMs, mma tensor-core attention).
+ * cache in float32 (SIMT kernels). EAGLE_DTYPE_BF16 models keep weights in
+ * bfloat16, the KV cache in IEEE half (11-bit significand at two bytes;
+ * stores saturate at +-65504), the residual stream, features, queries and
+ * softmax statistics in float32, and feed every GEMM with activations split
+ * into hi/lo bfloat16 pairs (x = hi + lo, two tensor-core products accumulated
+ * in float32), so GEMM inputs carry ~16 significant bits (tcgen05 tensor-core
+ * GEMMs). Attention products are half x half with float32 accumulation (mma
+ * tensor-core attention).
  */
 #ifndef EAGLE_H
 #define EAGLE_H
@@ -263,7 +265,8 @@ eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K
                                   size_t scratch_bytes, void* stream);
 
 /* Tree attention for one sequence over a KV cache slice: queries Q [rows][n_heads][hd]
- * (float32, RoPE applied), keys/values K,V [n_kv_heads][cap][hd] (dtype); row r attends to slots
+ * (float32, RoPE applied), keys/values K,V [n_kv_heads][cap][hd] (the KV-cache type of dtype:
+ * float32 for EAGLE_DTYPE_F32, IEEE half for EAGLE_DTYPE_BF16); row r attends to slots
  * [0, prefix) and to slot prefix + i of the tree block for each bit i set in
  * mask[r] (two uint64 words). Output O [rows][n_heads][hd] (dtype elements). */
 size_t eagle_op_attention_scratch_bytes(int32_t rows, int32_t n_heads, int32_t hd, int32_t prefix);

@@ -110,9 +110,11 @@ def _attn_case(cuda, dt, rows, hq, hkv, hd, prefix, shape):
         bits = [i for i in range(rows) if (int(masks[r, i // 64]) >> (i % 64)) & 1]
         vis.append(np.concatenate([np.arange(prefix), prefix + np.array(bits)]).astype(np.int64))
     ref = OC.attention_rows(q, k.transpose(1, 0, 2), v.transpose(1, 0, 2), vis).reshape(rows, hq, hd)
-    T = (lambda a: _bf16(a).to(cuda)) if dt == "bf16" else (lambda a: torch.from_numpy(a).to(cuda))
+    # a bf16 model's cache holds half values: the bf16-rounded inputs are exact in half
+    T = (lambda a: _bf16(a).to(torch.float16).to(cuda)) if dt == "bf16" else (lambda a: torch.from_numpy(a).to(cuda))
     from eagle_speculative_decoding_02_gb300 import op_tree_attention
-    o = op_tree_attention(T(q), T(k), T(v), torch.from_numpy(masks.view(np.int64)).to(cuda), prefix)
+    o = op_tree_attention(torch.from_numpy(q).to(cuda), T(k), T(v), torch.from_numpy(masks.view(np.int64)).to(cuda),
+                          prefix)
     return o.float().cpu().numpy(), ref
 
 
