@@ -1,280 +1,38 @@
-// Tree-masked attention on tensor cores (f16 mma.sync m16n8k16, fp32 softmax).
-//
-// "EAGLE (LLM decoding)", section "How EAGLE works": tree attention verifies
-// every draft node in one forward pass. A query row (node j, query head h) of
-// group g sees the prefix slots [0, prefix) and the slots prefix + i of the
-// tree block whose bit i is set in node j's ancestor mask.
-//
-// Split-K flash decode: CTA (chunk c, KV head and 64-row block, group) takes
-// either prefix keys [128 c, 128 c + 128) or, for c == ceil(prefix / 128), the
-// tree block, and 64 of the group's rows x G = Hq / Hkv query heads sharing
-// that KV head (the GQA rows form the M dimension of the MMA). Each CTA stages
-// its K and V chunks in shared memory once with cp.async (V fragments are read
-// transposed with ldmatrix.trans); each of its 4 warps runs one 16-row tile with
-// an online softmax and writes an unnormalised partial (max, sum, O).
-// The KV cache of a bf16 model holds IEEE half values; q (float32) and the
-// probabilities P enter the products rounded to half, so both MMAs are
-// f16 x f16 with fp32 accumulation.
-// attn_merge combines the partials of a row in chunk order.
-// Chunk boundaries are absolute slot multiples of 128, independent of how many
-// rows are verified.
-#include <cmath>
-
-#include "kernels.h"
+// Standalone tree-attention kernels (one work item per CTA, then a merge
+// kernel); the bodies live in attention_tc.cuh.
+#include "attention_tc.cuh"
 
 namespace eg {
 namespace {
 
-constexpr int kCK = 128;   // keys per chunk
-constexpr int kMaxGroupRows = 128;  // rows of one group (tree rows, or one 128-row prefill block)
-constexpr int kPad = 8;    // half padding per shared-memory row (rows 16-byte aligned, conflict-free)
-constexpr int kAttnThreads = 128;  // 4 warps, one 16-row tile each
-constexpr int kRowBlock = 64;      // GQA rows (node x query head) per CTA
-
-using half = __half;
-
-__device__ __forceinline__ uint32_t ld_b32(const half* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Two floats -> packed half2 (x in the low half).
-__device__ __forceinline__ uint32_t pack_half2(float x, float y) {
-  const __half2 h = __floats2half2_rn(x, y);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__host__ __device__ __forceinline__ int n_prefix_chunks(int prefix) { return (prefix + kCK - 1) / kCK; }
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
-               "l"(gmem), "r"(src_bytes)
-               : "memory");
-}
-
-// Four 8x8 b16 matrices, transposed, from shared memory (one row address per lane).
-__device__ __forceinline__ void ldsm_x4_trans(const half* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
-}
+using namespace attn;
+// Keys per chunk: the same as the persistent layer-stack kernel's, so that both
+// paths sum every attention output in the same order (bit-identical rows).
+constexpr int kCK = 64;
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n_chunk_slots) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  half* Ks = reinterpret_cast<half*>(smem_raw);                 // [kCK][HD + kPad]
-  half* Vs = Ks + kCK * (HD + kPad);                            // [kCK][HD + kPad]
+  half* Ks = reinterpret_cast<half*>(smem_raw);  // [kCK][HD + kPad]
+  half* Vs = Ks + kCK * (HD + kPad);             // [kCK][HD + kPad]
   // programmatic dependent launch: every CTA waits for the producer of q / K / V before any read
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const Group g = a.groups[blockIdx.z];
-  const int rb_count = (kMaxGroupRows * (a.Hq / a.Hkv) + kRowBlock - 1) / kRowBlock;
-  const int kvh = blockIdx.y / rb_count, rb = blockIdx.y % rb_count;
-  const int chunk = blockIdx.x;
-  const int nck = n_prefix_chunks(g.prefix);
-  const bool block = chunk == nck;
-  if (chunk > nck || (block && g.block_len <= 0) || rb * kRowBlock >= g.nrows * (a.Hq / a.Hkv)) return;
-  const int key0 = block ? g.prefix : chunk * kCK;
-  const int nkeys = block ? g.block_len : min(kCK, g.prefix - key0);
-  const int G = a.Hq / a.Hkv;
-  const int R = g.nrows * G;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // stage K and V of the chunk (row-major) with asynchronous 16-byte copies, all
-  // in flight at once; keys past nkeys are zero-filled
-  const half* Kg = reinterpret_cast<const half*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
-  const half* Vg = reinterpret_cast<const half*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
-  constexpr int VEC = 8;  // halves per 16-byte vector
-  for (int e = tid; e < kCK * HD / VEC; e += kAttnThreads) {
-    const int key = e / (HD / VEC), d0 = (e % (HD / VEC)) * VEC;
-    const int n = key < nkeys ? 16 : 0;
-    const size_t go = (size_t)min(key, nkeys - 1) * HD + d0;
-    cp_async16(Ks + key * (HD + kPad) + d0, Kg + go, n);
-    cp_async16(Vs + key * (HD + kPad) + d0, Vg + go, n);
-  }
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-
-  const float sl2 = a.scale * 1.4426950408889634f;  // scores in log2 units
-  const int quad = lane >> 2, qi = lane & 3;
-  for (int mt = rb * (kRowBlock / 16) + warp; mt * 16 < R && mt < (rb + 1) * (kRowBlock / 16); mt += kAttnThreads / 32) {
-    // rows r0 = mt*16 + quad and r1 = r0 + 8 of this tile: (node, head) = (r / G, r % G)
-    int node[2], qh[2];
-    bool rv[2];
-    uint64_t mk0[2], mk1[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int r = mt * 16 + quad + 8 * i;
-      rv[i] = r < R;
-      node[i] = rv[i] ? r / G : 0;
-      qh[i] = kvh * G + (rv[i] ? r % G : 0);
-      const int row = g.row0 + node[i];
-      mk0[i] = block && rv[i] ? a.mask[2 * row] : 0ull;
-      mk1[i] = block && rv[i] ? a.mask[2 * row + 1] : 0ull;
-    }
-    // q (float32) times the softmax scale in log2 units, rounded to half A fragments
-    uint32_t qa[HD / 16][4];
-#pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float* qp = a.q + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
-        const float2 x0 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + qi * 2) : make_float2(0.f, 0.f);
-        const float2 x1 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + 8 + qi * 2) : make_float2(0.f, 0.f);
-        qa[kk][i] = pack_half2(x0.x * sl2, x0.y * sl2);
-        qa[kk][i + 2] = pack_half2(x1.x * sl2, x1.y * sl2);
-      }
-    }
-    float o[HD / 8][4];
-#pragma unroll
-    for (int dt = 0; dt < HD / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-    for (int kb = 0; kb < nkeys; kb += 64) {
-      float s[8][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const half* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
-          mma16816(s[nt], qa[kk], ld_b32(kp), ld_b32(kp + 8));
-        }
-      }
-      // mask; c-fragment (row quad (+8), key kb + nt*8 + qi*2 + {0,1})
-      float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = e >> 1;
-          const int key = kb + nt * 8 + qi * 2 + (e & 1);
-          bool vis = key < nkeys && rv[i];
-          if (block && vis) vis = ((key < 64 ? (mk0[i] >> key) : (mk1[i] >> (key - 64))) & 1ull) != 0;
-          s[nt][e] = vis ? s[nt][e] : -INFINITY;
-          mx[i] = fmaxf(mx[i], s[nt][e]);
-        }
-      }
-      float corr[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-        const float mn = fmaxf(mrow[i], mx[i]);
-        corr[i] = (mn == -INFINITY) ? 1.f : exp2f(mrow[i] - mn);
-        mrow[i] = mn;
-      }
-      float sum[2] = {0.f, 0.f};
-      uint32_t pa[4][4];  // P as half A fragments
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = e >> 1;
-          const float p = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mrow[i]);
-          s[nt][e] = p;
-          sum[i] += p;
-        }
-        // P as the A operand of P.V: keys 16*kk2 .. of this 64-key block
-        const int kk2 = nt >> 1, hi = nt & 1;
-        pa[kk2][0 + 2 * hi] = pack_half2(s[nt][0], s[nt][1]);
-        pa[kk2][1 + 2 * hi] = pack_half2(s[nt][2], s[nt][3]);
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
-        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
-        lrow[i] = lrow[i] * corr[i] + sum[i];
-      }
-#pragma unroll
-      for (int dt = 0; dt < HD / 8; ++dt) {
-        o[dt][0] *= corr[0];
-        o[dt][1] *= corr[0];
-        o[dt][2] *= corr[1];
-        o[dt][3] *= corr[1];
-      }
-      // B fragments of V (k = key, n = dim) from the row-major V tile with ldmatrix.trans:
-      // lane l addresses row (key) kb + 16 kk2 + 8 ((l >> 3) & 1) + (l & 7) of dim tile dt + (l >> 4)
-#pragma unroll
-      for (int kk2 = 0; kk2 < 4; ++kk2) {
-#pragma unroll
-        for (int dt = 0; dt < HD / 8; dt += 2) {
-          const int key = kb + kk2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-          const half* vp = Vs + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vp, b0, b1, b2, b3);
-          mma16816(o[dt], pa[kk2], b0, b1);
-          mma16816(o[dt + 1], pa[kk2], b2, b3);
-        }
-      }
-    }
-    // partials: index (row * Hq + qh) * slots + chunk
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      if (!rv[i]) continue;
-      const size_t pr = ((size_t)(g.row0 + node[i]) * a.Hq + qh[i]) * n_chunk_slots + chunk;
-      float* po = a.part + pr * (HD + 2);
-      if (qi == 0) {
-        po[HD] = mrow[i];
-        po[HD + 1] = lrow[i];
-      }
-#pragma unroll
-      for (int dt = 0; dt < HD / 8; ++dt)
-        *reinterpret_cast<float2*>(po + dt * 8 + qi * 2) = make_float2(o[dt][2 * i], o[dt][2 * i + 1]);
-    }
-  }
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
+  attn_item<HD, kCK>(a, blockIdx.x, blockIdx.y, blockIdx.z, n_chunk_slots, Ks, Vs, threadIdx.x, BlockSync{});
 }
 
-// One warp per (row, query head): combine the row's chunk partials in chunk order.
 template <int HD>
-__global__ void attn_merge_kernel(AttnArgs a, const int* __restrict__ row_grp, int n_chunk_slots) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (w >= a.M * a.Hq) return;
-  const int row = w / a.Hq, qh = w % a.Hq;
-  const Group g = a.groups[row_grp ? row_grp[row] : 0];
-  const int nck = n_prefix_chunks(g.prefix) + (g.block_len > 0 ? 1 : 0);
-  const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
-  // chunk maxima and sums: one load per lane and chunk, all lanes at once
-  float M = -INFINITY;
-  for (int c = lane; c < nck; c += 32) M = fmaxf(M, base[(size_t)c * (HD + 2) + HD]);
-  M = warp_max(M);
-  float L = 0.f;
-  for (int c = lane; c < nck; c += 32) {
-    const float m = base[(size_t)c * (HD + 2) + HD];
-    if (m != -INFINITY) L += exp2f(m - M) * base[(size_t)c * (HD + 2) + HD + 1];
-  }
-  L = warp_sum(L);
-  // weighted sum of the chunk outputs in chunk order (independent loads, unrolled)
-  float acc[HD / 32];
-#pragma unroll
-  for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < nck; ++c) {
-    const float* p = base + (size_t)c * (HD + 2);
-    const float m = p[HD];
-    const float wgt = m == -INFINITY ? 0.f : exp2f(m - M);
-#pragma unroll
-    for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * p[lane + 32 * i];
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const size_t ob = ((size_t)row * a.Hq + qh) * HD;
-#pragma unroll
-  for (int i = 0; i < HD / 32; ++i) store_hilo<bf16>(reinterpret_cast<bf16*>(a.o), a.o_lo, ob + lane + 32 * i, acc[i] * inv);
+__global__ void attn_merge_kernel(AttnArgs a, int n_chunk_slots) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
+  const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (w < a.M * a.Hq) attn_merge_warp<HD, kCK>(a, w, threadIdx.x & 31, n_chunk_slots);
 }
 
 template <int HD>
 cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
-  const int slots = n_prefix_chunks(a.max_prefix) + 1;
-  const size_t smem = 2 * (size_t)kCK * (HD + kPad) * 2;
+  const int slots = n_prefix_chunks(a.max_prefix, kCK) + 1;
+  const size_t smem = smem_bytes<HD, kCK>();
   static bool smem_set = false;
   if (!smem_set) {
     cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -284,7 +42,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  const int rb_count = (kMaxGroupRows * (a.Hq / a.Hkv) + kRowBlock - 1) / kRowBlock;
+  const int rb_count = row_blocks(a.Hq, a.Hkv);
   cfg.gridDim = dim3(slots, a.Hkv * rb_count, a.n_groups);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
@@ -297,13 +55,13 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   cfg.gridDim = dim3((warps + 3) / 4);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, a, a.row_grp, slots);
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, a, slots);
 }
 
 }  // namespace
 
 size_t attention_tc_scratch_bytes(int M, int Hq, int hd, int max_prefix) {
-  const size_t slots = (size_t)n_prefix_chunks(max_prefix) + 1;
+  const size_t slots = (size_t)n_prefix_chunks(max_prefix, kCK) + 1;
   return (size_t)M * Hq * slots * (hd + 2) * sizeof(float);
 }
 

@@ -1,0 +1,288 @@
+// Tree-masked attention on tensor cores (f16 mma.sync m16n8k16, fp32 softmax):
+// the work-item and merge bodies, shared by the standalone kernels and the
+// persistent layer-stack kernel.
+//
+// "EAGLE (LLM decoding)", section "How EAGLE works": tree attention verifies
+// every draft node in one forward pass. A query row (node j, query head h) of
+// group g sees the prefix slots [0, prefix) and the slots prefix + i of the
+// tree block whose bit i is set in node j's ancestor mask.
+//
+// Split-K flash decode: work item (chunk c, KV head and 64-row block, group)
+// takes either prefix keys [CK c, CK c + CK) or, for c == ceil(prefix / CK),
+// the tree block, and 64 of the group's rows x G = Hq / Hkv query heads sharing
+// that KV head (the GQA rows form the M dimension of the MMA). An item stages
+// its keys in shared memory with cp.async (V fragments are read transposed with
+// ldmatrix.trans); each of its 4 warps runs one 16-row tile with an online
+// softmax and writes an unnormalised partial (max, sum, O). attn_merge_warp
+// combines the partials of a row in chunk order. Chunk boundaries are absolute
+// slot multiples of CK, independent of how many rows are verified. The KV cache
+// of a bf16 model holds IEEE half values; q (float32, pre-scaled) and the
+// probabilities P enter the products rounded to half, so both MMAs are
+// f16 x f16 with fp32 accumulation.
+#pragma once
+
+#include <cmath>
+
+#include "kernels.h"
+
+namespace eg {
+namespace attn {
+
+constexpr int kMaxGroupRows = 128;  // rows of one group (tree rows, or one 128-row prefill block)
+constexpr int kPad = 8;             // half padding per shared-memory row (rows 16-byte aligned, conflict-free)
+constexpr int kAttnThreads = 128;   // 4 warps, one 16-row tile each
+constexpr int kRowBlock = 64;       // GQA rows (node x query head) per work item
+
+// Row blocks per (KV head, group) in the item grid.
+__host__ __device__ inline int row_blocks(int Hq, int Hkv) {
+  return (kMaxGroupRows * (Hq / Hkv) + kRowBlock - 1) / kRowBlock;
+}
+// Shared memory of one item: K and V of CK keys.
+template <int HD, int CK>
+constexpr size_t smem_bytes() { return 2 * (size_t)CK * (HD + kPad) * sizeof(__half); }
+
+using half = __half;
+
+__device__ __forceinline__ uint32_t ld_b32(const half* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed half2 (x in the low half).
+__device__ __forceinline__ uint32_t pack_half2(float x, float y) {
+  const __half2 h = __floats2half2_rn(x, y);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__host__ __device__ __forceinline__ int n_prefix_chunks(int prefix, int ck) { return (prefix + ck - 1) / ck; }
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+
+// Four 8x8 b16 matrices, transposed, from shared memory (one row address per lane).
+__device__ __forceinline__ void ldsm_x4_trans(const half* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
+// One work item, run by 128 threads (ranks tid = 0..127, sync() a barrier over
+// them): chunk `chunk` of group `z` for KV head and row block `y`. Ks and Vs hold
+// CK x (HD + kPad) halves each; the caller syncs before reusing them. The tree
+// block (up to kMaxGroupRows keys) passes through them CK keys at a time, with
+// the online-softmax state kept in registers. Each of the 4 warps owns one
+// 16-row tile of the 64-row block. Returns without work (and without syncing)
+// for items past the group's keys or rows.
+template <int HD, int CK, typename Sync>
+__device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chunk_slots, half* Ks, half* Vs,
+                          int tid, Sync sync) {
+  static_assert(CK % 64 == 0 && kRowBlock == 16 * (kAttnThreads / 32), "one 16-row tile per warp");
+  const Group g = a.groups[z];
+  const int rb_count = row_blocks(a.Hq, a.Hkv);
+  const int kvh = y / rb_count, rb = y % rb_count;
+  const int nck = n_prefix_chunks(g.prefix, CK);
+  const bool block = chunk == nck;
+  if (chunk > nck || (block && g.block_len <= 0) || rb * kRowBlock >= g.nrows * (a.Hq / a.Hkv)) return;
+  const int key0 = block ? g.prefix : chunk * CK;
+  const int nkeys = block ? min(g.block_len, kMaxGroupRows) : min(CK, g.prefix - key0);
+  const int G = a.Hq / a.Hkv;
+  const int R = g.nrows * G;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int mt = rb * (kRowBlock / 16) + warp;  // this warp's 16-row tile
+  const bool active = mt * 16 < R;
+
+  const float sl2 = a.scale * 1.4426950408889634f;  // scores in log2 units
+  const int quad = lane >> 2, qi = lane & 3;
+  // rows r0 = mt*16 + quad and r1 = r0 + 8 of this tile: (node, head) = (r / G, r % G)
+  int node[2], qh[2];
+  bool rv[2];
+  uint64_t mk0[2], mk1[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = mt * 16 + quad + 8 * i;
+    rv[i] = active && r < R;
+    node[i] = rv[i] ? r / G : 0;
+    qh[i] = kvh * G + (rv[i] ? r % G : 0);
+    const int row = g.row0 + node[i];
+    mk0[i] = block && rv[i] ? a.mask[2 * row] : 0ull;
+    mk1[i] = block && rv[i] ? a.mask[2 * row + 1] : 0ull;
+  }
+  // q (float32) times the softmax scale in log2 units, rounded to half A fragments
+  uint32_t qa[HD / 16][4];
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float* qp = a.q + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
+      const float2 x0 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + qi * 2) : make_float2(0.f, 0.f);
+      const float2 x1 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + 8 + qi * 2) : make_float2(0.f, 0.f);
+      qa[kk][i] = pack_half2(x0.x * sl2, x0.y * sl2);
+      qa[kk][i + 2] = pack_half2(x1.x * sl2, x1.y * sl2);
+    }
+  }
+  float o[HD / 8][4];
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+  const half* Kg = reinterpret_cast<const half*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
+  const half* Vg = reinterpret_cast<const half*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
+  constexpr int VEC = 8;  // halves per 16-byte vector
+  for (int kc0 = 0; kc0 < nkeys; kc0 += CK) {
+    const int nk = min(CK, nkeys - kc0);
+    if (kc0 > 0) sync();  // every warp is done with the previous sub-chunk
+    // stage keys kc0 .. kc0 + CK of the chunk (row-major) with asynchronous 16-byte
+    // copies, all in flight at once; keys past nk are zero-filled
+    for (int e = tid; e < CK * HD / VEC; e += kAttnThreads) {
+      const int key = e / (HD / VEC), d0 = (e % (HD / VEC)) * VEC;
+      const int n = key < nk ? 16 : 0;
+      const size_t go = (size_t)(kc0 + min(key, nk - 1)) * HD + d0;
+      cp_async16(Ks + key * (HD + kPad) + d0, Kg + go, n);
+      cp_async16(Vs + key * (HD + kPad) + d0, Vg + go, n);
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    sync();
+    if (!active) continue;
+    for (int kb = 0; kb < nk; kb += 64) {
+      float s[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const half* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
+          mma16816(s[nt], qa[kk], ld_b32(kp), ld_b32(kp + 8));
+        }
+      }
+      // mask; c-fragment (row quad (+8), chunk key kc0 + kb + nt*8 + qi*2 + {0,1})
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const int key = kc0 + kb + nt * 8 + qi * 2 + (e & 1);
+          bool vis = key < nkeys && rv[i];
+          if (block && vis) vis = ((key < 64 ? (mk0[i] >> key) : (mk1[i] >> (key - 64))) & 1ull) != 0;
+          s[nt][e] = vis ? s[nt][e] : -INFINITY;
+          mx[i] = fmaxf(mx[i], s[nt][e]);
+        }
+      }
+      float corr[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        const float mn = fmaxf(mrow[i], mx[i]);
+        corr[i] = (mn == -INFINITY) ? 1.f : exp2f(mrow[i] - mn);
+        mrow[i] = mn;
+      }
+      float sum[2] = {0.f, 0.f};
+      uint32_t pa[4][4];  // P as half A fragments
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const float p = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mrow[i]);
+          s[nt][e] = p;
+          sum[i] += p;
+        }
+        // P as the A operand of P.V: keys 16*kk2 .. of this 64-key block
+        const int kk2 = nt >> 1, hi = nt & 1;
+        pa[kk2][0 + 2 * hi] = pack_half2(s[nt][0], s[nt][1]);
+        pa[kk2][1 + 2 * hi] = pack_half2(s[nt][2], s[nt][3]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
+        lrow[i] = lrow[i] * corr[i] + sum[i];
+      }
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; ++dt) {
+        o[dt][0] *= corr[0];
+        o[dt][1] *= corr[0];
+        o[dt][2] *= corr[1];
+        o[dt][3] *= corr[1];
+      }
+      // B fragments of V (k = key, n = dim) from the row-major V tile with ldmatrix.trans:
+      // lane l addresses row (key) kb + 16 kk2 + 8 ((l >> 3) & 1) + (l & 7) of dim tile dt + (l >> 4)
+#pragma unroll
+      for (int kk2 = 0; kk2 < 4; ++kk2) {
+#pragma unroll
+        for (int dt = 0; dt < HD / 8; dt += 2) {
+          const int key = kb + kk2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const half* vp = Vs + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(vp, b0, b1, b2, b3);
+          mma16816(o[dt], pa[kk2], b0, b1);
+          mma16816(o[dt + 1], pa[kk2], b2, b3);
+        }
+      }
+    }
+  }
+  if (!active) return;
+  // partials: index (row * Hq + qh) * slots + chunk
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (!rv[i]) continue;
+    const size_t pr = ((size_t)(g.row0 + node[i]) * a.Hq + qh[i]) * n_chunk_slots + chunk;
+    float* po = a.part + pr * (HD + 2);
+    if (qi == 0) {
+      po[HD] = mrow[i];
+      po[HD + 1] = lrow[i];
+    }
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt)
+      *reinterpret_cast<float2*>(po + dt * 8 + qi * 2) = make_float2(o[dt][2 * i], o[dt][2 * i + 1]);
+  }
+}
+
+// One warp per (row, query head) w < M * Hq: combine the row's chunk partials in chunk order.
+template <int HD, int CK>
+__device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_slots) {
+  const int row = w / a.Hq, qh = w % a.Hq;
+  const Group g = a.groups[a.row_grp ? a.row_grp[row] : 0];
+  const int nck = n_prefix_chunks(g.prefix, CK) + (g.block_len > 0 ? 1 : 0);
+  const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
+  // chunk maxima and sums: one load per lane and chunk, all lanes at once
+  float M = -INFINITY;
+  for (int c = lane; c < nck; c += 32) M = fmaxf(M, base[(size_t)c * (HD + 2) + HD]);
+  M = warp_max(M);
+  float L = 0.f;
+  for (int c = lane; c < nck; c += 32) {
+    const float m = base[(size_t)c * (HD + 2) + HD];
+    if (m != -INFINITY) L += exp2f(m - M) * base[(size_t)c * (HD + 2) + HD + 1];
+  }
+  L = warp_sum(L);
+  // weighted sum of the chunk outputs in chunk order (independent loads, unrolled)
+  float acc[HD / 32];
+#pragma unroll
+  for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < nck; ++c) {
+    const float* p = base + (size_t)c * (HD + 2);
+    const float m = p[HD];
+    const float wgt = m == -INFINITY ? 0.f : exp2f(m - M);
+#pragma unroll
+    for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * p[lane + 32 * i];
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const size_t ob = ((size_t)row * a.Hq + qh) * HD;
+#pragma unroll
+  for (int i = 0; i < HD / 32; ++i) store_hilo<bf16>(reinterpret_cast<bf16*>(a.o), a.o_lo, ob + lane + 32 * i, acc[i] * inv);
+}
+
+}  // namespace attn
+}  // namespace eg

@@ -1,6 +1,8 @@
 // Host-side launchers of the EAGLE step kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace eg {
@@ -16,6 +18,12 @@ cudaError_t gemm_simt(const T* X, const T* W, int M, int N, int K, const EpiPara
 size_t gemm_tc_scratch_bytes(int M, int N, int K);
 cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N, int K, const EpiParams& ep,
                     void* scratch, int* status, cudaStream_t s);
+
+// 2D bf16 tensor map of a row-major [rows][cols] matrix, box [box_rows][64],
+// 128-byte swizzle (the operand format of the tcgen05 kernels).
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
+// SMs of the current device (capped at the scratch-sizing bound).
+int num_sms();
 
 // ---- attention ---------------------------------------------------------------------------------
 struct AttnArgs {
