@@ -66,6 +66,7 @@ SIGNATURES = {
     "eagle_step_kernel_count": (C.c_int32, [C.c_void_p, C.c_int32]),
     "eagle_sync_status": (C.c_int, [C.c_void_p]),
     "eagle_committed_counts": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "eagle_set_trace": (C.c_int, [C.c_void_p, C.c_void_p, C.c_size_t, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "eagle_destroy": (C.c_int, [C.c_void_p]),
     "eagle_last_error": (C.c_char_p, [C.c_void_p]),
     "eagle_op_gemm_scratch_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),

@@ -17,6 +17,7 @@
 
 #include "../../include/eagle.h"
 #include "kernels.h"
+#include "stack.h"
 #include "step.h"
 
 namespace eg {
@@ -36,6 +37,14 @@ struct LayerPtrs {
 };
 
 // Host-derived sizes of a configuration.
+// One persistent-kernel program: kind 0 = verify (target layers + LM head),
+// kind 1 = draft head forward (FC + head layer + LM head top-k) over M rows
+// whose features live at row hbase of the draft buffers.
+struct ProgSpec {
+  int kind = 0, M = 0, hbase = 0, k = 0;
+  int n_phases = 0, n_counters = 0, first = 0;  // first: index of its first phase in the program array
+};
+
 struct Dims {
   int B = 0, d = 0, Hq = 0, Hkv = 0, hd = 0, ffn = 0, V = 0, Lyr = 0, cap = 0, cap_d = 0, P_max = 0, out_cap = 0;
   int qd = 0, kvd = 0, nqkv = 0;
@@ -49,6 +58,10 @@ struct Dims {
   // static topology (host)
   std::vector<int> s_parent, s_rank, s_depth, s_lrow, s_sidx, s_level_nodes, s_level_count;
   std::vector<uint64_t> s_smask, s_anc;
+  // Persistent-kernel programs (bf16 models, up to kStackMaxRows rows): the
+  // verify pass, and the draft head's forward at catch-up and at every depth.
+  std::vector<ProgSpec> progs;
+  int stack_M = 0, stack_phases_max = 0, stack_counters_max = 0, stack_phases_total = 0;
 };
 
 struct Layout {
@@ -120,6 +133,10 @@ struct eagle_ctx {
   void* gemm_scratch = nullptr;
   size_t gemm_scratch_bytes = 0;
   float* attn_part = nullptr;
+  eg::StackPhase* stack_prog = nullptr;  // every program's phases, back to back
+  void* stack_scratch = nullptr;
+  float* stack_part = nullptr;
+  unsigned long long* trace = nullptr;   // caller's phase-trace buffer (eagle_set_trace)
   cudaGraphExec_t graph_exec[2] = {nullptr, nullptr};  // captured step: [0] speculative, [1] vanilla
   int graph_kernels[2] = {-1, -1};                       // kernel nodes in each captured step
 };
@@ -261,6 +278,27 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
     why = "kv_cap too small for max_prompt + max_new + tree";
     return EAGLE_ERR_INVALID_ARG;
   }
+  if (dm.bf16 && dm.nqkv % kTileN == 0 && dm.qd % 64 == 0 && dm.V % kTileN == 0) {
+    const int layer_tiles = dm.nqkv / kTileN + dm.d / kTileN + 2 * dm.ffn / kTileN + dm.d / kTileN;
+    auto add = [&](int kind, int M, int hbase, int k) {
+      if (!stack_supported(M, dm.hd)) return;
+      ProgSpec p;
+      p.kind = kind; p.M = M; p.hbase = hbase; p.k = k;
+      const int layers = kind == 0 ? dm.Lyr : 1;
+      p.n_phases = 6 * layers + 1 + (kind == 1 ? 1 : 0);  // per layer: QKV, attention, merge, O, gate/up, down
+      p.n_counters = layers * layer_tiles + dm.ntV + (kind == 1 ? dm.d / kTileN : 0);
+      p.first = dm.stack_phases_total;
+      dm.stack_phases_total += p.n_phases;
+      dm.stack_M = std::max(dm.stack_M, M);
+      dm.stack_phases_max = std::max(dm.stack_phases_max, p.n_phases);
+      dm.stack_counters_max = std::max(dm.stack_counters_max, p.n_counters);
+      dm.progs.push_back(p);
+    };
+    add(0, dm.B * dm.NR, 0, 1);
+    add(1, dm.B * dm.D1, 0, dm.k);
+    for (int t = 1; t < dm.D; ++t)
+      if (dm.level_rows[t] > 0) add(1, dm.B * dm.level_rows[t], dm.level_base[t], dm.k);
+  }
   return EAGLE_OK;
 }
 
@@ -273,7 +311,7 @@ struct Offsets {
   size_t L, c, root, pend_tok, pend_feat, n_out, out, acc_len, acc_path, L_prev, hist, status;
   size_t p_score, p_token, p_parent, p_depth, p_cid, p_frow, p_smask, p_count, p_front, p_nfront;
   size_t s_parent, s_rank, s_depth, s_lrow, s_sidx, s_smask, s_lnodes, s_lcount;
-  size_t rope_cos, rope_sin, kc, vc, kc_d, vc_d, gemm, attn_part;
+  size_t rope_cos, rope_sin, kc, vc, kc_d, vc_d, gemm, attn_part, stack_prog, stack_scratch, stack_part;
   size_t gemm_bytes;
   size_t total;
 };
@@ -337,6 +375,10 @@ Offsets plan(const Dims& dm) {
   o.gemm_bytes = g;
   o.gemm = L.take(std::max<size_t>(g, 256));
   o.attn_part = L.take(std::max<size_t>(dm.bf16 ? attention_tc_scratch_bytes((int)M, dm.Hq, dm.hd, dm.cap_d) : 0, 256));
+  o.stack_prog = L.take((size_t)dm.stack_phases_total * sizeof(StackPhase));
+  o.stack_scratch = L.take(dm.progs.empty() ? 0 : stack_scratch_bytes(dm.stack_M, dm.stack_phases_max,
+                                                                          dm.stack_counters_max));
+  o.stack_part = L.take(dm.progs.empty() ? 0 : stack_attention_part_bytes(dm.stack_M, dm.Hq, dm.hd, dm.cap_d));
   o.total = L.total;
   return o;
 }
@@ -377,76 +419,180 @@ struct Eng {
     return e;
   }
 
+  // Sinks of a forward phase's op sequence: Direct runs each op as its own
+  // kernel(s); Record appends it to a persistent-kernel program.
+  struct Direct {
+    eagle_ctx* c;
+    eagle_status gemm(const void* X, const bf16* X_lo, const void* W, int M, int N, int K, const EpiParams& e) {
+      return Eng::gemm(c, X, X_lo, W, M, N, K, e);
+    }
+    eagle_status attention(const AttnArgs& a) { return Eng::attention(c, a); }
+  };
+  struct Record {
+    eagle_ctx* c;
+    StackProgramBuilder* b;
+    eagle_status gemm(const void* X, const bf16* X_lo, const void* W, int M, int N, int K, const EpiParams& e) {
+      (void)M;
+      StackGemmDesc g{(const bf16*)W, (const bf16*)X, X_lo, c->dm.M_max, N, K, e};
+      b->gemm(g);
+      return b->ok ? EAGLE_OK : fail(c, EAGLE_ERR_UNSUPPORTED, "persistent program: GEMM shape");
+    }
+    eagle_status attention(const AttnArgs& a) {
+      AttnArgs r = a;
+      r.part = c->stack_part;
+      b->attention(r);
+      return EAGLE_OK;
+    }
+  };
+
   // One pre-norm decoder layer over M rows whose (hb, ssq_b) hold the layer input.
-  static eagle_status layer(eagle_ctx* c, const LayerPtrs& lw, void* kc, void* vc, int cap, int M, int n_groups,
-                            float* h, const float* gain_next) {
+  template <typename Sink>
+  static eagle_status layer(eagle_ctx* c, Sink& sink, const LayerPtrs& lw, void* kc, void* vc, int cap, int M,
+                            int n_groups, float* h, const float* gain_next) {
     const Dims& dm = c->dm;
     EpiParams e = epi(c, kEpiQkv, M, dm.nqkv);
     e.ssq_in = c->ssq_b; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d;
     e.out = c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
     e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = c->rows;
-    EG_TRY(gemm(c, c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e));
+    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e));
 
     AttnArgs a{};
     a.q = (const float*)c->q; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo); a.groups = c->groups; a.n_groups = n_groups;
     a.mask = c->rows.mask; a.row_grp = c->rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap;
     a.max_prefix = cap; a.scale = 1.f / std::sqrt((float)dm.hd); a.part = c->attn_part; a.status = c->st.status;
-    EG_TRY(attention(c, a));
+    EG_TRY(sink.attention(a));
 
     e = epi(c, kEpiResid, M, dm.d);
     e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
-    EG_TRY(gemm(c, c->attn, lo(c->attn_lo), lw.wo, M, dm.d, dm.qd, e));
+    EG_TRY(sink.gemm(c->attn, lo(c->attn_lo), lw.wo, M, dm.d, dm.qd, e));
 
     e = epi(c, kEpiSwiglu, M, 2 * dm.ffn);
     e.ssq_in = c->ssq_a; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.out = c->act; e.ffn = dm.ffn;
     e.out_lo = lo(c->act_lo);
-    EG_TRY(gemm(c, c->hb, lo(c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e));
+    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e));
 
     e = epi(c, kEpiResid, M, dm.d);
     e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = gain_next;
-    EG_TRY(gemm(c, c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e));
+    EG_TRY(sink.gemm(c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e));
+    return EAGLE_OK;
+  }
+
+  // LM-head GEMM with per-tile top-k records (merged by lm_head_merge).
+  template <typename Sink>
+  static eagle_status lm_head_gemm(eagle_ctx* c, Sink& sink, const void* X, const bf16* X_lo, const float* ssq,
+                                   int M, int k, float* logits) {
+    const Dims& dm = c->dm;
+    EpiParams e = epi(c, kEpiLmHead, M, dm.V);
+    e.ssq_in = ssq; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.topk = k; e.y = logits;
+    e.rec_val = c->rec_val; e.rec_idx = c->rec_idx; e.rec_max = c->rec_max; e.rec_sum = c->rec_sum;
+    return sink.gemm(X, X_lo, c->lm_head, M, dm.V, dm.d, e);
+  }
+
+  static eagle_status lm_head_merge(eagle_ctx* c, int M, int k, int* idx, float* val, float* lse) {
+    EG_CK(topk_merge(c->rec_val, c->rec_idx, c->rec_max, c->rec_sum, c->dm.ntV, M, k, idx, val, lse, c->stream));
     return EAGLE_OK;
   }
 
   static eagle_status lm_head(eagle_ctx* c, const void* X, const bf16* X_lo, const float* ssq, int M, int k,
                               int* idx, float* val, float* lse, float* logits) {
+    Direct d{c};
+    EG_TRY(lm_head_gemm(c, d, X, X_lo, ssq, M, k, logits));
+    return lm_head_merge(c, M, k, idx, val, lse);
+  }
+
+  template <typename Sink>
+  static eagle_status target_layers(eagle_ctx* c, Sink& sink, int M, int n_groups) {
     const Dims& dm = c->dm;
-    EpiParams e = epi(c, kEpiLmHead, M, dm.V);
-    e.ssq_in = ssq; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.topk = k; e.y = logits;
-    e.rec_val = c->rec_val; e.rec_idx = c->rec_idx; e.rec_max = c->rec_max; e.rec_sum = c->rec_sum;
-    EG_TRY(gemm(c, X, X_lo, c->lm_head, M, dm.V, dm.d, e));
-    EG_CK(topk_merge(c->rec_val, c->rec_idx, c->rec_max, c->rec_sum, dm.ntV, M, k, idx, val, lse, c->stream));
+    const size_t kvl = (size_t)dm.B * dm.Hkv * dm.cap * dm.hd * sizeof(T);
+    for (int l = 0; l < dm.Lyr; ++l) {
+      const float* gn = l + 1 < dm.Lyr ? c->layers[l + 1].attn_norm : c->final_norm;
+      EG_TRY(layer(c, sink, c->layers[l], (char*)c->kc + l * kvl, (char*)c->vc + l * kvl, dm.cap, M, n_groups,
+                   c->h_tgt, gn));
+    }
+    return EAGLE_OK;
+  }
+
+  static eagle_status embed(eagle_ctx* c, int M) {
+    const Dims& dm = c->dm;
+    EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok, M, dm.d, c->layers[0].attn_norm, c->h_tgt, (T*)c->hb,
+                        lo(c->hb_lo), c->ssq_b, c->stream));
     return EAGLE_OK;
   }
 
   static eagle_status target_stack(eagle_ctx* c, int M, int n_groups) {
+    Direct d{c};
+    EG_TRY(embed(c, M));
+    return target_layers(c, d, M, n_groups);
+  }
+
+  // FC([feature ; E(token)]) -> head layer -> (k > 0) LM head, over rows whose features sit at row hbase.
+  template <typename Sink>
+  static eagle_status draft_ops(eagle_ctx* c, Sink& sink, int M, int n_groups, int hbase, int k) {
     const Dims& dm = c->dm;
-    const size_t es = sizeof(T);
-    const size_t kvl = (size_t)dm.B * dm.Hkv * dm.cap * dm.hd;
-    EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok, M, dm.d, c->layers[0].attn_norm, c->h_tgt, (T*)c->hb,
-                        lo(c->hb_lo), c->ssq_b, c->stream));
-    for (int l = 0; l < dm.Lyr; ++l) {
-      const float* gn = l + 1 < dm.Lyr ? c->layers[l + 1].attn_norm : c->final_norm;
-      EG_TRY(layer(c, c->layers[l], (char*)c->kc + l * kvl * es, (char*)c->vc + l * kvl * es, dm.cap, M, n_groups,
-                   c->h_tgt, gn));
+    float* h = c->h_dft + (size_t)hbase * dm.d;
+    EpiParams e = epi(c, kEpiFc, M, dm.d);
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
+    EG_TRY(sink.gemm(c->xfc, lo(c->xfc_lo), c->fc, M, dm.d, 2 * dm.d, e));
+    EG_TRY(layer(c, sink, c->head, c->kc_d, c->vc_d, dm.cap_d, M, n_groups, h, c->final_norm));
+    if (k > 0) EG_TRY(lm_head_gemm(c, sink, c->hb, lo(c->hb_lo), c->ssq_b, M, k, nullptr));
+    return EAGLE_OK;
+  }
+
+  static const ProgSpec* find_prog(eagle_ctx* c, int kind, int M, int hbase, int k) {
+    for (const ProgSpec& p : c->dm.progs)
+      if (p.kind == kind && p.M == M && p.hbase == hbase && p.k == k) return &p;
+    return nullptr;
+  }
+
+  static eagle_status run_prog(eagle_ctx* c, const ProgSpec& p, int n_phases) {
+    unsigned long long* trace = p.kind == 0 ? c->trace : nullptr;
+    EG_CK(stack_run(c->stack_prog + p.first, n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
+                    c->stack_scratch, c->st.status, trace, c->stream));
+    return EAGLE_OK;
+  }
+
+  // Record every program of the context into the workspace (at init).
+  static eagle_status build_programs(eagle_ctx* c) {
+    const Dims& dm = c->dm;
+    if (sizeof(T) != 2 || dm.progs.empty()) return EAGLE_OK;
+    std::vector<StackPhase> all;
+    for (const ProgSpec& p : dm.progs) {
+      StackProgramBuilder b;
+      b.M = p.M;
+      b.MT = stack_mt(p.M);
+      b.has_lo = true;
+      Record r{c, &b};
+      if (p.kind == 0) {
+        EG_TRY(target_layers(c, r, p.M, dm.B));
+        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c->hb_lo), c->ssq_b, p.M, 1, nullptr));
+      } else {
+        EG_TRY(draft_ops(c, r, p.M, dm.B, p.hbase, p.k));
+      }
+      if ((int)b.phases.size() != p.n_phases || b.n_counters != p.n_counters)
+        return fail(c, EAGLE_ERR_UNSUPPORTED, "persistent program: phase count");
+      all.insert(all.end(), b.phases.begin(), b.phases.end());
     }
+    EG_CK(cudaMemcpyAsync(c->stack_prog, all.data(), all.size() * sizeof(StackPhase), cudaMemcpyHostToDevice,
+                          c->stream));
+    EG_CK(cudaStreamSynchronize(c->stream));  // `all` is a host temporary
     return EAGLE_OK;
   }
 
   // Draft head over the phase's rows: FC([feature ; E(token)]) then the head layer, then (k > 0) LM-head top-k.
   static eagle_status draft_forward(eagle_ctx* c, const float* feat, int M, int n_groups, int hbase, int k) {
     const Dims& dm = c->dm;
-    float* h = c->h_dft + (size_t)hbase * dm.d;
     EG_CK(fc_input<T>(feat, c->rows.fsrc, (const T*)c->embed, c->rows.tok, M, dm.d, (T*)c->xfc, lo(c->xfc_lo),
                       c->stream));
-    EpiParams e = epi(c, kEpiFc, M, dm.d);
-    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
-    EG_TRY(gemm(c, c->xfc, lo(c->xfc_lo), c->fc, M, dm.d, 2 * dm.d, e));
-    EG_TRY(layer(c, c->head, c->kc_d, c->vc_d, dm.cap_d, M, n_groups, h, c->final_norm));
+    const ProgSpec* p = n_groups == dm.B ? find_prog(c, 1, M, hbase, k) : nullptr;
+    if (p) {
+      EG_TRY(run_prog(c, *p, p->n_phases));
+    } else {
+      Direct d{c};
+      EG_TRY(draft_ops(c, d, M, n_groups, hbase, k));
+    }
     if (k > 0)
-      EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, k, c->dtopk_idx + (size_t)hbase * k,
-                     c->dtopk_val + (size_t)hbase * k,
-                     c->dlse + hbase, nullptr));
+      EG_TRY(lm_head_merge(c, M, k, c->dtopk_idx + (size_t)hbase * k, c->dtopk_val + (size_t)hbase * k,
+                           c->dlse + hbase));
     return EAGLE_OK;
   }
 
@@ -500,8 +646,20 @@ struct Eng {
     const Dims& dm = c->dm;
     const int M = dm.B * tree.n_rows;
     EG_CK(setup_verify_rows(c->st, tree, c->rows, c->groups, c->stream));
-    EG_TRY(target_stack(c, M, dm.B));
-    EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits));
+    const ProgSpec* p = find_prog(c, 0, M, 0, 1);
+    if (p) {
+      // one persistent launch for every layer (and the LM head unless logits are wanted)
+      EG_TRY(embed(c, M));
+      EG_TRY(run_prog(c, *p, d_logits ? p->n_phases - 1 : p->n_phases));
+      if (d_logits) {
+        Direct d{c};
+        EG_TRY(lm_head_gemm(c, d, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, d_logits));
+      }
+      EG_TRY(lm_head_merge(c, M, 1, c->vargmax, nullptr, nullptr));
+    } else {
+      EG_TRY(target_stack(c, M, dm.B));
+      EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits));
+    }
     if (d_argmax)
       EG_CK(cudaMemcpyAsync(d_argmax, c->vargmax, (size_t)M * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
     return EAGLE_OK;
@@ -627,6 +785,8 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->rope_cos = (float*)P(o.rope_cos); c->rope_sin = (float*)P(o.rope_sin);
   c->kc = P(o.kc); c->vc = P(o.vc); c->kc_d = P(o.kc_d); c->vc_d = P(o.vc_d);
   c->gemm_scratch = P(o.gemm); c->gemm_scratch_bytes = o.gemm_bytes; c->attn_part = (float*)P(o.attn_part);
+  c->stack_prog = (StackPhase*)P(o.stack_prog); c->stack_scratch = P(o.stack_scratch);
+  c->stack_part = (float*)P(o.stack_part);
 
   // Zero the workspace (tile counters, status, caches), then upload the tables.
   cudaError_t e = cudaMemsetAsync(d_ws, 0, o.total, c->stream);
@@ -671,6 +831,11 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   if (e != cudaSuccess) {
     delete c;
     return EAGLE_ERR_CUDA;
+  }
+  const eagle_status ps = dispatch(c, [&](auto E) { return decltype(E)::build_programs(c); });
+  if (ps != EAGLE_OK) {
+    delete c;
+    return ps;
   }
   *out = c;
   return EAGLE_OK;
@@ -887,6 +1052,26 @@ eagle_status eagle_sync_status(eagle_ctx* c) {
 eagle_status eagle_committed_counts(eagle_ctx* c, int32_t* d_counts) {
   if (!c || !d_counts) return EAGLE_ERR_INVALID_ARG;
   EG_CK(cudaMemcpyAsync(d_counts, c->st.n_out, c->dm.B * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+  return EAGLE_OK;
+}
+
+eagle_status eagle_set_trace(eagle_ctx* c, uint64_t* d_trace, size_t n, int32_t* n_phases, int32_t* n_ctas) {
+  if (!c) return EAGLE_ERR_INVALID_ARG;
+  const ProgSpec* v = nullptr;
+  for (const ProgSpec& p : c->dm.progs)
+    if (p.kind == 0) v = &p;
+  const int ph = v ? v->n_phases : 0, ctas = v ? stack_ctas() : 0;
+  if (n_phases) *n_phases = ph;
+  if (n_ctas) *n_ctas = ctas;
+  if (d_trace && (!v || n < (size_t)(ph + 1) * ctas)) return EAGLE_ERR_INVALID_ARG;
+  c->trace = reinterpret_cast<unsigned long long*>(d_trace);
+  // captured steps bake the trace pointer: drop them
+  for (int i = 0; i < 2; ++i)
+    if (c->graph_exec[i]) {
+      cudaGraphExecDestroy(c->graph_exec[i]);
+      c->graph_exec[i] = nullptr;
+      c->graph_kernels[i] = -1;
+    }
   return EAGLE_OK;
 }
 

@@ -1,0 +1,73 @@
+// Persistent layer-stack forward (bf16 models, up to 128 token rows).
+//
+// One cooperative launch runs a whole program of phases - the GEMMs of every
+// decoder layer with their fused epilogues, tree attention and its merge, and
+// the LM head - on one CTA per SM. Phase p may read only what phases < p wrote;
+// the kernel orders them with grid-wide arrival counters. The weight boxes of
+// every GEMM phase do not depend on earlier phases, so each CTA's weight
+// producer streams them ahead across phase boundaries; only the activation
+// boxes of phase p wait for phase p - 1 to finish.
+#pragma once
+
+#include <vector>
+
+#include "kernels.h"
+
+namespace eg {
+
+enum StackPhaseKind : int { kPhaseGemm = 0, kPhaseAttn = 1, kPhaseMerge = 2 };
+
+struct StackPhase {   // 128-byte aligned (CUtensorMap)
+  CUtensorMap tmW;    // GEMM weight [N][K], box [128][64]
+  CUtensorMap tmX;    // GEMM activations [rows][K], box [MT][64]
+  CUtensorMap tmXlo;  // low halves of the activations (hi/lo pair)
+  int kind = kPhaseGemm;
+  int N = 0, K = 0, n_tiles = 0, kbt = 0;
+  long long T = 0;    // (tile, 64-wide k-block) units
+  int cnt_off = 0;    // first split-K arrival counter of this phase
+  EpiParams ep;       // GEMM epilogue
+  AttnArgs at;        // attention / merge
+};
+
+// One GEMM phase: Y = (X + X_lo) W^T over the program's M rows, then epilogue ep.
+struct StackGemmDesc {
+  const bf16* W;
+  const bf16* X;
+  const bf16* X_lo;   // may be NULL
+  int rows_cap;       // rows of the X buffers (>= M)
+  int N, K;
+  EpiParams ep;
+};
+
+// Host-side builder of a program (tensor maps are encoded here).
+struct StackProgramBuilder {
+  int M = 0, MT = 0;
+  bool has_lo = false;
+  std::vector<StackPhase> phases;
+  int n_counters = 0;
+  bool ok = true;
+  void gemm(const StackGemmDesc& g);
+  void attention(const AttnArgs& a);  // adds the attention phase and its merge phase
+};
+
+// Largest M the persistent kernel takes.
+constexpr int kStackMaxRows = 128;
+bool stack_supported(int M, int hd);
+// Token rows of one MMA tile for M rows (the activation box height).
+int stack_mt(int M);
+// CTAs of one launch (one per SM).
+int stack_ctas();
+// Bytes of device scratch for programs over at most M rows, n_phases phases and
+// n_counters split-K counters: phase counters, split-K counters, partial sums
+// (zero-initialised by the caller once).
+size_t stack_scratch_bytes(int M, int n_phases, int n_counters);
+// Attention partial buffer of the persistent kernel.
+size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix);
+// Runs the program (d_phases: device copy of builder.phases) on stack_ctas()
+// CTAs. Scratch counters must be zero on entry; the kernel leaves them zero.
+// trace (may be NULL): [n_phases + 1][stack_ctas()] %globaltimer stamps - row p
+// = when each CTA finished phase p, the last row = when it started.
+cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
+                      void* scratch, int* status, unsigned long long* trace, cudaStream_t s);
+
+}  // namespace eg

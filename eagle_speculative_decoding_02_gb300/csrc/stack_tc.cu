@@ -1,0 +1,648 @@
+// Persistent layer-stack forward on the sm_103a tensor cores (tcgen05 + TMA).
+//
+// At one verify or draft step of EAGLE ("EAGLE (LLM decoding)", section "How
+// EAGLE works") every decoder layer multiplies a few dozen token rows by its
+// weight matrices: each GEMM is a 5-35 us stream of weights, and as separate
+// kernels each pays a launch, a pipeline fill and a split-K tail. Here one
+// cooperative launch (one CTA per SM) runs the whole program of phases:
+//
+//   GEMM   swap-AB tcgen05 tiles (128 weight rows x MT token rows, fp32 in TMEM),
+//          (tile, 64-wide k-block) units split evenly over the CTAs (stream-K),
+//          split tiles summed by the last-arriving CTA in ascending CTA order,
+//          then the fused epilogue (RMSNorm row scale, RoPE + KV write, SwiGLU,
+//          residual add + next norm, LM-head top-k records).
+//   ATTN   tree-attention work items (64-key chunk, KV head x 64-row block, group)
+//          run by the epilogue warps, partials to global memory.
+//   MERGE  one warp per (row, query head) combines the partials in chunk order.
+//
+// Phase p reads only what phases < p wrote. A CTA that has finished all its
+// epilogue work of phase p adds one to counter done[p] (release); consumers of
+// phase p wait until it reaches the grid size (acquire). Weight boxes depend on
+// nothing, so the weight producer streams the weights of later GEMM phases into
+// its ring while earlier phases finish; only the activation boxes of phase p
+// wait for done[p - 1].
+//
+// Warp roles (224 threads):
+//   warp 0     weight producer (one lane): weight ring (SW stages)
+//   warp 1     TMEM allocator and MMA issuer (one lane)
+//   warps 2-5  epilogue, attention and merge (128 threads)
+//   warp 6     activation producer (one lane): activation ring (SX stages)
+// Every wait is bounded (2 s); on a timeout the CTA records kStTimeout, stops
+// issuing work, drains its copies and returns; other CTAs then time out on
+// their own waits.
+#include <cuda.h>
+
+#include "attention_tc.cuh"
+#include "epilogue.cuh"
+#include "stack.h"
+#include "tc_ptx.cuh"
+
+namespace eg {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 224;
+constexpr int kXWarp = 6;                  // activation producer warp
+constexpr int kBK = 64;
+constexpr int kWBytes = kTileN * kBK * 2;  // 16 KB weight box
+constexpr int kSub = 32;                   // epilogue rows per sub-tile
+constexpr int kLdt = kTileN + 1;
+constexpr int kMaxW = 12;                  // weight ring stages (upper bound)
+constexpr int kAttnCK = 64;                // keys per attention chunk
+constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
+constexpr int kHdMax = 128;
+constexpr int kMaxCtas = 160;              // partial buffer sizing bound
+constexpr size_t kUnionBytes =
+    attn::smem_bytes<kHdMax, kAttnCK>() > (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4
+        ? attn::smem_bytes<kHdMax, kAttnCK>()
+        : (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4;
+
+struct StackArgs {
+  const StackPhase* ph;
+  int n_phases;
+  int M, MT, has_lo, sw, sx;
+  uint32_t tmem_cols;
+  unsigned* done;    // [n_phases] phase counters, then the exit counter
+  int* tile_cnt;     // [n_counters] split-K arrival counters
+  int n_counters;
+  float* partial;    // [G][2][MT][128]
+  int* status;
+  unsigned long long* trace;  // optional: [n_phases + 1][G] %globaltimer stamps
+};
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// A GEMM phase of T units runs on its first Gp = min(G, T) CTAs: CTA c < Gp owns
+// units [c T / Gp, (c + 1) T / Gp) (at least one), exactly as the standalone GEMM
+// splits the same shape, so both sum every output in the same order.
+__device__ __forceinline__ int phase_ctas(long long T, int G) { return (int)min((long long)G, T); }
+__device__ __forceinline__ long long unit_start(long long T, int c, int Gp) { return (long long)c * T / Gp; }
+__device__ __forceinline__ int cta_of(long long T, long long u, int Gp) { return (int)(((u + 1) * Gp - 1) / T); }
+
+// This CTA's units [u, u1) of GEMM phase p; next() moves to the next GEMM phase
+// in which the CTA has units.
+struct Cursor {
+  int p = -1;
+  long long u = 0, u1 = 0;
+  __device__ bool next(const StackArgs& a, int c, int G) {
+    for (++p; p < a.n_phases; ++p) {
+      if (a.ph[p].kind != kPhaseGemm) continue;
+      const long long T = a.ph[p].T;
+      const int Gp = phase_ctas(T, G);
+      if (c >= Gp) continue;
+      u = unit_start(T, c, Gp);
+      u1 = unit_start(T, c + 1, Gp);
+      return true;
+    }
+    return false;
+  }
+};
+
+// Bounded wait until done[p] reaches G (one thread).
+__device__ bool wait_phase(const StackArgs& a, int p, unsigned G, volatile int* abort_flag) {
+  if (ld_acquire(a.done + p) >= G) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire(a.done + p) >= G) return true;
+    if ((i & 15) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        set_status(a.status, kStTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// The attention work items that have keys and rows, in order (group, KV head,
+// row block, chunk): count() counts them, item() decodes one.
+template <int CK>
+struct AttnItems {
+  const AttnArgs& at;
+  __device__ int rbs(const Group& g) const {
+    return (g.nrows * (at.Hq / at.Hkv) + attn::kRowBlock - 1) / attn::kRowBlock;
+  }
+  __device__ int chunks(const Group& g) const {
+    return attn::n_prefix_chunks(g.prefix, CK) + (g.block_len > 0 ? 1 : 0);
+  }
+  __device__ int count() const {
+    int n = 0;
+    for (int z = 0; z < at.n_groups; ++z) {
+      const Group g = at.groups[z];
+      n += chunks(g) * at.Hkv * rbs(g);
+    }
+    return n;
+  }
+  __device__ void item(int i, int& chunk, int& y, int& z) const {
+    const int rb_count = attn::row_blocks(at.Hq, at.Hkv);
+    for (z = 0; z < at.n_groups; ++z) {
+      const Group g = at.groups[z];
+      const int nc = chunks(g), nr = rbs(g), n = nc * at.Hkv * nr;
+      if (i < n) {
+        chunk = i % nc;
+        const int rest = i / nc;
+        y = (rest / nr) * rb_count + rest % nr;
+        return;
+      }
+      i -= n;
+    }
+    chunk = 0;
+    y = 0;
+    z = 0;
+  }
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int SW = a.sw, SX = a.sx, MT = a.MT;
+  const int xbox = MT * kBK * 2;
+  const int xbytes = xbox * (a.has_lo ? 2 : 1);
+  uint8_t* wring = smem;
+  uint8_t* xring = wring + (size_t)SW * kWBytes;
+  uint8_t* uni = xring + (size_t)SX * xbytes;  // epilogue tile or attention K/V
+  float* tile = reinterpret_cast<float*>(uni);
+  float* rscale = tile + kSub * kLdt;
+  half* Ks = reinterpret_cast<half*>(uni);
+  half* Vs = Ks + kAttnCK * (HD + attn::kPad);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(uni + kUnionBytes);
+  uint64_t* wfull = bars;
+  uint64_t* wempty = wfull + SW;
+  uint64_t* xfull = wempty + SW;
+  uint64_t* xempty = xfull + SX;
+  uint64_t* afull = xempty + SX;
+  uint64_t* aempty = afull + 2;
+  uint64_t* drain = aempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+  volatile int* exit_last = abort_flag + 2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x, G = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    *exit_last = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (a.trace && threadIdx.x == 0) a.trace[(size_t)a.n_phases * G + c] = globaltimer();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ weight producer
+      // Weight boxes depend on no phase: stream them through the ring as fast as
+      // the MMA frees stages, across phase boundaries.
+      uint64_t pol_w;  // weights are read once
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+      Cursor W;
+      bool more = W.next(a, c, G);
+      long long iw = 0;
+      bool ok = true;
+      while (more && ok) {
+        const int s = (int)(iw % SW);
+        if (iw >= SW && !mbar_wait(&wempty[s], (uint32_t)((iw / SW) - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const StackPhase& P = a.ph[W.p];
+        const int t = (int)(W.u / P.kbt), kb = (int)(W.u % P.kbt);
+        mbar_expect_tx(&wfull[s], (uint32_t)kWBytes);
+        tma_load_2d_hint(wring + (size_t)s * kWBytes, &P.tmW, &wfull[s], kb * kBK, t * kTileN, pol_w);
+        ++iw;
+        if (++W.u == W.u1) more = W.next(a, c, G);
+      }
+      if (!ok) {
+        // drain (bounded): every box issued must land before the CTA exits
+        for (long long j = (iw > SW ? iw - SW : 0); j < iw; ++j) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(&wfull[j % SW], (uint32_t)(j / SW) & 1) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == kXWarp) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ activation producer
+      // The activation boxes of phase p wait until every CTA has finished phase p - 1.
+      uint64_t pol_x;  // activations are read by every CTA
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+      Cursor X;
+      bool more = X.next(a, c, G);
+      long long ix = 0;
+      int ready = -1;
+      bool ok = true;
+      while (more && ok) {
+        if (ready != X.p) {
+          if (X.p > 0 && !wait_phase(a, X.p - 1, (unsigned)G, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async();  // the phase's activations were written by other CTAs' generic stores
+          ready = X.p;
+        }
+        const int s = (int)(ix % SX);
+        if (ix >= SX && !mbar_wait(&xempty[s], (uint32_t)((ix / SX) - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const StackPhase& P = a.ph[X.p];
+        const int kb = (int)(X.u % P.kbt);
+        uint8_t* dst = xring + (size_t)s * xbytes;
+        mbar_expect_tx(&xfull[s], (uint32_t)xbytes);
+        tma_load_2d_hint(dst, &P.tmX, &xfull[s], kb * kBK, 0, pol_x);
+        if (a.has_lo) tma_load_2d_hint(dst + xbox, &P.tmXlo, &xfull[s], kb * kBK, 0, pol_x);
+        ++ix;
+        if (++X.u == X.u1) more = X.next(a, c, G);
+      }
+      if (!ok) {
+        for (long long j = (ix > SX ? ix - SX : 0); j < ix; ++j) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(&xfull[j % SX], (uint32_t)(j / SX) & 1) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16(MT);
+      Cursor C;
+      bool more = C.next(a, c, G);
+      long long i = 0;
+      int f = 0;
+      bool ok = true;
+      while (more && ok) {
+        const int kbt = a.ph[C.p].kbt;
+        const int t = (int)(C.u / kbt);
+        const int kb0 = (int)(C.u - (long long)t * kbt);
+        const int kb1 = (int)min((long long)kbt, C.u1 - (long long)t * kbt);
+        const int buf = f & 1;
+        if (f >= 2 && !mbar_wait(&aempty[buf], (uint32_t)((f >> 1) - 1) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * MT);
+        for (int kb = kb0; kb < kb1; ++kb, ++i) {
+          const int sw = (int)(i % SW), sx = (int)(i % SX);
+          if (!mbar_wait(&wfull[sw], (uint32_t)(i / SW) & 1, abort_flag, a.status) ||
+              !mbar_wait(&xfull[sx], (uint32_t)(i / SX) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aw = smem_u32(wring + (size_t)sw * kWBytes);
+          const uint32_t ax = smem_u32(xring + (size_t)sx * xbytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            umma(d, sw128_desc(aw + k * 32), sw128_desc(ax + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            if (a.has_lo) umma(d, sw128_desc(aw + k * 32), sw128_desc(ax + xbox + k * 32), idesc, 1u);
+          }
+          umma_commit(&wempty[sw]);
+          umma_commit(&xempty[sx]);
+        }
+        if (!ok) break;
+        umma_commit(&afull[buf]);
+        ++f;
+        C.u = (long long)t * kbt + kb1;
+        if (C.u >= C.u1) more = C.next(a, c, G);
+      }
+      // no MMA may still be writing tensor memory when it is freed
+      umma_commit(drain);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------------ epilogue, attention, merge
+    const int etid = threadIdx.x - 64;
+    const int ew = etid >> 5;             // epilogue warp 0..3
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int col = q * 32 + lane;        // weight row within the tile = output column
+    const int rows_valid = min(MT, a.M);
+    int f = 0;
+    bool alive = true;
+    for (int p = 0; p < a.n_phases; ++p) {
+      const StackPhase& P = a.ph[p];
+      if (p > 0 && alive) alive = epi_all(etid != 0 || wait_phase(a, p - 1, (unsigned)G, abort_flag));
+      if (alive && P.kind == kPhaseGemm) {
+        const EpiParams& ep = P.ep;
+        const long long T = P.T;
+        const int kbt = P.kbt;
+        const int Gp = phase_ctas(T, G);
+        const long long u0 = c < Gp ? unit_start(T, c, Gp) : 0, u1 = c < Gp ? unit_start(T, c + 1, Gp) : 0;
+        const int t_first = (int)(u0 / kbt);
+        for (long long u = u0; u < u1 && alive;) {
+          const int t = (int)(u / kbt);
+          const int kb0 = (int)(u - (long long)t * kbt);
+          const int kb1 = (int)min((long long)kbt, u1 - (long long)t * kbt);
+          const bool whole = kb0 == 0 && kb1 == kbt;
+          const int buf = f & 1;
+          const bool ok = epi_all(mbar_wait(&afull[buf], (uint32_t)(f >> 1) & 1, abort_flag, a.status));
+          tc_fence_after();
+          const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MT);
+          const int n0 = t * kTileN;
+          if (!ok) {
+            alive = false;
+          } else if (whole) {
+            for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+              float v[32];
+              tmem_ld32(tb + r0, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) tile[j * kLdt + col] = v[j];
+              EpilogueSync{}();
+              run_epilogue<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, rscale, etid, EpilogueSync{});
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[buf]);
+          } else {
+            // split tile: leave the fragment in this CTA's slot; the last of the
+            // tile's CTAs to arrive sums every fragment in ascending CTA order
+            float* slot = a.partial + ((size_t)c * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
+            for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+              float v[32];
+              tmem_ld32(tb + r0, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (r0 + j < rows_valid) __stcg(slot + (size_t)(r0 + j) * kTileN + col, v[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[buf]);
+            __threadfence();
+            EpilogueSync{}();
+            const long long tu0 = (long long)t * kbt, tu1 = (long long)(t + 1) * kbt - 1;
+            const int c0 = cta_of(T, tu0, Gp), c1 = cta_of(T, tu1, Gp);
+            if (etid == 0) {
+              int* cnt = a.tile_cnt + P.cnt_off + t;
+              const int prev = atomicAdd(cnt, 1);
+              const int last = prev == (c1 - c0);
+              if (last) *cnt = 0;
+              *last_flag = last;
+            }
+            EpilogueSync{}();
+            if (*last_flag) {
+              __threadfence();
+              // each thread sums 4 adjacent columns of 8 rows per 32-row sub-tile
+              const int c4 = 4 * lane;
+              for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+                float4 acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cc = c0; cc <= c1; cc += 2) {
+                  // two fragments' loads in flight together, added in CTA order
+                  const bool two = cc + 1 <= c1;
+                  const float* f0 = a.partial +
+                                    ((size_t)cc * 2 + (t != (int)(unit_start(T, cc, Gp) / kbt) ? 1 : 0)) *
+                                        (size_t)MT * kTileN;
+                  const float* f1 = two ? a.partial + ((size_t)(cc + 1) * 2 +
+                                                       (t != (int)(unit_start(T, cc + 1, Gp) / kbt) ? 1 : 0)) *
+                                                          (size_t)MT * kTileN
+                                        : f0;
+                  float4 x0[8], x1[8];
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + ew * 8 + i;
+                    const bool in = r < rows_valid;
+                    x0[i] = in ? __ldcg(reinterpret_cast<const float4*>(f0 + (size_t)r * kTileN + c4))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x1[i] = (in && two) ? __ldcg(reinterpret_cast<const float4*>(f1 + (size_t)r * kTileN + c4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                  }
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    acc[i].x += x0[i].x; acc[i].y += x0[i].y; acc[i].z += x0[i].z; acc[i].w += x0[i].w;
+                  }
+                  if (two) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                      acc[i].x += x1[i].x; acc[i].y += x1[i].y; acc[i].z += x1[i].z; acc[i].w += x1[i].w;
+                    }
+                  }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  float* tr = tile + (ew * 8 + i) * kLdt + c4;
+                  tr[0] = acc[i].x; tr[1] = acc[i].y; tr[2] = acc[i].z; tr[3] = acc[i].w;
+                }
+                EpilogueSync{}();
+                run_epilogue<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, rscale, etid,
+                                   EpilogueSync{});
+              }
+            }
+          }
+          ++f;
+          u = (long long)(t + 1) * kbt;
+        }
+      } else if (alive && P.kind == kPhaseAttn) {
+        const AttnArgs& at = P.at;
+        const AttnItems<kAttnCK> items{at};
+        const int n = items.count();
+        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCK) + 1;
+        const int i0 = (int)((long long)c * n / G), i1 = (int)((long long)(c + 1) * n / G);
+        for (int i = i0; i < i1; ++i) {
+          int chunk, y, z;
+          items.item(i, chunk, y, z);
+          EpilogueSync{}();  // the previous item's readers of Ks / Vs are done
+          attn::attn_item<HD, kAttnCK>(at, chunk, y, z, slots, Ks, Vs, etid, EpilogueSync{});
+        }
+      } else if (alive && P.kind == kPhaseMerge) {
+        const AttnArgs& at = P.at;
+        const int n = at.M * at.Hq;
+        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCK) + 1;
+        const int w0 = (int)((long long)c * n / G), w1 = (int)((long long)(c + 1) * n / G);
+        for (int w = w0 + ew; w < w1; w += 4) attn::attn_merge_warp<HD, kAttnCK>(at, w, lane, slots);
+      }
+      // phase done: every epilogue thread's writes happen before the release
+      EpilogueSync{}();
+      if (etid == 0) {
+        __threadfence();
+        fence_proxy_async();
+        red_release_add(a.done + p, 1u);
+        if (a.trace) a.trace[(size_t)p * G + c] = globaltimer();
+      }
+    }
+  }
+  // the producer and MMA roles ran on lane 0 only: reconverge each warp before the
+  // block barrier and the warp-wide (.sync.aligned) TMEM dealloc
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // the last CTA out returns every counter to zero for the next launch
+    __threadfence();
+    const unsigned prev = atomicAdd(a.done + a.n_phases, 1u);
+    *exit_last = prev == (unsigned)(G - 1);
+  }
+  __syncthreads();
+  if (*exit_last) {
+    __threadfence();
+    for (int i = threadIdx.x; i <= a.n_phases; i += kThreads) a.done[i] = 0u;
+    for (int i = threadIdx.x; i < a.n_counters; i += kThreads) a.tile_cnt[i] = 0;
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+  }
+}
+
+struct Layout {
+  int sw, sx;
+  size_t smem;
+};
+
+Layout layout(int MT, bool has_lo) {
+  Layout l{};
+  const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
+  l.sx = MT <= 64 ? 3 : 2;
+  const size_t fixed = kUnionBytes + (size_t)(2 * kMaxW + 2 * 3 + 5) * 8 + 16 + 1024;
+  const long long room = (long long)kSmemBudget - (long long)fixed - (long long)l.sx * (long long)xbytes;
+  l.sw = (int)std::min<long long>(kMaxW, room / kWBytes);
+  l.smem = (size_t)l.sw * kWBytes + (size_t)l.sx * xbytes + fixed;
+  return l;
+}
+
+int round_mt(int M) {
+  int MT = ((M + 31) / 32) * 32;
+  return MT < 32 ? 32 : MT;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+int stack_mt(int M) { return round_mt(M); }
+
+int stack_ctas() { return num_sms(); }
+
+bool stack_supported(int M, int hd) { return M >= 1 && M <= kStackMaxRows && (hd == 64 || hd == 128); }
+
+size_t stack_scratch_bytes(int M, int n_phases, int n_counters) {
+  return align256((size_t)(n_phases + 1) * 4) + align256((size_t)n_counters * 4) +
+         (size_t)kMaxCtas * 2 * round_mt(M) * kTileN * 4;
+}
+
+size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix) {
+  const size_t slots = (size_t)attn::n_prefix_chunks(max_prefix, kAttnCK) + 1;
+  return (size_t)M * Hq * slots * (hd + 2) * sizeof(float);
+}
+
+void StackProgramBuilder::gemm(const StackGemmDesc& g) {
+  StackPhase ph{};
+  ph.kind = kPhaseGemm;
+  ph.N = g.N;
+  ph.K = g.K;
+  if (g.N % kTileN || g.K % kBK || g.rows_cap < M || !g.W || !g.X) { ok = false; return; }
+  if (((reinterpret_cast<uintptr_t>(g.W) | reinterpret_cast<uintptr_t>(g.X) |
+        reinterpret_cast<uintptr_t>(g.X_lo)) & 15) != 0) { ok = false; return; }
+  if (has_lo != (g.X_lo != nullptr)) { ok = false; return; }
+  ph.n_tiles = g.N / kTileN;
+  ph.kbt = g.K / kBK;
+  ph.T = (long long)ph.n_tiles * ph.kbt;
+  ph.cnt_off = n_counters;
+  n_counters += ph.n_tiles;
+  ph.ep = g.ep;
+  ph.ep.M = M;
+  if (!make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN) || !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
+      (g.X_lo && !make_tmap_bf16(&ph.tmXlo, g.X_lo, g.rows_cap, g.K, MT))) {
+    ok = false;
+    return;
+  }
+  if (!g.X_lo) ph.tmXlo = ph.tmX;
+  phases.push_back(ph);
+}
+
+void StackProgramBuilder::attention(const AttnArgs& a) {
+  StackPhase ph{};
+  ph.kind = kPhaseAttn;
+  ph.at = a;
+  ph.at.M = M;
+  phases.push_back(ph);
+  ph.kind = kPhaseMerge;
+  phases.push_back(ph);
+}
+
+cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
+                      void* scratch, int* status, unsigned long long* trace, cudaStream_t s) {
+  if (!stack_supported(M, hd) || n_phases <= 0 || !scratch) return cudaErrorInvalidValue;
+  const int MT = round_mt(M);
+  const Layout l = layout(MT, has_lo);
+  if (l.sw < 2) return cudaErrorInvalidValue;
+  StackArgs a{};
+  a.ph = d_phases;
+  a.n_phases = n_phases;
+  a.M = M;
+  a.MT = MT;
+  a.has_lo = has_lo;
+  a.sw = l.sw;
+  a.sx = l.sx;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * MT)) cols <<= 1;
+  a.tmem_cols = cols;
+  char* base = reinterpret_cast<char*>(scratch);
+  a.done = reinterpret_cast<unsigned*>(base);
+  base += align256((size_t)(n_phases + 1) * 4);
+  a.tile_cnt = reinterpret_cast<int*>(base);
+  a.n_counters = n_counters;
+  base += align256((size_t)n_counters * 4);
+  a.partial = reinterpret_cast<float*>(base);
+  a.status = status;
+  a.trace = trace;
+  auto kernel = hd == 128 ? stack_tc_kernel<128> : stack_tc_kernel<64>;
+  static bool attr_set[2] = {false, false};
+  bool& set = attr_set[hd == 128 ? 1 : 0];
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  const int G = num_sms();
+  if (G > kMaxCtas) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = l.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident at once: phases wait on each other
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace eg

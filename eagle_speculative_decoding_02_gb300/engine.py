@@ -180,6 +180,19 @@ class EagleEngine:
         self._call("eagle_committed_counts", out.data_ptr())
         return out
 
+    def trace_layout(self) -> tuple[int, int]:
+        """(phases, CTAs) of the persistent verify pass; (0, 0) if the verify pass is not persistent."""
+        ph, ctas = C.c_int32(0), C.c_int32(0)
+        self.lib.eagle_set_trace(self.ctx, None, 0, C.byref(ph), C.byref(ctas))
+        return ph.value, ctas.value
+
+    def set_trace(self, buf: torch.Tensor | None) -> None:
+        """Record per-phase CTA completion times (int64 ns, [phases + 1, CTAs]) of every later verify pass."""
+        self._trace = buf
+        ptr = buf.data_ptr() if buf is not None else None
+        n = buf.numel() if buf is not None else 0
+        L.check("eagle_set_trace", self.lib.eagle_set_trace(self.ctx, ptr, n, None, None), self.ctx)
+
     def close(self) -> None:
         if getattr(self, "ctx", None):
             self.lib.eagle_destroy(self.ctx)

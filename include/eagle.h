@@ -275,6 +275,18 @@ eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_head
                                      const void* d_v, const uint64_t* d_mask, void* d_o, void* d_scratch,
                                      size_t scratch_bytes, void* stream);
 
+/* Phase trace of the verify pass (profiling aid; no counterpart in the pages).
+ * On a bf16 context whose verify pass runs as one persistent launch, reports
+ * that program's phase count P (per layer: QKV, attention, merge, O, gate/up,
+ * down; then the LM head) and the CTA count C; either output may be NULL.
+ * With d_trace non-NULL (device memory of n >= (P + 1) * C uint64 words, owned
+ * by the caller and kept alive while set), every later verify launch writes
+ * d_trace[p * C + c] = %globaltimer (ns) when CTA c finished phase p, and
+ * d_trace[P * C + c] = when CTA c started. d_trace NULL turns tracing off.
+ * EAGLE_ERR_INVALID_ARG if n is too small or the context has no persistent
+ * verify pass (then P = C = 0). Drops any captured step graph. */
+eagle_status eagle_set_trace(eagle_ctx* ctx, uint64_t* d_trace, size_t n, int32_t* n_phases, int32_t* n_ctas);
+
 /* Failure-detection self-test (no counterpart in the pages): one GPU thread
  * waits, with the same bounded wait as the GEMM pipeline's mbarrier waits, on
  * a barrier that nothing arrives on. After the wait's time limit (2 s) it gives
