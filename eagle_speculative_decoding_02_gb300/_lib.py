@@ -72,6 +72,8 @@ SIGNATURES = {
     "eagle_op_gemm_scratch_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "eagle_op_gemm": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "eagle_op_gemm_persistent_scratch_bytes": (C.c_size_t, [C.c_int32] * 5),
+    "eagle_op_gemm_persistent": (C.c_int, [C.c_int32] * 5 + [C.c_void_p] * 8 + [C.c_size_t, C.c_void_p]),
     "eagle_op_gemm_noalloc": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_void_p]),
     "eagle_selftest_bounded_wait": (C.c_int, [C.c_void_p, C.c_void_p]),

@@ -123,8 +123,10 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const float* qp = a.q + (((size_t)(g.row0 + node[i])) * a.Hq + qh[i]) * HD;
-      const float2 x0 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + qi * 2) : make_float2(0.f, 0.f);
-      const float2 x1 = rv[i] ? *reinterpret_cast<const float2*>(qp + kk * 16 + 8 + qi * 2) : make_float2(0.f, 0.f);
+      // q and the partials are read through L2: in the persistent kernel they were
+      // written earlier in the same launch by other SMs
+      const float2 x0 = rv[i] ? __ldcg(reinterpret_cast<const float2*>(qp + kk * 16 + qi * 2)) : make_float2(0.f, 0.f);
+      const float2 x1 = rv[i] ? __ldcg(reinterpret_cast<const float2*>(qp + kk * 16 + 8 + qi * 2)) : make_float2(0.f, 0.f);
       qa[kk][i] = pack_half2(x0.x * sl2, x0.y * sl2);
       qa[kk][i + 2] = pack_half2(x1.x * sl2, x1.y * sl2);
     }
@@ -258,12 +260,12 @@ __device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_
   const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
   // chunk maxima and sums: one load per lane and chunk, all lanes at once
   float M = -INFINITY;
-  for (int c = lane; c < nck; c += 32) M = fmaxf(M, base[(size_t)c * (HD + 2) + HD]);
+  for (int c = lane; c < nck; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (HD + 2) + HD));
   M = warp_max(M);
   float L = 0.f;
   for (int c = lane; c < nck; c += 32) {
-    const float m = base[(size_t)c * (HD + 2) + HD];
-    if (m != -INFINITY) L += exp2f(m - M) * base[(size_t)c * (HD + 2) + HD + 1];
+    const float m = __ldcg(base + (size_t)c * (HD + 2) + HD);
+    if (m != -INFINITY) L += exp2f(m - M) * __ldcg(base + (size_t)c * (HD + 2) + HD + 1);
   }
   L = warp_sum(L);
   // weighted sum of the chunk outputs in chunk order (independent loads, unrolled)
@@ -273,10 +275,10 @@ __device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_
 #pragma unroll 4
   for (int c = 0; c < nck; ++c) {
     const float* p = base + (size_t)c * (HD + 2);
-    const float m = p[HD];
+    const float m = __ldcg(p + HD);
     const float wgt = m == -INFINITY ? 0.f : exp2f(m - M);
 #pragma unroll
-    for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * p[lane + 32 * i];
+    for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * __ldcg(p + lane + 32 * i);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const size_t ob = ((size_t)row * a.Hq + qh) * HD;

@@ -544,10 +544,11 @@ struct Eng {
     return nullptr;
   }
 
-  static eagle_status run_prog(eagle_ctx* c, const ProgSpec& p, int n_phases) {
+  static eagle_status run_prog(eagle_ctx* c, const ProgSpec& p, float* lm_logits = nullptr) {
     unsigned long long* trace = p.kind == 0 ? c->trace : nullptr;
-    EG_CK(stack_run(c->stack_prog + p.first, n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
-                    c->stack_scratch, c->st.status, trace, c->stream));
+    EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
+                    c->stack_scratch, c->dm.stack_phases_max, c->dm.stack_counters_max, c->st.status, trace,
+                    lm_logits, c->stream));
     return EAGLE_OK;
   }
 
@@ -585,7 +586,7 @@ struct Eng {
                       c->stream));
     const ProgSpec* p = n_groups == dm.B ? find_prog(c, 1, M, hbase, k) : nullptr;
     if (p) {
-      EG_TRY(run_prog(c, *p, p->n_phases));
+      EG_TRY(run_prog(c, *p));
     } else {
       Direct d{c};
       EG_TRY(draft_ops(c, d, M, n_groups, hbase, k));
@@ -648,13 +649,9 @@ struct Eng {
     EG_CK(setup_verify_rows(c->st, tree, c->rows, c->groups, c->stream));
     const ProgSpec* p = find_prog(c, 0, M, 0, 1);
     if (p) {
-      // one persistent launch for every layer (and the LM head unless logits are wanted)
+      // one persistent launch for every layer and the LM head (which also stores the logits if wanted)
       EG_TRY(embed(c, M));
-      EG_TRY(run_prog(c, *p, d_logits ? p->n_phases - 1 : p->n_phases));
-      if (d_logits) {
-        Direct d{c};
-        EG_TRY(lm_head_gemm(c, d, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, d_logits));
-      }
+      EG_TRY(run_prog(c, *p, d_logits));
       EG_TRY(lm_head_merge(c, M, 1, c->vargmax, nullptr, nullptr));
     } else {
       EG_TRY(target_stack(c, M, dm.B));

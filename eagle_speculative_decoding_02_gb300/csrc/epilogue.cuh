@@ -19,6 +19,10 @@ constexpr int kEpiRowSmemFloats = 4 * kEpiRows;
 // so that their latencies overlap.
 constexpr int kEpiBatch = 8;
 
+// Inputs that earlier phases of the same persistent launch may have written
+// (row sums of squares, the residual stream) are read through L2 (ld.global.cg):
+// the SM's L1 is not coherent with other SMs' stores within one launch.
+//
 // rowsm must hold kEpiRowSmemFloats words of shared memory; msub <= kEpiRows.
 // Run by 128 threads with ranks tid = 0..127; sync() must be a barrier over
 // exactly those threads.
@@ -41,9 +45,9 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
       int j = 0;
       for (; j + kEpiBatch <= p.n_ssq_in; j += kEpiBatch) {
 #pragma unroll
-        for (int q = 0; q < kEpiBatch; ++q) part[q] += s_in[(size_t)(j + q) * p.M];
+        for (int q = 0; q < kEpiBatch; ++q) part[q] += __ldcg(s_in + (size_t)(j + q) * p.M);
       }
-      for (; j < p.n_ssq_in; ++j) part[0] += s_in[(size_t)j * p.M];
+      for (; j < p.n_ssq_in; ++j) part[0] += __ldcg(s_in + (size_t)j * p.M);
       float s = 0.f;
 #pragma unroll
       for (int q = 0; q < kEpiBatch; ++q) s += part[q];
@@ -131,7 +135,7 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
           float hv[kEpiBatch];
 #pragma unroll
           for (int q = 0; q < kEpiBatch; ++q)  // residual loads of the batch, ahead of its stores
-            hv[q] = (p.kind == kEpiResid && mb + q < msub) ? p.h[(size_t)(m0 + mb + q) * p.N + n] : 0.f;
+            hv[q] = (p.kind == kEpiResid && mb + q < msub) ? __ldcg(p.h + (size_t)(m0 + mb + q) * p.N + n) : 0.f;
 #pragma unroll
           for (int q = 0; q < kEpiBatch; ++q) {
             const int m = mb + q;

@@ -57,17 +57,22 @@ bool stack_supported(int M, int hd);
 int stack_mt(int M);
 // CTAs of one launch (one per SM).
 int stack_ctas();
-// Bytes of device scratch for programs over at most M rows, n_phases phases and
-// n_counters split-K counters: phase counters, split-K counters, partial sums
-// (zero-initialised by the caller once).
-size_t stack_scratch_bytes(int M, int n_phases, int n_counters);
+// Bytes of device scratch shared by programs of at most M rows, max_phases
+// phases and max_counters split-K counters: phase counters, split-K counters,
+// partial sums (zero-initialised by the caller once).
+size_t stack_scratch_bytes(int M, int max_phases, int max_counters);
 // Attention partial buffer of the persistent kernel.
 size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix);
 // Runs the program (d_phases: device copy of builder.phases) on stack_ctas()
-// CTAs. Scratch counters must be zero on entry; the kernel leaves them zero.
+// CTAs. scratch holds stack_scratch_bytes(M', max_phases, max_counters) bytes
+// for capacities that every program sharing it fits (the layout is derived from
+// them alone). Scratch counters must be zero on entry; the kernel leaves them zero.
 // trace (may be NULL): [n_phases + 1][stack_ctas()] %globaltimer stamps - row p
 // = when each CTA finished phase p, the last row = when it started.
+// y_last (may be NULL): replaces the output pointer y of the last phase's
+// epilogue for this launch (the LM head's optional logits).
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
-                      void* scratch, int* status, unsigned long long* trace, cudaStream_t s);
+                      void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
+                      float* y_last, cudaStream_t s);
 
 }  // namespace eg

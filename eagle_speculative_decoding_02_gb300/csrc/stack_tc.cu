@@ -32,6 +32,7 @@
 // their own waits.
 #include <cuda.h>
 
+#include "../../include/eagle.h"
 #include "attention_tc.cuh"
 #include "epilogue.cuh"
 #include "stack.h"
@@ -53,10 +54,8 @@ constexpr int kAttnCK = 64;                // keys per attention chunk
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
 constexpr int kHdMax = 128;
 constexpr int kMaxCtas = 160;              // partial buffer sizing bound
-constexpr size_t kUnionBytes =
-    attn::smem_bytes<kHdMax, kAttnCK>() > (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4
-        ? attn::smem_bytes<kHdMax, kAttnCK>()
-        : (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4;
+constexpr size_t kTileBytes = (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4;  // epilogue staging
+constexpr size_t kAttnBytes = attn::smem_bytes<kHdMax, kAttnCK>();             // attention K and V
 
 struct StackArgs {
   const StackPhase* ph;
@@ -69,6 +68,7 @@ struct StackArgs {
   float* partial;    // [G][2][MT][128]
   int* status;
   unsigned long long* trace;  // optional: [n_phases + 1][G] %globaltimer stamps
+  float* y_last;              // optional: output y of the last phase's epilogue (LM-head logits)
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -171,12 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   const int xbytes = xbox * (a.has_lo ? 2 : 1);
   uint8_t* wring = smem;
   uint8_t* xring = wring + (size_t)SW * kWBytes;
-  uint8_t* uni = xring + (size_t)SX * xbytes;  // epilogue tile or attention K/V
-  float* tile = reinterpret_cast<float*>(uni);
-  float* rscale = tile + kSub * kLdt;
-  half* Ks = reinterpret_cast<half*>(uni);
+  // Attention and merge phases run while the activation ring is idle (the next
+  // GEMM phase's boxes wait for them to finish), so their K / V buffers alias it.
+  half* Ks = reinterpret_cast<half*>(xring);
   half* Vs = Ks + kAttnCK * (HD + attn::kPad);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(uni + kUnionBytes);
+  float* tile = reinterpret_cast<float*>(xring + (size_t)SX * xbytes);
+  float* rscale = tile + kSub * kLdt;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes);
   uint64_t* wfull = bars;
   uint64_t* wempty = wfull + SW;
   uint64_t* xfull = wempty + SW;
@@ -359,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       const StackPhase& P = a.ph[p];
       if (p > 0 && alive) alive = epi_all(etid != 0 || wait_phase(a, p - 1, (unsigned)G, abort_flag));
       if (alive && P.kind == kPhaseGemm) {
-        const EpiParams& ep = P.ep;
+        EpiParams ep = P.ep;
+        if (a.y_last && p == a.n_phases - 1) ep.y = a.y_last;
         const long long T = P.T;
         const int kbt = P.kbt;
         const int Gp = phase_ctas(T, G);
@@ -528,8 +530,11 @@ struct Layout {
 Layout layout(int MT, bool has_lo) {
   Layout l{};
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
-  l.sx = MT <= 64 ? 3 : 2;
-  const size_t fixed = kUnionBytes + (size_t)(2 * kMaxW + 2 * 3 + 5) * 8 + 16 + 1024;
+  // activation stages: about as many as weight stages (each unit needs one of
+  // each), and enough bytes for the attention buffers that alias the ring
+  l.sx = MT <= 32 ? 6 : (MT <= 64 ? 6 : 3);
+  while ((size_t)l.sx * xbytes < kAttnBytes) ++l.sx;
+  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 2 * 8 + 5) * 8 + 16 + 1024;
   const long long room = (long long)kSmemBudget - (long long)fixed - (long long)l.sx * (long long)xbytes;
   l.sw = (int)std::min<long long>(kMaxW, room / kWBytes);
   l.smem = (size_t)l.sw * kWBytes + (size_t)l.sx * xbytes + fixed;
@@ -551,8 +556,8 @@ int stack_ctas() { return num_sms(); }
 
 bool stack_supported(int M, int hd) { return M >= 1 && M <= kStackMaxRows && (hd == 64 || hd == 128); }
 
-size_t stack_scratch_bytes(int M, int n_phases, int n_counters) {
-  return align256((size_t)(n_phases + 1) * 4) + align256((size_t)n_counters * 4) +
+size_t stack_scratch_bytes(int M, int max_phases, int max_counters) {
+  return align256((size_t)(max_phases + 1) * 4) + align256((size_t)max_counters * 4) +
          (size_t)kMaxCtas * 2 * round_mt(M) * kTileN * 4;
 }
 
@@ -597,8 +602,10 @@ void StackProgramBuilder::attention(const AttnArgs& a) {
 }
 
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
-                      void* scratch, int* status, unsigned long long* trace, cudaStream_t s) {
-  if (!stack_supported(M, hd) || n_phases <= 0 || !scratch) return cudaErrorInvalidValue;
+                      void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
+                      float* y_last, cudaStream_t s) {
+  if (!stack_supported(M, hd) || n_phases <= 0 || !scratch || n_phases > max_phases || n_counters > max_counters)
+    return cudaErrorInvalidValue;
   const int MT = round_mt(M);
   const Layout l = layout(MT, has_lo);
   if (l.sw < 2) return cudaErrorInvalidValue;
@@ -613,15 +620,18 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * MT)) cols <<= 1;
   a.tmem_cols = cols;
+  // the layout depends only on the capacities, never on this program: programs
+  // of every size share one scratch
   char* base = reinterpret_cast<char*>(scratch);
   a.done = reinterpret_cast<unsigned*>(base);
-  base += align256((size_t)(n_phases + 1) * 4);
+  base += align256((size_t)(max_phases + 1) * 4);
   a.tile_cnt = reinterpret_cast<int*>(base);
   a.n_counters = n_counters;
-  base += align256((size_t)n_counters * 4);
+  base += align256((size_t)max_counters * 4);
   a.partial = reinterpret_cast<float*>(base);
   a.status = status;
   a.trace = trace;
+  a.y_last = y_last;
   auto kernel = hd == 128 ? stack_tc_kernel<128> : stack_tc_kernel<64>;
   static bool attr_set[2] = {false, false};
   bool& set = attr_set[hd == 128 ? 1 : 0];
@@ -646,3 +656,74 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
 }
 
 }  // namespace eg
+
+// ------------------------------------------------------------------ op entry point
+namespace eg {
+namespace {
+size_t op_prog_bytes(int n_phases) { return align256((size_t)n_phases * sizeof(StackPhase)); }
+size_t op_rec_bytes(int M, int N, int k) {
+  const size_t nt = (size_t)((N + kTileN - 1) / kTileN) * M;
+  return k > 0 ? 2 * align256(nt * k * 4) + 2 * align256(nt * 4) : 0;
+}
+}  // namespace
+}  // namespace eg
+
+extern "C" {
+
+size_t eagle_op_gemm_persistent_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t n_phases, int32_t k) {
+  using namespace eg;
+  if (M < 1 || N < 1 || K < 1 || n_phases < 1 || k < 0 || k > kMaxTopK) return 0;
+  return op_prog_bytes(n_phases) + op_rec_bytes(M, N, k) +
+         stack_scratch_bytes(M, n_phases, n_phases * ((N + kTileN - 1) / kTileN));
+}
+
+eagle_status eagle_op_gemm_persistent(int32_t M, int32_t N, int32_t K, int32_t n_phases, int32_t k, const void* x,
+                                      const void* x_lo, const void* w, float* y, int32_t* idx, float* val,
+                                      float* lse, void* scratch, size_t scratch_bytes, void* stream) {
+  using namespace eg;
+  if (M < 1 || N < 1 || K < 1 || n_phases < 1 || k < 0 || k > kMaxTopK || !x || !w || !scratch)
+    return EAGLE_ERR_INVALID_ARG;
+  if ((k == 0 || n_phases > 1) && !y) return EAGLE_ERR_INVALID_ARG;
+  if (k > 0 && !idx) return EAGLE_ERR_INVALID_ARG;
+  if (!stack_supported(M, 128) || N % kTileN || K % kBK) return EAGLE_ERR_UNSUPPORTED;
+  if (scratch_bytes < eagle_op_gemm_persistent_scratch_bytes(M, N, K, n_phases, k)) return EAGLE_ERR_WORKSPACE;
+  char* p = reinterpret_cast<char*>(scratch);
+  StackPhase* d_prog = reinterpret_cast<StackPhase*>(p);
+  p += op_prog_bytes(n_phases);
+  const size_t nt = (size_t)((N + kTileN - 1) / kTileN) * M;
+  EpiParams lm;
+  lm.kind = kEpiLmHead;
+  lm.N = N;
+  lm.topk = k;
+  if (k > 0) {
+    lm.rec_val = reinterpret_cast<float*>(p); p += align256(nt * k * 4);
+    lm.rec_idx = reinterpret_cast<int*>(p); p += align256(nt * k * 4);
+    lm.rec_max = reinterpret_cast<float*>(p); p += align256(nt * 4);
+    lm.rec_sum = reinterpret_cast<float*>(p); p += align256(nt * 4);
+  }
+  StackProgramBuilder b;
+  b.M = M;
+  b.MT = stack_mt(M);
+  b.has_lo = x_lo != nullptr;
+  EpiParams st;
+  st.kind = kEpiStore;
+  st.N = N;
+  st.y = y;
+  for (int i = 0; i < n_phases; ++i)
+    b.gemm(StackGemmDesc{(const bf16*)w, (const bf16*)x, (const bf16*)x_lo, M, N, K,
+                         (k > 0 && i == n_phases - 1) ? lm : st});
+  if (!b.ok) return EAGLE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(d_prog, b.phases.data(), b.phases.size() * sizeof(StackPhase), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return EAGLE_ERR_CUDA;
+  cudaError_t err = stack_run(d_prog, n_phases, M, x_lo != nullptr, 128, b.n_counters, p, n_phases, b.n_counters,
+                              nullptr, nullptr, nullptr, s);
+  if (err == cudaSuccess && k > 0)
+    err = topk_merge(lm.rec_val, lm.rec_idx, lm.rec_max, lm.rec_sum, (N + kTileN - 1) / kTileN, M, k, idx, val, lse,
+                     s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);  // b.phases is a host temporary
+  return err == cudaSuccess ? EAGLE_OK : (err == cudaErrorInvalidValue ? EAGLE_ERR_UNSUPPORTED : EAGLE_ERR_CUDA);
+}
+
+}  // extern "C"

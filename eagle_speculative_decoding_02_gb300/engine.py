@@ -230,6 +230,31 @@ def op_gemm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
     return y
 
 
+def op_gemm_persistent(x: torch.Tensor, w: torch.Tensor, n_phases: int = 1, x_lo: torch.Tensor | None = None,
+                       k: int = 0, scratch: torch.Tensor | None = None):
+    """n_phases GEMM phases Y = (X + X_lo) W^T in one persistent launch (bf16, M <= 128).
+
+    k == 0: returns Y. k > 0: the last phase is the LM-head top-k epilogue; returns (Y of the earlier
+    phases or None, idx [M, k], val [M, k], lse [M])."""
+    lib = L.load()
+    M, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if (k == 0 or n_phases > 1) else None
+    idx = torch.empty((M, max(k, 1)), dtype=torch.int32, device=x.device)
+    val = torch.empty((M, max(k, 1)), dtype=torch.float32, device=x.device)
+    lse = torch.empty((M,), dtype=torch.float32, device=x.device)
+    if scratch is None:
+        nb = lib.eagle_op_gemm_persistent_scratch_bytes(M, N, K, n_phases, k)
+        scratch = torch.zeros(int(nb), dtype=torch.uint8, device=x.device)
+    s = torch.cuda.current_stream(x.device).cuda_stream
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    L.check("eagle_op_gemm_persistent",
+            lib.eagle_op_gemm_persistent(M, N, K, n_phases, k, x.data_ptr(), ptr(x_lo), w.data_ptr(), ptr(y),
+                                         idx.data_ptr(), val.data_ptr(), lse.data_ptr(), scratch.data_ptr(),
+                                         scratch.numel(), s))
+    return y if k == 0 else (y, idx, val, lse)
+
+
 def op_lmhead_topk(x: torch.Tensor, w: torch.Tensor, k: int):
     lib = L.load()
     M, K = x.shape

@@ -259,6 +259,22 @@ eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, const void* 
 /* LM head + per-row top-k: for each row m of X [M,K], the k largest logits of
  * X W^T (W [N,K]) as (index, value) ordered by value desc then index asc, and
  * the row's log-sum-exp. d_idx/d_val [M][k], d_lse [M]. */
+/* The same products run by the persistent layer-stack kernel (the kernel of the
+ * verify and draft passes), for checking its work split against eagle_op_gemm
+ * and eagle_op_lmhead_topk: n_phases GEMM phases Y = (X + X_lo) W^T in one
+ * cooperative launch, each waiting for the previous one. k == 0: every phase
+ * stores Y into d_y. k > 0: the last phase is the LM-head epilogue instead
+ * (top-k per row, merged into d_idx/d_val/d_lse as eagle_op_lmhead_topk does;
+ * d_val and d_lse may be NULL). bf16 only; 1 <= M <= 128, N % 128 == 0,
+ * K % 64 == 0, k <= 16. d_scratch: eagle_op_gemm_persistent_scratch_bytes()
+ * bytes, zeroed once before first use (the kernel leaves its counters zero).
+ * Synchronises `stream` before returning. */
+size_t eagle_op_gemm_persistent_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t n_phases, int32_t k);
+eagle_status eagle_op_gemm_persistent(int32_t M, int32_t N, int32_t K, int32_t n_phases, int32_t k,
+                                      const void* d_x, const void* d_x_lo, const void* d_w, float* d_y,
+                                      int32_t* d_idx, float* d_val, float* d_lse, void* d_scratch,
+                                      size_t scratch_bytes, void* stream);
+
 size_t eagle_op_lmhead_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t k, int32_t dtype);
 eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k, const void* d_x,
                                   const void* d_w, int32_t* d_idx, float* d_val, float* d_lse, void* d_scratch,
