@@ -51,7 +51,9 @@ constexpr size_t kNoAllocScratchBytes = kCounterBytes + (size_t)kNsmSizing * 2 *
 
 struct TcArgs {
   int M, MT, m_chunks, n_tiles, kbt, G, stages;
-  int has_lo;      // activations come as a hi/lo pair: a second X box per stage and a second MMA per k-step
+  int has_lo;      // activations come as a hi/lo pair: a second X box per stage, right after the first
+  int wide;        // has_lo and 2 MT <= 256: one MMA of N = 2 MT per k-step covers both boxes, the
+                   // accumulator holds the hi products in columns [0, MT) and the lo ones in [MT, 2 MT)
   long long T;
   uint32_t tmem_cols;
   int* counters;   // [m_chunks][n_tiles], zero on entry and on exit
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      const uint32_t idesc = idesc_bf16(MT);
+      const uint32_t idesc = idesc_bf16(a.wide ? 2 * MT : MT);
+      const int accw = a.wide ? 2 * MT : MT;
       int it = 0, f = 0;
       bool ok = true;
       for (long long u = u0; u < u1 && ok;) {
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = f & 1;
         if (f >= 2 && !mbar_wait(&aempty[buf], ((f >> 1) - 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * MT);
+        const uint32_t d = tmem + (uint32_t)(buf * accw);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
           if (!mbar_wait(&full[s], (it / S) & 1, abort_flag, a.status)) {
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             umma(d, sw128_desc(sw + k * 32), sw128_desc(sx + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            if (a.has_lo) umma(d, sw128_desc(sw + k * 32), sw128_desc(sx + xbytes + k * 32), idesc, 1u);
+            if (a.has_lo && !a.wide) umma(d, sw128_desc(sw + k * 32), sw128_desc(sx + xbytes + k * 32), idesc, 1u);
           }
           umma_commit(&empty[s]);
         }
@@ -234,12 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = f & 1;
       const bool ok = epi_all(mbar_wait(&afull[buf], (f >> 1) & 1, abort_flag, a.status));
       tc_fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MT);
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * (a.wide ? 2 * MT : MT));
       const int n0 = t * kTileN;
       if (whole) {
         for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
           float v[32];
-          tmem_ld32(tb + r0, v);
+          tmem_ld32_pair(tb + r0, a.wide ? MT : 0, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) tile[j * kLdt + col] = ok ? v[j] : 0.f;
           EpilogueSync{}();
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* slot = a.partial + (((size_t)mc * a.G + c) * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
         for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
           float v[32];
-          tmem_ld32(tb + r0, v);
+          tmem_ld32_pair(tb + r0, a.wide ? MT : 0, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (r0 + j < rows_valid) slot[(size_t)(r0 + j) * kTileN + col] = v[j];
@@ -371,7 +374,7 @@ int num_sms() {
 namespace {
 
 struct Plan {
-  int MT, m_chunks, n_tiles, kbt, G, stages;
+  int MT, m_chunks, n_tiles, kbt, G, stages, wide;
   long long T;
   uint32_t tmem_cols;
   size_t smem, counters_bytes, partial_bytes;
@@ -389,8 +392,9 @@ Plan plan(int M, int N, int K, int nsm, bool has_lo) {
   // case, including the LM head); plain one-tile-per-CTA for large prefills.
   const bool split = p.m_chunks <= 4 || (long long)p.m_chunks * p.n_tiles < 2LL * nsm;
   p.G = split ? (int)std::min<long long>(nsm, p.T) : p.n_tiles;
+  p.wide = has_lo && 2 * p.MT <= 256;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * p.MT)) cols <<= 1;
+  while (cols < (uint32_t)(2 * (p.wide ? 2 * p.MT : p.MT))) cols <<= 1;
   p.tmem_cols = cols;
   const size_t stage = kWBytes + (size_t)p.MT * kBK * 2 * (has_lo ? 2 : 1);
   const size_t fixed = (size_t)kSub * kLdt * 4 + kEpiRowSmemFloats * 4 + (2 * kMaxStages + 5) * 8 + 16 + 1024;
@@ -443,6 +447,7 @@ cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N
   a.T = p.T;
   a.tmem_cols = p.tmem_cols;
   a.has_lo = X_lo != nullptr;
+  a.wide = p.wide;
   a.counters = reinterpret_cast<int*>(scratch);
   a.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + p.counters_bytes);
   a.status = status;

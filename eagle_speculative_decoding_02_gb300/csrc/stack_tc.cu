@@ -23,10 +23,13 @@
 // wait for done[p - 1].
 //
 // Warp roles (224 threads):
-//   warp 0     weight producer (one lane): weight ring (SW stages)
+//   warp 0     weight producer (one lane): weight half of each ring slot
 //   warp 1     TMEM allocator and MMA issuer (one lane)
 //   warps 2-5  epilogue, attention and merge (128 threads)
-//   warp 6     activation producer (one lane): activation ring (SX stages)
+//   warp 6     activation producer (one lane): activation half of each ring slot
+// Unit i uses ring slot i % S in both halves; one full barrier per slot takes
+// both producers' arrivals and bytes, one empty barrier (the MMA's commit)
+// frees the slot for both, as in a single-producer pipeline.
 // Every wait is bounded (2 s); on a timeout the CTA records kStTimeout, stops
 // issuing work, drains its copies and returns; other CTAs then time out on
 // their own waits.
@@ -166,23 +169,22 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int SW = a.sw, SX = a.sx, MT = a.MT;
+  const int S = a.sw, MT = a.MT;
+  const int accw = a.has_lo ? 2 * MT : MT;  // accumulator columns per buffer
   const int xbox = MT * kBK * 2;
   const int xbytes = xbox * (a.has_lo ? 2 : 1);
   uint8_t* wring = smem;
-  uint8_t* xring = wring + (size_t)SW * kWBytes;
+  uint8_t* xring = wring + (size_t)S * kWBytes;
   // Attention and merge phases run while the activation ring is idle (the next
   // GEMM phase's boxes wait for them to finish), so their K / V buffers alias it.
   half* Ks = reinterpret_cast<half*>(xring);
   half* Vs = Ks + kAttnCK * (HD + attn::kPad);
-  float* tile = reinterpret_cast<float*>(xring + (size_t)SX * xbytes);
+  float* tile = reinterpret_cast<float*>(xring + (size_t)S * xbytes);
   float* rscale = tile + kSub * kLdt;
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes);
-  uint64_t* wfull = bars;
-  uint64_t* wempty = wfull + SW;
-  uint64_t* xfull = wempty + SW;
-  uint64_t* xempty = xfull + SX;
-  uint64_t* afull = xempty + SX;
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* afull = empty + S;
   uint64_t* aempty = afull + 2;
   uint64_t* drain = aempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -194,13 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   const int c = blockIdx.x, G = gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < SW; ++s) {
-      mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], 1);
-    }
-    for (int s = 0; s < SX; ++s) {
-      mbar_init(&xfull[s], 1);
-      mbar_init(&xempty[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 2);  // the weight and the activation producer
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&afull[b], 1);
@@ -236,23 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       long long iw = 0;
       bool ok = true;
       while (more && ok) {
-        const int s = (int)(iw % SW);
-        if (iw >= SW && !mbar_wait(&wempty[s], (uint32_t)((iw / SW) - 1) & 1, abort_flag, a.status)) {
+        const int s = (int)(iw % S);
+        if (iw >= S && !mbar_wait(&empty[s], (uint32_t)((iw / S) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
         }
         const StackPhase& P = a.ph[W.p];
         const int t = (int)(W.u / P.kbt), kb = (int)(W.u % P.kbt);
-        mbar_expect_tx(&wfull[s], (uint32_t)kWBytes);
-        tma_load_2d_hint(wring + (size_t)s * kWBytes, &P.tmW, &wfull[s], kb * kBK, t * kTileN, pol_w);
+        mbar_expect_tx(&full[s], (uint32_t)kWBytes);
+        tma_load_2d_hint(wring + (size_t)s * kWBytes, &P.tmW, &full[s], kb * kBK, t * kTileN, pol_w);
         ++iw;
         if (++W.u == W.u1) more = W.next(a, c, G);
       }
       if (!ok) {
         // drain (bounded): every box issued must land before the CTA exits
-        for (long long j = (iw > SW ? iw - SW : 0); j < iw; ++j) {
+        for (long long j = (iw > S ? iw - S : 0); j < iw; ++j) {
           const unsigned long long t0 = globaltimer();
-          while (!mbar_try_wait(&wfull[j % SW], (uint32_t)(j / SW) & 1) && globaltimer() - t0 < kTimeoutNs) {
+          while (!mbar_try_wait(&full[j % S], (uint32_t)(j / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
           }
         }
       }
@@ -277,24 +275,24 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           fence_proxy_async();  // the phase's activations were written by other CTAs' generic stores
           ready = X.p;
         }
-        const int s = (int)(ix % SX);
-        if (ix >= SX && !mbar_wait(&xempty[s], (uint32_t)((ix / SX) - 1) & 1, abort_flag, a.status)) {
+        const int s = (int)(ix % S);
+        if (ix >= S && !mbar_wait(&empty[s], (uint32_t)((ix / S) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
         }
         const StackPhase& P = a.ph[X.p];
         const int kb = (int)(X.u % P.kbt);
         uint8_t* dst = xring + (size_t)s * xbytes;
-        mbar_expect_tx(&xfull[s], (uint32_t)xbytes);
-        tma_load_2d_hint(dst, &P.tmX, &xfull[s], kb * kBK, 0, pol_x);
-        if (a.has_lo) tma_load_2d_hint(dst + xbox, &P.tmXlo, &xfull[s], kb * kBK, 0, pol_x);
+        mbar_expect_tx(&full[s], (uint32_t)xbytes);
+        tma_load_2d_hint(dst, &P.tmX, &full[s], kb * kBK, 0, pol_x);
+        if (a.has_lo) tma_load_2d_hint(dst + xbox, &P.tmXlo, &full[s], kb * kBK, 0, pol_x);
         ++ix;
         if (++X.u == X.u1) more = X.next(a, c, G);
       }
       if (!ok) {
-        for (long long j = (ix > SX ? ix - SX : 0); j < ix; ++j) {
+        for (long long j = (ix > S ? ix - S : 0); j < ix; ++j) {
           const unsigned long long t0 = globaltimer();
-          while (!mbar_try_wait(&xfull[j % SX], (uint32_t)(j / SX) & 1) && globaltimer() - t0 < kTimeoutNs) {
+          while (!mbar_try_wait(&full[j % S], (uint32_t)(j / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
           }
         }
       }
@@ -302,7 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16(MT);
+      // hi/lo pairs: one MMA of N = 2 MT over both boxes (hi products in accumulator
+      // columns [0, MT), lo ones in [MT, 2 MT), added by the epilogue)
+      const uint32_t idesc = idesc_bf16(a.has_lo ? 2 * MT : MT);
       Cursor C;
       bool more = C.next(a, c, G);
       long long i = 0;
@@ -316,11 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
         const int buf = f & 1;
         if (f >= 2 && !mbar_wait(&aempty[buf], (uint32_t)((f >> 1) - 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * MT);
+        const uint32_t d = tmem + (uint32_t)(buf * accw);
         for (int kb = kb0; kb < kb1; ++kb, ++i) {
-          const int sw = (int)(i % SW), sx = (int)(i % SX);
-          if (!mbar_wait(&wfull[sw], (uint32_t)(i / SW) & 1, abort_flag, a.status) ||
-              !mbar_wait(&xfull[sx], (uint32_t)(i / SX) & 1, abort_flag, a.status)) {
+          const int sw = (int)(i % S), sx = sw;
+          if (!mbar_wait(&full[sw], (uint32_t)(i / S) & 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
@@ -330,10 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             umma(d, sw128_desc(aw + k * 32), sw128_desc(ax + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            if (a.has_lo) umma(d, sw128_desc(aw + k * 32), sw128_desc(ax + xbox + k * 32), idesc, 1u);
           }
-          umma_commit(&wempty[sw]);
-          umma_commit(&xempty[sx]);
+          umma_commit(&empty[sw]);
         }
         if (!ok) break;
         umma_commit(&afull[buf]);
@@ -375,14 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           const int buf = f & 1;
           const bool ok = epi_all(mbar_wait(&afull[buf], (uint32_t)(f >> 1) & 1, abort_flag, a.status));
           tc_fence_after();
-          const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MT);
+          const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * accw);
           const int n0 = t * kTileN;
           if (!ok) {
             alive = false;
           } else if (whole) {
             for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
               float v[32];
-              tmem_ld32(tb + r0, v);
+              tmem_ld32_pair(tb + r0, a.has_lo ? MT : 0, v);
 #pragma unroll
               for (int j = 0; j < 32; ++j) tile[j * kLdt + col] = v[j];
               EpilogueSync{}();
@@ -397,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
             float* slot = a.partial + ((size_t)c * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
             for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
               float v[32];
-              tmem_ld32(tb + r0, v);
+              tmem_ld32_pair(tb + r0, a.has_lo ? MT : 0, v);
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 if (r0 + j < rows_valid) __stcg(slot + (size_t)(r0 + j) * kTileN + col, v[j]);
@@ -532,12 +529,14 @@ Layout layout(int MT, bool has_lo) {
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
   // activation stages: about as many as weight stages (each unit needs one of
   // each), and enough bytes for the attention buffers that alias the ring
-  l.sx = MT <= 32 ? 6 : (MT <= 64 ? 6 : 3);
-  while ((size_t)l.sx * xbytes < kAttnBytes) ++l.sx;
+  // S slots of one weight box and one activation box each (the attention buffers
+  // alias the activation halves, which need at least kAttnBytes)
   const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 2 * 8 + 5) * 8 + 16 + 1024;
-  const long long room = (long long)kSmemBudget - (long long)fixed - (long long)l.sx * (long long)xbytes;
-  l.sw = (int)std::min<long long>(kMaxW, room / kWBytes);
-  l.smem = (size_t)l.sw * kWBytes + (size_t)l.sx * xbytes + fixed;
+  const long long room = (long long)kSmemBudget - (long long)fixed;
+  l.sw = (int)std::min<long long>(kMaxW, room / (long long)(kWBytes + xbytes));
+  l.sx = l.sw;
+  if ((size_t)l.sx * xbytes < kAttnBytes) l.sw = l.sx = 0;  // rejected by stack_run
+  l.smem = (size_t)l.sw * (kWBytes + xbytes) + fixed;
   return l;
 }
 
@@ -618,7 +617,7 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.sw = l.sw;
   a.sx = l.sx;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * MT)) cols <<= 1;
+  while (cols < (uint32_t)(2 * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
   a.tmem_cols = cols;
   // the layout depends only on the capacities, never on this program: programs
   // of every size share one scratch

@@ -129,5 +129,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 accumulator columns at taddr, plus (lo_off != 0) the 32 columns lo_off
+// further on added to them: the hi and lo halves of a wide hi/lo accumulator.
+__device__ __forceinline__ void tmem_ld32_pair(uint32_t taddr, int lo_off, float* v) {
+  tmem_ld32(taddr, v);
+  if (lo_off) {
+    float w[32];
+    tmem_ld32(taddr + (uint32_t)lo_off, w);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += w[i];
+  }
+}
+
 }  // namespace tc
 }  // namespace eg
