@@ -6,19 +6,21 @@ namespace eg {
 namespace {
 
 using namespace attn;
-// Keys per chunk: the same as the persistent layer-stack kernel's, so that both
-// paths sum every attention output in the same order (bit-identical rows).
-constexpr int kCK = 64;
+// Keys per work item and per staging sub-chunk: the same as the persistent
+// layer-stack kernel's, so that both paths sum every attention output in the
+// same order (bit-identical rows).
+constexpr int kCKI = 256;
+constexpr int kCKS = 64;
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(AttnArgs a, int n_chunk_slots) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  half* Ks = reinterpret_cast<half*>(smem_raw);  // [kCK][HD + kPad]
-  half* Vs = Ks + kCK * (HD + kPad);             // [kCK][HD + kPad]
+  half* buf = reinterpret_cast<half*>(smem_raw);  // two staging buffers, each K then V
   // programmatic dependent launch: every CTA waits for the producer of q / K / V before any read
   pdl_wait();
   if (threadIdx.x == 0) pdl_trigger();
-  attn_item<HD, kCK>(a, blockIdx.x, blockIdx.y, blockIdx.z, n_chunk_slots, Ks, Vs, threadIdx.x, BlockSync{});
+  attn_item<HD, kCKI, kCKS>(a, blockIdx.x, blockIdx.y, blockIdx.z, n_chunk_slots, buf, 2, threadIdx.x,
+                            BlockSync{});
 }
 
 template <int HD>
@@ -26,13 +28,13 @@ __global__ void attn_merge_kernel(AttnArgs a, int n_chunk_slots) {
   pdl_wait();
   if (threadIdx.x == 0) pdl_trigger();
   const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (w < a.M * a.Hq) attn_merge_warp<HD, kCK>(a, w, threadIdx.x & 31, n_chunk_slots);
+  if (w < a.M * a.Hq) attn_merge_warp<HD, kCKI>(a, w, threadIdx.x & 31, n_chunk_slots);
 }
 
 template <int HD>
 cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
-  const int slots = n_prefix_chunks(a.max_prefix, kCK) + 1;
-  const size_t smem = smem_bytes<HD, kCK>();
+  const int slots = n_prefix_chunks(a.max_prefix, kCKI) + 1;
+  const size_t smem = 2 * smem_bytes<HD, kCKS>();  // double-buffered sub-chunks
   static bool smem_set = false;
   if (!smem_set) {
     cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -61,7 +63,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
 }  // namespace
 
 size_t attention_tc_scratch_bytes(int M, int Hq, int hd, int max_prefix) {
-  const size_t slots = (size_t)n_prefix_chunks(max_prefix, kCK) + 1;
+  const size_t slots = (size_t)n_prefix_chunks(max_prefix, kCKI) + 1;
   return (size_t)M * Hq * slots * (hd + 2) * sizeof(float);
 }
 

@@ -8,14 +8,15 @@
 // tree block whose bit i is set in node j's ancestor mask.
 //
 // Split-K flash decode: work item (chunk c, KV head and 64-row block, group)
-// takes either prefix keys [CK c, CK c + CK) or, for c == ceil(prefix / CK),
+// takes either prefix keys [CKI c, CKI c + CKI) or, for c == ceil(prefix / CKI),
 // the tree block, and 64 of the group's rows x G = Hq / Hkv query heads sharing
-// that KV head (the GQA rows form the M dimension of the MMA). An item stages
-// its keys in shared memory with cp.async (V fragments are read transposed with
-// ldmatrix.trans); each of its 4 warps runs one 16-row tile with an online
+// that KV head (the GQA rows form the M dimension of the MMA). An item streams
+// its keys through shared memory in sub-chunks of CKS keys with cp.async, the
+// next sub-chunk in flight while the current one is used (V fragments are read
+// transposed with ldmatrix.trans); each of its 4 warps runs one 16-row tile with an online
 // softmax and writes an unnormalised partial (max, sum, O). attn_merge_warp
 // combines the partials of a row in chunk order. Chunk boundaries are absolute
-// slot multiples of CK, independent of how many rows are verified. The KV cache
+// slot multiples of CKI, independent of how many rows are verified or batched. The KV cache
 // of a bf16 model holds IEEE half values; q (float32, pre-scaled) and the
 // probabilities P enter the products rounded to half, so both MMAs are
 // f16 x f16 with fp32 accumulation.
@@ -37,9 +38,9 @@ constexpr int kRowBlock = 64;       // GQA rows (node x query head) per work ite
 __host__ __device__ inline int row_blocks(int Hq, int Hkv) {
   return (kMaxGroupRows * (Hq / Hkv) + kRowBlock - 1) / kRowBlock;
 }
-// Shared memory of one item: K and V of CK keys.
-template <int HD, int CK>
-constexpr size_t smem_bytes() { return 2 * (size_t)CK * (HD + kPad) * sizeof(__half); }
+// Shared memory of one staging buffer: K and V of CKS keys.
+template <int HD, int CKS>
+constexpr size_t smem_bytes() { return 2 * (size_t)CKS * (HD + kPad) * sizeof(__half); }
 
 using half = __half;
 
@@ -76,24 +77,25 @@ __device__ __forceinline__ void ldsm_x4_trans(const half* p, uint32_t& r0, uint3
 }
 
 // One work item, run by 128 threads (ranks tid = 0..127, sync() a barrier over
-// them): chunk `chunk` of group `z` for KV head and row block `y`. Ks and Vs hold
-// CK x (HD + kPad) halves each; the caller syncs before reusing them. The tree
-// block (up to kMaxGroupRows keys) passes through them CK keys at a time, with
-// the online-softmax state kept in registers. Each of the 4 warps owns one
-// 16-row tile of the 64-row block. Returns without work (and without syncing)
-// for items past the group's keys or rows.
-template <int HD, int CK, typename Sync>
-__device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chunk_slots, half* Ks, half* Vs,
+// them): chunk `chunk` (CKI keys) of group `z` for KV head and row block `y`.
+// The chunk's keys pass through shared memory CKS at a time: buf holds nbuf
+// (1 or 2) staging buffers, each K then V of CKS x (HD + kPad) halves; with two
+// the next sub-chunk is staged while the current one is computed. The caller
+// syncs before reusing buf. The online-softmax state stays in registers. Each of the 4
+// warps owns one 16-row tile of the 64-row block. Returns without work (and
+// without syncing) for items past the group's keys or rows.
+template <int HD, int CKI, int CKS, typename Sync>
+__device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chunk_slots, half* buf, int nbuf,
                           int tid, Sync sync) {
-  static_assert(CK % 64 == 0 && kRowBlock == 16 * (kAttnThreads / 32), "one 16-row tile per warp");
+  static_assert(CKS % 64 == 0 && CKI % CKS == 0 && kRowBlock == 16 * (kAttnThreads / 32), "tiling");
   const Group g = a.groups[z];
   const int rb_count = row_blocks(a.Hq, a.Hkv);
   const int kvh = y / rb_count, rb = y % rb_count;
-  const int nck = n_prefix_chunks(g.prefix, CK);
+  const int nck = n_prefix_chunks(g.prefix, CKI);
   const bool block = chunk == nck;
   if (chunk > nck || (block && g.block_len <= 0) || rb * kRowBlock >= g.nrows * (a.Hq / a.Hkv)) return;
-  const int key0 = block ? g.prefix : chunk * CK;
-  const int nkeys = block ? min(g.block_len, kMaxGroupRows) : min(CK, g.prefix - key0);
+  const int key0 = block ? g.prefix : chunk * CKI;
+  const int nkeys = block ? min(g.block_len, kMaxGroupRows) : min(CKI, g.prefix - key0);
   const int G = a.Hq / a.Hkv;
   const int R = g.nrows * G;
   const int warp = tid >> 5, lane = tid & 31;
@@ -139,21 +141,38 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
   const half* Kg = reinterpret_cast<const half*>(a.kc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
   const half* Vg = reinterpret_cast<const half*>(a.vc) + (((size_t)g.seq * a.Hkv + kvh) * a.cap + key0) * HD;
   constexpr int VEC = 8;  // halves per 16-byte vector
-  for (int kc0 = 0; kc0 < nkeys; kc0 += CK) {
-    const int nk = min(CK, nkeys - kc0);
-    if (kc0 > 0) sync();  // every warp is done with the previous sub-chunk
-    // stage keys kc0 .. kc0 + CK of the chunk (row-major) with asynchronous 16-byte
-    // copies, all in flight at once; keys past nk are zero-filled
-    for (int e = tid; e < CK * HD / VEC; e += kAttnThreads) {
+  // stage keys kc0 .. kc0 + CKS of the chunk (row-major) into buffer b with
+  // asynchronous 16-byte copies, all in flight at once; keys past the chunk are zero-filled
+  constexpr int kBuf = CKS * (HD + kPad);  // halves of one K (or V) buffer
+  auto stage = [&](int kc0, int b) {
+    const int nk = min(CKS, nkeys - kc0);
+    half* Kd = buf + b * 2 * kBuf;
+    half* Vd = Kd + kBuf;
+    for (int e = tid; e < CKS * HD / VEC; e += kAttnThreads) {
       const int key = e / (HD / VEC), d0 = (e % (HD / VEC)) * VEC;
       const int n = key < nk ? 16 : 0;
       const size_t go = (size_t)(kc0 + min(key, nk - 1)) * HD + d0;
-      cp_async16(Ks + key * (HD + kPad) + d0, Kg + go, n);
-      cp_async16(Vs + key * (HD + kPad) + d0, Vg + go, n);
+      cp_async16(Kd + key * (HD + kPad) + d0, Kg + go, n);
+      cp_async16(Vd + key * (HD + kPad) + d0, Vg + go, n);
     }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  const int nsub = (nkeys + CKS - 1) / CKS;
+  stage(0, 0);
+  for (int j = 0; j < nsub; ++j) {
+    const int kc0 = j * CKS;
+    const int nk = min(CKS, nkeys - kc0);
+    const int bcur = nbuf == 2 ? (j & 1) : 0;
+    if (nbuf == 2 && j + 1 < nsub) {
+      stage(kc0 + CKS, bcur ^ 1);  // its buffer was freed by the sync that ended sub-chunk j - 1
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
     sync();
-    if (!active) continue;
+    const half* Kb = buf + bcur * 2 * kBuf;
+    const half* Vb = Kb + kBuf;
+    if (active) {
     for (int kb = 0; kb < nk; kb += 64) {
       float s[8][4];
 #pragma unroll
@@ -162,7 +181,7 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
       for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
-          const half* kp = Ks + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
+          const half* kp = Kb + (kb + nt * 8 + quad) * (HD + kPad) + kk * 16 + qi * 2;
           mma16816(s[nt], qa[kk], ld_b32(kp), ld_b32(kp + 8));
         }
       }
@@ -225,7 +244,7 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
 #pragma unroll
         for (int dt = 0; dt < HD / 8; dt += 2) {
           const int key = kb + kk2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-          const half* vp = Vs + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
+          const half* vp = Vb + key * (HD + kPad) + (dt + (lane >> 4)) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4_trans(vp, b0, b1, b2, b3);
           mma16816(o[dt], pa[kk2], b0, b1);
@@ -233,6 +252,9 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
         }
       }
     }
+    }  // active
+    sync();  // every warp is done with buffer bcur before it is staged again
+    if (nbuf == 1 && j + 1 < nsub) stage(kc0 + CKS, 0);
   }
   if (!active) return;
   // partials: index (row * Hq + qh) * slots + chunk
@@ -252,11 +274,11 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
 }
 
 // One warp per (row, query head) w < M * Hq: combine the row's chunk partials in chunk order.
-template <int HD, int CK>
+template <int HD, int CKI>
 __device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_slots) {
   const int row = w / a.Hq, qh = w % a.Hq;
   const Group g = a.groups[a.row_grp ? a.row_grp[row] : 0];
-  const int nck = n_prefix_chunks(g.prefix, CK) + (g.block_len > 0 ? 1 : 0);
+  const int nck = n_prefix_chunks(g.prefix, CKI) + (g.block_len > 0 ? 1 : 0);
   const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
   // chunk maxima and sums: one load per lane and chunk, all lanes at once
   float M = -INFINITY;

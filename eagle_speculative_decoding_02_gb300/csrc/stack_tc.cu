@@ -8,7 +8,8 @@
 //
 //   GEMM   swap-AB tcgen05 tiles (128 weight rows x MT token rows, fp32 in TMEM),
 //          (tile, 64-wide k-block) units split evenly over the CTAs (stream-K),
-//          split tiles summed by the last-arriving CTA in ascending CTA order,
+//          split tiles summed at the end of the phase by all their CTAs, each a
+//          slice of the rows, in ascending CTA order,
 //          then the fused epilogue (RMSNorm row scale, RoPE + KV write, SwiGLU,
 //          residual add + next norm, LM-head top-k records).
 //   ATTN   tree-attention work items (64-key chunk, KV head x 64-row block, group)
@@ -53,12 +54,14 @@ constexpr int kWBytes = kTileN * kBK * 2;  // 16 KB weight box
 constexpr int kSub = 32;                   // epilogue rows per sub-tile
 constexpr int kLdt = kTileN + 1;
 constexpr int kMaxW = 12;                  // weight ring stages (upper bound)
-constexpr int kAttnCK = 64;                // keys per attention chunk
+constexpr int kAttnCKI = 256;              // keys per attention work item (as the standalone kernel)
+constexpr int kAttnCKS = 64;               // keys per staging sub-chunk
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
 constexpr int kHdMax = 128;
 constexpr int kMaxCtas = 160;              // partial buffer sizing bound
+constexpr int kEpiThreads = 128;           // epilogue warps 2-5
 constexpr size_t kTileBytes = (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4;  // epilogue staging
-constexpr size_t kAttnBytes = attn::smem_bytes<kHdMax, kAttnCK>();             // attention K and V
+constexpr size_t kAttnBytes = attn::smem_bytes<kHdMax, kAttnCKS>();            // one attention K/V buffer
 
 struct StackArgs {
   const StackPhase* ph;
@@ -127,6 +130,24 @@ __device__ bool wait_phase(const StackArgs& a, int p, unsigned G, volatile int* 
   }
 }
 
+// Bounded wait until split-K counter i reaches n (one thread).
+__device__ bool wait_count(const StackArgs& a, int i, unsigned n, volatile int* abort_flag) {
+  const unsigned* p = reinterpret_cast<const unsigned*>(a.tile_cnt + i);
+  if (ld_acquire(p) >= n) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t k = 1;; ++k) {
+    if (ld_acquire(p) >= n) return true;
+    if ((k & 15) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        set_status(a.status, kStTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // The attention work items that have keys and rows, in order (group, KV head,
 // row block, chunk): count() counts them, item() decodes one.
 template <int CK>
@@ -177,8 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   uint8_t* xring = wring + (size_t)S * kWBytes;
   // Attention and merge phases run while the activation ring is idle (the next
   // GEMM phase's boxes wait for them to finish), so their K / V buffers alias it.
-  half* Ks = reinterpret_cast<half*>(xring);
-  half* Vs = Ks + kAttnCK * (HD + attn::kPad);
+  // two staging buffers when the activation halves hold them, else one
+  const int nbuf = (size_t)S * xbytes >= 2 * kAttnBytes ? 2 : 1;
+  half* abuf = reinterpret_cast<half*>(xring);
   float* tile = reinterpret_cast<float*>(xring + (size_t)S * xbytes);
   float* rscale = tile + kSub * kLdt;
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes);
@@ -364,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
         const int Gp = phase_ctas(T, G);
         const long long u0 = c < Gp ? unit_start(T, c, Gp) : 0, u1 = c < Gp ? unit_start(T, c + 1, Gp) : 0;
         const int t_first = (int)(u0 / kbt);
+        int seg_t[2], nseg = 0;  // split tiles of this CTA in this phase (its first and last at most)
         for (long long u = u0; u < u1 && alive;) {
           const int t = (int)(u / kbt);
           const int kb0 = (int)(u - (long long)t * kbt);
@@ -389,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&aempty[buf]);
           } else {
-            // split tile: leave the fragment in this CTA's slot; the last of the
-            // tile's CTAs to arrive sums every fragment in ascending CTA order
+            // split tile: leave the fragment in this CTA's slot and count it in; the
+            // tile is finished at the end of the phase, once every fragment is in
             float* slot = a.partial + ((size_t)c * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
             for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
               float v[32];
@@ -404,87 +427,90 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
             if (lane == 0) mbar_arrive(&aempty[buf]);
             __threadfence();
             EpilogueSync{}();
-            const long long tu0 = (long long)t * kbt, tu1 = (long long)(t + 1) * kbt - 1;
-            const int c0 = cta_of(T, tu0, Gp), c1 = cta_of(T, tu1, Gp);
-            if (etid == 0) {
-              int* cnt = a.tile_cnt + P.cnt_off + t;
-              const int prev = atomicAdd(cnt, 1);
-              const int last = prev == (c1 - c0);
-              if (last) *cnt = 0;
-              *last_flag = last;
-            }
-            EpilogueSync{}();
-            if (*last_flag) {
-              __threadfence();
-              // each thread sums 4 adjacent columns of 8 rows per 32-row sub-tile
-              const int c4 = 4 * lane;
-              for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
-                float4 acc[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int cc = c0; cc <= c1; cc += 2) {
-                  // two fragments' loads in flight together, added in CTA order
-                  const bool two = cc + 1 <= c1;
-                  const float* f0 = a.partial +
-                                    ((size_t)cc * 2 + (t != (int)(unit_start(T, cc, Gp) / kbt) ? 1 : 0)) *
-                                        (size_t)MT * kTileN;
-                  const float* f1 = two ? a.partial + ((size_t)(cc + 1) * 2 +
-                                                       (t != (int)(unit_start(T, cc + 1, Gp) / kbt) ? 1 : 0)) *
-                                                          (size_t)MT * kTileN
-                                        : f0;
-                  float4 x0[8], x1[8];
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + ew * 8 + i;
-                    const bool in = r < rows_valid;
-                    x0[i] = in ? __ldcg(reinterpret_cast<const float4*>(f0 + (size_t)r * kTileN + c4))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x1[i] = (in && two) ? __ldcg(reinterpret_cast<const float4*>(f1 + (size_t)r * kTileN + c4))
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                  }
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    acc[i].x += x0[i].x; acc[i].y += x0[i].y; acc[i].z += x0[i].z; acc[i].w += x0[i].w;
-                  }
-                  if (two) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                      acc[i].x += x1[i].x; acc[i].y += x1[i].y; acc[i].z += x1[i].z; acc[i].w += x1[i].w;
-                    }
-                  }
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  float* tr = tile + (ew * 8 + i) * kLdt + c4;
-                  tr[0] = acc[i].x; tr[1] = acc[i].y; tr[2] = acc[i].z; tr[3] = acc[i].w;
-                }
-                EpilogueSync{}();
-                run_epilogue<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, rscale, etid,
-                                   EpilogueSync{});
-              }
-            }
+            if (etid == 0) red_release_add(reinterpret_cast<unsigned*>(a.tile_cnt + P.cnt_off + t), 1u);
+            seg_t[nseg++] = t;
           }
           ++f;
           u = (long long)(t + 1) * kbt;
         }
+        // Distributed fixup: the n CTAs that share a split tile each sum one slice
+        // of its rows over all n fragments, in ascending CTA order (the standalone
+        // GEMM's order), and run the epilogue on that slice. Every CTA of the
+        // cooperative launch is resident, so waiting for the others' fragments is safe.
+        for (int si = 0; si < nseg && alive; ++si) {
+          const int t = seg_t[si];
+          const int n0 = t * kTileN;
+          const int c0 = cta_of(T, (long long)t * kbt, Gp), c1 = cta_of(T, (long long)(t + 1) * kbt - 1, Gp);
+          const int nc = c1 - c0 + 1, me = c - c0;
+          const int r_lo = me * rows_valid / nc, r_hi = (me + 1) * rows_valid / nc;
+          alive = epi_all(etid != 0 || wait_count(a, P.cnt_off + t, (unsigned)nc, abort_flag));
+          if (!alive || r_lo >= r_hi) continue;
+          for (int rb0 = r_lo; rb0 < r_hi; rb0 += kSub) {
+            const int nr = min(kSub, r_hi - rb0);
+            const int pairs = nr * (kTileN / 4);  // (row, 4-column group) pairs of this block
+            for (int p0 = 0; p0 < pairs; p0 += 4 * kEpiThreads) {
+              float4 acc[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int cb = c0; cb <= c1; cb += 4) {
+                // up to 4 fragments x 4 pairs of loads in flight, added in CTA order
+                float4 x[4][4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int cc = cb + k;
+                  const float* fp = cc <= c1 ? a.partial + ((size_t)cc * 2 +
+                                                            (t != (int)(unit_start(T, cc, Gp) / kbt) ? 1 : 0)) *
+                                                               (size_t)MT * kTileN
+                                             : nullptr;
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const int pr = p0 + j * kEpiThreads + etid;
+                    x[k][j] = (fp && pr < pairs)
+                                  ? __ldcg(reinterpret_cast<const float4*>(fp + (size_t)(rb0 + pr / 32) * kTileN +
+                                                                           (pr % 32) * 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                  }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  if (cb + k > c1) break;
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    acc[j].x += x[k][j].x; acc[j].y += x[k][j].y; acc[j].z += x[k][j].z; acc[j].w += x[k][j].w;
+                  }
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int pr = p0 + j * kEpiThreads + etid;
+                if (pr < pairs) {
+                  float* tr = tile + (pr / 32) * kLdt + (pr % 32) * 4;
+                  tr[0] = acc[j].x; tr[1] = acc[j].y; tr[2] = acc[j].z; tr[3] = acc[j].w;
+                }
+              }
+            }
+            EpilogueSync{}();
+            run_epilogue<bf16>(ep, tile, kLdt, rb0, nr, n0, rscale, etid, EpilogueSync{});
+          }
+        }
       } else if (alive && P.kind == kPhaseAttn) {
         const AttnArgs& at = P.at;
-        const AttnItems<kAttnCK> items{at};
+        const AttnItems<kAttnCKI> items{at};
         const int n = items.count();
-        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCK) + 1;
+        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCKI) + 1;
         const int i0 = (int)((long long)c * n / G), i1 = (int)((long long)(c + 1) * n / G);
         for (int i = i0; i < i1; ++i) {
           int chunk, y, z;
           items.item(i, chunk, y, z);
           EpilogueSync{}();  // the previous item's readers of Ks / Vs are done
-          attn::attn_item<HD, kAttnCK>(at, chunk, y, z, slots, Ks, Vs, etid, EpilogueSync{});
+          attn::attn_item<HD, kAttnCKI, kAttnCKS>(at, chunk, y, z, slots, abuf, nbuf, etid, EpilogueSync{});
         }
       } else if (alive && P.kind == kPhaseMerge) {
         const AttnArgs& at = P.at;
         const int n = at.M * at.Hq;
-        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCK) + 1;
+        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCKI) + 1;
         const int w0 = (int)((long long)c * n / G), w1 = (int)((long long)(c + 1) * n / G);
-        for (int w = w0 + ew; w < w1; w += 4) attn::attn_merge_warp<HD, kAttnCK>(at, w, lane, slots);
+        for (int w = w0 + ew; w < w1; w += 4) attn::attn_merge_warp<HD, kAttnCKI>(at, w, lane, slots);
       }
       // phase done: every epilogue thread's writes happen before the release
       EpilogueSync{}();
@@ -561,7 +587,7 @@ size_t stack_scratch_bytes(int M, int max_phases, int max_counters) {
 }
 
 size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix) {
-  const size_t slots = (size_t)attn::n_prefix_chunks(max_prefix, kAttnCK) + 1;
+  const size_t slots = (size_t)attn::n_prefix_chunks(max_prefix, kAttnCKI) + 1;
   return (size_t)M * Hq * slots * (hd + 2) * sizeof(float);
 }
 
