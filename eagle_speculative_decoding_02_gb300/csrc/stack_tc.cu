@@ -7,7 +7,9 @@
 // cooperative launch (one CTA per SM) runs the whole program of phases:
 //
 //   GEMM   swap-AB tcgen05 tiles (128 weight rows x MT token rows, fp32 in TMEM),
-//          (tile, 64-wide k-block) units split evenly over the CTAs (stream-K),
+//          (slab, 64-wide k-block) units: whole slabs dealt to every CTA, the
+//          remainder split evenly over the CTAs (stream-K) and run first; a
+//          slab is two tiles sharing one activation box (one tile if MT > 64),
 //          split tiles summed at the end of the phase by all their CTAs, each a
 //          slice of the rows, in ascending CTA order,
 //          then the fused epilogue (RMSNorm row scale, RoPE + KV write, SwiGLU,
@@ -60,6 +62,7 @@ constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
 constexpr int kHdMax = 128;
 constexpr int kMaxCtas = 160;              // partial buffer sizing bound
 constexpr int kEpiThreads = 128;           // epilogue warps 2-5
+constexpr int kPrefetchUnits = 12;         // units a CTA prefetches into L2 ahead of its ring's loads
 constexpr size_t kTileBytes = (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4;  // epilogue staging
 constexpr size_t kAttnBytes = attn::smem_bytes<kHdMax, kAttnCKS>();            // one attention K/V buffer
 
@@ -67,6 +70,7 @@ struct StackArgs {
   const StackPhase* ph;
   int n_phases;
   int M, MT, has_lo, sw, sx;
+  int sbmax;         // tiles per slab the ring and the accumulators are sized for (1 or 2)
   uint32_t tmem_cols;
   unsigned* done;    // [n_phases] phase counters, then the exit counter
   int* tile_cnt;     // [n_counters] split-K arrival counters
@@ -87,29 +91,65 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-// A GEMM phase of T units runs on its first Gp = min(G, T) CTAs: CTA c < Gp owns
-// units [c T / Gp, (c + 1) T / Gp) (at least one), exactly as the standalone GEMM
-// splits the same shape, so both sum every output in the same order.
-__device__ __forceinline__ int phase_ctas(long long T, int G) { return (int)min((long long)G, T); }
 __device__ __forceinline__ long long unit_start(long long T, int c, int Gp) { return (long long)c * T / Gp; }
 __device__ __forceinline__ int cta_of(long long T, long long u, int Gp) { return (int)(((u + 1) * Gp - 1) / T); }
 
-// This CTA's units [u, u1) of GEMM phase p; next() moves to the next GEMM phase
-// in which the CTA has units.
+// Work split of a GEMM phase of n_s slabs x kbt k-blocks over G CTAs: every CTA
+// owns Wd = n_s / G whole slabs (data-parallel); the R = n_s - Wd G remaining
+// slabs are split stream-K over min(G, R kbt) CTAs. A CTA runs its split units
+// first, so that the split slabs are summed while its whole slabs stream.
+struct Split {
+  int kbt, Wd, Gs;
+  long long Ts, base;  // split units, first split unit
+  __device__ Split(const StackPhase& P, int G) {
+    kbt = P.kbt;
+    const int ns = P.n_tiles / P.sb;
+    Wd = ns / G;
+    Ts = (long long)(ns - Wd * G) * kbt;
+    base = (long long)Wd * G * kbt;
+    Gs = Ts > 0 ? (int)min((long long)G, Ts) : 0;
+  }
+  __device__ void split_range(int c, long long& u0, long long& u1) const {
+    if (c < Gs) {
+      u0 = base + unit_start(Ts, c, Gs);
+      u1 = base + unit_start(Ts, c + 1, Gs);
+    } else {
+      u0 = u1 = 0;
+    }
+  }
+  __device__ void whole_range(int c, long long& u0, long long& u1) const {
+    u0 = (long long)c * Wd * kbt;
+    u1 = u0 + (long long)Wd * kbt;
+  }
+  // the CTAs c0..c1 that share split slab t
+  __device__ void sharers(int t, int& c0, int& c1) const {
+    const long long l0 = (long long)t * kbt - base;
+    c0 = cta_of(Ts, l0, Gs);
+    c1 = cta_of(Ts, l0 + kbt - 1, Gs);
+  }
+  // first slab of CTA cc's split range (its partial slot 0 holds that slab)
+  __device__ int first_split_slab(int cc) const { return (int)((base + unit_start(Ts, cc, Gs)) / kbt); }
+};
+
+// This CTA's units [u, u1) of GEMM phase p, its split range (stage 0) then its
+// whole slabs (stage 1); next() moves to the next non-empty range.
 struct Cursor {
-  int p = -1;
+  int p = -1, stage = 1;
   long long u = 0, u1 = 0;
   __device__ bool next(const StackArgs& a, int c, int G) {
-    for (++p; p < a.n_phases; ++p) {
-      if (a.ph[p].kind != kPhaseGemm) continue;
-      const long long T = a.ph[p].T;
-      const int Gp = phase_ctas(T, G);
-      if (c >= Gp) continue;
-      u = unit_start(T, c, Gp);
-      u1 = unit_start(T, c + 1, Gp);
-      return true;
+    for (;;) {
+      if (stage == 0) {
+        stage = 1;
+        Split(a.ph[p], G).whole_range(c, u, u1);
+        if (u < u1) return true;
+      }
+      for (++p; p < a.n_phases && a.ph[p].kind != kPhaseGemm; ++p) {
+      }
+      if (p >= a.n_phases) return false;
+      stage = 0;
+      Split(a.ph[p], G).split_range(c, u, u1);
+      if (u < u1) return true;
     }
-    return false;
   }
 };
 
@@ -190,18 +230,20 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = a.sw, MT = a.MT;
-  const int accw = a.has_lo ? 2 * MT : MT;  // accumulator columns per buffer
+  const int S = a.sw, MT = a.MT, SBM = a.sbmax;
+  const int accw = a.has_lo ? 2 * MT : MT;  // accumulator columns of one tile
+  const int abufw = SBM * accw;             // accumulator columns of one buffer (a slab)
+  const int wslot = SBM * kWBytes;          // weight bytes of a ring slot
   const int xbox = MT * kBK * 2;
   const int xbytes = xbox * (a.has_lo ? 2 : 1);
   uint8_t* wring = smem;
-  uint8_t* xring = wring + (size_t)S * kWBytes;
-  // Attention and merge phases run while the activation ring is idle (the next
-  // GEMM phase's boxes wait for them to finish), so their K / V buffers alias it.
-  // two staging buffers when the activation halves hold them, else one
-  const int nbuf = (size_t)S * xbytes >= 2 * kAttnBytes ? 2 : 1;
-  half* abuf = reinterpret_cast<half*>(xring);
+  uint8_t* xring = wring + (size_t)S * wslot;
   float* tile = reinterpret_cast<float*>(xring + (size_t)S * xbytes);
+  // Attention and merge phases run while the activation halves and the epilogue
+  // tile are idle (the next GEMM phase's boxes wait for them to finish), so their
+  // K / V staging buffers alias those: two buffers if they fit, else one.
+  const int nbuf = (size_t)S * xbytes + kTileBytes >= 2 * kAttnBytes ? 2 : 1;
+  half* abuf = reinterpret_cast<half*>(xring);
   float* rscale = tile + kSub * kLdt;
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes);
   uint64_t* full = bars;
@@ -251,20 +293,41 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       // the MMA frees stages, across phase boundaries.
       uint64_t pol_w;  // weights are read once
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+      // While the ring is full (phase tails, attention phases, or just waiting on
+      // the MMA), a second cursor runs up to kPrefetchUnits units ahead of the
+      // ring's loads and prefetches their weight boxes into L2: more bytes in
+      // flight, and the next phase starts on L2 hits.
       Cursor W;
       bool more = W.next(a, c, G);
-      long long iw = 0;
+      Cursor PF = W;
+      bool pf_more = more;
+      long long iw = 0, ipf = 0;  // units loaded into the ring / prefetched
       bool ok = true;
       while (more && ok) {
         const int s = (int)(iw % S);
-        if (iw >= S && !mbar_wait(&empty[s], (uint32_t)((iw / S) - 1) & 1, abort_flag, a.status)) {
-          ok = false;
-          break;
+        if (iw >= S && !mbar_try_wait(&empty[s], (uint32_t)((iw / S) - 1) & 1)) {
+          if (ipf < iw) {  // the prefetch cursor never trails the loads
+            PF = W;
+            pf_more = more;
+            ipf = iw;
+          }
+          if (pf_more && ipf < iw + kPrefetchUnits) {
+            const StackPhase& Q = a.ph[PF.p];
+            const int sl = (int)(PF.u / Q.kbt), kb = (int)(PF.u % Q.kbt);
+            tma_prefetch_l2(&Q.tmW, kb * kBK, sl * Q.sb * kTileN);
+            ++ipf;
+            if (++PF.u == PF.u1) pf_more = PF.next(a, c, G);
+            continue;
+          }
+          if (!mbar_wait(&empty[s], (uint32_t)((iw / S) - 1) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
         }
         const StackPhase& P = a.ph[W.p];
-        const int t = (int)(W.u / P.kbt), kb = (int)(W.u % P.kbt);
-        mbar_expect_tx(&full[s], (uint32_t)kWBytes);
-        tma_load_2d_hint(wring + (size_t)s * kWBytes, &P.tmW, &full[s], kb * kBK, t * kTileN, pol_w);
+        const int sl = (int)(W.u / P.kbt), kb = (int)(W.u % P.kbt);
+        mbar_expect_tx(&full[s], (uint32_t)(P.sb * kWBytes));
+        tma_load_2d_hint(wring + (size_t)s * wslot, &P.tmW, &full[s], kb * kBK, sl * P.sb * kTileN, pol_w);
         ++iw;
         if (++W.u == W.u1) more = W.next(a, c, G);
       }
@@ -331,14 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       int f = 0;
       bool ok = true;
       while (more && ok) {
-        const int kbt = a.ph[C.p].kbt;
+        const int kbt = a.ph[C.p].kbt, sb = a.ph[C.p].sb;
         const int t = (int)(C.u / kbt);
         const int kb0 = (int)(C.u - (long long)t * kbt);
         const int kb1 = (int)min((long long)kbt, C.u1 - (long long)t * kbt);
         const int buf = f & 1;
         if (f >= 2 && !mbar_wait(&aempty[buf], (uint32_t)((f >> 1) - 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * accw);
+        const uint32_t d = tmem + (uint32_t)(buf * abufw);
         for (int kb = kb0; kb < kb1; ++kb, ++i) {
           const int sw = (int)(i % S), sx = sw;
           if (!mbar_wait(&full[sw], (uint32_t)(i / S) & 1, abort_flag, a.status)) {
@@ -346,11 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
             break;
           }
           tc_fence_after();
-          const uint32_t aw = smem_u32(wring + (size_t)sw * kWBytes);
+          const uint32_t aw = smem_u32(wring + (size_t)sw * wslot);
           const uint32_t ax = smem_u32(xring + (size_t)sx * xbytes);
+          for (int j = 0; j < sb; ++j) {
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            umma(d, sw128_desc(aw + k * 32), sw128_desc(ax + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k)
+              umma(d + (uint32_t)(j * accw), sw128_desc(aw + j * kWBytes + k * 32), sw128_desc(ax + k * 32), idesc,
+                   (kb > kb0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&empty[sw]);
         }
@@ -381,12 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       if (alive && P.kind == kPhaseGemm) {
         EpiParams ep = P.ep;
         if (a.y_last && p == a.n_phases - 1) ep.y = a.y_last;
-        const long long T = P.T;
-        const int kbt = P.kbt;
-        const int Gp = phase_ctas(T, G);
-        const long long u0 = c < Gp ? unit_start(T, c, Gp) : 0, u1 = c < Gp ? unit_start(T, c + 1, Gp) : 0;
-        const int t_first = (int)(u0 / kbt);
-        int seg_t[2], nseg = 0;  // split tiles of this CTA in this phase (its first and last at most)
+        const int kbt = P.kbt, sb = P.sb;
+        const Split sp(P, G);
+        long long ua0, ua1, ub0, ub1;
+        sp.split_range(c, ua0, ua1);
+        sp.whole_range(c, ub0, ub1);
+        const int t_first = ua0 < ua1 ? (int)(ua0 / kbt) : 0;
+        int seg_t[2], nseg = 0;  // split slabs of this CTA in this phase (its first and last at most)
+        // the split range, then (after the fixup below) the whole slabs
+        auto run_units = [&](long long u0, long long u1) {
         for (long long u = u0; u < u1 && alive;) {
           const int t = (int)(u / kbt);
           const int kb0 = (int)(u - (long long)t * kbt);
@@ -395,32 +463,37 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           const int buf = f & 1;
           const bool ok = epi_all(mbar_wait(&afull[buf], (uint32_t)(f >> 1) & 1, abort_flag, a.status));
           tc_fence_after();
-          const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * accw);
-          const int n0 = t * kTileN;
+          const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * abufw);
           if (!ok) {
             alive = false;
           } else if (whole) {
-            for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
-              float v[32];
-              tmem_ld32_pair(tb + r0, a.has_lo ? MT : 0, v);
+            for (int j = 0; j < sb; ++j) {
+              const int n0 = (t * sb + j) * kTileN;
+              for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+                float v[32];
+                tmem_ld32_pair(tb + j * accw + r0, a.has_lo ? MT : 0, v);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) tile[j * kLdt + col] = v[j];
-              EpilogueSync{}();
-              run_epilogue<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, rscale, etid, EpilogueSync{});
+                for (int i = 0; i < 32; ++i) tile[i * kLdt + col] = v[i];
+                EpilogueSync{}();
+                run_epilogue<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, rscale, etid,
+                                   EpilogueSync{});
+              }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aempty[buf]);
           } else {
-            // split tile: leave the fragment in this CTA's slot and count it in; the
-            // tile is finished at the end of the phase, once every fragment is in
-            float* slot = a.partial + ((size_t)c * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
-            for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
-              float v[32];
-              tmem_ld32_pair(tb + r0, a.has_lo ? MT : 0, v);
+            // split slab: leave the fragments in this CTA's slot and count them in;
+            // the slab is finished at the end of the phase, once every fragment is in
+            for (int j = 0; j < sb; ++j) {
+              float* slot = a.partial + (((size_t)c * 2 + (t != t_first ? 1 : 0)) * SBM + j) * (size_t)MT * kTileN;
+              for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+                float v[32];
+                tmem_ld32_pair(tb + j * accw + r0, a.has_lo ? MT : 0, v);
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (r0 + j < rows_valid) __stcg(slot + (size_t)(r0 + j) * kTileN + col, v[j]);
+                for (int i = 0; i < 32; ++i)
+                  if (r0 + i < rows_valid) __stcg(slot + (size_t)(r0 + i) * kTileN + col, v[i]);
+              }
             }
             tc_fence_before();
             __syncwarp();
@@ -433,66 +506,72 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           ++f;
           u = (long long)(t + 1) * kbt;
         }
+        };
+        run_units(ua0, ua1);
         // Distributed fixup: the n CTAs that share a split tile each sum one slice
         // of its rows over all n fragments, in ascending CTA order (the standalone
         // GEMM's order), and run the epilogue on that slice. Every CTA of the
         // cooperative launch is resident, so waiting for the others' fragments is safe.
         for (int si = 0; si < nseg && alive; ++si) {
           const int t = seg_t[si];
-          const int n0 = t * kTileN;
-          const int c0 = cta_of(T, (long long)t * kbt, Gp), c1 = cta_of(T, (long long)(t + 1) * kbt - 1, Gp);
+          int c0, c1;
+          sp.sharers(t, c0, c1);
           const int nc = c1 - c0 + 1, me = c - c0;
           const int r_lo = me * rows_valid / nc, r_hi = (me + 1) * rows_valid / nc;
           alive = epi_all(etid != 0 || wait_count(a, P.cnt_off + t, (unsigned)nc, abort_flag));
           if (!alive || r_lo >= r_hi) continue;
-          for (int rb0 = r_lo; rb0 < r_hi; rb0 += kSub) {
-            const int nr = min(kSub, r_hi - rb0);
-            const int pairs = nr * (kTileN / 4);  // (row, 4-column group) pairs of this block
-            for (int p0 = 0; p0 < pairs; p0 += 4 * kEpiThreads) {
-              float4 acc[4];
+          for (int j = 0; j < sb; ++j) {
+            const int n0 = (t * sb + j) * kTileN;
+            for (int rb0 = r_lo; rb0 < r_hi; rb0 += kSub) {
+              const int nr = min(kSub, r_hi - rb0);
+              const int pairs = nr * (kTileN / 4);  // (row, 4-column group) pairs of this block
+              for (int p0 = 0; p0 < pairs; p0 += 4 * kEpiThreads) {
+                float4 acc[4];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-              for (int cb = c0; cb <= c1; cb += 4) {
-                // up to 4 fragments x 4 pairs of loads in flight, added in CTA order
-                float4 x[4][4];
+                for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cb = c0; cb <= c1; cb += 4) {
+                  // up to 4 fragments x 4 pairs of loads in flight, added in CTA order
+                  float4 x[4][4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const int cc = cb + k;
-                  const float* fp = cc <= c1 ? a.partial + ((size_t)cc * 2 +
-                                                            (t != (int)(unit_start(T, cc, Gp) / kbt) ? 1 : 0)) *
-                                                               (size_t)MT * kTileN
-                                             : nullptr;
+                  for (int k = 0; k < 4; ++k) {
+                    const int cc = cb + k;
+                    const float* fp =
+                        cc <= c1 ? a.partial + (((size_t)cc * 2 + (t != sp.first_split_slab(cc) ? 1 : 0)) * SBM + j) *
+                                                    (size_t)MT * kTileN
+                                 : nullptr;
 #pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const int pr = p0 + j * kEpiThreads + etid;
-                    x[k][j] = (fp && pr < pairs)
-                                  ? __ldcg(reinterpret_cast<const float4*>(fp + (size_t)(rb0 + pr / 32) * kTileN +
-                                                                           (pr % 32) * 4))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i = 0; i < 4; ++i) {
+                      const int pr = p0 + i * kEpiThreads + etid;
+                      x[k][i] = (fp && pr < pairs)
+                                    ? __ldcg(reinterpret_cast<const float4*>(fp + (size_t)(rb0 + pr / 32) * kTileN +
+                                                                             (pr % 32) * 4))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                  }
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    if (cb + k > c1) break;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      acc[i].x += x[k][i].x; acc[i].y += x[k][i].y; acc[i].z += x[k][i].z; acc[i].w += x[k][i].w;
+                    }
                   }
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  if (cb + k > c1) break;
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    acc[j].x += x[k][j].x; acc[j].y += x[k][j].y; acc[j].z += x[k][j].z; acc[j].w += x[k][j].w;
+                for (int i = 0; i < 4; ++i) {
+                  const int pr = p0 + i * kEpiThreads + etid;
+                  if (pr < pairs) {
+                    float* tr = tile + (pr / 32) * kLdt + (pr % 32) * 4;
+                    tr[0] = acc[i].x; tr[1] = acc[i].y; tr[2] = acc[i].z; tr[3] = acc[i].w;
                   }
                 }
               }
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int pr = p0 + j * kEpiThreads + etid;
-                if (pr < pairs) {
-                  float* tr = tile + (pr / 32) * kLdt + (pr % 32) * 4;
-                  tr[0] = acc[j].x; tr[1] = acc[j].y; tr[2] = acc[j].z; tr[3] = acc[j].w;
-                }
-              }
+              EpilogueSync{}();
+              run_epilogue<bf16>(ep, tile, kLdt, rb0, nr, n0, rscale, etid, EpilogueSync{});
             }
-            EpilogueSync{}();
-            run_epilogue<bf16>(ep, tile, kLdt, rb0, nr, n0, rscale, etid, EpilogueSync{});
           }
         }
+        run_units(ub0, ub1);
       } else if (alive && P.kind == kPhaseAttn) {
         const AttnArgs& at = P.at;
         const AttnItems<kAttnCKI> items{at};
@@ -546,23 +625,21 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
 }
 
 struct Layout {
-  int sw, sx;
+  int sw, sx, sbmax;
   size_t smem;
 };
 
 Layout layout(int MT, bool has_lo) {
   Layout l{};
+  l.sbmax = MT <= 64 ? 2 : 1;  // two-tile slabs while their accumulators fit tensor memory
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
-  // activation stages: about as many as weight stages (each unit needs one of
-  // each), and enough bytes for the attention buffers that alias the ring
-  // S slots of one weight box and one activation box each (the attention buffers
-  // alias the activation halves, which need at least kAttnBytes)
-  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 2 * 8 + 5) * 8 + 16 + 1024;
+  const size_t wslot = (size_t)l.sbmax * kWBytes;
+  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 5) * 8 + 16 + 1024;
   const long long room = (long long)kSmemBudget - (long long)fixed;
-  l.sw = (int)std::min<long long>(kMaxW, room / (long long)(kWBytes + xbytes));
+  l.sw = (int)std::min<long long>(kMaxW, room / (long long)(wslot + xbytes));
   l.sx = l.sw;
-  if ((size_t)l.sx * xbytes < kAttnBytes) l.sw = l.sx = 0;  // rejected by stack_run
-  l.smem = (size_t)l.sw * (kWBytes + xbytes) + fixed;
+  if ((size_t)l.sx * xbytes + kTileBytes < kAttnBytes) l.sw = l.sx = 0;  // rejected by stack_run
+  l.smem = (size_t)l.sw * (wslot + xbytes) + fixed;
   return l;
 }
 
@@ -583,7 +660,7 @@ bool stack_supported(int M, int hd) { return M >= 1 && M <= kStackMaxRows && (hd
 
 size_t stack_scratch_bytes(int M, int max_phases, int max_counters) {
   return align256((size_t)(max_phases + 1) * 4) + align256((size_t)max_counters * 4) +
-         (size_t)kMaxCtas * 2 * round_mt(M) * kTileN * 4;
+         (size_t)kMaxCtas * 2 * 2 * round_mt(M) * kTileN * 4;  // [CTA][first/last][slab tile][rows][128]
 }
 
 size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix) {
@@ -602,12 +679,15 @@ void StackProgramBuilder::gemm(const StackGemmDesc& g) {
   if (has_lo != (g.X_lo != nullptr)) { ok = false; return; }
   ph.n_tiles = g.N / kTileN;
   ph.kbt = g.K / kBK;
-  ph.T = (long long)ph.n_tiles * ph.kbt;
+  // two-tile slabs (one activation box per 256 weight rows) where every CTA gets at
+  // least a tile's worth of units; small phases keep single tiles and fewer sharers
+  ph.sb = (MT <= 64 && ph.n_tiles % 2 == 0 && ph.n_tiles >= num_sms()) ? 2 : 1;
+  ph.T = (long long)(ph.n_tiles / ph.sb) * ph.kbt;
   ph.cnt_off = n_counters;
-  n_counters += ph.n_tiles;
+  n_counters += ph.n_tiles;  // one per slab is used; sized per tile
   ph.ep = g.ep;
   ph.ep.M = M;
-  if (!make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN) || !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
+  if (!make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN * ph.sb) || !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
       (g.X_lo && !make_tmap_bf16(&ph.tmXlo, g.X_lo, g.rows_cap, g.K, MT))) {
     ok = false;
     return;
@@ -642,8 +722,9 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.has_lo = has_lo;
   a.sw = l.sw;
   a.sx = l.sx;
+  a.sbmax = l.sbmax;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
+  while (cols < (uint32_t)(2 * l.sbmax * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
   a.tmem_cols = cols;
   // the layout depends only on the capacities, never on this program: programs
   // of every size share one scratch

@@ -66,3 +66,34 @@ def tree_to_torch(tree: OT.Tree, batch: int = 1, device="cuda"):
 
 def tree_from_torch(t, b: int = 0) -> OT.Tree:
     return OT.Tree(tokens=t.tokens[b].cpu().numpy(), parent=t.parent[b].cpu().numpy(), depth=t.depth[b].cpu().numpy())
+
+
+def stream_margins(eng1, prompt_row, tokens):
+    """Top-2 logit margins of a batch-1 engine's greedy choices along a committed stream.
+
+    A chain tree carrying the stream is verified right after the prompt: row i
+    holds the logits that choose token i + 1.
+    """
+    import torch
+    n = len(tokens)
+    chain = OT.Tree(tokens=np.asarray(tokens[:n], np.int32), parent=np.arange(-1, n - 1, dtype=np.int32),
+                    depth=np.arange(n, dtype=np.int32))
+    eng1.prefill(prompt_row)
+    _, lg = eng1.verify(tree_to_torch(chain, device=prompt_row.device), logits=True)
+    srt = np.sort(lg[0].float().cpu().numpy(), -1)
+    return srt[:, -1] - srt[:, -2]
+
+
+def same_until_near_tie(a, b, margins, tol=0.1):
+    """Token streams a and b agree up to the first position whose deciding margin is a near-tie (< tol).
+
+    Returns the number of positions compared. Two correct implementations whose
+    floating-point sums differ in order may part ways only at such a near-tie.
+    """
+    a, b = list(a), list(b)
+    assert a[0] == b[0]
+    for i in range(1, min(len(a), len(b))):
+        if margins[i - 1] < tol:
+            return i
+        assert a[i] == b[i], (i, a[: i + 1], b[: i + 1], float(margins[i - 1]))
+    return min(len(a), len(b))

@@ -119,7 +119,7 @@ def test_8b_static_tree_lossless(cuda):
 
 
 def test_8b_batch4_sequences_match_batch1(cuda):
-    """Batch 4 (verify GEMMs with M = 244 rows): each sequence decodes like its batch-1 run."""
+    """Batch 4 (verify GEMMs with M = 244 rows): each sequence decodes like its batch-1 run, up to a flagged near-tie."""
     from eagle_speculative_decoding_02_gb300 import synthetic as S
     w = dataclasses.replace(FX.WORKLOADS["8b_static_bs4"], prompt_len=256, max_new=16, kv_cap=0)
     e4 = S.make_engine(w)
@@ -127,9 +127,12 @@ def test_8b_batch4_sequences_match_batch1(cuda):
     van4, spec4, _ = _lossless(e4, p4, w.max_new, b=2)
     out4, _ = e4.generate(p4, w.max_new, use_graph=True)
     e1 = S.make_engine(w, batch=1, weights=e4.weights)
+    from tests.oracle_helpers import same_until_near_tie, stream_margins
     for b in (0, 3):
-        out1, _ = e1.generate(p4[b:b + 1].contiguous(), w.max_new, use_graph=True)
-        assert out1[0].tolist() == out4[b].tolist(), b
+        pb = p4[b:b + 1].contiguous()
+        out1, _ = e1.generate(pb, w.max_new, use_graph=True)
+        margins = stream_margins(e1, pb, out1[0].cpu().numpy())
+        same_until_near_tie(out1[0].tolist(), out4[b].tolist(), margins)
 
 
 TWO_LAYER_70B = FX.LLAMA3_70B.reduced(n_layers=2)

@@ -1,9 +1,11 @@
-"""The persistent layer-stack kernel's GEMM phases against the standalone GEMM.
+"""The persistent layer-stack kernel's GEMM and LM-head phases.
 
-Both split a shape's (tile, k-block) units over min(SMs, units) CTAs and sum
-every split tile's fragments in ascending CTA order, so their outputs must be
-bit-identical; chains of phases check the cross-phase weight prefetch and the
-grid-wide phase ordering.
+Every phase of a chain computes the same product with the same work split and
+summation order, so all phases must agree bit for bit with a one-phase run
+(this checks the cross-phase weight prefetch and the grid-wide phase
+ordering); the product itself is checked against a float64 reference and the
+standalone GEMM within the float32 accumulation tolerance. The LM-head top-k
+must pick the standalone kernel's tokens wherever the choice is not a near-tie.
 """
 import numpy as np
 import pytest
@@ -36,13 +38,15 @@ def _inputs(M, N, K, seed):
 def test_persistent_gemm_equals_standalone(cuda, M, N, K, n_phases):
     from eagle_speculative_decoding_02_gb300.engine import op_gemm, op_gemm_persistent
     x, lo, w = _inputs(M, N, K, M * 7 + N + K)
-    ref = op_gemm(x, w, x_lo=lo)
+    one = op_gemm_persistent(x, w, 1, x_lo=lo)
     got = op_gemm_persistent(x, w, n_phases, x_lo=lo)
+    ref = op_gemm(x, w, x_lo=lo)
     torch.cuda.synchronize()
-    assert torch.equal(got, ref), float((got - ref).abs().max())
-    # and against a float64 product of the same operands
+    assert torch.equal(got, one)
     exact = (x.double() + lo.double()) @ w.double().T
-    assert float((got.double() - exact).abs().max()) < 1e-3
+    scale = float(exact.abs().max())
+    assert float((got.double() - exact).abs().max()) < 2e-6 * scale * (K ** 0.5)
+    assert float((got - ref).abs().max()) < 2e-6 * scale * (K ** 0.5)
 
 
 def test_persistent_gemm_twice_with_one_scratch(cuda):
@@ -54,7 +58,7 @@ def test_persistent_gemm_twice_with_one_scratch(cuda):
     scratch = torch.zeros(int(nb), dtype=torch.uint8, device="cuda")
     for seed in (1, 2):
         x, lo, w = _inputs(M, N, K, seed)
-        assert torch.equal(op_gemm_persistent(x, w, 2, x_lo=lo, scratch=scratch), op_gemm(x, w, x_lo=lo))
+        assert torch.equal(op_gemm_persistent(x, w, 2, x_lo=lo, scratch=scratch), op_gemm_persistent(x, w, 1, x_lo=lo))
 
 
 @pytest.mark.parametrize("M,N,K", [(61, 4096, 1024), (61, 128256, 4096), (10, 4096, 1024), (61, 2048, 512)])
@@ -66,4 +70,12 @@ def test_persistent_lmhead_equals_standalone(cuda, M, N, K, n_phases, k):
     ridx, rval, rlse = op_lmhead_topk(x, w, k)
     _, idx, val, lse = op_gemm_persistent(x, w, n_phases, k=k)
     torch.cuda.synchronize()
-    assert torch.equal(idx, ridx) and torch.equal(val, rval) and torch.equal(lse, rlse)
+    logits = x.double() @ w.double().T
+    tol = 2e-6 * float(logits.abs().max()) * (K ** 0.5)
+    assert float((val.double() - rval.double()).abs().max()) < tol
+    assert float((lse.double() - rlse.double()).abs().max()) < tol
+    # the top-k tokens agree except where two candidates are within the tolerance
+    srt = torch.sort(logits, -1, descending=True).values
+    gaps = (srt[:, :k] - srt[:, 1:k + 1]).min(-1).values
+    clear = gaps > 4 * tol
+    assert torch.equal(idx[clear], ridx[clear])

@@ -184,7 +184,13 @@ def test_bf16_generate_teacher_forced(cuda):
 
 
 def test_batch_rows_are_independent(cuda):
-    """Each sequence of a batch-4 run commits the same tokens as its batch-1 run."""
+    """Each sequence of a batch-4 run commits the same tokens as its batch-1 run, up to a flagged near-tie.
+
+    Batch 4 verifies 244 rows (standalone kernels) and batch 1 verifies 61 (the
+    persistent kernel): their float sums run in different orders, so they may
+    part only where the greedy choice is a near-tie.
+    """
+    from tests.oracle_helpers import same_until_near_tie, stream_margins
     shape = GQA_SMALL
     w = workload("8b_static", model=shape, prompt_len=32, max_new=16)
     prompts = FX.prompts(shape, 4, w.prompt_len)
@@ -192,5 +198,7 @@ def test_batch_rows_are_independent(cuda):
     o4, _ = e4.generate(torch.from_numpy(prompts).to(cuda), w.max_new)
     for b in range(4):
         e1 = _engine(w, batch=1, weights=e4.weights)
-        o1, _ = e1.generate(torch.from_numpy(prompts[b: b + 1]).to(cuda), w.max_new)
-        assert o1[0].tolist() == o4[b].tolist()
+        pb = torch.from_numpy(prompts[b: b + 1]).to(cuda)
+        o1, _ = e1.generate(pb, w.max_new)
+        margins = stream_margins(e1, pb, o1[0].cpu().numpy())
+        same_until_near_tie(o1[0].tolist(), o4[b].tolist(), margins)
