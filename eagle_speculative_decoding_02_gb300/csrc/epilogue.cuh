@@ -15,35 +15,55 @@ namespace eg {
 // row scale, RoPE position, KV slot and sequence of each row.
 constexpr int kEpiRows = 32;
 constexpr int kEpiRowSmemFloats = 4 * kEpiRows;
-// Loads of one thread are batched this many rows at a time, ahead of any store,
-// so that their latencies overlap.
+// The row sum of squares is accumulated in kEpiBatch interleaved partial sums
+// (fixed order); per-column loads of one thread (RoPE tables, residual) are
+// issued kEpiLoadBatch rows at a time, ahead of any store, so that their
+// latencies overlap.
 constexpr int kEpiBatch = 8;
+constexpr int kEpiLoadBatch = 16;
+
+// Per-row inputs of an epilogue: the RMSNorm scale of the GEMM input row and,
+// for the QKV epilogue, its RoPE position, KV slot and sequence. Entry m
+// describes row m0 + m of the call.
+struct EpiRows {
+  float* scale;
+  int* pos;
+  int* slot;
+  int* seq;
+  __device__ EpiRows at(int off) const { return {scale + off, pos + off, slot + off, seq + off}; }
+};
+// Row arrays of `cap` rows carved out of 4 * cap words of shared memory.
+__device__ inline EpiRows epi_rows(float* sm, int cap) {
+  return {sm, reinterpret_cast<int*>(sm + cap), reinterpret_cast<int*>(sm + 2 * cap),
+          reinterpret_cast<int*>(sm + 3 * cap)};
+}
 
 // Inputs that earlier phases of the same persistent launch may have written
 // (row sums of squares, the residual stream) are read through L2 (ld.global.cg):
 // the SM's L1 is not coherent with other SMs' stores within one launch.
-//
-// rowsm must hold kEpiRowSmemFloats words of shared memory; msub <= kEpiRows.
-// Run by 128 threads with ranks tid = 0..127; sync() must be a barrier over
-// exactly those threads.
-template <typename T, typename Sync>
-__device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, int msub, int n0,
-                             float* rowsm, int tid, Sync sync) {
-  const int ncols = min(kTileN, p.N - n0);
-  float* rscale = rowsm;
-  int* rpos = reinterpret_cast<int*>(rowsm + kEpiRows);
-  int* rslot = rpos + kEpiRows;
-  int* rseq = rslot + kEpiRows;
-  if (tid < msub) {
-    const int m = tid;
-    float r = 1.f;
+
+// Fills r for rows m0 .. m0 + msub - 1; thread tid of nthr takes rows tid,
+// tid + nthr, ... The row scale sums the input's column-tile partials j in
+// partial sum j % kEpiBatch (complete batches), the rest into partial 0, then
+// adds the partials in order; its loads are issued 32 at a time.
+__device__ inline void load_epi_rows(const EpiParams& p, int m0, int msub, EpiRows r, int tid, int nthr) {
+  for (int m = tid; m < msub; m += nthr) {
+    float sc = 1.f;
     if (p.ssq_in) {
       const float* s_in = p.ssq_in + m0 + m;
       float part[kEpiBatch];
 #pragma unroll
       for (int q = 0; q < kEpiBatch; ++q) part[q] = 0.f;
+      const int nfull = p.n_ssq_in - p.n_ssq_in % kEpiBatch;
       int j = 0;
-      for (; j + kEpiBatch <= p.n_ssq_in; j += kEpiBatch) {
+      for (; j + 4 * kEpiBatch <= nfull; j += 4 * kEpiBatch) {
+        float v[4 * kEpiBatch];
+#pragma unroll
+        for (int q = 0; q < 4 * kEpiBatch; ++q) v[q] = __ldcg(s_in + (size_t)(j + q) * p.M);
+#pragma unroll
+        for (int q = 0; q < 4 * kEpiBatch; ++q) part[q % kEpiBatch] += v[q];
+      }
+      for (; j < nfull; j += kEpiBatch) {
 #pragma unroll
         for (int q = 0; q < kEpiBatch; ++q) part[q] += __ldcg(s_in + (size_t)(j + q) * p.M);
       }
@@ -51,17 +71,28 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
       float s = 0.f;
 #pragma unroll
       for (int q = 0; q < kEpiBatch; ++q) s += part[q];
-      r = rsqrtf(s * p.inv_d_in + p.eps);
+      sc = rsqrtf(s * p.inv_d_in + p.eps);
     }
-    rscale[m] = r;
+    r.scale[m] = sc;
     if (p.kind == kEpiQkv) {
-      rpos[m] = p.rows.pos[m0 + m];
-      rslot[m] = p.rows.slot[m0 + m];
-      rseq[m] = p.rows.seq[m0 + m];
+      r.pos[m] = p.rows.pos[m0 + m];
+      r.slot[m] = p.rows.slot[m0 + m];
+      r.seq[m] = p.rows.seq[m0 + m];
     }
   }
-  sync();
+}
 
+// The epilogue proper, with the row inputs already in r (visible to all 128
+// threads); msub <= kEpiRows. Run by 128 threads with ranks tid = 0..127; sync()
+// must be a barrier over exactly those threads.
+template <typename T, typename Sync>
+__device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, int msub, int n0, EpiRows r,
+                              int tid, Sync sync) {
+  const int ncols = min(kTileN, p.N - n0);
+  const float* rscale = r.scale;
+  const int* rpos = r.pos;
+  const int* rslot = r.slot;
+  const int* rseq = r.seq;
   switch (p.kind) {
     case kEpiStore: {
       for (int m = 0; m < msub; ++m)
@@ -79,10 +110,10 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
         const int fi = i < half ? i : i - half;
         const int nn = n - p.q_dim - (region == 2 ? p.kv_dim : 0);
         const int kvh = nn / hd;
-        for (int mb = 0; mb < msub; mb += kEpiBatch) {
-          float cs[kEpiBatch], sn[kEpiBatch];
+        for (int mb = 0; mb < msub; mb += kEpiLoadBatch) {
+          float cs[kEpiLoadBatch], sn[kEpiLoadBatch];
 #pragma unroll
-          for (int q = 0; q < kEpiBatch; ++q) {  // the batch's table loads, all in flight together
+          for (int q = 0; q < kEpiLoadBatch; ++q) {  // the batch's table loads, all in flight together
             cs[q] = 1.f;
             sn[q] = 0.f;
             if (region < 2 && mb + q < msub) {
@@ -92,7 +123,7 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
             }
           }
 #pragma unroll
-          for (int q = 0; q < kEpiBatch; ++q) {
+          for (int q = 0; q < kEpiLoadBatch; ++q) {
             const int m = mb + q;
             if (m >= msub) break;
             float v = tile[m * ldt + c] * rscale[m];
@@ -131,13 +162,13 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
       if (c < ncols) {
         const int n = n0 + c;
         const float gn = p.gain[n];
-        for (int mb = 0; mb < msub; mb += kEpiBatch) {
-          float hv[kEpiBatch];
+        for (int mb = 0; mb < msub; mb += kEpiLoadBatch) {
+          float hv[kEpiLoadBatch];
 #pragma unroll
-          for (int q = 0; q < kEpiBatch; ++q)  // residual loads of the batch, ahead of its stores
+          for (int q = 0; q < kEpiLoadBatch; ++q)  // residual loads of the batch, ahead of its stores
             hv[q] = (p.kind == kEpiResid && mb + q < msub) ? __ldcg(p.h + (size_t)(m0 + mb + q) * p.N + n) : 0.f;
 #pragma unroll
-          for (int q = 0; q < kEpiBatch; ++q) {
+          for (int q = 0; q < kEpiLoadBatch; ++q) {
             const int m = mb + q;
             if (m >= msub) break;
             const size_t at = (size_t)(m0 + m) * p.N + n;
@@ -207,6 +238,16 @@ __device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, i
     }
   }
   sync();
+}
+
+// Loads the row inputs into rowsm (kEpiRowSmemFloats words), then runs the epilogue.
+template <typename T, typename Sync>
+__device__ void run_epilogue(const EpiParams& p, float* tile, int ldt, int m0, int msub, int n0,
+                             float* rowsm, int tid, Sync sync) {
+  const EpiRows r = epi_rows(rowsm, kEpiRows);
+  load_epi_rows(p, m0, msub, r, tid, 128);
+  sync();
+  epilogue_body<T>(p, tile, ldt, m0, msub, n0, r, tid, sync);
 }
 
 }  // namespace eg

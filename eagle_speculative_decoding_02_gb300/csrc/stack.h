@@ -18,13 +18,12 @@ namespace eg {
 enum StackPhaseKind : int { kPhaseGemm = 0, kPhaseAttn = 1, kPhaseMerge = 2 };
 
 struct StackPhase {   // 128-byte aligned (CUtensorMap)
-  CUtensorMap tmW;    // GEMM weight [N][K], box [128 sb][64]
+  CUtensorMap tmW;    // GEMM weight [N][K], box [128][64]
   CUtensorMap tmX;    // GEMM activations [rows][K], box [MT][64]
   CUtensorMap tmXlo;  // low halves of the activations (hi/lo pair)
   int kind = kPhaseGemm;
   int N = 0, K = 0, n_tiles = 0, kbt = 0;
-  int sb = 1;         // tiles per slab: a unit is (slab of sb 128-row tiles, 64-wide k-block)
-  long long T = 0;    // units: (n_tiles / sb) * kbt
+  long long T = 0;    // units (128-row tile, 64-wide k-block): n_tiles * kbt
   int cnt_off = 0;    // first split-K arrival counter of this phase
   EpiParams ep;       // GEMM epilogue
   AttnArgs at;        // attention / merge

@@ -7,9 +7,8 @@
 // cooperative launch (one CTA per SM) runs the whole program of phases:
 //
 //   GEMM   swap-AB tcgen05 tiles (128 weight rows x MT token rows, fp32 in TMEM),
-//          (slab, 64-wide k-block) units: whole slabs dealt to every CTA, the
-//          remainder split evenly over the CTAs (stream-K) and run first; a
-//          slab is two tiles sharing one activation box (one tile if MT > 64),
+//          (tile, 64-wide k-block) units: whole tiles dealt to every CTA, the
+//          remainder split evenly over the CTAs (stream-K) and run first,
 //          split tiles summed at the end of the phase by all their CTAs, each a
 //          slice of the rows, in ascending CTA order,
 //          then the fused epilogue (RMSNorm row scale, RoPE + KV write, SwiGLU,
@@ -62,15 +61,14 @@ constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
 constexpr int kHdMax = 128;
 constexpr int kMaxCtas = 160;              // partial buffer sizing bound
 constexpr int kEpiThreads = 128;           // epilogue warps 2-5
-constexpr int kPrefetchUnits = 12;         // units a CTA prefetches into L2 ahead of its ring's loads
-constexpr size_t kTileBytes = (size_t)(kSub * kLdt + kEpiRowSmemFloats) * 4;  // epilogue staging
+// epilogue staging: one sub-tile, then the row inputs of every row of the phase
+constexpr size_t kTileBytes = (size_t)(kSub * kLdt + 4 * kStackMaxRows) * 4;
 constexpr size_t kAttnBytes = attn::smem_bytes<kHdMax, kAttnCKS>();            // one attention K/V buffer
 
 struct StackArgs {
   const StackPhase* ph;
   int n_phases;
   int M, MT, has_lo, sw, sx;
-  int sbmax;         // tiles per slab the ring and the accumulators are sized for (1 or 2)
   uint32_t tmem_cols;
   unsigned* done;    // [n_phases] phase counters, then the exit counter
   int* tile_cnt;     // [n_counters] split-K arrival counters
@@ -94,61 +92,93 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 __device__ __forceinline__ long long unit_start(long long T, int c, int Gp) { return (long long)c * T / Gp; }
 __device__ __forceinline__ int cta_of(long long T, long long u, int Gp) { return (int)(((u + 1) * Gp - 1) / T); }
 
-// Work split of a GEMM phase of n_s slabs x kbt k-blocks over G CTAs: every CTA
-// owns Wd = n_s / G whole slabs (data-parallel); the R = n_s - Wd G remaining
-// slabs are split stream-K over min(G, R kbt) CTAs. A CTA runs its split units
-// first, so that the split slabs are summed while its whole slabs stream.
+// Work split of a GEMM phase of n_s tiles x kbt k-blocks over G CTAs: every CTA
+// owns Wd = n_s / G whole tiles (data-parallel); the R = n_s - Wd G remaining
+// tiles are split stream-K over min(G, R kbt) CTAs. A CTA runs its split units
+// first, so that the split tiles are summed while its whole tiles stream.
 struct Split {
   int kbt, Wd, Gs;
   long long Ts, base;  // split units, first split unit
   __device__ Split(const StackPhase& P, int G) {
     kbt = P.kbt;
-    const int ns = P.n_tiles / P.sb;
+    const int ns = P.n_tiles;
     Wd = ns / G;
     Ts = (long long)(ns - Wd * G) * kbt;
     base = (long long)Wd * G * kbt;
     Gs = Ts > 0 ? (int)min((long long)G, Ts) : 0;
   }
-  __device__ void split_range(int c, long long& u0, long long& u1) const {
+  __device__ void split_range(int c, int& u0, int& u1) const {
     if (c < Gs) {
-      u0 = base + unit_start(Ts, c, Gs);
-      u1 = base + unit_start(Ts, c + 1, Gs);
+      u0 = (int)(base + unit_start(Ts, c, Gs));
+      u1 = (int)(base + unit_start(Ts, c + 1, Gs));
     } else {
       u0 = u1 = 0;
     }
   }
-  __device__ void whole_range(int c, long long& u0, long long& u1) const {
-    u0 = (long long)c * Wd * kbt;
-    u1 = u0 + (long long)Wd * kbt;
+  __device__ void whole_range(int c, int& u0, int& u1) const {
+    u0 = c * Wd * kbt;
+    u1 = u0 + Wd * kbt;
   }
-  // the CTAs c0..c1 that share split slab t
+  // the CTAs c0..c1 that share split tile t
   __device__ void sharers(int t, int& c0, int& c1) const {
     const long long l0 = (long long)t * kbt - base;
     c0 = cta_of(Ts, l0, Gs);
     c1 = cta_of(Ts, l0 + kbt - 1, Gs);
   }
-  // first slab of CTA cc's split range (its partial slot 0 holds that slab)
-  __device__ int first_split_slab(int cc) const { return (int)((base + unit_start(Ts, cc, Gs)) / kbt); }
+  // first tile of CTA cc's split range (its partial slot 0 holds that tile)
+  __device__ int first_split_tile(int cc) const { return (int)((base + unit_start(Ts, cc, Gs)) / kbt); }
 };
 
 // This CTA's units [u, u1) of GEMM phase p, its split range (stage 0) then its
-// whole slabs (stage 1); next() moves to the next non-empty range.
+// whole tiles (stage 1); unit u is k-block kb of tile sl. next() moves to the
+// next non-empty range; advance() steps one unit. The producer and MMA loops run
+// on one thread each, so the per-unit bookkeeping avoids integer division.
 struct Cursor {
   int p = -1, stage = 1;
-  long long u = 0, u1 = 0;
+  int u = 0, u1 = 0, kbt = 1, sl = 0, kb = 0;
+  __device__ bool start(const StackArgs& a) {
+    kbt = a.ph[p].kbt;
+    sl = u / kbt;
+    kb = u - sl * kbt;
+    return true;
+  }
   __device__ bool next(const StackArgs& a, int c, int G) {
     for (;;) {
       if (stage == 0) {
         stage = 1;
         Split(a.ph[p], G).whole_range(c, u, u1);
-        if (u < u1) return true;
+        if (u < u1) return start(a);
       }
       for (++p; p < a.n_phases && a.ph[p].kind != kPhaseGemm; ++p) {
       }
       if (p >= a.n_phases) return false;
       stage = 0;
       Split(a.ph[p], G).split_range(c, u, u1);
-      if (u < u1) return true;
+      if (u < u1) return start(a);
+    }
+  }
+  // step n units within the current tile (kb + n <= kbt)
+  __device__ bool advance(const StackArgs& a, int c, int G, int n = 1) {
+    u += n;
+    kb += n;
+    if (kb == kbt) {
+      kb = 0;
+      ++sl;
+    }
+    return u < u1 || next(a, c, G);
+  }
+};
+
+// Position in the ring: slot s of round r (the r-th pass over the S slots).
+// A slot's full barrier completes once per round (parity r & 1); a producer
+// refilling slot s in round r >= 1 waits for empty completion r - 1.
+struct RingPos {
+  int s = 0;
+  uint32_t r = 0;
+  __device__ void step(int S) {
+    if (++s == S) {
+      s = 0;
+      ++r;
     }
   }
 };
@@ -230,10 +260,10 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = a.sw, MT = a.MT, SBM = a.sbmax;
+  const int S = a.sw, MT = a.MT;
   const int accw = a.has_lo ? 2 * MT : MT;  // accumulator columns of one tile
-  const int abufw = SBM * accw;             // accumulator columns of one buffer (a slab)
-  const int wslot = SBM * kWBytes;          // weight bytes of a ring slot
+  const int abufw = accw;                   // accumulator columns of one buffer
+  const int wslot = kWBytes;                // weight bytes of a ring slot
   const int xbox = MT * kBK * 2;
   const int xbytes = xbox * (a.has_lo ? 2 : 1);
   uint8_t* wring = smem;
@@ -244,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   // K / V staging buffers alias those: two buffers if they fit, else one.
   const int nbuf = (size_t)S * xbytes + kTileBytes >= 2 * kAttnBytes ? 2 : 1;
   half* abuf = reinterpret_cast<half*>(xring);
-  float* rscale = tile + kSub * kLdt;
+  const EpiRows prow = epi_rows(tile + kSub * kLdt, kStackMaxRows);  // row inputs of the current GEMM phase
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
@@ -293,43 +323,25 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       // the MMA frees stages, across phase boundaries.
       uint64_t pol_w;  // weights are read once
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
-      // While the ring is full (phase tails, attention phases, or just waiting on
-      // the MMA), a second cursor runs up to kPrefetchUnits units ahead of the
-      // ring's loads and prefetches their weight boxes into L2: more bytes in
-      // flight, and the next phase starts on L2 hits.
+      // (Prefetching further weight boxes into L2 while the ring is full was
+      // measured slower: the extra requests delay the ring's own loads and the
+      // attention phase's KV reads.)
       Cursor W;
       bool more = W.next(a, c, G);
-      Cursor PF = W;
-      bool pf_more = more;
-      long long iw = 0, ipf = 0;  // units loaded into the ring / prefetched
+      RingPos rp;
+      long long iw = 0;  // units loaded into the ring
       bool ok = true;
       while (more && ok) {
-        const int s = (int)(iw % S);
-        if (iw >= S && !mbar_try_wait(&empty[s], (uint32_t)((iw / S) - 1) & 1)) {
-          if (ipf < iw) {  // the prefetch cursor never trails the loads
-            PF = W;
-            pf_more = more;
-            ipf = iw;
-          }
-          if (pf_more && ipf < iw + kPrefetchUnits) {
-            const StackPhase& Q = a.ph[PF.p];
-            const int sl = (int)(PF.u / Q.kbt), kb = (int)(PF.u % Q.kbt);
-            tma_prefetch_l2(&Q.tmW, kb * kBK, sl * Q.sb * kTileN);
-            ++ipf;
-            if (++PF.u == PF.u1) pf_more = PF.next(a, c, G);
-            continue;
-          }
-          if (!mbar_wait(&empty[s], (uint32_t)((iw / S) - 1) & 1, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
+        const int s = rp.s;
+        if (rp.r > 0 && !mbar_wait(&empty[s], (rp.r - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
         }
-        const StackPhase& P = a.ph[W.p];
-        const int sl = (int)(W.u / P.kbt), kb = (int)(W.u % P.kbt);
-        mbar_expect_tx(&full[s], (uint32_t)(P.sb * kWBytes));
-        tma_load_2d_hint(wring + (size_t)s * wslot, &P.tmW, &full[s], kb * kBK, sl * P.sb * kTileN, pol_w);
+        mbar_expect_tx(&full[s], (uint32_t)kWBytes);
+        tma_load_2d_hint(wring + (size_t)s * wslot, &a.ph[W.p].tmW, &full[s], W.kb * kBK, W.sl * kTileN, pol_w);
         ++iw;
-        if (++W.u == W.u1) more = W.next(a, c, G);
+        rp.step(S);
+        more = W.advance(a, c, G);
       }
       if (!ok) {
         // drain (bounded): every box issued must land before the CTA exits
@@ -348,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
       Cursor X;
       bool more = X.next(a, c, G);
+      RingPos rp;
       long long ix = 0;
       int ready = -1;
       bool ok = true;
@@ -360,19 +373,19 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           fence_proxy_async();  // the phase's activations were written by other CTAs' generic stores
           ready = X.p;
         }
-        const int s = (int)(ix % S);
-        if (ix >= S && !mbar_wait(&empty[s], (uint32_t)((ix / S) - 1) & 1, abort_flag, a.status)) {
+        const int s = rp.s;
+        if (rp.r > 0 && !mbar_wait(&empty[s], (rp.r - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
         }
         const StackPhase& P = a.ph[X.p];
-        const int kb = (int)(X.u % P.kbt);
         uint8_t* dst = xring + (size_t)s * xbytes;
         mbar_expect_tx(&full[s], (uint32_t)xbytes);
-        tma_load_2d_hint(dst, &P.tmX, &full[s], kb * kBK, 0, pol_x);
-        if (a.has_lo) tma_load_2d_hint(dst + xbox, &P.tmXlo, &full[s], kb * kBK, 0, pol_x);
+        tma_load_2d_hint(dst, &P.tmX, &full[s], X.kb * kBK, 0, pol_x);
+        if (a.has_lo) tma_load_2d_hint(dst + xbox, &P.tmXlo, &full[s], X.kb * kBK, 0, pol_x);
         ++ix;
-        if (++X.u == X.u1) more = X.next(a, c, G);
+        rp.step(S);
+        more = X.advance(a, c, G);
       }
       if (!ok) {
         for (long long j = (ix > S ? ix - S : 0); j < ix; ++j) {
@@ -390,40 +403,34 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       const uint32_t idesc = idesc_bf16(a.has_lo ? 2 * MT : MT);
       Cursor C;
       bool more = C.next(a, c, G);
-      long long i = 0;
+      RingPos rp;
       int f = 0;
       bool ok = true;
       while (more && ok) {
-        const int kbt = a.ph[C.p].kbt, sb = a.ph[C.p].sb;
-        const int t = (int)(C.u / kbt);
-        const int kb0 = (int)(C.u - (long long)t * kbt);
-        const int kb1 = (int)min((long long)kbt, C.u1 - (long long)t * kbt);
+        const int kb0 = C.kb, kb1 = min(C.kbt, kb0 + (C.u1 - C.u));  // this tile's k-blocks in the range
         const int buf = f & 1;
         if (f >= 2 && !mbar_wait(&aempty[buf], (uint32_t)((f >> 1) - 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * abufw);
-        for (int kb = kb0; kb < kb1; ++kb, ++i) {
-          const int sw = (int)(i % S), sx = sw;
-          if (!mbar_wait(&full[sw], (uint32_t)(i / S) & 1, abort_flag, a.status)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int sw = rp.s, sx = sw;
+          if (!mbar_wait(&full[sw], rp.r & 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t aw = smem_u32(wring + (size_t)sw * wslot);
           const uint32_t ax = smem_u32(xring + (size_t)sx * xbytes);
-          for (int j = 0; j < sb; ++j) {
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              umma(d + (uint32_t)(j * accw), sw128_desc(aw + j * kWBytes + k * 32), sw128_desc(ax + k * 32), idesc,
-                   (kb > kb0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < kBK / 16; ++k)
+            umma(d, sw128_desc(aw + k * 32), sw128_desc(ax + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           umma_commit(&empty[sw]);
+          rp.step(S);
         }
         if (!ok) break;
         umma_commit(&afull[buf]);
         ++f;
-        C.u = (long long)t * kbt + kb1;
-        if (C.u >= C.u1) more = C.next(a, c, G);
+        more = C.advance(a, c, G, kb1 - kb0);
       }
       // no MMA may still be writing tensor memory when it is freed
       umma_commit(drain);
@@ -446,19 +453,23 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       if (alive && P.kind == kPhaseGemm) {
         EpiParams ep = P.ep;
         if (a.y_last && p == a.n_phases - 1) ep.y = a.y_last;
-        const int kbt = P.kbt, sb = P.sb;
+        // the phase's row inputs (RMSNorm scales, RoPE rows) once, while the first
+        // accumulator streams in
+        load_epi_rows(ep, 0, rows_valid, prow, etid, kEpiThreads);
+        EpilogueSync{}();
+        const int kbt = P.kbt;
         const Split sp(P, G);
-        long long ua0, ua1, ub0, ub1;
+        int ua0, ua1, ub0, ub1;
         sp.split_range(c, ua0, ua1);
         sp.whole_range(c, ub0, ub1);
         const int t_first = ua0 < ua1 ? (int)(ua0 / kbt) : 0;
-        int seg_t[2], nseg = 0;  // split slabs of this CTA in this phase (its first and last at most)
-        // the split range, then (after the fixup below) the whole slabs
-        auto run_units = [&](long long u0, long long u1) {
-        for (long long u = u0; u < u1 && alive;) {
-          const int t = (int)(u / kbt);
-          const int kb0 = (int)(u - (long long)t * kbt);
-          const int kb1 = (int)min((long long)kbt, u1 - (long long)t * kbt);
+        int seg_t[2], nseg = 0;  // split tiles of this CTA in this phase (its first and last at most)
+        // the split range, then (after the fixup below) the whole tiles
+        auto run_units = [&](int u0, int u1) {
+        for (int u = u0; u < u1 && alive;) {
+          const int t = u / kbt;
+          const int kb0 = u - t * kbt;
+          const int kb1 = min(kbt, u1 - t * kbt);
           const bool whole = kb0 == 0 && kb1 == kbt;
           const int buf = f & 1;
           const bool ok = epi_all(mbar_wait(&afull[buf], (uint32_t)(f >> 1) & 1, abort_flag, a.status));
@@ -467,33 +478,29 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           if (!ok) {
             alive = false;
           } else if (whole) {
-            for (int j = 0; j < sb; ++j) {
-              const int n0 = (t * sb + j) * kTileN;
-              for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
-                float v[32];
-                tmem_ld32_pair(tb + j * accw + r0, a.has_lo ? MT : 0, v);
+            const int n0 = t * kTileN;
+            for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+              float v[32];
+              tmem_ld32_pair(tb + r0, a.has_lo ? MT : 0, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) tile[i * kLdt + col] = v[i];
-                EpilogueSync{}();
-                run_epilogue<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, rscale, etid,
-                                   EpilogueSync{});
-              }
+              for (int i = 0; i < 32; ++i) tile[i * kLdt + col] = v[i];
+              EpilogueSync{}();
+              epilogue_body<bf16>(ep, tile, kLdt, r0, min(kSub, rows_valid - r0), n0, prow.at(r0), etid,
+                                 EpilogueSync{});
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aempty[buf]);
           } else {
-            // split slab: leave the fragments in this CTA's slot and count them in;
-            // the slab is finished at the end of the phase, once every fragment is in
-            for (int j = 0; j < sb; ++j) {
-              float* slot = a.partial + (((size_t)c * 2 + (t != t_first ? 1 : 0)) * SBM + j) * (size_t)MT * kTileN;
-              for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
-                float v[32];
-                tmem_ld32_pair(tb + j * accw + r0, a.has_lo ? MT : 0, v);
+            // split tile: leave the fragment in this CTA's slot and count it in; the
+            // tile is finished after the split range, once every fragment is in
+            float* slot = a.partial + ((size_t)c * 2 + (t != t_first ? 1 : 0)) * (size_t)MT * kTileN;
+            for (int r0 = 0; r0 < rows_valid; r0 += kSub) {
+              float v[32];
+              tmem_ld32_pair(tb + r0, a.has_lo ? MT : 0, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (r0 + i < rows_valid) __stcg(slot + (size_t)(r0 + i) * kTileN + col, v[i]);
-              }
+              for (int i = 0; i < 32; ++i)
+                if (r0 + i < rows_valid) __stcg(slot + (size_t)(r0 + i) * kTileN + col, v[i]);
             }
             tc_fence_before();
             __syncwarp();
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
             seg_t[nseg++] = t;
           }
           ++f;
-          u = (long long)(t + 1) * kbt;
+          u = (t + 1) * kbt;
         }
         };
         run_units(ua0, ua1);
@@ -517,58 +524,58 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
           int c0, c1;
           sp.sharers(t, c0, c1);
           const int nc = c1 - c0 + 1, me = c - c0;
+          // fragment slot: CTAs after c0 start their split range inside tile t (slot 0);
+          // c0 holds t in slot 1 when its range starts in an earlier tile
+          const int slot_c0 = sp.first_split_tile(c0) != t ? 1 : 0;
           const int r_lo = me * rows_valid / nc, r_hi = (me + 1) * rows_valid / nc;
           alive = epi_all(etid != 0 || wait_count(a, P.cnt_off + t, (unsigned)nc, abort_flag));
           if (!alive || r_lo >= r_hi) continue;
-          for (int j = 0; j < sb; ++j) {
-            const int n0 = (t * sb + j) * kTileN;
-            for (int rb0 = r_lo; rb0 < r_hi; rb0 += kSub) {
-              const int nr = min(kSub, r_hi - rb0);
-              const int pairs = nr * (kTileN / 4);  // (row, 4-column group) pairs of this block
-              for (int p0 = 0; p0 < pairs; p0 += 4 * kEpiThreads) {
-                float4 acc[4];
+          const int n0 = t * kTileN;
+          for (int rb0 = r_lo; rb0 < r_hi; rb0 += kSub) {
+            const int nr = min(kSub, r_hi - rb0);
+            const int pairs = nr * (kTileN / 4);  // (row, 4-column group) pairs of this block
+            for (int p0 = 0; p0 < pairs; p0 += 4 * kEpiThreads) {
+              float4 acc[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int cb = c0; cb <= c1; cb += 4) {
-                  // up to 4 fragments x 4 pairs of loads in flight, added in CTA order
-                  float4 x[4][4];
+              for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int cb = c0; cb <= c1; cb += 4) {
+                // up to 4 fragments x 4 pairs of loads in flight, added in CTA order
+                float4 x[4][4];
 #pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    const int cc = cb + k;
-                    const float* fp =
-                        cc <= c1 ? a.partial + (((size_t)cc * 2 + (t != sp.first_split_slab(cc) ? 1 : 0)) * SBM + j) *
-                                                    (size_t)MT * kTileN
-                                 : nullptr;
+                for (int k = 0; k < 4; ++k) {
+                  const int cc = cb + k;
+                  const float* fp =
+                      cc <= c1 ? a.partial + ((size_t)cc * 2 + (cc == c0 ? slot_c0 : 0)) * (size_t)MT * kTileN
+                               : nullptr;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                      const int pr = p0 + i * kEpiThreads + etid;
-                      x[k][i] = (fp && pr < pairs)
-                                    ? __ldcg(reinterpret_cast<const float4*>(fp + (size_t)(rb0 + pr / 32) * kTileN +
-                                                                             (pr % 32) * 4))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                  }
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    if (cb + k > c1) break;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                      acc[i].x += x[k][i].x; acc[i].y += x[k][i].y; acc[i].z += x[k][i].z; acc[i].w += x[k][i].w;
-                    }
+                  for (int i = 0; i < 4; ++i) {
+                    const int pr = p0 + i * kEpiThreads + etid;
+                    x[k][i] = (fp && pr < pairs)
+                                  ? __ldcg(reinterpret_cast<const float4*>(fp + (size_t)(rb0 + pr / 32) * kTileN +
+                                                                           (pr % 32) * 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                   }
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int pr = p0 + i * kEpiThreads + etid;
-                  if (pr < pairs) {
-                    float* tr = tile + (pr / 32) * kLdt + (pr % 32) * 4;
-                    tr[0] = acc[i].x; tr[1] = acc[i].y; tr[2] = acc[i].z; tr[3] = acc[i].w;
+                for (int k = 0; k < 4; ++k) {
+                  if (cb + k > c1) break;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    acc[i].x += x[k][i].x; acc[i].y += x[k][i].y; acc[i].z += x[k][i].z; acc[i].w += x[k][i].w;
                   }
                 }
               }
-              EpilogueSync{}();
-              run_epilogue<bf16>(ep, tile, kLdt, rb0, nr, n0, rscale, etid, EpilogueSync{});
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int pr = p0 + i * kEpiThreads + etid;
+                if (pr < pairs) {
+                  float* tr = tile + (pr / 32) * kLdt + (pr % 32) * 4;
+                  tr[0] = acc[i].x; tr[1] = acc[i].y; tr[2] = acc[i].z; tr[3] = acc[i].w;
+                }
+              }
             }
+            EpilogueSync{}();
+            epilogue_body<bf16>(ep, tile, kLdt, rb0, nr, n0, prow.at(rb0), etid, EpilogueSync{});
           }
         }
         run_units(ub0, ub1);
@@ -625,15 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
 }
 
 struct Layout {
-  int sw, sx, sbmax;
+  int sw, sx;
   size_t smem;
 };
 
 Layout layout(int MT, bool has_lo) {
   Layout l{};
-  l.sbmax = MT <= 64 ? 2 : 1;  // two-tile slabs while their accumulators fit tensor memory
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
-  const size_t wslot = (size_t)l.sbmax * kWBytes;
+  const size_t wslot = kWBytes;
   const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 5) * 8 + 16 + 1024;
   const long long room = (long long)kSmemBudget - (long long)fixed;
   l.sw = (int)std::min<long long>(kMaxW, room / (long long)(wslot + xbytes));
@@ -660,7 +666,7 @@ bool stack_supported(int M, int hd) { return M >= 1 && M <= kStackMaxRows && (hd
 
 size_t stack_scratch_bytes(int M, int max_phases, int max_counters) {
   return align256((size_t)(max_phases + 1) * 4) + align256((size_t)max_counters * 4) +
-         (size_t)kMaxCtas * 2 * 2 * round_mt(M) * kTileN * 4;  // [CTA][first/last][slab tile][rows][128]
+         (size_t)kMaxCtas * 2 * round_mt(M) * kTileN * 4;  // [CTA][first/last split tile][rows][128]
 }
 
 size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix) {
@@ -679,15 +685,14 @@ void StackProgramBuilder::gemm(const StackGemmDesc& g) {
   if (has_lo != (g.X_lo != nullptr)) { ok = false; return; }
   ph.n_tiles = g.N / kTileN;
   ph.kbt = g.K / kBK;
-  // two-tile slabs (one activation box per 256 weight rows) where every CTA gets at
-  // least a tile's worth of units; small phases keep single tiles and fewer sharers
-  ph.sb = (MT <= 64 && ph.n_tiles % 2 == 0 && ph.n_tiles >= num_sms()) ? 2 : 1;
-  ph.T = (long long)(ph.n_tiles / ph.sb) * ph.kbt;
+  // (Two-tile units sharing one activation box were measured slower: more
+  // sharers per split tile and a shallower ring.)
+  ph.T = (long long)ph.n_tiles * ph.kbt;
   ph.cnt_off = n_counters;
-  n_counters += ph.n_tiles;  // one per slab is used; sized per tile
+  n_counters += ph.n_tiles;  // one arrival counter per tile
   ph.ep = g.ep;
   ph.ep.M = M;
-  if (!make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN * ph.sb) || !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
+  if (!make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN) || !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
       (g.X_lo && !make_tmap_bf16(&ph.tmXlo, g.X_lo, g.rows_cap, g.K, MT))) {
     ok = false;
     return;
@@ -722,9 +727,8 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.has_lo = has_lo;
   a.sw = l.sw;
   a.sx = l.sx;
-  a.sbmax = l.sbmax;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * l.sbmax * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
+  while (cols < (uint32_t)(2 * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
   a.tmem_cols = cols;
   // the layout depends only on the capacities, never on this program: programs
   // of every size share one scratch
