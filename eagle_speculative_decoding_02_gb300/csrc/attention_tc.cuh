@@ -273,34 +273,49 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
   }
 }
 
-// One warp per (row, query head) w < M * Hq: combine the row's chunk partials in chunk order.
+// One warp per (row, query head) w < M * Hq: combine the row's chunk partials
+// (max m_c, sum l_c, unnormalised O_c) in chunk order. Chunks are taken 8 at a
+// time with every load of the block in flight at once: with M the running
+// maximum, weights exp2(m_c - M) scale l_c and O_c, and the running sums are
+// rescaled when a later block raises M.
 template <int HD, int CKI>
 __device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_slots) {
+  constexpr int kB = 8;
   const int row = w / a.Hq, qh = w % a.Hq;
   const Group g = a.groups[a.row_grp ? a.row_grp[row] : 0];
   const int nck = n_prefix_chunks(g.prefix, CKI) + (g.block_len > 0 ? 1 : 0);
   const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
-  // chunk maxima and sums: one load per lane and chunk, all lanes at once
-  float M = -INFINITY;
-  for (int c = lane; c < nck; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (HD + 2) + HD));
-  M = warp_max(M);
-  float L = 0.f;
-  for (int c = lane; c < nck; c += 32) {
-    const float m = __ldcg(base + (size_t)c * (HD + 2) + HD);
-    if (m != -INFINITY) L += exp2f(m - M) * __ldcg(base + (size_t)c * (HD + 2) + HD + 1);
-  }
-  L = warp_sum(L);
-  // weighted sum of the chunk outputs in chunk order (independent loads, unrolled)
+  float M = -INFINITY, L = 0.f;
   float acc[HD / 32];
 #pragma unroll
   for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < nck; ++c) {
-    const float* p = base + (size_t)c * (HD + 2);
-    const float m = __ldcg(p + HD);
-    const float wgt = m == -INFINITY ? 0.f : exp2f(m - M);
+  for (int c0 = 0; c0 < nck; c0 += kB) {
+    float mc[kB], lc[kB], oc[kB][HD / 32];
 #pragma unroll
-    for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * __ldcg(p + lane + 32 * i);
+    for (int j = 0; j < kB; ++j) {
+      const float* p = base + (size_t)(c0 + j) * (HD + 2);
+      const bool in = c0 + j < nck;
+      mc[j] = in ? __ldcg(p + HD) : -INFINITY;
+      lc[j] = in ? __ldcg(p + HD + 1) : 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 32; ++i) oc[j][i] = in ? __ldcg(p + lane + 32 * i) : 0.f;
+    }
+    float Mb = M;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) Mb = fmaxf(Mb, mc[j]);
+    if (Mb == -INFINITY) continue;  // nothing visible yet
+    const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);
+    L *= r;
+#pragma unroll
+    for (int i = 0; i < HD / 32; ++i) acc[i] *= r;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const float wgt = mc[j] == -INFINITY ? 0.f : exp2f(mc[j] - Mb);
+      L += wgt * lc[j];
+#pragma unroll
+      for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * oc[j][i];
+    }
+    M = Mb;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const size_t ob = ((size_t)row * a.Hq + qh) * HD;
