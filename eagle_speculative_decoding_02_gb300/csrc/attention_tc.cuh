@@ -62,6 +62,17 @@ __device__ __forceinline__ uint32_t pack_half2(float x, float y) {
 
 __host__ __device__ __forceinline__ int n_prefix_chunks(int prefix, int ck) { return (prefix + ck - 1) / ck; }
 
+// Split partials of chunk slot c (of `slots`) and pair w = row * Hq + query head
+// (of Mw = M * Hq): the unnormalised output in HD / 32 blocks of 32 columns,
+// [slots][HD / 32][Mw][32] (a row's block is 128 contiguous bytes), then the
+// (max, sum) pairs [slots][Mw][2]; slots * Mw * (HD + 2) floats in all.
+struct PartLayout {
+  float* base;
+  int Mw, slots, hd;
+  __device__ float* o(int c, int w, int blk) const { return base + (((size_t)c * (hd / 32) + blk) * Mw + w) * 32; }
+  __device__ float* ml(int c, int w) const { return base + (size_t)slots * hd * Mw + ((size_t)c * Mw + w) * 2; }
+};
+
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
                    static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
@@ -257,49 +268,55 @@ __device__ void attn_item(const AttnArgs& a, int chunk, int y, int z, int n_chun
     if (nbuf == 1 && j + 1 < nsub) stage(kc0 + CKS, 0);
   }
   if (!active) return;
-  // partials: index (row * Hq + qh) * slots + chunk
+  const PartLayout pl{a.part, a.M * a.Hq, n_chunk_slots, HD};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     if (!rv[i]) continue;
-    const size_t pr = ((size_t)(g.row0 + node[i]) * a.Hq + qh[i]) * n_chunk_slots + chunk;
-    float* po = a.part + pr * (HD + 2);
-    if (qi == 0) {
-      po[HD] = mrow[i];
-      po[HD + 1] = lrow[i];
-    }
+    const int w = (g.row0 + node[i]) * a.Hq + qh[i];
+    if (qi == 0) *reinterpret_cast<float2*>(pl.ml(chunk, w)) = make_float2(mrow[i], lrow[i]);
 #pragma unroll
     for (int dt = 0; dt < HD / 8; ++dt)
-      *reinterpret_cast<float2*>(po + dt * 8 + qi * 2) = make_float2(o[dt][2 * i], o[dt][2 * i + 1]);
+      *reinterpret_cast<float2*>(pl.o(chunk, w, dt / 4) + (dt % 4) * 8 + qi * 2) =
+          make_float2(o[dt][2 * i], o[dt][2 * i + 1]);
   }
 }
 
 // One warp per (row, query head) w < M * Hq: combine the row's chunk partials
-// (max m_c, sum l_c, unnormalised O_c) in chunk order. Chunks are taken 8 at a
-// time with every load of the block in flight at once: with M the running
-// maximum, weights exp2(m_c - M) scale l_c and O_c, and the running sums are
-// rescaled when a later block raises M.
+// (max m_c, sum l_c, unnormalised O_c) in chunk order. Chunks are taken 16 at a
+// time with every load of the block in flight at once, the first block's loads
+// issued before the row's group (and so its chunk count) is known: slots past
+// the group's chunks hold stale but finite values and are masked out. With M
+// the running maximum, weights exp2(m_c - M) scale l_c and O_c, and the running
+// sums are rescaled when a later block raises M.
 template <int HD, int CKI>
 __device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_slots) {
-  constexpr int kB = 8;
+  constexpr int kB = 16;
+  const PartLayout pl{a.part, a.M * a.Hq, n_chunk_slots, HD};
+  float mc[kB], lc[kB], oc[kB][HD / 32];
+  auto load = [&](int c0) {
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const bool in = c0 + j < n_chunk_slots;
+      const float2 ml = in ? __ldcg(reinterpret_cast<const float2*>(pl.ml(c0 + j, w))) : make_float2(-INFINITY, 0.f);
+      mc[j] = ml.x;
+      lc[j] = ml.y;
+#pragma unroll
+      for (int i = 0; i < HD / 32; ++i) oc[j][i] = in ? __ldcg(pl.o(c0 + j, w, i) + lane) : 0.f;
+    }
+  };
+  load(0);
   const int row = w / a.Hq, qh = w % a.Hq;
   const Group g = a.groups[a.row_grp ? a.row_grp[row] : 0];
   const int nck = n_prefix_chunks(g.prefix, CKI) + (g.block_len > 0 ? 1 : 0);
-  const float* base = a.part + (size_t)w * n_chunk_slots * (HD + 2);
   float M = -INFINITY, L = 0.f;
   float acc[HD / 32];
 #pragma unroll
   for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
   for (int c0 = 0; c0 < nck; c0 += kB) {
-    float mc[kB], lc[kB], oc[kB][HD / 32];
+    if (c0 > 0) load(c0);
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const float* p = base + (size_t)(c0 + j) * (HD + 2);
-      const bool in = c0 + j < nck;
-      mc[j] = in ? __ldcg(p + HD) : -INFINITY;
-      lc[j] = in ? __ldcg(p + HD + 1) : 0.f;
-#pragma unroll
-      for (int i = 0; i < HD / 32; ++i) oc[j][i] = in ? __ldcg(p + lane + 32 * i) : 0.f;
-    }
+    for (int j = 0; j < kB; ++j)
+      if (c0 + j >= nck) mc[j] = -INFINITY;  // past the group's chunks
     float Mb = M;
 #pragma unroll
     for (int j = 0; j < kB; ++j) Mb = fmaxf(Mb, mc[j]);
@@ -310,10 +327,11 @@ __device__ void attn_merge_warp(const AttnArgs& a, int w, int lane, int n_chunk_
     for (int i = 0; i < HD / 32; ++i) acc[i] *= r;
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
-      const float wgt = mc[j] == -INFINITY ? 0.f : exp2f(mc[j] - Mb);
-      L += wgt * lc[j];
+      const bool use = mc[j] != -INFINITY;
+      const float wgt = use ? exp2f(mc[j] - Mb) : 0.f;
+      L += use ? wgt * lc[j] : 0.f;
 #pragma unroll
-      for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * oc[j][i];
+      for (int i = 0; i < HD / 32; ++i) acc[i] += use ? wgt * oc[j][i] : 0.f;
     }
     M = Mb;
   }

@@ -99,6 +99,11 @@ struct EpiParams {
   void* kc = nullptr;       // layer cache base [B][n_kv][cap][head_dim], KvOf<T> elements
   void* vc = nullptr;
   Rows rows{};
+  // optional: q again as half, times qg_scale, grouped by KV head,
+  // [n_kv][M][q_dim / head_dim / n_kv][head_dim] (the query tiles of the
+  // tensor-core attention: the GQA rows of one KV head are consecutive)
+  __half* qg = nullptr;
+  float qg_scale = 0.f;
   // kEpiSwiglu
   int ffn = 0;
   // kEpiResid / kEpiFc

@@ -103,6 +103,7 @@ struct eagle_ctx {
   float* ssq_a = nullptr;
   float* ssq_b = nullptr;
   void* q = nullptr;
+  __half* qg = nullptr;
   void* attn = nullptr;
   void* act = nullptr;
   void* xfc = nullptr;
@@ -304,7 +305,7 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
 
 struct Offsets {
   size_t rows_seq, rows_pos, rows_slot, rows_grp, rows_tok, rows_fsrc, rows_mask, groups;
-  size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, attn, act, xfc, lm_hb, lm_ssq, lm_src;
+  size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, qg, attn, act, xfc, lm_hb, lm_ssq, lm_src;
   size_t hb_lo, act_lo, attn_lo, xfc_lo, lm_hb_lo;
   size_t rec_val, rec_idx, rec_max, rec_sum, dtopk_idx, dtopk_val, dlse, vargmax, root_idx;
   size_t t_tok, t_par, t_dep, t_anc, vt_tok, vt_par, vt_dep, vt_anc;
@@ -329,7 +330,7 @@ Offsets plan(const Dims& dm) {
   o.h_dft = L.take((size_t)dm.M_dft * dm.d * 4);
   o.hb = L.take(M * dm.d * es);
   o.ssq_a = L.take(M * nt_d * 4); o.ssq_b = L.take(M * nt_d * 4);
-  o.q = L.take(M * dm.qd * 4); o.attn = L.take(M * dm.qd * es);
+  o.q = L.take(M * dm.qd * 4); o.qg = L.take(M * dm.qd * 2); o.attn = L.take(M * dm.qd * es);
   o.act = L.take(M * dm.ffn * es); o.xfc = L.take(M * 2 * dm.d * es);
   o.lm_hb = L.take((size_t)dm.B * dm.d * es); o.lm_ssq = L.take((size_t)dm.B * nt_d * 4);
   const size_t lo = dm.bf16 ? 2 : 0;  // low halves of the hi/lo GEMM inputs (bf16 models only)
@@ -453,13 +454,15 @@ struct Eng {
     EpiParams e = epi(c, kEpiQkv, M, dm.nqkv);
     e.ssq_in = c->ssq_b; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d;
     e.out = c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
+    const float scale = 1.f / std::sqrt((float)dm.hd);
+    e.qg = c->qg; e.qg_scale = scale * 1.4426950408889634f;
     e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = c->rows;
     EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e));
 
     AttnArgs a{};
-    a.q = (const float*)c->q; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo); a.groups = c->groups; a.n_groups = n_groups;
-    a.mask = c->rows.mask; a.row_grp = c->rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap;
-    a.max_prefix = cap; a.scale = 1.f / std::sqrt((float)dm.hd); a.part = c->attn_part; a.status = c->st.status;
+    a.q = (const float*)c->q; a.qg = c->qg; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo); a.groups = c->groups; a.n_groups = n_groups;
+    a.mask = c->rows.mask; a.row_grp = c->rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap; a.n_seq = dm.B;
+    a.max_prefix = cap; a.scale = scale; a.part = c->attn_part; a.status = c->st.status;
     EG_TRY(sink.attention(a));
 
     e = epi(c, kEpiResid, M, dm.d);
@@ -752,7 +755,7 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->groups = (Group*)P(o.groups);
   c->h_tgt = (float*)P(o.h_tgt); c->h_dft = (float*)P(o.h_dft); c->hb = P(o.hb);
   c->ssq_a = (float*)P(o.ssq_a); c->ssq_b = (float*)P(o.ssq_b);
-  c->q = P(o.q); c->attn = P(o.attn); c->act = P(o.act); c->xfc = P(o.xfc);
+  c->q = P(o.q); c->qg = (__half*)P(o.qg); c->attn = P(o.attn); c->act = P(o.act); c->xfc = P(o.xfc);
   c->lm_hb = P(o.lm_hb); c->lm_ssq = (float*)P(o.lm_ssq); c->lm_src = (int*)P(o.lm_src);
   c->hb_lo = (bf16*)P(o.hb_lo); c->act_lo = (bf16*)P(o.act_lo); c->attn_lo = (bf16*)P(o.attn_lo);
   c->xfc_lo = (bf16*)P(o.xfc_lo); c->lm_hb_lo = (bf16*)P(o.lm_hb_lo);

@@ -110,6 +110,14 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
         const int fi = i < half ? i : i - half;
         const int nn = n - p.q_dim - (region == 2 ? p.kv_dim : 0);
         const int kvh = nn / hd;
+        // this column's element of the grouped half queries, row 0
+        __half* qgc = nullptr;
+        int qg_row = 0;
+        if (region == 0 && p.qg) {
+          const int qh = n / hd, G = p.q_dim / hd / p.n_kv;
+          qgc = p.qg + ((size_t)(qh / G) * p.M * G + qh % G) * hd + i;
+          qg_row = G * hd;
+        }
         for (int mb = 0; mb < msub; mb += kEpiLoadBatch) {
           float cs[kEpiLoadBatch], sn[kEpiLoadBatch];
 #pragma unroll
@@ -133,6 +141,7 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
             }
             if (region == 0) {
               reinterpret_cast<float*>(p.out)[(size_t)(m0 + m) * p.q_dim + n] = v;
+              if (qgc) qgc[(size_t)(m0 + m) * qg_row] = __float2half_rn(v * p.qg_scale);
             } else if (rslot[m] >= 0) {
               const size_t at = (((size_t)rseq[m] * p.n_kv + kvh) * p.cap + rslot[m]) * hd + i;
               using KvT = typename KvOf<T>::type;

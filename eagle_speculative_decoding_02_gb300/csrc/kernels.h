@@ -22,12 +22,15 @@ cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N
 // 2D bf16 tensor map of a row-major [rows][cols] matrix, box [box_rows][64],
 // 128-byte swizzle (the operand format of the tcgen05 kernels).
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
+// The same for IEEE half elements (the KV cache of bf16 models).
+bool make_tmap_f16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
 // SMs of the current device (capped at the scratch-sizing bound).
 int num_sms();
 
 // ---- attention ---------------------------------------------------------------------------------
 struct AttnArgs {
   const float* q;     // [M][Hq][hd] float32 (RoPE applied)
+  const __half* qg;   // optional: q * scale * log2(e) as half, [Hkv][M][Hq / Hkv][hd]
   const void* kc;     // [B][Hkv][cap][hd]
   const void* vc;
   void* o;            // [M][Hq * hd]
@@ -37,6 +40,7 @@ struct AttnArgs {
   const uint64_t* mask;  // [M][2]
   const int* row_grp;    // [M] group of each row (NULL: all rows in group 0)
   int M, Hq, Hkv, hd, cap;
+  int n_seq;          // sequences the cache holds: kc / vc have n_seq * Hkv * cap rows
   int max_prefix;     // upper bound on any group's prefix (sizes the split grid)
   float scale;        // 1/sqrt(hd)
   float* part;        // split partials (tensor-core path)

@@ -18,9 +18,9 @@ namespace eg {
 enum StackPhaseKind : int { kPhaseGemm = 0, kPhaseAttn = 1, kPhaseMerge = 2 };
 
 struct StackPhase {   // 128-byte aligned (CUtensorMap)
-  CUtensorMap tmW;    // GEMM weight [N][K], box [128][64]
-  CUtensorMap tmX;    // GEMM activations [rows][K], box [MT][64]
-  CUtensorMap tmXlo;  // low halves of the activations (hi/lo pair)
+  CUtensorMap tmW;    // GEMM weight [N][K], box [128][64]; attention: K cache rows, box [128][64]
+  CUtensorMap tmX;    // GEMM activations [rows][K], box [MT][64]; attention: V cache rows
+  CUtensorMap tmXlo;  // low halves of the activations (hi/lo pair); attention: grouped half queries
   int kind = kPhaseGemm;
   int N = 0, K = 0, n_tiles = 0, kbt = 0;
   long long T = 0;    // units (128-row tile, 64-wide k-block): n_tiles * kbt

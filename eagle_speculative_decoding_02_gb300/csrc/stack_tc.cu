@@ -39,6 +39,7 @@
 
 #include "../../include/eagle.h"
 #include "attention_tc.cuh"
+#include "attention_umma.cuh"
 #include "epilogue.cuh"
 #include "stack.h"
 #include "tc_ptx.cuh"
@@ -55,20 +56,18 @@ constexpr int kWBytes = kTileN * kBK * 2;  // 16 KB weight box
 constexpr int kSub = 32;                   // epilogue rows per sub-tile
 constexpr int kLdt = kTileN + 1;
 constexpr int kMaxW = 12;                  // weight ring stages (upper bound)
-constexpr int kAttnCKI = 256;              // keys per attention work item (as the standalone kernel)
-constexpr int kAttnCKS = 64;               // keys per staging sub-chunk
+constexpr int kAttnCKI = attn::kUmKeys;    // keys per attention work item
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
-constexpr int kHdMax = 128;
 constexpr int kMaxCtas = 160;              // partial buffer sizing bound
 constexpr int kEpiThreads = 128;           // epilogue warps 2-5
 // epilogue staging: one sub-tile, then the row inputs of every row of the phase
 constexpr size_t kTileBytes = (size_t)(kSub * kLdt + 4 * kStackMaxRows) * 4;
-constexpr size_t kAttnBytes = attn::smem_bytes<kHdMax, kAttnCKS>();            // one attention K/V buffer
 
 struct StackArgs {
   const StackPhase* ph;
   int n_phases;
   int M, MT, has_lo, sw, sx;
+  int apad;          // bytes after the epilogue tile that complete the attention staging region
   uint32_t tmem_cols;
   unsigned* done;    // [n_phases] phase counters, then the exit counter
   int* tile_cnt;     // [n_counters] split-K arrival counters
@@ -219,40 +218,35 @@ __device__ bool wait_count(const StackArgs& a, int i, unsigned n, volatile int* 
 }
 
 // The attention work items that have keys and rows, in order (group, KV head,
-// row block, chunk): count() counts them, item() decodes one.
-template <int CK>
+// 128-row tile, chunk of 128 keys): count() counts them, item() decodes one.
 struct AttnItems {
   const AttnArgs& at;
-  __device__ int rbs(const Group& g) const {
-    return (g.nrows * (at.Hq / at.Hkv) + attn::kRowBlock - 1) / attn::kRowBlock;
-  }
+  __device__ int rts(const Group& g) const { return attn::um_row_tiles(g.nrows, at.Hq / at.Hkv); }
   __device__ int chunks(const Group& g) const {
-    return attn::n_prefix_chunks(g.prefix, CK) + (g.block_len > 0 ? 1 : 0);
+    return attn::n_prefix_chunks(g.prefix, kAttnCKI) + (g.block_len > 0 ? 1 : 0);
   }
   __device__ int count() const {
     int n = 0;
     for (int z = 0; z < at.n_groups; ++z) {
       const Group g = at.groups[z];
-      n += chunks(g) * at.Hkv * rbs(g);
+      n += chunks(g) * at.Hkv * rts(g);
     }
     return n;
   }
-  __device__ void item(int i, int& chunk, int& y, int& z) const {
-    const int rb_count = attn::row_blocks(at.Hq, at.Hkv);
+  __device__ void item(int i, int& chunk, int& kvh, int& rt, int& z) const {
     for (z = 0; z < at.n_groups; ++z) {
       const Group g = at.groups[z];
-      const int nc = chunks(g), nr = rbs(g), n = nc * at.Hkv * nr;
+      const int nc = chunks(g), nr = rts(g), n = nc * at.Hkv * nr;
       if (i < n) {
         chunk = i % nc;
         const int rest = i / nc;
-        y = (rest / nr) * rb_count + rest % nr;
+        kvh = rest / nr;
+        rt = rest % nr;
         return;
       }
       i -= n;
     }
-    chunk = 0;
-    y = 0;
-    z = 0;
+    chunk = kvh = rt = z = 0;
   }
 };
 
@@ -269,19 +263,19 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   uint8_t* wring = smem;
   uint8_t* xring = wring + (size_t)S * wslot;
   float* tile = reinterpret_cast<float*>(xring + (size_t)S * xbytes);
-  // Attention and merge phases run while the activation halves and the epilogue
-  // tile are idle (the next GEMM phase's boxes wait for them to finish), so their
-  // K / V staging buffers alias those: two buffers if they fit, else one.
-  const int nbuf = (size_t)S * xbytes + kTileBytes >= 2 * kAttnBytes ? 2 : 1;
-  half* abuf = reinterpret_cast<half*>(xring);
+  // Attention phases run while the activation halves and the epilogue tile are
+  // idle (the next GEMM phase's boxes wait for them to finish), so their Q, K / P
+  // and V tiles alias those (padded by apad bytes where they are too small).
   const EpiRows prow = epi_rows(tile + kSub * kLdt, kStackMaxRows);  // row inputs of the current GEMM phase
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile) + kTileBytes + a.apad);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* afull = empty + S;
   uint64_t* aempty = afull + 2;
   uint64_t* drain = aempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* at_kv = drain + 1;   // attention: K / V copies
+  uint64_t* at_mma = at_kv + 1;  // attention: S and O MMAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(at_mma + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   volatile int* exit_last = abort_flag + 2;
@@ -299,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
       mbar_init(&aempty[b], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(at_kv, 1);
+    mbar_init(at_mma, 1);
     *abort_flag = 0;
     *last_flag = 0;
     *exit_last = 0;
@@ -447,6 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
     const int rows_valid = min(MT, a.M);
     int f = 0;
     bool alive = true;
+    attn::UmState ust;  // attention items: staging at the activation ring, S / O in TMEM columns [0, 256)
+    ust.sm = xring;
+    ust.kv_bar = at_kv;
+    ust.mma_bar = at_mma;
+    ust.tmem = tmem;
     for (int p = 0; p < a.n_phases; ++p) {
       const StackPhase& P = a.ph[p];
       if (p > 0 && alive) alive = epi_all(etid != 0 || wait_phase(a, p - 1, (unsigned)G, abort_flag));
@@ -581,15 +582,25 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
         run_units(ub0, ub1);
       } else if (alive && P.kind == kPhaseAttn) {
         const AttnArgs& at = P.at;
-        const AttnItems<kAttnCKI> items{at};
+        const AttnItems items{at};
         const int n = items.count();
         const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCKI) + 1;
         const int i0 = (int)((long long)c * n / G), i1 = (int)((long long)(c + 1) * n / G);
-        for (int i = i0; i < i1; ++i) {
-          int chunk, y, z;
-          items.item(i, chunk, y, z);
-          EpilogueSync{}();  // the previous item's readers of Ks / Vs are done
-          attn::attn_item<HD, kAttnCKI, kAttnCKS>(at, chunk, y, z, slots, abuf, nbuf, etid, EpilogueSync{});
+        attn::UmItem cur{}, nxt{};
+        if (i0 < i1) {
+          items.item(i0, cur.chunk, cur.kvh, cur.rt, cur.z);
+          // the tiles alias the activation ring and the epilogue tile: fence this
+          // thread's generic writes there before the copies overwrite them
+          attn::fence_proxy_async_smem();
+          EpilogueSync{}();
+          if (etid == 0) attn::um_issue<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, ust);
+        }
+        for (int i = i0; i < i1 && alive; ++i) {
+          const bool has_next = i + 1 < i1;
+          if (has_next) items.item(i + 1, nxt.chunk, nxt.kvh, nxt.rt, nxt.z);
+          alive = attn::attn_item_um<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, has_next, nxt, slots, ust, etid, col,
+                                         abort_flag, EpilogueSync{});
+          cur = nxt;
         }
       } else if (alive && P.kind == kPhaseMerge) {
         const AttnArgs& at = P.at;
@@ -632,21 +643,30 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
 }
 
 struct Layout {
-  int sw, sx;
+  int sw, sx, apad;
   size_t smem;
 };
 
-Layout layout(int MT, bool has_lo) {
+// Ring stages: as many as fit once the attention tiles (aliasing the activation
+// halves and the epilogue tile, padded where those are smaller) are accounted for.
+Layout layout(int MT, bool has_lo, int hd) {
   Layout l{};
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
   const size_t wslot = kWBytes;
-  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 5) * 8 + 16 + 1024;
-  const long long room = (long long)kSmemBudget - (long long)fixed;
-  l.sw = (int)std::min<long long>(kMaxW, room / (long long)(wslot + xbytes));
-  l.sx = l.sw;
-  if ((size_t)l.sx * xbytes + kTileBytes < kAttnBytes) l.sw = l.sx = 0;  // rejected by stack_run
-  l.smem = (size_t)l.sw * (wslot + xbytes) + fixed;
-  return l;
+  const size_t attn = hd == 128 ? attn::um_smem_bytes<128>() : attn::um_smem_bytes<64>();
+  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 7) * 8 + 16 + 1024;
+  for (int s = kMaxW; s >= 2; --s) {
+    const size_t alias = (size_t)s * xbytes + kTileBytes;
+    const size_t pad = alias >= attn ? 0 : (attn - alias + 15) / 16 * 16;
+    const size_t smem = (size_t)s * (wslot + xbytes) + fixed + pad;
+    if (smem <= (size_t)kSmemBudget) {
+      l.sw = l.sx = s;
+      l.apad = (int)pad;
+      l.smem = smem;
+      return l;
+    }
+  }
+  return l;  // sw = 0: rejected by stack_run
 }
 
 int round_mt(int M) {
@@ -706,6 +726,16 @@ void StackProgramBuilder::attention(const AttnArgs& a) {
   ph.kind = kPhaseAttn;
   ph.at = a;
   ph.at.M = M;
+  // the items copy 128 rows (keys, or GQA query rows) x 64 halves per box
+  const long long rows = (long long)a.n_seq * a.Hkv * a.cap;
+  const long long qrows = (long long)M * a.Hq;  // [Hkv][M][Hq / Hkv] query rows
+  if (rows <= 0 || rows > (1ll << 31) - 1 || (a.hd != 64 && a.hd != 128) || !a.qg ||
+      !make_tmap_f16(&ph.tmW, a.kc, (int)rows, a.hd, attn::kUmKeys) ||
+      !make_tmap_f16(&ph.tmX, a.vc, (int)rows, a.hd, attn::kUmKeys) ||
+      !make_tmap_f16(&ph.tmXlo, a.qg, (int)qrows, a.hd, attn::kUmRows)) {
+    ok = false;
+    return;
+  }
   phases.push_back(ph);
   ph.kind = kPhaseMerge;
   phases.push_back(ph);
@@ -717,7 +747,7 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   if (!stack_supported(M, hd) || n_phases <= 0 || !scratch || n_phases > max_phases || n_counters > max_counters)
     return cudaErrorInvalidValue;
   const int MT = round_mt(M);
-  const Layout l = layout(MT, has_lo);
+  const Layout l = layout(MT, has_lo, hd);
   if (l.sw < 2) return cudaErrorInvalidValue;
   StackArgs a{};
   a.ph = d_phases;
@@ -727,7 +757,8 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.has_lo = has_lo;
   a.sw = l.sw;
   a.sx = l.sx;
-  uint32_t cols = 32;
+  a.apad = l.apad;
+  uint32_t cols = attn::kUmTmemCols;  // attention S and O
   while (cols < (uint32_t)(2 * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
   a.tmem_cols = cols;
   // the layout depends only on the capacities, never on this program: programs
