@@ -155,9 +155,10 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
     case kEpiSwiglu: {
       const int blk = n0 / kTileN;
       const int rr = min(64, p.ffn - blk * 64);
-      const int c = tid;
+      const int c = tid & 63;  // two threads per output column, on alternate rows
       if (c < rr) {
-        for (int m = 0; m < msub; ++m) {
+#pragma unroll 4
+        for (int m = tid >> 6; m < msub; m += 2) {
           const float g = tile[m * ldt + c] * rscale[m];
           const float u = tile[m * ldt + rr + c] * rscale[m];
           store_hilo<T>(reinterpret_cast<T*>(p.out), p.out_lo, (size_t)(m0 + m) * p.ffn + blk * 64 + c, silu_f(g) * u);

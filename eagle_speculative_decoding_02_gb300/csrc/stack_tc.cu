@@ -506,9 +506,11 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aempty[buf]);
-            __threadfence();
             EpilogueSync{}();
-            if (etid == 0) red_release_add(reinterpret_cast<unsigned*>(a.tile_cnt + P.cnt_off + t), 1u);
+            if (etid == 0) {  // the barrier orders the other threads' stores before this fence
+              __threadfence();
+              red_release_add(reinterpret_cast<unsigned*>(a.tile_cnt + P.cnt_off + t), 1u);
+            }
             seg_t[nseg++] = t;
           }
           ++f;
