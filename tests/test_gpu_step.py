@@ -162,6 +162,34 @@ def test_bf16_stepwise_parity(cuda, shape, tree):
     print("flagged near-ties:", flagged)
 
 
+@pytest.mark.parametrize("shape", [GQA_SMALL, GQA128], ids=["hd64", "hd128"])
+def test_bf16_batch2_stepwise_parity(cuda, shape):
+    """Two sequences verified by one persistent launch (two attention groups, 122 rows): each
+    sequence's logits and argmaxes match the oracle run on that sequence alone."""
+    w = workload("8b_static", model=shape, prompt_len=40, max_new=16)
+    cap = FX.kv_capacity(w)
+    m = model(shape, cap)
+    prompts = FX.prompts(shape, 2, w.prompt_len)
+    eng = _engine(w, batch=2)
+    eng.prefill(torch.from_numpy(prompts).to(cuda))
+    sts = [OD.prefill(m, prompts[b], cap) for b in range(2)]
+    flagged = 0
+    for step in range(4):
+        gtree = eng.draft_tree()
+        am, lg = eng.verify(gtree, logits=True)
+        feats = []
+        for b in range(2):
+            oam, ofeats, ologits = OD.verify(m, sts[b], tree_from_torch(gtree, b))
+            _check_logits(lg[b].cpu().numpy(), ologits, bf16=True)
+            flagged += _check_argmax(am[b].cpu().numpy(), ologits, bf16=True)
+            feats.append(ofeats)
+        a, toks = eng.accept_commit()
+        for b in range(2):
+            oa = OD.accept_commit(sts[b], tree_from_torch(gtree, b), am[b].cpu().numpy(), feats[b])
+            assert int(a[b]) == oa
+    print("flagged near-ties:", flagged)
+
+
 def test_bf16_generate_teacher_forced(cuda):
     """Every committed token equals the oracle's greedy choice on the GPU's own stream, or is a flagged near-tie."""
     shape = GQA128
