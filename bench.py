@@ -351,6 +351,24 @@ def main():
     v_ms = statistics.median(vms)
     verify = {"ms": v_ms, "gbs": vb / v_ms / 1e6, "frac": vb / v_ms / 1e6 / hbm, "bytes": vb}
 
+    # vanilla greedy decoding with the same kernels (a one-node tree per step), and the step rate
+    # projected at the pages' mean accepted length (random-init heads accept about nothing)
+    eng.step(2, vanilla=True, use_graph=True)
+    torch.cuda.synchronize()
+    n_van = 16
+    cv = eng.committed_counts().sum().item()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(eng.stream)
+    eng.step(n_van, vanilla=True, use_graph=True)
+    b.record(eng.stream)
+    torch.cuda.synchronize()
+    van_ms = a.elapsed_time(b)
+    vanilla = {"tokens_per_s": (eng.committed_counts().sum().item() - cv) / (van_ms / 1e3),
+               "ms_per_step": van_ms / n_van, "steps": n_van}
+    step_s = ms / args.steps / 1e3
+    projected = {"tokens_per_s_at_3.5": 3.5 * w.batch / step_s, "tokens_per_s_at_4.5": 4.5 * w.batch / step_s,
+                 "note": "projection, not a measurement: this step's time at the pages' 3.5-4.5 tokens per step"}
+
     # dominant kernel: the persistent layer-stack launch of the verify pass (every layer's GEMMs with
     # their epilogues, tree attention and its merge, the LM head); the timed region is one verify
     # pass on the library's stream, which adds two small kernels (embedding rows, top-k merge)
@@ -396,6 +414,7 @@ def main():
                            "l2": "no flush: every step streams ~16 GB of weights, far above the 129 MB L2"},
                 "tokens_timed": toks, "tokens_per_step": toks / args.steps / max(world, 1) / w.batch,
                 "verify": verify, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "vanilla": vanilla, "projected": projected,
                 "gpu_launches": n_launch * args.steps if n_launch > 0 else None,
                 "gpu_launches_per_step": n_launch, "clocks": clk}
         print(json.dumps(line), flush=True)
