@@ -13,8 +13,9 @@
 //          slice of the rows, in ascending CTA order,
 //          then the fused epilogue (RMSNorm row scale, RoPE + KV write, SwiGLU,
 //          residual add + next norm, LM-head top-k records).
-//   ATTN   tree-attention work items (64-key chunk, KV head x 64-row block, group)
-//          run by the epilogue warps, partials to global memory.
+//   ATTN   tree-attention work items (128-key chunk, KV head, 128-row tile,
+//          group) on the same tensor cores (attention_umma.cuh), run by the
+//          epilogue warps with S and O in tensor memory, partials to global memory.
 //   MERGE  one warp per (row, query head) combines the partials in chunk order.
 //
 // Phase p reads only what phases < p wrote. A CTA that has finished all its
