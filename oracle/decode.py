@@ -31,6 +31,15 @@ output on the tiny model (64 tokens) and on a reduced 8B-width model; trees
 with the vanilla continuation planted at a chosen depth are accepted to
 exactly that depth; after a commit the KV cache equals the one vanilla
 decoding builds for the same tokens.
+
+Pins of the draft half (tests/test_oracle_draft.py): with FC = [0 | I] and a
+head layer whose output projections are zero, every draft distribution is the
+closed form log_softmax(LMHead(RMSNorm(E(token)))) of the row's own token (the
+catch-up pairing, the prefill's draft cache, the static rank recursion and the
+scores); with FC = [I | 0] the root's draft distribution is the target's own;
+every tree row equals the head run autoregressively along its root-to-node
+path alone (positions and visible sets); EAGLE-2 equals a brute force over the
+enumerated paths of the top-k expansion.
 """
 from __future__ import annotations
 
@@ -103,7 +112,8 @@ def draft_static(m: Model, st: SeqState, kind: str) -> Tree:
     fhat_root, logp_root = draft_catchup(m, st)
     tokens = np.zeros(n + 1, np.int32)
     tokens[0] = st.root
-    kids_of = {0: topk(logp_root, k)[0]}
+    score = np.zeros(n + 1, np.float32)
+    kids_of = {0: topk(logp_root, k)}
     fhat_of = {0: fhat_root}
     slot_of: dict[int, int] = {}
     scratch = _Scratch(st.L)
@@ -111,7 +121,9 @@ def draft_static(m: Model, st: SeqState, kind: str) -> Tree:
     for t in range(1, int(depth.max()) + 1):
         level = [j for j in range(1, n + 1) if depth[j] == t]
         for j in level:
-            tokens[j] = kids_of[int(parent[j])][rank[j]]
+            idx, val = kids_of[int(parent[j])]
+            tokens[j] = idx[rank[j]]
+            score[j] = score[int(parent[j])] + val[rank[j]]
         grow = [j for j in level if j in has_kids]
         if not grow:
             continue
@@ -127,8 +139,8 @@ def draft_static(m: Model, st: SeqState, kind: str) -> Tree:
         lp = draft_logp(m, fh)
         for i, j in enumerate(grow):
             fhat_of[j] = fh[i]
-            kids_of[j] = topk(lp[i], k)[0]
-    return Tree(tokens=tokens, parent=parent.copy(), depth=depth.copy())
+            kids_of[j] = topk(lp[i], k)
+    return Tree(tokens=tokens, parent=parent.copy(), depth=depth.copy(), score=score)
 
 
 def _ancestors(parent: np.ndarray, j: int) -> list[int]:
@@ -175,6 +187,39 @@ def draft_dynamic(m: Model, st: SeqState, k: int, depth: int, n_nodes: int, tau:
                 pool.add(np.float32(pool.score[i] + cval[r]), cidx[r], i, t, (t, fr, r))
     tree, _ = rerank(pool, n_nodes, st.root)
     return tree, pool
+
+
+def draft_logp_on_tree(m: Model, st: SeqState, tree: Tree) -> np.ndarray:
+    """Draft log-probabilities over the vocabulary at every node of a given tree: [N+1, V].
+
+    Row 0 is the root's distribution (from the catch-up rows, as in
+    ``draft_catchup``); row j > 0 is the distribution of node j's children, from
+    node j's draft row: its parent's predicted feature with node j's own token,
+    at position L + depth(j) - 1, attending to the committed draft prefix, the
+    rows of its non-root ancestors and itself. This is the head's work for any
+    tree, whatever rule chose it, so a tree built elsewhere can be scored node
+    by node (teacher forcing of the draft). Rows are run one depth at a time,
+    parents before children; node j's row uses draft-cache slot L + j - 1.
+    """
+    fhat_root, logp_root = draft_catchup(m, st)
+    n = tree.n
+    out = np.zeros((n + 1, m.shape.vocab), np.float32)
+    out[0] = logp_root
+    fhat = {0: fhat_root}
+    L = st.L
+    slot = lambda j: L + j - 1
+    for t in range(1, int(tree.depth.max()) + 1 if n else 1):
+        level = [j for j in range(1, n + 1) if tree.depth[j] == t]
+        if not level:
+            continue
+        vis = [np.concatenate([np.arange(L), np.array([slot(a) for a in tree.path(j)[1:]])]) for j in level]
+        fh = draft_rows(m, st.dkv, np.stack([fhat[int(tree.parent[j])] for j in level]), tree.tokens[level],
+                        np.full(len(level), L + t - 1), np.array([slot(j) for j in level]), vis)
+        lp = draft_logp(m, fh)
+        for i, j in enumerate(level):
+            fhat[j] = fh[i]
+            out[j] = lp[i]
+    return out
 
 
 def verify(m: Model, st: SeqState, tree: Tree):

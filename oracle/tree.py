@@ -46,6 +46,10 @@ class Tree:
     tokens: np.ndarray   # [N+1] int32
     parent: np.ndarray   # [N+1] int32, -1 for the root
     depth: np.ndarray    # [N+1] int32
+    # [N+1] float32 cumulative draft log-confidence: the sum of the draft
+    # log-probabilities along the root-to-node path (0 at the root); set by the
+    # draft functions, None for trees built by hand
+    score: np.ndarray | None = None
 
     @property
     def n(self) -> int:
@@ -136,7 +140,8 @@ def rerank(pool: Pool, n: int, root_token: int) -> tuple[Tree, list[int]]:
     parent = [-1] + [0 if pool.parent[i] < 0 else where[pool.parent[i]] for i in top]
     tree = Tree(tokens=np.array([root_token] + [pool.token[i] for i in top], dtype=np.int32),
                 parent=np.array(parent, dtype=np.int32),
-                depth=np.array([0] + [pool.depth[i] for i in top], dtype=np.int32))
+                depth=np.array([0] + [pool.depth[i] for i in top], dtype=np.int32),
+                score=np.array([0.0] + [pool.score[i] for i in top], dtype=np.float32))
     return tree, top
 
 
