@@ -42,7 +42,7 @@ class EagleWeights(C.Structure):
 
 class EagleTree(C.Structure):
     _fields_ = [("n_rows", C.c_int32), ("tokens", C.c_void_p), ("parent", C.c_void_p), ("depth", C.c_void_p),
-                ("anc", C.c_void_p)]
+                ("anc", C.c_void_p), ("score", C.c_void_p)]
 
 
 class EagleStats(C.Structure):

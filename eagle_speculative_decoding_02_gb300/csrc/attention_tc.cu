@@ -35,11 +35,7 @@ template <int HD>
 cudaError_t launch(const AttnArgs& a, cudaStream_t s) {
   const int slots = n_prefix_chunks(a.max_prefix, kCKI) + 1;
   const size_t smem = 2 * smem_bytes<HD, kCKS>();  // double-buffered sub-chunks
-  static bool smem_set = false;
-  if (!smem_set) {
-    cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    smem_set = true;
-  }
+  if (!raise_smem_limit(reinterpret_cast<const void*>(attn_tc_kernel<HD>), (int)smem)) return cudaErrorInvalidValue;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;

@@ -18,7 +18,7 @@ constexpr int kMaxDepth = 8;
 constexpr int kMaxTopK = 16;
 
 // Device status word values (mirror eagle_status).
-enum : int { kStOk = 0, kStCapacity = 4, kStTimeout = 6 };
+enum : int { kStOk = 0, kStInvalid = 1, kStCapacity = 4, kStTimeout = 6 };
 
 template <typename T> __device__ __forceinline__ float to_f(T v);
 template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }

@@ -308,7 +308,7 @@ struct Offsets {
   size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, qg, attn, act, xfc, lm_hb, lm_ssq, lm_src;
   size_t hb_lo, act_lo, attn_lo, xfc_lo, lm_hb_lo;
   size_t rec_val, rec_idx, rec_max, rec_sum, dtopk_idx, dtopk_val, dlse, vargmax, root_idx;
-  size_t t_tok, t_par, t_dep, t_anc, vt_tok, vt_par, vt_dep, vt_anc;
+  size_t t_tok, t_par, t_dep, t_anc, t_score, vt_tok, vt_par, vt_dep, vt_anc;
   size_t L, c, root, pend_tok, pend_feat, n_out, out, acc_len, acc_path, L_prev, hist, status;
   size_t p_score, p_token, p_parent, p_depth, p_cid, p_frow, p_smask, p_count, p_front, p_nfront;
   size_t s_parent, s_rank, s_depth, s_lrow, s_sidx, s_smask, s_lnodes, s_lcount;
@@ -346,6 +346,7 @@ Offsets plan(const Dims& dm) {
   o.vargmax = L.take((size_t)dm.B * kMaxTreeRows * 4); o.root_idx = L.take((size_t)dm.B * 4);
   const size_t tn = (size_t)dm.B * kMaxTreeRows;
   o.t_tok = L.take(tn * 4); o.t_par = L.take(tn * 4); o.t_dep = L.take(tn * 4); o.t_anc = L.take(tn * 16);
+  o.t_score = L.take(tn * 4);
   o.vt_tok = L.take(dm.B * 4); o.vt_par = L.take(dm.B * 4); o.vt_dep = L.take(dm.B * 4); o.vt_anc = L.take(dm.B * 16);
   const size_t B = dm.B;
   o.L = L.take(B * 4); o.c = L.take(B * 4); o.root = L.take(B * 4);
@@ -632,8 +633,8 @@ struct Eng {
       const Level prev = t > 1 ? Level{dm.level_base[t - 1], dm.level_rows[t - 1]} : Level{0, 0};
       const Level next = t < dm.D ? Level{dm.level_base[t], dm.level_rows[t]} : Level{0, 0};
       if (dm.mode == EAGLE_TREE_STATIC) {
-        EG_CK(static_level(c->st, c->topo, t, c->dtopk_idx, catchup, prev, next, c->tree, c->rows, c->groups, dm.S,
-                           c->stream));
+        EG_CK(static_level(c->st, c->topo, t, c->dtopk_idx, c->dtopk_val, c->dlse, catchup, prev, next, c->tree,
+                           c->rows, c->groups, dm.S, c->stream));
       } else {
         const float ln_tau = (float)std::log((double)c->cfg.tau);
         EG_CK(eagle2_level(c->st, c->pool, t, dm.D, dm.k, ln_tau, c->dtopk_idx, c->dtopk_val, c->dlse, catchup,
@@ -691,6 +692,13 @@ eagle_status read_status(eagle_ctx* c) {
   EG_CK(cudaStreamSynchronize(c->stream));
   EG_CK(cudaMemcpy(&s, c->st.status, sizeof(int), cudaMemcpyDeviceToHost));
   if (s == kStCapacity) return fail(c, EAGLE_ERR_CAPACITY, "device: KV cache capacity exceeded");
+  if (s == kStInvalid) {
+    // the status word stays set and nothing was committed: the context is spent
+    fail(c, EAGLE_ERR_INVALID_ARG, "device: verified tree is inconsistent or has two siblings with one token, "
+                                   "or its accepted path is longer than the configured depth");
+    c->failed = true;
+    return EAGLE_ERR_INVALID_ARG;
+  }
   if (s == kStTimeout) return fail(c, EAGLE_ERR_TIMEOUT, "device: bounded wait timed out");
   if (s != 0) return fail(c, EAGLE_ERR_CUDA, "device: status " + std::to_string(s));
   return EAGLE_OK;
@@ -763,8 +771,9 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->rec_max = (float*)P(o.rec_max); c->rec_sum = (float*)P(o.rec_sum);
   c->dtopk_idx = (int*)P(o.dtopk_idx); c->dtopk_val = (float*)P(o.dtopk_val); c->dlse = (float*)P(o.dlse);
   c->vargmax = (int*)P(o.vargmax); c->root_idx = (int*)P(o.root_idx);
-  c->tree = TreeOut{dm.NR, (int*)P(o.t_tok), (int*)P(o.t_par), (int*)P(o.t_dep), (uint64_t*)P(o.t_anc)};
-  c->vtree = TreeOut{1, (int*)P(o.vt_tok), (int*)P(o.vt_par), (int*)P(o.vt_dep), (uint64_t*)P(o.vt_anc)};
+  c->tree = TreeOut{dm.NR, (int*)P(o.t_tok), (int*)P(o.t_par), (int*)P(o.t_dep), (uint64_t*)P(o.t_anc),
+                    (float*)P(o.t_score)};
+  c->vtree = TreeOut{1, (int*)P(o.vt_tok), (int*)P(o.vt_par), (int*)P(o.vt_dep), (uint64_t*)P(o.vt_anc), nullptr};
   State& st = c->st;
   st.L = (int*)P(o.L); st.c = (int*)P(o.c); st.root = (int*)P(o.root); st.pend_tok = (int*)P(o.pend_tok);
   st.pend_feat = (float*)P(o.pend_feat); st.n_out = (int*)P(o.n_out); st.out = (int*)P(o.out);
@@ -863,9 +872,10 @@ eagle_status eagle_draft_tree(eagle_ctx* c, eagle_tree* out) {
     EG_CK(cudaMemcpyAsync(out->parent, c->tree.parent, n * 4, cudaMemcpyDeviceToDevice, c->stream));
     EG_CK(cudaMemcpyAsync(out->depth, c->tree.depth, n * 4, cudaMemcpyDeviceToDevice, c->stream));
     EG_CK(cudaMemcpyAsync(out->anc, c->tree.anc, n * 16, cudaMemcpyDeviceToDevice, c->stream));
+    if (out->score) EG_CK(cudaMemcpyAsync(out->score, c->tree.score, n * 4, cudaMemcpyDeviceToDevice, c->stream));
     out->n_rows = c->tree.n_rows;
   } else if (out) {
-    *out = eagle_tree{c->tree.n_rows, c->tree.tokens, c->tree.parent, c->tree.depth, c->tree.anc};
+    *out = eagle_tree{c->tree.n_rows, c->tree.tokens, c->tree.parent, c->tree.depth, c->tree.anc, c->tree.score};
   }
   c->phase = 2;
   return EAGLE_OK;
@@ -877,7 +887,7 @@ eagle_status eagle_verify(eagle_ctx* c, const eagle_tree* tree, int32_t* d_argma
   if (!tree || tree->n_rows < 1 || tree->n_rows > EAGLE_MAX_TREE_ROWS || !tree->tokens || !tree->parent ||
       !tree->depth || !tree->anc)
     return fail(c, EAGLE_ERR_INVALID_ARG, "bad tree");
-  TreeOut t{tree->n_rows, tree->tokens, tree->parent, tree->depth, tree->anc};
+  TreeOut t{tree->n_rows, tree->tokens, tree->parent, tree->depth, tree->anc, nullptr};
   c->last_tree = t;
   EG_TRY(dispatch(c, [&](auto E) { return decltype(E)::verify(c, t, d_argmax, d_logits); }));
   c->phase = 3;

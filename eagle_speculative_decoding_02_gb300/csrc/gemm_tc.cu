@@ -22,6 +22,8 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/eagle.h"
 #include "epilogue.cuh"
@@ -372,15 +374,32 @@ bool make_tmap_f16(CUtensorMap* m, const void* base, int rows, int cols, int box
 }
 
 int num_sms() {
-  static int n = 0;
+  // per device ordinal: a process may drive GPUs of different SM counts
+  static int n_of[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) dev = 0;
+  int n = n_of[dev];
   if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (n <= 0) n = 148;
     if (n > kNsmSizing) n = kNsmSizing;
+    n_of[dev] = n;
   }
   return n;
+}
+
+bool raise_smem_limit(const void* kernel, int bytes) {
+  // cudaFuncSetAttribute applies to the current device only: once per (kernel, device)
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& kd : done)
+    if (kd.first == kernel && kd.second == dev) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.emplace_back(kernel, dev);
+  return true;
 }
 
 namespace {
@@ -444,10 +463,7 @@ cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N
   if (!make_tmap_bf16(&tmW, W, N, K, kTileN) || !make_tmap_bf16(&tmX, X, M, K, p.MT)) return cudaErrorInvalidValue;
   if (X_lo && !make_tmap_bf16(&tmXlo, X_lo, M, K, p.MT)) return cudaErrorInvalidValue;
   if (!X_lo) tmXlo = tmX;  // unused
-  static std::once_flag smem_attr;
-  std::call_once(smem_attr, [] {
-    cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-  });
+  if (!raise_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel), kSmemBudget)) return cudaErrorInvalidValue;
   TcArgs a{};
   a.M = M;
   a.MT = p.MT;

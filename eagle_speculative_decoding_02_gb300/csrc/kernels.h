@@ -26,6 +26,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int bo
 bool make_tmap_f16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
 // SMs of the current device (capped at the scratch-sizing bound).
 int num_sms();
+// Raise a kernel's dynamic shared-memory limit on the current device (once per device).
+bool raise_smem_limit(const void* kernel, int bytes);
 
 // ---- attention ---------------------------------------------------------------------------------
 struct AttnArgs {

@@ -777,13 +777,7 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.trace = trace;
   a.y_last = y_last;
   auto kernel = hd == 128 ? stack_tc_kernel<128> : stack_tc_kernel<64>;
-  static bool attr_set[2] = {false, false};
-  bool& set = attr_set[hd == 128 ? 1 : 0];
-  if (!set) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e != cudaSuccess) return e;
-    set = true;
-  }
+  if (!raise_smem_limit(reinterpret_cast<const void*>(kernel), kSmemBudget)) return cudaErrorInvalidValue;
   const int G = num_sms();
   if (G > kMaxCtas) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};

@@ -90,6 +90,28 @@ __global__ void setup_catchup_kernel(State st, Rows rows, Group* groups) {
   }
 }
 
+// Is row j of a sequence's tree (rows at `base`) consistent: root at row 0,
+// parents earlier in BFS order, depth = parent's depth + 1, ancestor mask =
+// parent's mask + its own bit, and a token distinct from its earlier siblings'
+// (padding rows carry token -1 and are exempt)?
+__device__ bool tree_row_ok(const TreeOut& tree, int base, int j) {
+  const int m = base + j;
+  const uint64_t a0 = tree.anc[2 * m], a1 = tree.anc[2 * m + 1];
+  if (j == 0) return tree.parent[m] == -1 && tree.depth[m] == 0 && a0 == 1ull && a1 == 0ull;
+  const int p = tree.parent[m];
+  if (p < 0 || p >= j) return false;
+  const int dj = tree.depth[m];
+  if (dj != tree.depth[base + p] + 1) return false;
+  uint64_t e0 = tree.anc[2 * (base + p)], e1 = tree.anc[2 * (base + p) + 1];
+  if (j < 64) e0 |= 1ull << j; else e1 |= 1ull << (j - 64);
+  if (a0 != e0 || a1 != e1) return false;
+  const int tok = tree.tokens[m];
+  if (tok >= 0)
+    for (int i = 1; i < j; ++i)
+      if (tree.parent[base + i] == p && tree.tokens[base + i] == tok) return false;
+  return true;
+}
+
 // Verify rows: tree row j of sequence b at position L + depth(j), KV slot L + j.
 __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* groups) {
   pdl_wait();
@@ -99,6 +121,8 @@ __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* gr
   const int L = st.L[b];
   const bool fits = L + NR <= st.cap;
   if (!fits && threadIdx.x == 0) set_status(st.status, kStCapacity);
+  for (int j = threadIdx.x; j < NR; j += blockDim.x)
+    if (!tree_row_ok(tree, b * NR, j)) set_status(st.status, kStInvalid);
   for (int j = threadIdx.x; j < NR; j += blockDim.x) {
     const int m = b * NR + j;
     rows.seq[m] = b;
@@ -160,6 +184,7 @@ __global__ void set_root_tree_kernel(State st, TreeOut tree) {
 
 // ---------------------------------------------------------------- static tree
 __global__ void static_level_kernel(State st, StaticTopo topo, int t, const int* __restrict__ topk_idx,
+                                    const float* __restrict__ topk_val, const float* __restrict__ lse,
                                     Level catchup, Level prev, Level next, TreeOut tree, Rows rows,
                                     Group* groups, int S) {
   pdl_wait();
@@ -168,13 +193,19 @@ __global__ void static_level_kernel(State st, StaticTopo topo, int t, const int*
   const int NR = topo.n_rows;
   const int L = st.L[b], c = st.c[b];
   const int root_row = catchup.base + b * catchup.per_seq + c - 1;
-  // tokens of depth-t nodes
+  // tokens of depth-t nodes, and their cumulative draft log-confidence (the
+  // parent's, written by the previous level, plus the node's own log-probability)
   for (int j = threadIdx.x; j < NR; j += blockDim.x) {
-    if (j == 0 && t == 1) tree.tokens[b * NR] = st.root[b];
+    if (j == 0 && t == 1) {
+      tree.tokens[b * NR] = st.root[b];
+      if (tree.score) tree.score[b * NR] = 0.f;
+    }
     if (topo.depth[j] != t) continue;
     const int p = topo.parent[j];
     const int prow = (p == 0) ? root_row : prev.base + b * prev.per_seq + topo.lrow[p];
-    tree.tokens[b * NR + j] = topk_idx[(size_t)prow * topo.k + topo.rank[j]];
+    const size_t at = (size_t)prow * topo.k + topo.rank[j];
+    tree.tokens[b * NR + j] = topk_idx[at];
+    if (tree.score) tree.score[b * NR + j] = (p == 0 ? 0.f : tree.score[b * NR + p]) + (topk_val[at] - lse[prow]);
   }
   if (next.per_seq == 0) return;
   __syncthreads();
@@ -410,6 +441,7 @@ __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, 
     tree.depth[base] = 0;
     tree.anc[2 * base] = 1ull;
     tree.anc[2 * base + 1] = 0ull;
+    if (tree.score) tree.score[base] = 0.f;
     for (int i = 0; i < NR - 1; ++i) {
       const int j = i + 1, m = base + j;
       if (i < n) {
@@ -419,6 +451,7 @@ __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, 
         tree.tokens[m] = pool.token[pb + e];
         tree.parent[m] = pj;
         tree.depth[m] = pool.depth[pb + e];
+        if (tree.score) tree.score[m] = pool.score[pb + e];
         uint64_t a0 = tree.anc[2 * (base + pj)], a1 = tree.anc[2 * (base + pj) + 1];
         if (j < 64) a0 |= 1ull << j; else a1 |= 1ull << (j - 64);
         tree.anc[2 * m] = a0;
@@ -428,6 +461,7 @@ __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, 
         tree.tokens[m] = -1;
         tree.parent[m] = 0;
         tree.depth[m] = 1;
+        if (tree.score) tree.score[m] = -INFINITY;
         uint64_t a0 = 1ull, a1 = 0ull;
         if (j < 64) a0 |= 1ull << j; else a1 |= 1ull << (j - 64);
         tree.anc[2 * m] = a0;
@@ -444,7 +478,7 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
   pdl_wait();
   pdl_trigger();
   __shared__ int path[kMaxDepth + 1];
-  __shared__ int s_a, s_bonus;
+  __shared__ int s_a, s_bonus, s_over;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int NR = tree.n_rows;
   const int base = b * NR;
@@ -462,8 +496,9 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
   }
   if (tid < 32) {
     int cur = 0, a = 0;
+    bool over = false;
     if (tid == 0) path[0] = 0;
-    while (a < st.D1 - 1) {
+    for (;;) {
       const int want = amax[base + cur];
       int found = 0x7fffffff;
       for (int j = 1 + tid; j < NR; j += 32)
@@ -471,6 +506,10 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
       if (found == 0x7fffffff) break;
+      if (a == st.D1 - 1) {  // the accepted path goes on past the catch-up capacity
+        over = true;
+        break;
+      }
       cur = found;
       ++a;
       if (tid == 0) path[a] = cur;
@@ -478,9 +517,20 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
     if (tid == 0) {
       s_a = a;
       s_bonus = amax[base + cur];
+      s_over = over;
     }
   }
   __syncthreads();
+  if (s_over) {
+    if (tid == 0) {
+      set_status(st.status, kStInvalid);
+      st.acc_len[b] = 0;
+      if (acc_out) acc_out[b] = -1;
+      if (tok_out)
+        for (int t = 0; t <= kMaxDepth; ++t) tok_out[b * (kMaxDepth + 1) + t] = -1;
+    }
+    return;
+  }
   const int a = s_a, bonus = s_bonus;
   const int L = st.L[b];
   // committed features: root and accepted nodes
@@ -573,9 +623,11 @@ cudaError_t set_root_tree(State st, TreeOut tree, cudaStream_t s) {
   return launch_pdl(set_root_tree_kernel, dim3(1), dim3(64), 0, s, st, tree);
 }
 
-cudaError_t static_level(State st, StaticTopo topo, int t, const int* topk_idx, Level catchup, Level prev,
-                         Level next, TreeOut tree, Rows rows, Group* groups, int S, cudaStream_t s) {
-  return launch_pdl(static_level_kernel, dim3(st.B), dim3(128), 0, s, st, topo, t, topk_idx, catchup, prev, next, tree, rows, groups, S);
+cudaError_t static_level(State st, StaticTopo topo, int t, const int* topk_idx, const float* topk_val,
+                         const float* lse, Level catchup, Level prev, Level next, TreeOut tree, Rows rows,
+                         Group* groups, int S, cudaStream_t s) {
+  return launch_pdl(static_level_kernel, dim3(st.B), dim3(128), 0, s, st, topo, t, topk_idx, topk_val, lse, catchup,
+                    prev, next, tree, rows, groups, S);
 }
 
 cudaError_t eagle2_level(State st, Pool pool, int t, int depth, int k, float ln_tau, const int* topk_idx,

@@ -51,6 +51,7 @@ struct TreeOut {
   int* parent;
   int* depth;
   uint64_t* anc;     // [B][n_rows][2]
+  float* score;      // [B][n_rows] cumulative draft log-confidence (NULL: not tracked)
 };
 
 // Dynamic (EAGLE-2) pool, per sequence capacity `cap` entries.
@@ -71,6 +72,8 @@ struct Pool {
 cudaError_t setup_prefill_rows(const int* prompt, int P, int c0, int CL, int B, bool draft, Rows rows,
                                Group* groups, cudaStream_t s);
 cudaError_t setup_catchup_rows(State st, Rows rows, Group* groups, cudaStream_t s);
+// Also checks the tree (BFS order, parent/depth/ancestor-mask consistency,
+// distinct sibling tokens) and records kStInvalid if it is not.
 cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, cudaStream_t s);
 cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, int CL, int P, int* root_out,
                            cudaStream_t s);
@@ -78,8 +81,9 @@ cudaError_t set_root_tree(State st, TreeOut tree, cudaStream_t s);
 
 // Static tree: assign the tokens of depth-t nodes from their parents' top-k
 // and, when t < depth_max, write the rows of the depth-t draft forward.
-cudaError_t static_level(State st, StaticTopo topo, int t, const int* topk_idx, Level catchup, Level prev,
-                         Level next, TreeOut tree, Rows rows, Group* groups, int S, cudaStream_t s);
+cudaError_t static_level(State st, StaticTopo topo, int t, const int* topk_idx, const float* topk_val,
+                         const float* lse, Level catchup, Level prev, Level next, TreeOut tree, Rows rows,
+                         Group* groups, int S, cudaStream_t s);
 
 // EAGLE-2: add the children of the frontier expanded at depth t-1 (or of the
 // root when t == 1), then, when t < depth, select the depth-t frontier and
@@ -91,6 +95,8 @@ cudaError_t eagle2_level(State st, Pool pool, int t, int depth, int k, float ln_
 cudaError_t eagle2_final(State st, Pool pool, int n_nodes, TreeOut tree, cudaStream_t s);
 
 // Greedy accept over the verified tree; commit tokens and features, advance L.
+// A path longer than D1 - 1 nodes (only a caller-built tree can hold one) is
+// not cut short: nothing is committed and kStInvalid is recorded.
 cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, int* acc_out,
                           int* tok_out, cudaStream_t s);
 // Move accepted K/V rows to contiguous slots in every layer.

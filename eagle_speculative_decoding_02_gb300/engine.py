@@ -68,10 +68,11 @@ class Tree:
     parent: torch.Tensor
     depth: torch.Tensor
     anc: torch.Tensor      # [B, n_rows, 2] int64 (bit patterns of uint64 masks)
+    score: torch.Tensor | None = None   # [B, n_rows] float32 cumulative draft log-confidence (drafted trees)
 
     def c(self) -> L.EagleTree:
         return L.EagleTree(self.n_rows, self.tokens.data_ptr(), self.parent.data_ptr(), self.depth.data_ptr(),
-                           self.anc.data_ptr())
+                           self.anc.data_ptr(), self.score.data_ptr() if self.score is not None else None)
 
 
 class EagleEngine:
@@ -135,7 +136,8 @@ class EagleEngine:
         tr = Tree(n, torch.empty((self.batch, n), dtype=torch.int32, device=self.device),
                   torch.empty((self.batch, n), dtype=torch.int32, device=self.device),
                   torch.empty((self.batch, n), dtype=torch.int32, device=self.device),
-                  torch.empty((self.batch, n, 2), dtype=torch.int64, device=self.device))
+                  torch.empty((self.batch, n, 2), dtype=torch.int64, device=self.device),
+                  torch.empty((self.batch, n), dtype=torch.float32, device=self.device))
         ct = tr.c()
         self._call("eagle_draft_tree", C.byref(ct))
         return tr

@@ -125,13 +125,24 @@ typedef struct {
   eagle_layer_weights head;            /* draft head decoder layer */
 } eagle_weights;
 
-/* A draft tree per sequence, BFS order, row 0 = root. Device arrays. */
+/* A draft tree per sequence, BFS order, row 0 = root. Device arrays.
+ * A tree passed to eagle_verify must be consistent: parent[0] = -1, depth[0] = 0,
+ * anc[0] = {1, 0}; for j > 0, 0 <= parent[j] < j, depth[j] = depth[parent[j]] + 1,
+ * anc[j] = anc[parent[j]] | bit j; and siblings carry distinct tokens (rows
+ * with token -1 are padding, never accepted), so that the greedy accepted path
+ * is unique. Trees deeper than the configured tree depth may be verified (for
+ * example a chain carrying a known continuation, to read its logits), but
+ * eagle_accept_commit refuses an accepted path longer than that depth. */
 typedef struct {
   int32_t n_rows;          /* N + 1, same for every sequence */
   int32_t* tokens;         /* [batch][n_rows] */
   int32_t* parent;         /* [batch][n_rows], -1 at the root */
   int32_t* depth;          /* [batch][n_rows] */
   uint64_t* anc;           /* [batch][n_rows][2]: bit i set when row i is on the root-to-row path (self included) */
+  float* score;            /* [batch][n_rows] or NULL: cumulative draft log-confidence of each row, the sum of
+                              the draft log-probabilities along its root-to-row path ([LPD] "EAGLE vs EAGLE-2";
+                              0 at the root, -inf at padding rows); written by eagle_draft_tree, unused by
+                              eagle_verify */
 } eagle_tree;
 
 typedef struct {
@@ -147,17 +158,26 @@ typedef struct eagle_ctx eagle_ctx;
 
 /* Bytes of device workspace eagle_init needs for this configuration. Host-only; no CUDA call. */
 eagle_status eagle_workspace_size(const eagle_config* cfg, size_t* bytes);
+/* (The workspace holds the KV caches of the target and the head, the rows of
+ * every forward, the decoding state and the kernels' scratch; [SDE] "Deep
+ * dive": the KV cache of the verified prefix is reused across steps.) */
 
 /* Validate the configuration, carve the workspace (256-byte aligned, owned by
- * the caller, contents overwritten) and bind the weights. Returns the context
- * through *out. The device current at this call must be the one holding all pointers. */
+ * the caller, contents overwritten) and bind the weights: the target decoder
+ * stack, and the draft head that shares its embedding, final norm and LM head
+ * ([SDE] "Technical insight": the head reuses the target's own LM head; [LPD]
+ * "How EAGLE works": a one-layer head over the target's top-layer feature).
+ * Returns the context through *out. The device current at this call must be
+ * the one holding all pointers. */
 eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d_workspace,
                         size_t workspace_bytes, void* stream, eagle_ctx** out);
 
-/* Target prefill of batch prompts of equal length prompt_len (d_tokens [batch][prompt_len]),
- * the head's catch-up over prompt rows 0..prompt_len-2, and the first new token
- * (greedy) per sequence, written to d_root_out [batch] when not NULL. Resets all
- * per-sequence state. */
+/* Target prefill of batch prompts of equal length prompt_len (d_tokens
+ * [batch][prompt_len]; ragged prompts are not supported), the head's rows over
+ * prompt positions 0..prompt_len-2 (feature f_i with the embedding of the next
+ * true token t_{i+1}: [SDE] "Technical insight", the shifted token sequence),
+ * and the first new token (greedy) per sequence, written to d_root_out [batch]
+ * when not NULL. Resets all per-sequence state. */
 eagle_status eagle_prefill(eagle_ctx* ctx, const int32_t* d_tokens, int32_t prompt_len,
                            int32_t* d_root_out);
 
@@ -174,22 +194,31 @@ eagle_status eagle_draft_tree(eagle_ctx* ctx, eagle_tree* out);
  * L + depth, K/V written to slots L + row. d_argmax [batch][n_rows] receives the
  * greedy token after each row; d_logits [batch][n_rows][vocab] float32 receives
  * the logits when not NULL (debug/parity path). The tree may be the one
- * eagle_draft_tree returned or any caller-built tree (n_rows <= 121). */
+ * eagle_draft_tree returned or any caller-built tree (n_rows <= 121). The tree
+ * is checked on the device against the rules stated at eagle_tree: a tree
+ * that breaks one sets the device status, nothing is committed by the
+ * following eagle_accept_commit, and the next eagle_sync_status returns
+ * EAGLE_ERR_INVALID_ARG (the context is then spent). */
 eagle_status eagle_verify(eagle_ctx* ctx, const eagle_tree* tree, int32_t* d_argmax, float* d_logits);
 
 /* Accept and commit ([SDE] "Deep dive": longest correct prefix): greedy walk
  * over the last verified tree, compaction of the accepted K/V to contiguous
- * slots, features kept for the next draft. d_accept_len [batch] (may be NULL)
+ * slots, features kept for the next draft. An accepted path longer than the
+ * configured tree depth (a caller-built tree) is not cut short: nothing is
+ * committed, *d_accept_len is -1 and the device status reports
+ * EAGLE_ERR_INVALID_ARG. d_accept_len [batch] (may be NULL)
  * receives the accepted draft length a; d_tokens_out [batch][EAGLE_MAX_DEPTH+1]
  * (may be NULL) the a+1 committed tokens (accepted nodes, then the bonus token),
  * padded with -1. */
 eagle_status eagle_accept_commit(eagle_ctx* ctx, int32_t* d_accept_len, int32_t* d_tokens_out);
 
-/* Prefill, then draft/verify/accept steps until every sequence has at least
- * max_new committed tokens (the prefill's first token counts); d_out
- * [batch][max_new] receives exactly max_new tokens per sequence. With
- * use_graph != 0 the step is captured once in a CUDA graph and replayed.
- * h_stats (may be NULL) is filled after the final synchronisation. */
+/* Speculative generation ([SDE] "Deep dive": draft a tree, verify it in one
+ * target pass, keep the longest correct prefix, repeat; the output equals the
+ * target's own greedy decoding): prefill, then draft/verify/accept steps until
+ * every sequence has at least max_new committed tokens (the prefill's first
+ * token counts); d_out [batch][max_new] receives exactly max_new tokens per
+ * sequence. With use_graph != 0 the step is captured once in a CUDA graph and
+ * replayed. h_stats (may be NULL) is filled after the final synchronisation. */
 eagle_status eagle_generate(eagle_ctx* ctx, const int32_t* d_prompt, int32_t prompt_len, int32_t max_new,
                             int32_t use_graph, int32_t* d_out, eagle_stats* h_stats);
 
@@ -252,13 +281,12 @@ eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const
  *     that device current; make that first call before any stream capture.
  *   - Every call shares the one array and clears the counters it uses before
  *     launching; calls that overlap on the GPU (other streams, other threads)
- *     race on it and must be serialised by the caller. */
+ *     race on it and must be serialised by the caller.
+ *   - There is no status word: if one of the kernel's bounded waits gives up
+ *     (2 s), the call has still returned EAGLE_OK and d_y is incomplete. */
 eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w, float* d_y,
                                    void* stream);
 
-/* LM head + per-row top-k: for each row m of X [M,K], the k largest logits of
- * X W^T (W [N,K]) as (index, value) ordered by value desc then index asc, and
- * the row's log-sum-exp. d_idx/d_val [M][k], d_lse [M]. */
 /* The same products run by the persistent layer-stack kernel (the kernel of the
  * verify and draft passes), for checking its work split against eagle_op_gemm
  * and eagle_op_lmhead_topk: n_phases GEMM phases Y = (X + X_lo) W^T in one
@@ -275,6 +303,9 @@ eagle_status eagle_op_gemm_persistent(int32_t M, int32_t N, int32_t K, int32_t n
                                       int32_t* d_idx, float* d_val, float* d_lse, void* d_scratch,
                                       size_t scratch_bytes, void* stream);
 
+/* LM head + per-row top-k: for each row m of X [M,K], the k largest logits of
+ * X W^T (W [N,K]) as (index, value) ordered by value desc then index asc, and
+ * the row's log-sum-exp. d_idx/d_val [M][k], d_lse [M]. */
 size_t eagle_op_lmhead_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t k, int32_t dtype);
 eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k, const void* d_x,
                                   const void* d_w, int32_t* d_idx, float* d_val, float* d_lse, void* d_scratch,

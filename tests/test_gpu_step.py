@@ -112,9 +112,9 @@ def _planted(van, a, extra, vocab, seed):
                    depth=np.array([0] + [depth[j] for j in order], np.int32))
 
 
-@pytest.mark.parametrize("a", [0, 1, 2, 3, 6])
+@pytest.mark.parametrize("a", [0, 1, 2, 3])
 def test_planted_tree_accept_lengths(cuda, a):
-    """A planted vanilla chain of length a is accepted to min(a, tree depth 3)."""
+    """A planted vanilla chain of length a (up to the tree depth, 3) is accepted to exactly a."""
     w = TINY
     cap = FX.kv_capacity(w)
     m = model(w.model, cap)
@@ -125,7 +125,6 @@ def test_planted_tree_accept_lengths(cuda, a):
     tree = _planted(van, a, 4, w.model.vocab, a)
     eng.verify(tree_to_torch(tree))
     acc, toks = eng.accept_commit()
-    a = min(a, 3)
     assert int(acc[0]) == a
     # the committed stream continues exactly like vanilla decoding
     out = [int(t) for t in toks[0].cpu().numpy() if t >= 0]
@@ -230,3 +229,36 @@ def test_batch_rows_are_independent(cuda):
         o1, _ = e1.generate(pb, w.max_new)
         margins = stream_margins(e1, pb, o1[0].cpu().numpy())
         same_until_near_tie(o1[0].tolist(), o4[b].tolist(), margins)
+
+
+def _bad_tree(kind, van, vocab):
+    """Planted trees that must commit nothing: the vanilla continuation one level deeper than the configured
+    depth (3), so that the accepted path would be longer than the catch-up capacity, or two siblings with
+    one token (the accepted path would not be unique)."""
+    if kind == "deep":
+        n = 5   # a chain of depth 4 > 3
+        return OT.Tree(tokens=np.array(van[:n], np.int32), parent=np.arange(-1, n - 1, dtype=np.int32),
+                       depth=np.arange(n, dtype=np.int32))
+    return OT.Tree(tokens=np.array([van[0], 7, 7], np.int32), parent=np.array([-1, 0, 0], np.int32),
+                   depth=np.array([0, 1, 1], np.int32))
+
+
+@pytest.mark.parametrize("kind", ["deep", "duplicate_siblings"])
+def test_invalid_trees_commit_nothing_and_are_reported(cuda, kind):
+    from eagle_speculative_decoding_02_gb300 import _lib as L
+    w = TINY
+    cap = FX.kv_capacity(w)
+    m = model(w.model, cap)
+    prompt = FX.prompts(w.model, 1, w.prompt_len)
+    van = OD.vanilla_greedy(m, prompt[0], 8, cap)
+    eng = _engine(w)
+    eng.prefill(torch.from_numpy(prompt).to(cuda))
+    eng.verify(tree_to_torch(_bad_tree(kind, van, w.model.vocab)))
+    a, _ = eng.accept_commit()
+    assert int(a[0]) <= 0                          # nothing committed
+    with pytest.raises(L.EagleError) as e:
+        eng.sync_status()
+    assert e.value.code == 1                       # EAGLE_ERR_INVALID_ARG
+    with pytest.raises(L.EagleError) as e2:
+        eng.step(1)
+    assert e2.value.code == 7                      # the context is spent

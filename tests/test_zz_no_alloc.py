@@ -57,3 +57,24 @@ def test_noalloc_rejects_shapes_beyond_its_maximum(cuda):
     assert lib.eagle_op_gemm_noalloc(65, 128, 128, x.data_ptr(), w.data_ptr(), y.data_ptr(), s) == 2
     assert lib.eagle_op_gemm_noalloc(8, 100, 128, x.data_ptr(), w.data_ptr(), y.data_ptr(), s) == 2
     assert lib.eagle_op_gemm_noalloc(8, 128, 128, None, w.data_ptr(), y.data_ptr(), s) == 1
+
+
+def test_noalloc_call_leaves_free_device_memory_unchanged(cuda):
+    """After a first call on the device, further calls take no device memory: the free memory the driver
+    reports is the same before and after them."""
+    from eagle_speculative_decoding_02_gb300 import _lib as L
+    lib = L.load()
+    M, N, K = 33, 2048, 1024
+    x = torch.ones((M, K), dtype=torch.bfloat16, device=cuda)
+    w = torch.ones((N, K), dtype=torch.bfloat16, device=cuda)
+    y = torch.empty((M, N), dtype=torch.float32, device=cuda)
+    s = C.c_void_p(torch.cuda.current_stream(cuda).cuda_stream)
+    assert lib.eagle_op_gemm_noalloc(M, N, K, x.data_ptr(), w.data_ptr(), y.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(cuda)
+    for _ in range(3):
+        assert lib.eagle_op_gemm_noalloc(M, N, K, x.data_ptr(), w.data_ptr(), y.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(cuda)
+    assert free1 == free0
+    assert torch.all(y == float(K))
