@@ -96,11 +96,47 @@ struct UmState {
   uint64_t* kv_bar;    // TMA of K and V
   uint64_t* mma_bar;   // tcgen05.commit of S, then of O
   uint32_t tmem;       // tensor-memory base (lane 0, column 0)
+  const Group* groups; // the launch's attention groups (a copy in shared memory)
   uint32_t kv_par = 0, mma_par = 0;
 };
 
-// An item: chunk of the group's keys (the last one is the tree block), KV head,
-// 128-row tile, group.
+// Balanced split of a group's keys. A group's rows see the slots [0, T),
+// T = prefix + block_len: the prefix (every key visible) and then the tree block
+// (keys seen through the ancestor masks). The slots are cut into parts of
+// ps <= 128 keys: ns = max(n0, ceil(T / 128)) parts requested, where n0 = the
+// CTAs per (KV head, row tile) pair of the whole phase, ps = ceil(T / ns), and
+// ceil(T / ps) non-empty parts result. With every part of equal size and, when
+// the keys allow it, no more items than CTAs, no CTA runs two items while
+// others wait (128-key chunks plus the tree block gave 160 items for 152 CTAs
+// at a 1040-key prefix). Part j covers slots [j ps, min((j + 1) ps, T)).
+__device__ __forceinline__ int um_part_keys(const Group& g, int n0) {
+  const int T = g.prefix + g.block_len;
+  const int ns = max(n0, (T + kUmKeys - 1) / kUmKeys);
+  return max(1, (T + ns - 1) / ns);
+}
+__device__ __forceinline__ int um_parts(const Group& g, int n0) {
+  const int T = g.prefix + g.block_len;
+  const int ps = um_part_keys(g, n0);
+  return (T + ps - 1) / ps;
+}
+
+// Partial slots per row that any phase may need: ceil(T / 128) <= the chunk
+// count of the longest prefix, and n0 <= max_ctas / Hkv.
+__host__ __device__ inline int um_part_slots(int max_prefix, int Hkv, int max_ctas) {
+  const int a = n_prefix_chunks(max_prefix, kUmKeys), b = max_ctas / Hkv;
+  return (a > b ? a : b) + 1;
+}
+
+// Bits off .. off + 31 of the 128-bit value (hi:lo), zero outside bits [0, 128).
+__device__ __forceinline__ uint32_t bits32(uint64_t lo, uint64_t hi, int off) {
+  if (off <= -32 || off >= 128) return 0u;
+  if (off < 0) return (uint32_t)(lo << (-off));
+  if (off == 0) return (uint32_t)lo;
+  if (off < 64) return (uint32_t)((lo >> off) | (hi << (64 - off)));
+  return (uint32_t)(hi >> (off - 64));
+}
+
+// An item: part of the group's keys, KV head, 128-row tile, group.
 struct UmItem {
   int chunk, kvh, rt, z;
 };
@@ -112,11 +148,11 @@ struct UmItem {
 // [Hkv * M * G][HD] and of the K / V caches as [n_seq * Hkv * cap][HD].
 template <int HD>
 __device__ void um_issue(const AttnArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                         const CUtensorMap* tmV, const UmItem& it, const UmState& st) {
-  const Group g = a.groups[it.z];
-  const int G = a.Hq / a.Hkv;
-  const int nck = n_prefix_chunks(g.prefix, kUmKeys);
-  const int key0 = it.chunk == nck ? g.prefix : it.chunk * kUmKeys;
+                         const CUtensorMap* tmV, const UmItem& it, int n0, const UmState& st) {
+  const int Hq = a.Hq, Hkv = a.Hkv, Mrows = a.M, cap = a.cap;
+  const Group g = st.groups[it.z];
+  const int G = Hq / Hkv;
+  const int key0 = it.chunk * um_part_keys(g, n0);
   uint8_t* sQ = st.sm;
   uint8_t* sV = sQ + (size_t)kUmRows * HD * 2;
   uint8_t* sK = sV + (size_t)kUmKeys * HD * 2;
@@ -124,8 +160,8 @@ __device__ void um_issue(const AttnArgs& a, const CUtensorMap* tmQ, const CUtens
   // earlier in the launch; the copies read them through the async proxy
   asm volatile("fence.proxy.async.global;" ::: "memory");
   mbar_expect_tx(st.kv_bar, (uint32_t)(3 * kUmRows * HD * 2));
-  const int ykv = (g.seq * a.Hkv + it.kvh) * a.cap + key0;
-  const int yq = (it.kvh * a.M + g.row0) * G + it.rt * kUmRows;
+  const int ykv = (g.seq * Hkv + it.kvh) * cap + key0;
+  const int yq = (it.kvh * Mrows + g.row0) * G + it.rt * kUmRows;
 #pragma unroll
   for (int h = 0; h < HD / 64; ++h) {
     tma_load_2d(sQ + h * kUmAtom, tmQ, st.kv_bar, h * 64, yq);
@@ -139,21 +175,26 @@ __device__ void um_issue(const AttnArgs& a, const CUtensorMap* tmQ, const CUtens
 // and thus its row of the tile. sync() is a barrier over the 128 threads. The
 // item's copies were issued (um_issue); once its MMAs are done and before its
 // partials go out, thread 0 issues those of `next` when has_next. The caller
-// passes only items with keys and rows. Returns false on a timeout (status set,
-// abort raised).
+// passes only items with keys and rows; n0 is the phase's parts request (see
+// um_part_keys). Returns false on a timeout (status set, abort raised).
 template <int HD, typename Sync>
 __device__ bool attn_item_um(const AttnArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                              const CUtensorMap* tmV, const UmItem& cur, bool has_next, const UmItem& next,
-                             int n_chunk_slots, UmState& st, int tid, int row, volatile int* abort_flag,
+                             int n0, int n_chunk_slots, UmState& st, int tid, int row, volatile int* abort_flag,
                              Sync sync) {
   static_assert(HD == 64 || HD == 128, "head dim");
-  const Group g = a.groups[cur.z];
-  const int G = a.Hq / a.Hkv;
+  // the arguments live in global memory: read them once into registers (the
+  // partial stores below could otherwise force reloads)
+  const int Hq = a.Hq, Hkv = a.Hkv, Mrows = a.M;
+  const uint64_t* const mask = a.mask;
+  float* const part = a.part;
+  int* const status = a.status;
+  const Group g = st.groups[cur.z];
+  const int G = Hq / Hkv;
   const int R = g.nrows * G;
-  const int nck = n_prefix_chunks(g.prefix, kUmKeys);
-  const bool block = cur.chunk == nck;
-  const int key0 = block ? g.prefix : cur.chunk * kUmKeys;
-  const int nkeys = block ? min(g.block_len, kUmKeys) : min(kUmKeys, g.prefix - key0);
+  const int ps = um_part_keys(g, n0);
+  const int key0 = cur.chunk * ps;                                  // the box's first slot
+  const int nkeys = min(ps, g.prefix + g.block_len - key0);         // this part's keys
   const int r = cur.rt * kUmRows + row;
   const bool rv = r < R;
   const int node = rv ? r / G : 0;
@@ -163,28 +204,31 @@ __device__ bool attn_item_um(const AttnArgs& a, const CUtensorMap* tmQ, const CU
   uint8_t* sK = sV + (size_t)kUmKeys * HD * 2;  // K, then P
   const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
 
-  // visibility of this row's keys, 32 per word: key < nkeys, and in the tree
-  // block the node's ancestor bit
+  // visibility of this row's keys, 32 per word: box row i (slot key0 + i) is
+  // visible when i < nkeys and the slot is in the prefix, or is tree-block slot
+  // prefix + t with bit t set in the node's ancestor mask
   uint32_t vis[kUmKeys / 32];
   {
-    uint64_t mk0 = ~0ull, mk1 = ~0ull;
-    if (block && rv) {
-      mk0 = a.mask[2 * (g.row0 + node)];
-      mk1 = a.mask[2 * (g.row0 + node) + 1];
+    uint64_t mk0 = 0ull, mk1 = 0ull;
+    if (rv && key0 + nkeys > g.prefix) {
+      mk0 = mask[2 * (g.row0 + node)];
+      mk1 = mask[2 * (g.row0 + node) + 1];
     }
+    const int npre = g.prefix - key0;  // box rows below the tree block
 #pragma unroll
     for (int b = 0; b < kUmKeys / 32; ++b) {
-      uint32_t w = (uint32_t)((b < 2 ? mk0 : mk1) >> ((b & 1) * 32));
-      const int left = nkeys - 32 * b;
-      w &= left >= 32 ? ~0u : (left <= 0 ? 0u : (1u << left) - 1u);
-      vis[b] = rv ? w : 0u;
+      const int nv = nkeys - 32 * b, np = npre - 32 * b;
+      const uint32_t valid = nv >= 32 ? ~0u : (nv <= 0 ? 0u : (1u << nv) - 1u);
+      const uint32_t pre = np >= 32 ? ~0u : (np <= 0 ? 0u : (1u << np) - 1u);
+      const uint32_t blk = bits32(mk0, mk1, key0 + 32 * b - g.prefix);
+      vis[b] = rv ? (valid & (pre | blk)) : 0u;
     }
   }
 
   // 1. S = Q K^T once the copies have landed
   bool ok = true;
   if (tid == 0) {
-    ok = mbar_wait(st.kv_bar, st.kv_par, abort_flag, a.status);
+    ok = mbar_wait(st.kv_bar, st.kv_par, abort_flag, status);
     if (ok) {
       tc_fence_after();
 #pragma unroll
@@ -198,7 +242,7 @@ __device__ bool attn_item_um(const AttnArgs& a, const CUtensorMap* tmQ, const CU
   }
   st.kv_par ^= 1;
   ok = epi_all(tid != 0 || ok);
-  if (ok) ok = epi_all(mbar_wait(st.mma_bar, st.mma_par, abort_flag, a.status));
+  if (ok) ok = epi_all(mbar_wait(st.mma_bar, st.mma_par, abort_flag, status));
   st.mma_par ^= 1;
   if (!ok) return false;  // (a timed-out wait leaves the CTA to abort; no MMA is left issued)
   tc_fence_after();
@@ -268,16 +312,16 @@ __device__ bool attn_item_um(const AttnArgs& a, const CUtensorMap* tmQ, const CU
     }
     umma_commit(st.mma_bar);
   }
-  ok = epi_all(mbar_wait(st.mma_bar, st.mma_par, abort_flag, a.status));
+  ok = epi_all(mbar_wait(st.mma_bar, st.mma_par, abort_flag, status));
   st.mma_par ^= 1;
   if (!ok) return false;
   tc_fence_after();
   // every tile is free again: the next item's copies overlap this item's output
-  if (tid == 0 && has_next) um_issue<HD>(a, tmQ, tmK, tmV, next, st);
+  if (tid == 0 && has_next) um_issue<HD>(a, tmQ, tmK, tmV, next, n0, st);
 
   // 4. the row's partial (tcgen05.ld is warp-wide: every lane loads)
-  const PartLayout pl{a.part, a.M * a.Hq, n_chunk_slots, HD};
-  const int w = (g.row0 + node) * a.Hq + qh;
+  const PartLayout pl{part, Mrows * Hq, n_chunk_slots, HD};
+  const int w = (g.row0 + node) * Hq + qh;
 #pragma unroll 1
   for (int b = 0; b < HD / 32; b += 2) {
     float o[2][32];
@@ -293,6 +337,129 @@ __device__ bool attn_item_um(const AttnArgs& a, const CUtensorMap* tmQ, const CU
   }
   if (rv) *reinterpret_cast<float2*>(pl.ml(cur.chunk, w)) = make_float2(mx, sum);
   tc_fence_before();
+  return true;
+}
+
+// The group holding verify row `row` (the groups partition the rows).
+__device__ __forceinline__ int um_group_of(const Group* groups, int n_groups, int row) {
+  for (int z = 0; z < n_groups; ++z)
+    if (row >= groups[z].row0 && row < groups[z].row0 + groups[z].nrows) return z;
+  return 0;
+}
+
+// Merge of the persistent kernel over this CTA's (row, query head) pairs
+// w in [w0, w1): the combination of each pair's part partials (max, sum,
+// unnormalised output) in part order, as attn_merge_warp computes it, with the
+// partials staged in shared memory first. For every part s and 32-column block,
+// the partials of consecutive pairs are contiguous in the partial buffer, so a
+// few bulk copies bring all of them in one round trip (instead of dozens of
+// dependent loads per pair, which made this phase latency-bound); the (max, sum)
+// pairs come by plain loads. Parts are taken in batches that fit `sm_bytes` of
+// shared memory at `sm`, with each pair's running (max, sum, output) kept there
+// between batches. Run by the 128 epilogue threads; bar = an mbarrier of this
+// CTA with parity *par. Returns false on a timeout.
+template <int HD, typename Sync>
+__device__ bool um_merge_staged(const AttnArgs& a, const Group* groups, int n0, int w0, int w1, int n_chunk_slots,
+                                uint8_t* sm, uint32_t sm_bytes, uint64_t* bar, uint32_t* par, int tid,
+                                volatile int* abort_flag, Sync sync) {
+  const int nw = w1 - w0;
+  if (nw <= 0) return true;
+  constexpr int NB = HD / 32;
+  // the arguments live in global memory: read them once into registers (the
+  // output stores below could otherwise force a reload after each of them)
+  const int Hq = a.Hq, n_groups = a.n_groups;
+  bf16* const out = reinterpret_cast<bf16*>(a.o);
+  bf16* const out_lo = a.o_lo;
+  int* const status = a.status;
+  const PartLayout pl{a.part, a.M * Hq, n_chunk_slots, HD};
+  const int ew = tid >> 5, lane = tid & 31;
+  float* run = reinterpret_cast<float*>(sm);  // [nw][HD + 2]: running output, then (max, sum)
+  const uint32_t run_bytes = ((uint32_t)nw * (HD + 2) * 4 + 127) & ~127u;
+  uint8_t* stage = sm + run_bytes;
+  const uint32_t per_part = (uint32_t)nw * (HD * 4 + 8);
+  const int sb = run_bytes + per_part <= sm_bytes ? (int)((sm_bytes - run_bytes) / per_part) : 0;
+  if (sb < 1) {
+    set_status(status, kStCapacity);
+    return false;
+  }
+  // the most parts any of these pairs' groups has
+  const int r0 = w0 / Hq, r1 = (w1 - 1) / Hq;
+  int nmax = 0;
+  for (int z = 0; z < n_groups; ++z) {
+    const Group g = groups[z];
+    if (g.row0 <= r1 && g.row0 + g.nrows > r0) nmax = max(nmax, um_parts(g, n0));
+  }
+  for (int s0 = 0; s0 < nmax; s0 += sb) {
+    const int ns = min(sb, nmax - s0);
+    float2* mls = reinterpret_cast<float2*>(stage + (size_t)ns * NB * nw * 128);  // [ns][nw]
+    if (tid == 0) {
+      // the partials were written by other SMs' generic stores earlier in the launch
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_expect_tx(bar, (uint32_t)ns * NB * nw * 128);
+      for (int s = 0; s < ns; ++s)
+        for (int b = 0; b < NB; ++b)
+          bulk_load(stage + ((size_t)s * NB + b) * nw * 128, pl.o(s0 + s, w0, b), (uint32_t)nw * 128, bar);
+    }
+    for (int i = tid; i < ns * nw; i += 128) {
+      const int s = i / nw, t = i - s * nw;
+      mls[i] = __ldcg(reinterpret_cast<const float2*>(pl.ml(s0 + s, w0 + t)));
+    }
+    sync();
+    const bool ok = epi_all(mbar_wait(bar, *par, abort_flag, status));
+    *par ^= 1;
+    if (!ok) return false;
+    const float* os = reinterpret_cast<const float*>(stage);
+    for (int t = ew; t < nw; t += 4) {
+      const int w = w0 + t, row = w / Hq, qh = w - row * Hq;
+      const int nck = um_parts(groups[um_group_of(groups, n_groups, row)], n0);
+      float M = -INFINITY, L = 0.f, acc[NB];
+      if (s0 == 0) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) acc[i] = 0.f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) acc[i] = run[(size_t)t * (HD + 2) + lane + 32 * i];
+        M = run[(size_t)t * (HD + 2) + HD];
+        L = run[(size_t)t * (HD + 2) + HD + 1];
+      }
+      const int se = min(s0 + ns, nck);
+      // (a plain loop: unrolling the parts, for more loads in flight, measured
+      // slower - this code runs once per layer, one warp per scheduler)
+      float Mb = M;
+      for (int s = s0; s < se; ++s) Mb = fmaxf(Mb, mls[(s - s0) * nw + t].x);
+      if (Mb != -INFINITY) {
+        const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);
+        L *= r;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) acc[i] *= r;
+        for (int s = s0; s < se; ++s) {
+          const float2 ml = mls[(s - s0) * nw + t];
+          if (ml.x == -INFINITY) continue;
+          const float wgt = exp2f(ml.x - Mb);
+          L += wgt * ml.y;
+#pragma unroll
+          for (int i = 0; i < NB; ++i) acc[i] += wgt * os[(((size_t)(s - s0) * NB + i) * nw + t) * 32 + lane];
+        }
+        M = Mb;
+      }
+      if (s0 + ns >= nmax) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t ob = ((size_t)row * Hq + qh) * HD;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) store_hilo<bf16>(out, out_lo, ob + lane + 32 * i, acc[i] * inv);
+      } else {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) run[(size_t)t * (HD + 2) + lane + 32 * i] = acc[i];
+        if (lane == 0) {
+          run[(size_t)t * (HD + 2) + HD] = M;
+          run[(size_t)t * (HD + 2) + HD + 1] = L;
+        }
+      }
+    }
+    // this batch's staging is read: the next batch's copies may overwrite it
+    fence_proxy_async_smem();
+    sync();
+  }
   return true;
 }
 

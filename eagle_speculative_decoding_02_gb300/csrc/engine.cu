@@ -43,6 +43,7 @@ struct LayerPtrs {
 struct ProgSpec {
   int kind = 0, M = 0, hbase = 0, k = 0;
   int n_phases = 0, n_counters = 0, first = 0;  // first: index of its first phase in the program array
+  int first_attn = -1;                          // its first attention phase (set when it is built)
 };
 
 struct Dims {
@@ -380,7 +381,7 @@ Offsets plan(const Dims& dm) {
   o.stack_prog = L.take((size_t)dm.stack_phases_total * sizeof(StackPhase));
   o.stack_scratch = L.take(dm.progs.empty() ? 0 : stack_scratch_bytes(dm.stack_M, dm.stack_phases_max,
                                                                           dm.stack_counters_max));
-  o.stack_part = L.take(dm.progs.empty() ? 0 : stack_attention_part_bytes(dm.stack_M, dm.Hq, dm.hd, dm.cap_d));
+  o.stack_part = L.take(dm.progs.empty() ? 0 : stack_attention_part_bytes(dm.stack_M, dm.Hq, dm.Hkv, dm.hd, dm.cap_d));
   o.total = L.total;
   return o;
 }
@@ -552,7 +553,7 @@ struct Eng {
     unsigned long long* trace = p.kind == 0 ? c->trace : nullptr;
     EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
                     c->stack_scratch, c->dm.stack_phases_max, c->dm.stack_counters_max, c->st.status, trace,
-                    lm_logits, c->stream));
+                    lm_logits, c->groups, c->dm.B, p.first_attn, c->stream));
     return EAGLE_OK;
   }
 
@@ -561,7 +562,7 @@ struct Eng {
     const Dims& dm = c->dm;
     if (sizeof(T) != 2 || dm.progs.empty()) return EAGLE_OK;
     std::vector<StackPhase> all;
-    for (const ProgSpec& p : dm.progs) {
+    for (ProgSpec& p : c->dm.progs) {
       StackProgramBuilder b;
       b.M = p.M;
       b.MT = stack_mt(p.M);
@@ -575,6 +576,7 @@ struct Eng {
       }
       if ((int)b.phases.size() != p.n_phases || b.n_counters != p.n_counters)
         return fail(c, EAGLE_ERR_UNSUPPORTED, "persistent program: phase count");
+      p.first_attn = b.first_attn;
       all.insert(all.end(), b.phases.begin(), b.phases.end());
     }
     EG_CK(cudaMemcpyAsync(c->stack_prog, all.data(), all.size() * sizeof(StackPhase), cudaMemcpyHostToDevice,

@@ -47,37 +47,44 @@ __device__ inline EpiRows epi_rows(float* sm, int cap) {
 // partial sum j % kEpiBatch (complete batches), the rest into partial 0, then
 // adds the partials in order; its loads are issued 32 at a time.
 __device__ inline void load_epi_rows(const EpiParams& p, int m0, int msub, EpiRows r, int tid, int nthr) {
+  // (fields read once: the shared-memory stores below may otherwise force reloads of p)
+  const float* const ssq_in = p.ssq_in;
+  const int n_ssq = p.n_ssq_in, M = p.M, kind = p.kind;
+  const float inv_d = p.inv_d_in, eps = p.eps;
+  const int* const rpos = p.rows.pos;
+  const int* const rslot = p.rows.slot;
+  const int* const rseq = p.rows.seq;
   for (int m = tid; m < msub; m += nthr) {
     float sc = 1.f;
-    if (p.ssq_in) {
-      const float* s_in = p.ssq_in + m0 + m;
+    if (ssq_in) {
+      const float* s_in = ssq_in + m0 + m;
       float part[kEpiBatch];
 #pragma unroll
       for (int q = 0; q < kEpiBatch; ++q) part[q] = 0.f;
-      const int nfull = p.n_ssq_in - p.n_ssq_in % kEpiBatch;
+      const int nfull = n_ssq - n_ssq % kEpiBatch;
       int j = 0;
       for (; j + 4 * kEpiBatch <= nfull; j += 4 * kEpiBatch) {
         float v[4 * kEpiBatch];
 #pragma unroll
-        for (int q = 0; q < 4 * kEpiBatch; ++q) v[q] = __ldcg(s_in + (size_t)(j + q) * p.M);
+        for (int q = 0; q < 4 * kEpiBatch; ++q) v[q] = __ldcg(s_in + (size_t)(j + q) * M);
 #pragma unroll
         for (int q = 0; q < 4 * kEpiBatch; ++q) part[q % kEpiBatch] += v[q];
       }
       for (; j < nfull; j += kEpiBatch) {
 #pragma unroll
-        for (int q = 0; q < kEpiBatch; ++q) part[q] += __ldcg(s_in + (size_t)(j + q) * p.M);
+        for (int q = 0; q < kEpiBatch; ++q) part[q] += __ldcg(s_in + (size_t)(j + q) * M);
       }
-      for (; j < p.n_ssq_in; ++j) part[0] += __ldcg(s_in + (size_t)j * p.M);
+      for (; j < n_ssq; ++j) part[0] += __ldcg(s_in + (size_t)j * M);
       float s = 0.f;
 #pragma unroll
       for (int q = 0; q < kEpiBatch; ++q) s += part[q];
-      sc = rsqrtf(s * p.inv_d_in + p.eps);
+      sc = rsqrtf(s * inv_d + eps);
     }
     r.scale[m] = sc;
-    if (p.kind == kEpiQkv) {
-      r.pos[m] = p.rows.pos[m0 + m];
-      r.slot[m] = p.rows.slot[m0 + m];
-      r.seq[m] = p.rows.seq[m0 + m];
+    if (kind == kEpiQkv) {
+      r.pos[m] = rpos[m0 + m];
+      r.slot[m] = rslot[m0 + m];
+      r.seq[m] = rseq[m0 + m];
     }
   }
 }
@@ -88,34 +95,58 @@ __device__ inline void load_epi_rows(const EpiParams& p, int m0, int msub, EpiRo
 template <typename T, typename Sync>
 __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, int msub, int n0, EpiRows r,
                               int tid, Sync sync) {
-  const int ncols = min(kTileN, p.N - n0);
+  // Every field is read once into a register: the global stores below could
+  // otherwise force the compiler to reload p's fields after each of them.
+  const int kind = p.kind, M = p.M, N = p.N;
+  const int ncols = min(kTileN, N - n0);
+  float* const y = p.y;
+  void* const out = p.out;
+  bf16* const out_lo = p.out_lo;
+  bf16* const hb_lo = p.hb_lo;
+  const int q_dim = p.q_dim, kv_dim = p.kv_dim, head_dim = p.head_dim, n_kv = p.n_kv, cap = p.cap;
+  const float* const rope_cos = p.rope_cos;
+  const float* const rope_sin = p.rope_sin;
+  void* const kc = p.kc;
+  void* const vc = p.vc;
+  __half* const qg = p.qg;
+  const float qg_scale = p.qg_scale;
+  const int ffn = p.ffn;
+  float* const h = p.h;
+  void* const hb = p.hb;
+  float* const ssq_out = p.ssq_out;
+  const float* const gain = p.gain;
+  const int topk = p.topk;
+  float* const rec_val = p.rec_val;
+  int* const rec_idx = p.rec_idx;
+  float* const rec_max = p.rec_max;
+  float* const rec_sum = p.rec_sum;
   const float* rscale = r.scale;
   const int* rpos = r.pos;
   const int* rslot = r.slot;
   const int* rseq = r.seq;
-  switch (p.kind) {
+  switch (kind) {
     case kEpiStore: {
       for (int m = 0; m < msub; ++m)
-        if (tid < ncols) p.y[(size_t)(m0 + m) * p.N + n0 + tid] = tile[m * ldt + tid] * rscale[m];
+        if (tid < ncols) y[(size_t)(m0 + m) * N + n0 + tid] = tile[m * ldt + tid] * rscale[m];
       break;
     }
     case kEpiQkv: {
       const int c = tid;
       if (c < ncols) {
         const int n = n0 + c;
-        const int hd = p.head_dim, half = hd >> 1;
+        const int hd = head_dim, half = hd >> 1;
         const int i = n % hd;
-        const int region = n < p.q_dim ? 0 : (n < p.q_dim + p.kv_dim ? 1 : 2);
+        const int region = n < q_dim ? 0 : (n < q_dim + kv_dim ? 1 : 2);
         const int partner = i < half ? c + half : c - half;
         const int fi = i < half ? i : i - half;
-        const int nn = n - p.q_dim - (region == 2 ? p.kv_dim : 0);
+        const int nn = n - q_dim - (region == 2 ? kv_dim : 0);
         const int kvh = nn / hd;
         // this column's element of the grouped half queries, row 0
         __half* qgc = nullptr;
         int qg_row = 0;
-        if (region == 0 && p.qg) {
-          const int qh = n / hd, G = p.q_dim / hd / p.n_kv;
-          qgc = p.qg + ((size_t)(qh / G) * p.M * G + qh % G) * hd + i;
+        if (region == 0 && qg) {
+          const int qh = n / hd, G = q_dim / hd / n_kv;
+          qgc = qg + ((size_t)(qh / G) * M * G + qh % G) * hd + i;
           qg_row = G * hd;
         }
         for (int mb = 0; mb < msub; mb += kEpiLoadBatch) {
@@ -126,8 +157,8 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
             sn[q] = 0.f;
             if (region < 2 && mb + q < msub) {
               const size_t at = (size_t)rpos[mb + q] * half + fi;
-              cs[q] = p.rope_cos[at];
-              sn[q] = p.rope_sin[at];
+              cs[q] = rope_cos[at];
+              sn[q] = rope_sin[at];
             }
           }
 #pragma unroll
@@ -140,12 +171,12 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
               v = i < half ? v * cs[q] - pv * sn[q] : v * cs[q] + pv * sn[q];
             }
             if (region == 0) {
-              reinterpret_cast<float*>(p.out)[(size_t)(m0 + m) * p.q_dim + n] = v;
-              if (qgc) qgc[(size_t)(m0 + m) * qg_row] = __float2half_rn(v * p.qg_scale);
+              reinterpret_cast<float*>(out)[(size_t)(m0 + m) * q_dim + n] = v;
+              if (qgc) qgc[(size_t)(m0 + m) * qg_row] = __float2half_rn(v * qg_scale);
             } else if (rslot[m] >= 0) {
-              const size_t at = (((size_t)rseq[m] * p.n_kv + kvh) * p.cap + rslot[m]) * hd + i;
+              const size_t at = (((size_t)rseq[m] * n_kv + kvh) * cap + rslot[m]) * hd + i;
               using KvT = typename KvOf<T>::type;
-              reinterpret_cast<KvT*>(region == 1 ? p.kc : p.vc)[at] = kv_from_f<T>(v);
+              reinterpret_cast<KvT*>(region == 1 ? kc : vc)[at] = kv_from_f<T>(v);
             }
           }
         }
@@ -154,14 +185,14 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
     }
     case kEpiSwiglu: {
       const int blk = n0 / kTileN;
-      const int rr = min(64, p.ffn - blk * 64);
+      const int rr = min(64, ffn - blk * 64);
       const int c = tid & 63;  // two threads per output column, on alternate rows
       if (c < rr) {
 #pragma unroll 4
         for (int m = tid >> 6; m < msub; m += 2) {
           const float g = tile[m * ldt + c] * rscale[m];
           const float u = tile[m * ldt + rr + c] * rscale[m];
-          store_hilo<T>(reinterpret_cast<T*>(p.out), p.out_lo, (size_t)(m0 + m) * p.ffn + blk * 64 + c, silu_f(g) * u);
+          store_hilo<T>(reinterpret_cast<T*>(out), out_lo, (size_t)(m0 + m) * ffn + blk * 64 + c, silu_f(g) * u);
         }
       }
       break;
@@ -171,20 +202,20 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
       const int c = tid;
       if (c < ncols) {
         const int n = n0 + c;
-        const float gn = p.gain[n];
+        const float gn = gain[n];
         for (int mb = 0; mb < msub; mb += kEpiLoadBatch) {
           float hv[kEpiLoadBatch];
 #pragma unroll
           for (int q = 0; q < kEpiLoadBatch; ++q)  // residual loads of the batch, ahead of its stores
-            hv[q] = (p.kind == kEpiResid && mb + q < msub) ? __ldcg(p.h + (size_t)(m0 + mb + q) * p.N + n) : 0.f;
+            hv[q] = (kind == kEpiResid && mb + q < msub) ? __ldcg(h + (size_t)(m0 + mb + q) * N + n) : 0.f;
 #pragma unroll
           for (int q = 0; q < kEpiLoadBatch; ++q) {
             const int m = mb + q;
             if (m >= msub) break;
-            const size_t at = (size_t)(m0 + m) * p.N + n;
+            const size_t at = (size_t)(m0 + m) * N + n;
             const float hn = hv[q] + tile[m * ldt + c] * rscale[m];
-            p.h[at] = hn;
-            store_hilo<T>(reinterpret_cast<T*>(p.hb), p.hb_lo, at, hn * gn);
+            h[at] = hn;
+            store_hilo<T>(reinterpret_cast<T*>(hb), hb_lo, at, hn * gn);
             tile[m * ldt + c] = hn * hn;
           }
         }
@@ -197,7 +228,7 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
         float s = tile[m * ldt + lane] + tile[m * ldt + lane + 32] + tile[m * ldt + lane + 64] +
                   tile[m * ldt + lane + 96];
         s = warp_sum(s);
-        if (lane == 0) p.ssq_out[(size_t)(n0 / kTileN) * p.M + m0 + m] = s;
+        if (lane == 0) ssq_out[(size_t)(n0 / kTileN) * M + m0 + m] = s;
       }
       break;
     }
@@ -212,19 +243,19 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
           const int c = lane + 32 * j;
           idx[j] = n0 + c;
           v[j] = c < ncols ? tile[m * ldt + c] * rscale[m] : -INFINITY;
-          if (p.y && c < ncols) p.y[(size_t)(m0 + m) * p.N + n0 + c] = v[j];
+          if (y && c < ncols) y[(size_t)(m0 + m) * N + n0 + c] = v[j];
         }
         float mx = warp_max(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
         float se = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) se += (lane + 32 * j < ncols) ? __expf(v[j] - mx) : 0.f;
         se = warp_sum(se);
-        const size_t rec = (size_t)ti * p.M + m0 + m;
+        const size_t rec = (size_t)ti * M + m0 + m;
         if (lane == 0) {
-          p.rec_max[rec] = mx;
-          p.rec_sum[rec] = se;
+          rec_max[rec] = mx;
+          rec_sum[rec] = se;
         }
-        for (int k = 0; k < p.topk; ++k) {
+        for (int k = 0; k < topk; ++k) {
           float bv = v[0];
           int bi = idx[0], bj = 0;
 #pragma unroll
@@ -239,8 +270,8 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
               if (j == bj) v[j] = -INFINITY;
           }
           if (lane == 0) {
-            p.rec_val[rec * p.topk + k] = wv;
-            p.rec_idx[rec * p.topk + k] = wi < p.N ? wi : -1;
+            rec_val[rec * topk + k] = wv;
+            rec_idx[rec * topk + k] = wi < N ? wi : -1;
           }
         }
       }

@@ -45,6 +45,7 @@ struct StackProgramBuilder {
   bool has_lo = false;
   std::vector<StackPhase> phases;
   int n_counters = 0;
+  int first_attn = -1;  // index of the first attention phase
   bool ok = true;
   void gemm(const StackGemmDesc& g);
   void attention(const AttnArgs& a);  // adds the attention phase and its merge phase
@@ -62,7 +63,7 @@ int stack_ctas();
 // partial sums (zero-initialised by the caller once).
 size_t stack_scratch_bytes(int M, int max_phases, int max_counters);
 // Attention partial buffer of the persistent kernel.
-size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix);
+size_t stack_attention_part_bytes(int M, int Hq, int Hkv, int hd, int max_prefix);
 // Runs the program (d_phases: device copy of builder.phases) on stack_ctas()
 // CTAs. scratch holds stack_scratch_bytes(M', max_phases, max_counters) bytes
 // for capacities that every program sharing it fits (the layout is derived from
@@ -71,8 +72,12 @@ size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix);
 // = when each CTA finished phase p, the last row = when it started.
 // y_last (may be NULL): replaces the output pointer y of the last phase's
 // epilogue for this launch (the LM head's optional logits).
+// groups / n_groups (<= 128): the groups every attention phase of the program
+// reads (each CTA keeps a copy in shared memory); NULL / 0 without attention.
+// first_attn: index of the program's first attention phase (-1 if none); every
+// attention phase of a program has the same rows, heads and groups.
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
                       void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
-                      float* y_last, cudaStream_t s);
+                      float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s);
 
 }  // namespace eg

@@ -61,6 +61,7 @@ constexpr int kAttnCKI = attn::kUmKeys;    // keys per attention work item
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
 constexpr int kMaxCtas = 160;              // partial buffer sizing bound
 constexpr int kEpiThreads = 128;           // epilogue warps 2-5
+constexpr int kMaxGroups = 128;            // attention groups kept in shared memory
 // epilogue staging: one sub-tile, then the row inputs of every row of the phase
 constexpr size_t kTileBytes = (size_t)(kSub * kLdt + 4 * kStackMaxRows) * 4;
 
@@ -77,6 +78,9 @@ struct StackArgs {
   int* status;
   unsigned long long* trace;  // optional: [n_phases + 1][G] %globaltimer stamps
   float* y_last;              // optional: output y of the last phase's epilogue (LM-head logits)
+  const Group* groups;        // attention groups of every attention phase (NULL if none)
+  int n_groups;               // <= kMaxGroups
+  int first_attn;             // index of the first attention phase, -1 if none (all share rows and groups)
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -188,6 +192,7 @@ __device__ bool wait_phase(const StackArgs& a, int p, unsigned G, volatile int* 
   if (ld_acquire(a.done + p) >= G) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);  // back off: the other warps of the SM keep working meanwhile
     if (ld_acquire(a.done + p) >= G) return true;
     if ((i & 15) == 0) {
       if (*abort_flag) return false;
@@ -206,6 +211,7 @@ __device__ bool wait_count(const StackArgs& a, int i, unsigned n, volatile int* 
   if (ld_acquire(p) >= n) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t k = 1;; ++k) {
+    __nanosleep(64);
     if (ld_acquire(p) >= n) return true;
     if ((k & 15) == 0) {
       if (*abort_flag) return false;
@@ -219,25 +225,33 @@ __device__ bool wait_count(const StackArgs& a, int i, unsigned n, volatile int* 
 }
 
 // The attention work items that have keys and rows, in order (group, KV head,
-// 128-row tile, chunk of 128 keys): count() counts them, item() decodes one.
+// 128-row tile, part of the keys): count() counts them, item() decodes one. The
+// keys of every group are split into parts by the balanced rule of
+// attn::um_part_keys, with n0 = the CTAs per (KV head, row tile) pair.
 struct AttnItems {
-  const AttnArgs& at;
-  __device__ int rts(const Group& g) const { return attn::um_row_tiles(g.nrows, at.Hq / at.Hkv); }
-  __device__ int chunks(const Group& g) const {
-    return attn::n_prefix_chunks(g.prefix, kAttnCKI) + (g.block_len > 0 ? 1 : 0);
+  const Group* groups;  // the phase's groups (shared-memory copy)
+  int n_groups, Hkv, G;  // (copied: the arguments live in global memory)
+  int n0 = 1;
+  __device__ AttnItems(const AttnArgs& a, const Group* g, int n_ctas)
+      : groups(g), n_groups(a.n_groups), Hkv(a.Hkv), G(a.Hq / a.Hkv) {
+    int pairs = 0;
+    for (int z = 0; z < n_groups; ++z) pairs += Hkv * rts(groups[z]);
+    n0 = pairs > 0 ? max(1, n_ctas / pairs) : 1;
   }
+  __device__ int rts(const Group& g) const { return attn::um_row_tiles(g.nrows, G); }
+  __device__ int chunks(const Group& g) const { return attn::um_parts(g, n0); }
   __device__ int count() const {
     int n = 0;
-    for (int z = 0; z < at.n_groups; ++z) {
-      const Group g = at.groups[z];
-      n += chunks(g) * at.Hkv * rts(g);
+    for (int z = 0; z < n_groups; ++z) {
+      const Group g = groups[z];
+      n += chunks(g) * Hkv * rts(g);
     }
     return n;
   }
   __device__ void item(int i, int& chunk, int& kvh, int& rt, int& z) const {
-    for (z = 0; z < at.n_groups; ++z) {
-      const Group g = at.groups[z];
-      const int nc = chunks(g), nr = rts(g), n = nc * at.Hkv * nr;
+    for (z = 0; z < n_groups; ++z) {
+      const Group g = groups[z];
+      const int nc = chunks(g), nr = rts(g), n = nc * Hkv * nr;
       if (i < n) {
         chunk = i % nc;
         const int rest = i / nc;
@@ -280,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   volatile int* exit_last = abort_flag + 2;
+  Group* sgroups = reinterpret_cast<Group*>(tmem_slot + 4);  // kMaxGroups entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, G = gridDim.x;
@@ -301,6 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
     *exit_last = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // the groups of the attention phases, read once (the item loops decode them often)
+  for (int i = threadIdx.x; i < a.n_groups; i += kThreads) sgroups[i] = a.groups[i];
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(a.tmem_cols)
@@ -445,10 +462,29 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
     int f = 0;
     bool alive = true;
     attn::UmState ust;  // attention items: staging at the activation ring, S / O in TMEM columns [0, 256)
+    ust.groups = sgroups;
     ust.sm = xring;
     ust.kv_bar = at_kv;
     ust.mma_bar = at_mma;
     ust.tmem = tmem;
+    // The attention phases of a program share their rows and groups: this CTA's
+    // items and merge pairs are decoded once, while the first phase streams.
+    struct {
+      int n0 = 1, slots = 0, i0 = 0, i1 = 0, w0 = 0, w1 = 0;
+      attn::UmItem first{};
+    } plan;
+    if (a.first_attn >= 0) {
+      const AttnArgs& at = a.ph[a.first_attn].at;
+      const AttnItems items(at, sgroups, G);
+      const int n = items.count(), nm = at.M * at.Hq;
+      plan.n0 = items.n0;
+      plan.slots = attn::um_part_slots(at.max_prefix, at.Hkv, kMaxCtas);
+      plan.i0 = (int)((long long)c * n / G);
+      plan.i1 = (int)((long long)(c + 1) * n / G);
+      plan.w0 = (int)((long long)c * nm / G);
+      plan.w1 = (int)((long long)(c + 1) * nm / G);
+      if (plan.i0 < plan.i1) items.item(plan.i0, plan.first.chunk, plan.first.kvh, plan.first.rt, plan.first.z);
+    }
     for (int p = 0; p < a.n_phases; ++p) {
       const StackPhase& P = a.ph[p];
       if (p > 0 && alive) alive = epi_all(etid != 0 || wait_phase(a, p - 1, (unsigned)G, abort_flag));
@@ -585,32 +621,26 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
         run_units(ub0, ub1);
       } else if (alive && P.kind == kPhaseAttn) {
         const AttnArgs& at = P.at;
-        const AttnItems items{at};
-        const int n = items.count();
-        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCKI) + 1;
-        const int i0 = (int)((long long)c * n / G), i1 = (int)((long long)(c + 1) * n / G);
-        attn::UmItem cur{}, nxt{};
-        if (i0 < i1) {
-          items.item(i0, cur.chunk, cur.kvh, cur.rt, cur.z);
+        attn::UmItem cur = plan.first, nxt{};
+        if (plan.i0 < plan.i1) {
           // the tiles alias the activation ring and the epilogue tile: fence this
           // thread's generic writes there before the copies overwrite them
           attn::fence_proxy_async_smem();
           EpilogueSync{}();
-          if (etid == 0) attn::um_issue<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, ust);
+          if (etid == 0) attn::um_issue<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, plan.n0, ust);
         }
-        for (int i = i0; i < i1 && alive; ++i) {
-          const bool has_next = i + 1 < i1;
-          if (has_next) items.item(i + 1, nxt.chunk, nxt.kvh, nxt.rt, nxt.z);
-          alive = attn::attn_item_um<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, has_next, nxt, slots, ust, etid, col,
-                                         abort_flag, EpilogueSync{});
+        for (int i = plan.i0; i < plan.i1 && alive; ++i) {
+          const bool has_next = i + 1 < plan.i1;
+          if (has_next) AttnItems(at, sgroups, G).item(i + 1, nxt.chunk, nxt.kvh, nxt.rt, nxt.z);
+          alive = attn::attn_item_um<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, has_next, nxt, plan.n0, plan.slots, ust,
+                                         etid, col, abort_flag, EpilogueSync{});
           cur = nxt;
         }
       } else if (alive && P.kind == kPhaseMerge) {
-        const AttnArgs& at = P.at;
-        const int n = at.M * at.Hq;
-        const int slots = attn::n_prefix_chunks(at.max_prefix, kAttnCKI) + 1;
-        const int w0 = (int)((long long)c * n / G), w1 = (int)((long long)(c + 1) * n / G);
-        for (int w = w0 + ew; w < w1; w += 4) attn::attn_merge_warp<HD, kAttnCKI>(at, w, lane, slots);
+        // the attention items' staging region is free (their phase is complete)
+        alive = attn::um_merge_staged<HD>(P.at, sgroups, plan.n0, plan.w0, plan.w1, plan.slots, xring,
+                                          (uint32_t)attn::um_smem_bytes<HD>(), at_kv, &ust.kv_par, etid,
+                                          abort_flag, EpilogueSync{});
       }
       // phase done: every epilogue thread's writes happen before the release
       EpilogueSync{}();
@@ -657,7 +687,7 @@ Layout layout(int MT, bool has_lo, int hd) {
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
   const size_t wslot = kWBytes;
   const size_t attn = hd == 128 ? attn::um_smem_bytes<128>() : attn::um_smem_bytes<64>();
-  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 7) * 8 + 16 + 1024;
+  const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 7) * 8 + 16 + kMaxGroups * sizeof(Group) + 1024;
   for (int s = kMaxW; s >= 2; --s) {
     const size_t alias = (size_t)s * xbytes + kTileBytes;
     const size_t pad = alias >= attn ? 0 : (attn - alias + 15) / 16 * 16;
@@ -692,8 +722,8 @@ size_t stack_scratch_bytes(int M, int max_phases, int max_counters) {
          (size_t)kMaxCtas * 2 * round_mt(M) * kTileN * 4;  // [CTA][first/last split tile][rows][128]
 }
 
-size_t stack_attention_part_bytes(int M, int Hq, int hd, int max_prefix) {
-  const size_t slots = (size_t)attn::n_prefix_chunks(max_prefix, kAttnCKI) + 1;
+size_t stack_attention_part_bytes(int M, int Hq, int Hkv, int hd, int max_prefix) {
+  const size_t slots = (size_t)attn::um_part_slots(max_prefix, Hkv, kMaxCtas);
   return (size_t)M * Hq * slots * (hd + 2) * sizeof(float);
 }
 
@@ -739,6 +769,7 @@ void StackProgramBuilder::attention(const AttnArgs& a) {
     ok = false;
     return;
   }
+  if (first_attn < 0) first_attn = (int)phases.size();
   phases.push_back(ph);
   ph.kind = kPhaseMerge;
   phases.push_back(ph);
@@ -746,9 +777,10 @@ void StackProgramBuilder::attention(const AttnArgs& a) {
 
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
                       void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
-                      float* y_last, cudaStream_t s) {
+                      float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s) {
   if (!stack_supported(M, hd) || n_phases <= 0 || !scratch || n_phases > max_phases || n_counters > max_counters)
     return cudaErrorInvalidValue;
+  if (n_groups < 0 || n_groups > kMaxGroups || (n_groups > 0 && !groups)) return cudaErrorInvalidValue;
   const int MT = round_mt(M);
   const Layout l = layout(MT, has_lo, hd);
   if (l.sw < 2) return cudaErrorInvalidValue;
@@ -776,6 +808,9 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.status = status;
   a.trace = trace;
   a.y_last = y_last;
+  a.groups = groups;
+  a.n_groups = n_groups;
+  a.first_attn = first_attn < n_phases ? first_attn : -1;
   auto kernel = hd == 128 ? stack_tc_kernel<128> : stack_tc_kernel<64>;
   if (!raise_smem_limit(reinterpret_cast<const void*>(kernel), kSmemBudget)) return cudaErrorInvalidValue;
   const int G = num_sms();
@@ -856,7 +891,7 @@ eagle_status eagle_op_gemm_persistent(int32_t M, int32_t N, int32_t K, int32_t n
       cudaSuccess)
     return EAGLE_ERR_CUDA;
   cudaError_t err = stack_run(d_prog, n_phases, M, x_lo != nullptr, 128, b.n_counters, p, n_phases, b.n_counters,
-                              nullptr, nullptr, nullptr, s);
+                              nullptr, nullptr, nullptr, nullptr, 0, -1, s);
   if (err == cudaSuccess && k > 0)
     err = topk_merge(lm.rec_val, lm.rec_idx, lm.rec_max, lm.rec_sum, (N + kTileN - 1) / kTileN, M, k, idx, val, lse,
                      s);
