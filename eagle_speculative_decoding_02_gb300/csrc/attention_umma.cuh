@@ -392,14 +392,13 @@ __device__ bool um_merge_staged(const AttnArgs& a, const Group* groups, int n0, 
   for (int s0 = 0; s0 < nmax; s0 += sb) {
     const int ns = min(sb, nmax - s0);
     float2* mls = reinterpret_cast<float2*>(stage + (size_t)ns * NB * nw * 128);  // [ns][nw]
-    if (tid == 0) {
-      // the partials were written by other SMs' generic stores earlier in the launch
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      mbar_expect_tx(bar, (uint32_t)ns * NB * nw * 128);
-      for (int s = 0; s < ns; ++s)
-        for (int b = 0; b < NB; ++b)
-          bulk_load(stage + ((size_t)s * NB + b) * nw * 128, pl.o(s0 + s, w0, b), (uint32_t)nw * 128, bar);
-    }
+    // thread 0 announces the bytes, then the copies are issued by as many
+    // threads (a transaction count may run ahead of its announcement)
+    if (tid == 0) mbar_expect_tx(bar, (uint32_t)ns * NB * nw * 128);
+    // the partials were written by other SMs' generic stores earlier in the launch
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    for (int i = tid; i < ns * NB; i += 128)
+      bulk_load(stage + (size_t)i * nw * 128, pl.o(s0 + i / NB, w0, i % NB), (uint32_t)nw * 128, bar);
     for (int i = tid; i < ns * nw; i += 128) {
       const int s = i / nw, t = i - s * nw;
       mls[i] = __ldcg(reinterpret_cast<const float2*>(pl.ml(s0 + s, w0 + t)));
@@ -423,22 +422,36 @@ __device__ bool um_merge_staged(const AttnArgs& a, const Group* groups, int n0, 
         L = run[(size_t)t * (HD + 2) + HD + 1];
       }
       const int se = min(s0 + ns, nck);
-      // (a plain loop: unrolling the parts, for more loads in flight, measured
-      // slower - this code runs once per layer, one warp per scheduler)
-      float Mb = M;
-      for (int s = s0; s < se; ++s) Mb = fmaxf(Mb, mls[(s - s0) * nw + t].x);
-      if (Mb != -INFINITY) {
-        const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      // kJ parts at a time with no branch: every load reads a valid slot (the
+      // index is clamped) and parts past se weigh zero, so all the loads of a
+      // batch are independent and issue together (one part after another would
+      // be a chain of dependent loads and branches on one warp per scheduler)
+      constexpr int kJ = 8;
+      for (int sj = s0; sj < se; sj += kJ) {
+        float mm[kJ], ll[kJ], ov[kJ][NB];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+          const int sl = min(sj + j, se - 1) - s0;
+          const float2 ml = mls[sl * nw + t];
+          mm[j] = sj + j < se ? ml.x : -INFINITY;
+          ll[j] = ml.y;
+#pragma unroll
+          for (int i = 0; i < NB; ++i) ov[j][i] = os[(((size_t)sl * NB + i) * nw + t) * 32 + lane];
+        }
+        float Mb = M;
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) Mb = fmaxf(Mb, mm[j]);
+        const float Ms = Mb == -INFINITY ? 0.f : Mb;  // (every weight is 0 then)
+        const float r = M == -INFINITY ? 0.f : exp2f(M - Ms);
         L *= r;
 #pragma unroll
         for (int i = 0; i < NB; ++i) acc[i] *= r;
-        for (int s = s0; s < se; ++s) {
-          const float2 ml = mls[(s - s0) * nw + t];
-          if (ml.x == -INFINITY) continue;
-          const float wgt = exp2f(ml.x - Mb);
-          L += wgt * ml.y;
 #pragma unroll
-          for (int i = 0; i < NB; ++i) acc[i] += wgt * os[(((size_t)(s - s0) * NB + i) * nw + t) * 32 + lane];
+        for (int j = 0; j < kJ; ++j) {
+          const float wgt = exp2f(mm[j] - Ms);  // exp2(-inf) = 0 for masked parts
+          L += wgt * ll[j];
+#pragma unroll
+          for (int i = 0; i < NB; ++i) acc[i] += wgt * ov[j][i];
         }
         M = Mb;
       }
