@@ -168,3 +168,40 @@ def test_70b_full_lossless(cuda):
     _lossless(eng, S.prompts(w), w.max_new)
     del eng
     torch.cuda.empty_cache()
+
+
+def test_8b_full_depth_eagle2_against_oracle(cuda):
+    """The 32-layer 8B-shaped model with its EAGLE-2 tree against the oracle at full depth (64-token prompt,
+    6 steps): the draft trees (identical, or parted only at a flagged near-tie with every node's draft
+    log-probability within 0.05 of the oracle's on the GPU's tree), the verify logits (max-abs and cosine),
+    the greedy tokens (equal except at flagged near-ties) and the accepted lengths."""
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    from tests.test_gpu_draft import _gpu_tree, check_draft
+    w = dataclasses.replace(FX.WORKLOADS["8b_eagle2"], prompt_len=64, max_new=64)
+    cap = FX.kv_capacity(w)
+    m = OM.build_model(FX.LLAMA3_8B, cap)
+    prompt = FX.prompts(FX.LLAMA3_8B, 1, w.prompt_len)
+    eng = S.make_engine(w)
+    root = eng.prefill(torch.from_numpy(prompt).to(cuda)).cpu().numpy()
+    st = OD.prefill(m, prompt[0], cap)
+    assert root[0] == st.root
+    flagged, worst, same = 0, 0.0, 0
+    for step in range(6):
+        gtree = eng.draft_tree()
+        gt = _gpu_tree(gtree)
+        s, fl = check_draft(m, st, w, gt, 0.05)
+        same += s
+        am, lg = eng.verify(gtree, logits=True)
+        oam, ofeats, ologits = OD.verify(m, st, gt)
+        got = lg[0, : gt.n + 1].cpu().numpy()
+        err = float(np.abs(got - ologits).max())
+        cos = float((got.ravel() @ ologits.ravel()) / (np.linalg.norm(got) * np.linalg.norm(ologits)))
+        worst = max(worst, err)
+        assert err < 0.05 and cos >= 0.999, (step, err, cos)
+        g_am = am[0, : gt.n + 1].cpu().numpy()
+        assert not ((g_am != oam) & (_margins(ologits) >= 0.1)).any(), step
+        flagged += int((g_am != oam).sum())
+        a, _ = eng.accept_commit()
+        assert int(a[0]) == OD.accept_commit(st, gt, g_am, ofeats)
+    print(f"full depth: {same}/6 draft trees identical, max |logit err| {worst:.4f}, {flagged} flagged near-ties, "
+          f"committed {st.out[:12]}...")
