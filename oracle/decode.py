@@ -49,8 +49,9 @@ import numpy as np
 
 import fixtures as FX
 
-from .core import F32, argmax, topk
+from .core import F32, topk
 from .model import KVCache, Model, causal_visible, draft_logp, draft_rows, logits_of, target_rows
+from .sampling import GREEDY, Sampler
 from .tree import Pool, Tree, accept, rerank, select_frontier, static_layout, static_paths
 
 
@@ -65,21 +66,23 @@ class SeqState:
     dkv: KVCache
     accepted: list[int] = dataclasses.field(default_factory=list)
     n_flagged: int = 0
+    sampler: Sampler = GREEDY    # the target's choice: argmax (T = 0) or its seeded sample
+    seq: int = 0                 # sequence index (keys the sampler's noise)
 
 
-def prefill(m: Model, prompt: np.ndarray, cap: int) -> SeqState:
-    """Target over the prompt (causal), first new token, and the head over prompt rows 0..P-2."""
+def prefill(m: Model, prompt: np.ndarray, cap: int, sampler: Sampler = GREEDY, seq: int = 0) -> SeqState:
+    """Target over the prompt (causal), first new token (position P), and the head over prompt rows 0..P-2."""
     s = m.shape
     P = len(prompt)
     kv = KVCache(s.n_layers, cap, s.n_kv_heads, s.head_dim)
     dkv = KVCache(1, cap, s.n_kv_heads, s.head_dim)
     pos = np.arange(P)
     feats = target_rows(m, kv, prompt, pos, pos, causal_visible(0, P))
-    root = int(argmax(logits_of(m, feats[-1:]))[0])
+    root = int(sampler.choose(logits_of(m, feats[-1:]), seq, np.array([P]))[0])
     if P > 1:
         draft_rows(m, dkv, feats[:P - 1], prompt[1:], pos[:P - 1], pos[:P - 1], causal_visible(0, P - 1))
     return SeqState(L=P, root=root, pend_feats=feats[P - 1:], pend_tokens=np.array([root], np.int32),
-                    out=[root], kv=kv, dkv=dkv)
+                    out=[root], kv=kv, dkv=dkv, sampler=sampler, seq=seq)
 
 
 def draft_catchup(m: Model, st: SeqState) -> tuple[np.ndarray, np.ndarray]:
@@ -223,7 +226,8 @@ def draft_logp_on_tree(m: Model, st: SeqState, tree: Tree) -> np.ndarray:
 
 
 def verify(m: Model, st: SeqState, tree: Tree):
-    """Target forward over every tree row in one pass; returns (argmax [N+1], features, logits)."""
+    """Target forward over every tree row in one pass; returns (the target's choice after each row [N+1]:
+    argmax, or at T > 0 its sample of the token at position L + depth + 1; features; logits)."""
     L = st.L
     slots = L + np.arange(tree.n + 1)
     pos = L + tree.depth
@@ -231,7 +235,7 @@ def verify(m: Model, st: SeqState, tree: Tree):
     vis = [np.concatenate([prefix, L + np.array(tree.path(j))]) for j in range(tree.n + 1)]
     feats = target_rows(m, st.kv, tree.tokens, pos, slots, vis)
     logits = logits_of(m, feats)
-    return argmax(logits), feats, logits
+    return st.sampler.choose(logits, st.seq, pos + 1), feats, logits
 
 
 def accept_commit(st: SeqState, tree: Tree, amax: np.ndarray, feats: np.ndarray) -> int:
@@ -258,9 +262,9 @@ def draft_tree(m: Model, st: SeqState, w: FX.Workload) -> Tree:
 
 
 def speculative_generate(m: Model, prompt: np.ndarray, w: FX.Workload, max_new: int | None = None,
-                         cap: int | None = None) -> SeqState:
+                         cap: int | None = None, sampler: Sampler = GREEDY, seq: int = 0) -> SeqState:
     max_new = w.max_new if max_new is None else max_new
-    st = prefill(m, prompt, cap or FX.kv_capacity(w))
+    st = prefill(m, prompt, cap or FX.kv_capacity(w), sampler, seq)
     while len(st.out) < max_new:
         tree = draft_tree(m, st, w)
         amax, feats, _ = verify(m, st, tree)
@@ -269,18 +273,24 @@ def speculative_generate(m: Model, prompt: np.ndarray, w: FX.Workload, max_new: 
     return st
 
 
-def vanilla_greedy(m: Model, prompt: np.ndarray, max_new: int, cap: int) -> list[int]:
-    """One target forward per token, argmax each time."""
+def vanilla_decode(m: Model, prompt: np.ndarray, max_new: int, cap: int, sampler: Sampler = GREEDY,
+                   seq: int = 0) -> list[int]:
+    """One target forward per token, the target's choice each time (argmax, or its seeded sample)."""
     s = m.shape
     P = len(prompt)
     kv = KVCache(s.n_layers, cap, s.n_kv_heads, s.head_dim)
     pos = np.arange(P)
     feats = target_rows(m, kv, prompt, pos, pos, causal_visible(0, P))
-    x = int(argmax(logits_of(m, feats[-1:]))[0])
+    x = int(sampler.choose(logits_of(m, feats[-1:]), seq, np.array([P]))[0])
     out, L = [x], P
     while len(out) < max_new:
         f = target_rows(m, kv, np.array([x], np.int32), np.array([L]), np.array([L]), [np.arange(L + 1)])
-        x = int(argmax(logits_of(m, f))[0])
+        x = int(sampler.choose(logits_of(m, f), seq, np.array([L + 1]))[0])
         out.append(x)
         L += 1
     return out
+
+
+def vanilla_greedy(m: Model, prompt: np.ndarray, max_new: int, cap: int) -> list[int]:
+    """One target forward per token, argmax each time."""
+    return vanilla_decode(m, prompt, max_new, cap)
