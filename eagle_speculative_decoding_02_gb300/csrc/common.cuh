@@ -113,6 +113,14 @@ struct EpiParams {
   const float* gain = nullptr;
   // kEpiLmHead
   int topk = 1;
+  // sampling (inv_temp > 0): the top-k is taken of logit * inv_temp + Gumbel noise
+  // (sample_gumbel) of (seq, position + 1, token) of each row; samp_pos / samp_seq
+  // give a row's position and sequence, through samp_idx[row] when not NULL
+  float inv_temp = 0.f;
+  unsigned long long seed = 0;
+  const int* samp_pos = nullptr;
+  const int* samp_seq = nullptr;
+  const int* samp_idx = nullptr;
   float* rec_val = nullptr; // [ntiles][M][topk]
   int* rec_idx = nullptr;
   float* rec_max = nullptr; // [ntiles][M]
@@ -153,6 +161,25 @@ struct EpilogueSync {
 };
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.f + __expf(-x)); }
+
+// SplitMix64's output function (Steele, Lea & Flood, OOPSLA 2014).
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Gumbel noise of vocabulary entry v of the token at position pos of sequence
+// seq: -log(-log(u)), u from a counter of (seed, seq, pos, v) (the definition
+// in include/eagle.h). argmax over v of logit / T + noise samples softmax(logit / T).
+__device__ __forceinline__ float sample_gumbel(unsigned long long seed, int seq, int pos, int v) {
+  constexpr unsigned long long G = 0x9E3779B97F4A7C15ull;
+  const unsigned long long k1 = mix64(seed + (unsigned long long)(seq + 1) * G);
+  const unsigned long long k2 = mix64(k1 + (unsigned long long)(pos + 1) * G);
+  const unsigned long long z = mix64(k2 + (unsigned long long)(v + 1) * G);
+  const float u = ((float)(z >> 40) + 0.5f) * 5.9604644775390625e-08f;  // exact: (0, 1) on a 2^-24 grid
+  return -logf(-logf(u));
+}
 
 // Warp arg-max on (value desc, index asc).
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {

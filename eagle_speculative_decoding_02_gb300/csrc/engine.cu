@@ -56,6 +56,8 @@ struct Dims {
   int CL = 0;                       // prefill chunk length per sequence
   int M_tgt = 0, M_dft = 0, M_max = 0, M_lm = 0, n_groups_max = 0, ntV = 0, pool_cap = 0;
   bool bf16 = false;
+  float inv_temp = 0.f;             // 1 / temperature, 0 for greedy decoding
+  unsigned long long seed = 0;      // sampler seed
   // static topology (host)
   std::vector<int> s_parent, s_rank, s_depth, s_lrow, s_sidx, s_level_nodes, s_level_count;
   std::vector<uint64_t> s_smask, s_anc;
@@ -181,6 +183,9 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
   if (cfg.head_dim != 64 && cfg.head_dim != 128) { why = "head_dim must be 64 or 128"; return EAGLE_ERR_UNSUPPORTED; }
   if (cfg.n_heads % cfg.n_kv_heads) return bad("n_kv_heads must divide n_heads");
   if (!(cfg.rms_eps > 0.f) || !(cfg.rope_theta > 0.f)) return bad("rms_eps / rope_theta");
+  if (!(cfg.temperature >= 0.f) || !std::isfinite(cfg.temperature)) return bad("temperature must be finite, >= 0");
+  dm.inv_temp = cfg.temperature > 0.f ? 1.f / cfg.temperature : 0.f;
+  dm.seed = cfg.seed;
   dm.B = cfg.batch; dm.d = cfg.d; dm.Hq = cfg.n_heads; dm.Hkv = cfg.n_kv_heads; dm.hd = cfg.head_dim;
   dm.ffn = cfg.ffn; dm.V = cfg.vocab; dm.Lyr = cfg.n_layers; dm.cap = cfg.kv_cap; dm.P_max = cfg.max_prompt;
   dm.qd = dm.Hq * dm.hd; dm.kvd = dm.Hkv * dm.hd; dm.nqkv = dm.qd + 2 * dm.kvd;
@@ -482,14 +487,21 @@ struct Eng {
     return EAGLE_OK;
   }
 
-  // LM-head GEMM with per-tile top-k records (merged by lm_head_merge).
+  // LM-head GEMM with per-tile top-k records (merged by lm_head_merge). choose:
+  // the rows pick the target's next token (verify, prefill), so at T > 0 the
+  // records are of the Gumbel-perturbed logits (the sample); the rows' positions
+  // and sequences are in c->rows, through idx (row -> rows entry) when not NULL.
   template <typename Sink>
   static eagle_status lm_head_gemm(eagle_ctx* c, Sink& sink, const void* X, const bf16* X_lo, const float* ssq,
-                                   int M, int k, float* logits) {
+                                   int M, int k, float* logits, bool choose = false, const int* idx = nullptr) {
     const Dims& dm = c->dm;
     EpiParams e = epi(c, kEpiLmHead, M, dm.V);
     e.ssq_in = ssq; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.topk = k; e.y = logits;
     e.rec_val = c->rec_val; e.rec_idx = c->rec_idx; e.rec_max = c->rec_max; e.rec_sum = c->rec_sum;
+    if (choose && dm.inv_temp > 0.f) {
+      e.inv_temp = dm.inv_temp; e.seed = dm.seed;
+      e.samp_pos = c->rows.pos; e.samp_seq = c->rows.seq; e.samp_idx = idx;
+    }
     return sink.gemm(X, X_lo, c->lm_head, M, dm.V, dm.d, e);
   }
 
@@ -499,9 +511,10 @@ struct Eng {
   }
 
   static eagle_status lm_head(eagle_ctx* c, const void* X, const bf16* X_lo, const float* ssq, int M, int k,
-                              int* idx, float* val, float* lse, float* logits) {
+                              int* idx, float* val, float* lse, float* logits, bool choose = false,
+                              const int* rows_idx = nullptr) {
     Direct d{c};
-    EG_TRY(lm_head_gemm(c, d, X, X_lo, ssq, M, k, logits));
+    EG_TRY(lm_head_gemm(c, d, X, X_lo, ssq, M, k, logits, choose, rows_idx));
     return lm_head_merge(c, M, k, idx, val, lse);
   }
 
@@ -570,7 +583,7 @@ struct Eng {
       Record r{c, &b};
       if (p.kind == 0) {
         EG_TRY(target_layers(c, r, p.M, dm.B));
-        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c->hb_lo), c->ssq_b, p.M, 1, nullptr));
+        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c->hb_lo), c->ssq_b, p.M, 1, nullptr, true));
       } else {
         EG_TRY(draft_ops(c, r, p.M, dm.B, p.hbase, p.k));
       }
@@ -616,7 +629,8 @@ struct Eng {
         EG_CK(cudaMemcpyAsync(c->lm_src, src.data(), dm.B * sizeof(int), cudaMemcpyHostToDevice, c->stream));
         EG_CK(gather_rows<T>((const T*)c->hb, lo(c->hb_lo), c->ssq_b, M, c->lm_src, dm.B, dm.d, (T*)c->lm_hb,
                              lo(c->lm_hb_lo), c->lm_ssq, c->stream));
-        EG_TRY(lm_head(c, c->lm_hb, lo(c->lm_hb_lo), c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr));
+        EG_TRY(lm_head(c, c->lm_hb, lo(c->lm_hb_lo), c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr,
+                       true, c->lm_src));
         EG_CK(prefill_finish(c->st, c->root_idx, c->h_tgt, cl, P, root_out, c->stream));
         EG_CK(cudaStreamSynchronize(c->stream));  // src is a host temporary
       }
@@ -661,7 +675,7 @@ struct Eng {
       EG_TRY(lm_head_merge(c, M, 1, c->vargmax, nullptr, nullptr));
     } else {
       EG_TRY(target_stack(c, M, dm.B));
-      EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits));
+      EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits, true));
     }
     if (d_argmax)
       EG_CK(cudaMemcpyAsync(d_argmax, c->vargmax, (size_t)M * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));

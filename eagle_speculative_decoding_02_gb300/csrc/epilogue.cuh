@@ -54,6 +54,10 @@ __device__ inline void load_epi_rows(const EpiParams& p, int m0, int msub, EpiRo
   const int* const rpos = p.rows.pos;
   const int* const rslot = p.rows.slot;
   const int* const rseq = p.rows.seq;
+  const bool sampling = kind == kEpiLmHead && p.inv_temp > 0.f;
+  const int* const spos = p.samp_pos;
+  const int* const sseq = p.samp_seq;
+  const int* const sidx = p.samp_idx;
   for (int m = tid; m < msub; m += nthr) {
     float sc = 1.f;
     if (ssq_in) {
@@ -85,6 +89,10 @@ __device__ inline void load_epi_rows(const EpiParams& p, int m0, int msub, EpiRo
       r.pos[m] = rpos[m0 + m];
       r.slot[m] = rslot[m0 + m];
       r.seq[m] = rseq[m0 + m];
+    } else if (sampling) {  // the position of the token this row chooses, and its sequence
+      const int src = sidx ? sidx[m0 + m] : m0 + m;
+      r.pos[m] = spos[src] + 1;
+      r.seq[m] = sseq[src];
     }
   }
 }
@@ -116,6 +124,8 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
   float* const ssq_out = p.ssq_out;
   const float* const gain = p.gain;
   const int topk = p.topk;
+  const float inv_temp = p.inv_temp;
+  const unsigned long long seed = p.seed;
   float* const rec_val = p.rec_val;
   int* const rec_idx = p.rec_idx;
   float* const rec_max = p.rec_max;
@@ -244,6 +254,8 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
           idx[j] = n0 + c;
           v[j] = c < ncols ? tile[m * ldt + c] * rscale[m] : -INFINITY;
           if (y && c < ncols) y[(size_t)(m0 + m) * N + n0 + c] = v[j];
+          // sampling: the records (and so the merged top-1) are of the perturbed values
+          if (inv_temp > 0.f && c < ncols) v[j] = v[j] * inv_temp + sample_gumbel(seed, rseq[m], rpos[m], n0 + c);
         }
         float mx = warp_max(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
         float se = 0.f;

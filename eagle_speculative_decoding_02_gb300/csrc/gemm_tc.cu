@@ -413,7 +413,12 @@ struct Plan {
 
 Plan plan(int M, int N, int K, int nsm, bool has_lo) {
   Plan p{};
-  p.MT = M > 256 ? 256 : ((M + 31) / 32) * 32;
+  // Token rows per tile: up to 256, but 128 with hi/lo activation pairs, so that
+  // one MMA of N = 2 MT <= 256 covers both halves and a stage (weight box plus
+  // two activation boxes, 48 KB) leaves room for four or more stages (a 256-row
+  // pair tile took 80 KB stages, two of them, and measured 3-7x slower at 244 rows).
+  const int mt_max = has_lo ? 128 : 256;
+  p.MT = M > mt_max ? mt_max : ((M + 31) / 32) * 32;
   if (p.MT < 32) p.MT = 32;
   p.m_chunks = (M + p.MT - 1) / p.MT;
   p.n_tiles = N / kTileN;
@@ -440,13 +445,16 @@ Plan plan(int M, int N, int K, int nsm, bool has_lo) {
 }  // namespace
 
 size_t gemm_tc_scratch_bytes(int M, int N, int K) {
-  // enough for any M' <= M on up to kNsmSizing SMs
+  // enough for any M' <= M on up to kNsmSizing SMs, with or without hi/lo pairs
   size_t best = kCounterBytes;
-  const int chunks = (M + 255) / 256;
-  for (int mc = 1; mc <= chunks; ++mc) {
-    const int Mp = mc == 1 ? std::min(M, 256) : mc * 256;
-    const Plan p = plan(Mp, N, K, kNsmSizing, true);
-    best = std::max(best, p.counters_bytes + p.partial_bytes);
+  for (int lo = 0; lo < 2; ++lo) {
+    const int mt = lo ? 128 : 256;
+    const int chunks = (M + mt - 1) / mt;
+    for (int mc = 1; mc <= chunks; ++mc) {
+      const int Mp = mc == 1 ? std::min(M, mt) : mc * mt;
+      const Plan p = plan(Mp, N, K, kNsmSizing, lo != 0);
+      best = std::max(best, p.counters_bytes + p.partial_bytes);
+    }
   }
   return best;
 }

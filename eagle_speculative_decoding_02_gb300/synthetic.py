@@ -25,7 +25,8 @@ def device_weights(m: FX.ModelShape, device="cuda") -> ModelWeights:
 
 def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: int | None = None,
                 max_new: int | None = None, prompt_len: int | None = None, kv_cap: int | None = None,
-                tree: str | None = None, n_nodes: int | None = None, device="cuda") -> EagleEngine:
+                tree: str | None = None, n_nodes: int | None = None, temperature: float = 0.0, seed: int = 0,
+                device="cuda") -> EagleEngine:
     m = w.model
     if weights is None:
         weights = device_weights(m, device)
@@ -37,7 +38,8 @@ def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: i
     cap = kv_cap or FX.kv_capacity(wl)
     kw = dict(n_layers=m.n_layers, d=m.d, n_heads=m.n_heads, n_kv_heads=m.n_kv_heads, head_dim=m.head_dim,
               ffn=m.ffn, vocab=m.vocab, rope_theta=m.rope_theta, rms_eps=m.rms_eps, bf16=m.bf16, batch=batch,
-              kv_cap=cap, max_prompt=prompt_len, max_new=max_new, weights=weights, device=device)
+              kv_cap=cap, max_prompt=prompt_len, max_new=max_new, weights=weights, device=device,
+              temperature=temperature, seed=seed)
     if tree == "static":
         parent, rank = named(w.static_tree)
         return EagleEngine(tree_mode=L.TREE_STATIC, n_nodes=len(parent) - 1, static_parent=parent,

@@ -101,6 +101,18 @@ typedef struct {
   int32_t top_k;
   int32_t depth;
   float tau;
+  /* The target's choice of each next token ([SDE] "Technical insight": a
+   * drafted token is accepted when it matches the target's argmax, or its
+   * sample): temperature 0 = greedy argmax; temperature T > 0 = a sample of
+   * softmax(logits / T), drawn by the Gumbel-max rule with noise
+   *   g = -log(-log(u)),  u = ((z >> 40) + 0.5) 2^-24,
+   *   z = mix64(mix64(mix64(seed + (b+1) G) + (p+1) G) + (v+1) G),
+   * for sequence b, token position p, vocabulary entry v (mix64 = SplitMix64's
+   * output function, G = 0x9E3779B97F4A7C15). The noise depends on the position
+   * only, so speculative sampling commits exactly the tokens vanilla sampling
+   * with the same seed commits. The draft tree is built by draft top-k either way. */
+  float temperature;
+  uint64_t seed;
 } eagle_config;
 
 /* Device pointers of one decoder layer. Matrices are row-major [out, in]
