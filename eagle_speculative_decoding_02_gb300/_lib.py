@@ -27,7 +27,7 @@ class EagleConfig(C.Structure):
                 ("max_prompt", C.c_int32), ("max_new", C.c_int32), ("tree_mode", C.c_int32),
                 ("n_nodes", C.c_int32), ("static_parent", C.POINTER(C.c_int32)),
                 ("static_rank", C.POINTER(C.c_int32)), ("top_k", C.c_int32), ("depth", C.c_int32),
-                ("tau", C.c_float), ("temperature", C.c_float), ("seed", C.c_uint64)]
+                ("tau", C.c_float), ("temperature", C.c_float), ("seed", C.c_uint64), ("n_nodes_min", C.c_int32)]
 
 
 class EagleLayerWeights(C.Structure):

@@ -246,6 +246,7 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
         dm.s_anc[2 * j + a / 64] |= 1ull << (a % 64);
         if (a == 0) break;
       }
+    if (cfg.n_nodes_min != 0) return bad("n_nodes_min applies to dynamic trees only");
   } else if (cfg.tree_mode == EAGLE_TREE_DYNAMIC) {
     if (cfg.top_k < 1 || cfg.top_k > 11) return bad("top_k must be in 1..11");
     if (cfg.depth < 1 || cfg.depth > kMaxDepth) return bad("depth must be in 1..8");
@@ -257,6 +258,7 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
     dm.pool_cap = dm.k + (dm.D - 1) * dm.k * dm.k;
     if (dm.pool_cap > 1024) return bad("pool larger than 1024");
     if (dm.pool_cap < dm.n_nodes) return bad("n_nodes exceeds the candidate pool");
+    if (cfg.n_nodes_min < 0 || cfg.n_nodes_min > cfg.n_nodes) return bad("n_nodes_min must be in 0..n_nodes");
   } else {
     return bad("tree_mode");
   }
@@ -659,7 +661,9 @@ struct Eng {
       if (next.per_seq > 0)
         EG_TRY(draft_forward(c, c->h_dft, dm.B * next.per_seq, dm.B, next.base, dm.k));
     }
-    if (dm.mode == EAGLE_TREE_DYNAMIC) EG_CK(eagle2_final(c->st, c->pool, dm.n_nodes, c->tree, c->stream));
+    if (dm.mode == EAGLE_TREE_DYNAMIC)
+      EG_CK(eagle2_final(c->st, c->pool, dm.n_nodes, c->cfg.n_nodes_min, (float)std::log((double)c->cfg.tau), c->tree,
+                         c->stream));
     return EAGLE_OK;
   }
 

@@ -135,13 +135,24 @@ __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* gr
     rows.mask[2 * m] = tree.anc[2 * m];
     rows.mask[2 * m + 1] = tree.anc[2 * m + 1];
   }
+  // the attention group holds the tree's real rows: a drafted tree of fewer
+  // nodes than rows ends in padding rows (token -1), which no row attends to
+  // and accept never takes
+  __shared__ int s_real;
+  if (threadIdx.x == 0) s_real = NR;
+  __syncthreads();
+  for (int j = 1 + threadIdx.x; j < NR; j += blockDim.x)
+    if (tree.tokens[b * NR + j] < 0) atomicMin(&s_real, j);
+  __syncthreads();
+  for (int j = s_real + threadIdx.x; j < NR; j += blockDim.x)  // padding rows come last
+    if (tree.tokens[b * NR + j] >= 0) set_status(st.status, kStInvalid);
   if (threadIdx.x == 0) {
     Group g;
     g.seq = b;
     g.row0 = b * NR;
-    g.nrows = NR;
+    g.nrows = s_real;
     g.prefix = fits ? L : 0;
-    g.block_len = fits ? NR : 0;
+    g.block_len = fits ? s_real : 0;
     groups[b] = g;
   }
 }
@@ -395,7 +406,12 @@ __global__ void __launch_bounds__(256) eagle2_level_kernel(State st, Pool pool, 
   }
 }
 
-__global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, int n_nodes, TreeOut tree) {
+// n_min > 0: adaptive node count, the candidates whose cumulative confidence
+// reaches tau (score >= ln_tau), clamped to [n_min, n_nodes] (reading of the
+// 40-120 adaptive count of "EAGLE (LLM decoding)", "EAGLE vs EAGLE-2"); each
+// sequence gets its own count, the remaining rows are padding.
+__global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, int n_nodes, int n_min, float ln_tau,
+                                                           TreeOut tree) {
   pdl_wait();
   pdl_trigger();
   __shared__ unsigned long long key[kPoolSort];
@@ -417,7 +433,16 @@ __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, 
     tpos[i] = 0;
   }
   bitonic_sort(key, val, n2);
-  const int n = min(n_nodes, cnt);
+  __shared__ int s_conf;
+  if (n_min > 0) {
+    if (tid == 0) s_conf = 0;
+    __syncthreads();
+    int mine = 0;
+    for (int i = tid; i < cnt; i += blockDim.x) mine += pool.score[pb + i] >= ln_tau;
+    if (mine) atomicAdd(&s_conf, mine);
+    __syncthreads();
+  }
+  const int n = n_min > 0 ? min(min(max(s_conf, n_min), n_nodes), cnt) : min(n_nodes, cnt);
   // re-sort the selected nodes by creation id (depth first): BFS order
   __syncthreads();
   int n3 = 1;
@@ -638,8 +663,8 @@ cudaError_t eagle2_level(State st, Pool pool, int t, int depth, int k, float ln_
                                            next, rows, groups, S);
 }
 
-cudaError_t eagle2_final(State st, Pool pool, int n_nodes, TreeOut tree, cudaStream_t s) {
-  return launch_pdl(eagle2_final_kernel, dim3(st.B), dim3(256), 0, s, st, pool, n_nodes, tree);
+cudaError_t eagle2_final(State st, Pool pool, int n_nodes, int n_min, float ln_tau, TreeOut tree, cudaStream_t s) {
+  return launch_pdl(eagle2_final_kernel, dim3(st.B), dim3(256), 0, s, st, pool, n_nodes, n_min, ln_tau, tree);
 }
 
 cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, int* acc_out,

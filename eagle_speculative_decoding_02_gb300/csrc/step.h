@@ -91,8 +91,9 @@ cudaError_t static_level(State st, StaticTopo topo, int t, const int* topk_idx, 
 cudaError_t eagle2_level(State st, Pool pool, int t, int depth, int k, float ln_tau, const int* topk_idx,
                          const float* topk_val, const float* lse, Level catchup, Level prev, Level next,
                          Rows rows, Group* groups, int S, cudaStream_t s);
-// Top-N of the pool in BFS order -> tree.
-cudaError_t eagle2_final(State st, Pool pool, int n_nodes, TreeOut tree, cudaStream_t s);
+// Top-N of the pool in BFS order -> tree (N = n_nodes, or with n_min > 0 the
+// per-sequence adaptive count between n_min and n_nodes; padding rows after).
+cudaError_t eagle2_final(State st, Pool pool, int n_nodes, int n_min, float ln_tau, TreeOut tree, cudaStream_t s);
 
 // Greedy accept over the verified tree; commit tokens and features, advance L.
 // A path longer than D1 - 1 nodes (only a caller-built tree can hold one) is

@@ -80,8 +80,8 @@ class EagleEngine:
 
     def __init__(self, *, n_layers, d, n_heads, n_kv_heads, head_dim, ffn, vocab, rope_theta, rms_eps, bf16,
                  batch, kv_cap, max_prompt, max_new, tree_mode, n_nodes, static_parent=None, static_rank=None,
-                 top_k=10, depth=6, tau=0.3, temperature=0.0, seed=0, weights: ModelWeights, device="cuda",
-                 stream=None):
+                 top_k=10, depth=6, tau=0.3, temperature=0.0, seed=0, n_nodes_min=0, weights: ModelWeights,
+                 device="cuda", stream=None):
         self.lib = L.load()
         self.device = torch.device(device)
         self.batch, self.max_new, self.vocab = batch, max_new, vocab
@@ -96,7 +96,7 @@ class EagleEngine:
                                  L.DTYPE_BF16 if bf16 else L.DTYPE_F32, batch, kv_cap, max_prompt, max_new,
                                  tree_mode, n_nodes, C.cast(sp, C.POINTER(C.c_int32)) if sp else None,
                                  C.cast(sr, C.POINTER(C.c_int32)) if sr else None, top_k, depth, tau,
-                                 float(temperature), int(seed))
+                                 float(temperature), int(seed), int(n_nodes_min))
         nbytes = C.c_size_t(0)
         L.check("eagle_workspace_size", self.lib.eagle_workspace_size(C.byref(self.cfg), C.byref(nbytes)))
         self.workspace = torch.empty(int(nbytes.value), dtype=torch.uint8, device=self.device)

@@ -45,7 +45,7 @@ def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: i
         return EagleEngine(tree_mode=L.TREE_STATIC, n_nodes=len(parent) - 1, static_parent=parent,
                            static_rank=rank, **kw)
     return EagleEngine(tree_mode=L.TREE_DYNAMIC, n_nodes=n_nodes or w.n_nodes, top_k=w.top_k, depth=w.depth,
-                       tau=w.tau, **kw)
+                       tau=w.tau, n_nodes_min=w.n_nodes_min, **kw)
 
 
 def prompts(w: FX.Workload, batch: int | None = None, length: int | None = None, device="cuda") -> torch.Tensor:

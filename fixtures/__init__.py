@@ -211,6 +211,7 @@ class Workload:
     depth: int = 6
     n_nodes: int = 60          # verified draft nodes, root excluded
     n_nodes_max: int = 120
+    n_nodes_min: int = 0       # > 0: adaptive EAGLE-2 node count between n_nodes_min and n_nodes
     tau: float = 0.3
     kv_cap: int = 0            # 0: prompt + max_new + margins
 

@@ -113,6 +113,12 @@ typedef struct {
    * with the same seed commits. The draft tree is built by draft top-k either way. */
   float temperature;
   uint64_t seed;
+  /* EAGLE_TREE_DYNAMIC, adaptive node count ([LPD] "EAGLE vs EAGLE-2": 40-120
+   * verified nodes instead of a fixed 60): when > 0, each sequence verifies the
+   * pool candidates whose cumulative confidence reaches tau, at least n_nodes_min
+   * and at most n_nodes of them (its tree's remaining rows are padding rows with
+   * token -1); 0 = every sequence verifies n_nodes. */
+  int32_t n_nodes_min;
 } eagle_config;
 
 /* Device pointers of one decoder layer. Matrices are row-major [out, in]
@@ -141,8 +147,8 @@ typedef struct {
  * A tree passed to eagle_verify must be consistent: parent[0] = -1, depth[0] = 0,
  * anc[0] = {1, 0}; for j > 0, 0 <= parent[j] < j, depth[j] = depth[parent[j]] + 1,
  * anc[j] = anc[parent[j]] | bit j; and siblings carry distinct tokens (rows
- * with token -1 are padding, never accepted), so that the greedy accepted path
- * is unique. Trees deeper than the configured tree depth may be verified (for
+ * with token -1 are padding, never accepted, and come after every real row),
+ * so that the greedy accepted path is unique. Trees deeper than the configured tree depth may be verified (for
  * example a chain carrying a known continuation, to read its logits), but
  * eagle_accept_commit refuses an accepted path longer than that depth. */
 typedef struct {

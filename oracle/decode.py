@@ -52,7 +52,7 @@ import fixtures as FX
 from .core import F32, topk
 from .model import KVCache, Model, causal_visible, draft_logp, draft_rows, logits_of, target_rows
 from .sampling import GREEDY, Sampler
-from .tree import Pool, Tree, accept, rerank, select_frontier, static_layout, static_paths
+from .tree import Pool, Tree, accept, adaptive_count, rerank, select_frontier, static_layout, static_paths
 
 
 @dataclasses.dataclass
@@ -156,8 +156,10 @@ def _ancestors(parent: np.ndarray, j: int) -> list[int]:
     return a[::-1]
 
 
-def draft_dynamic(m: Model, st: SeqState, k: int, depth: int, n_nodes: int, tau: float) -> tuple[Tree, Pool]:
-    """EAGLE-2 dynamic draft tree: expand the top-k by cumulative confidence, prune below tau, rerank top-N."""
+def draft_dynamic(m: Model, st: SeqState, k: int, depth: int, n_nodes: int, tau: float,
+                  n_min: int = 0) -> tuple[Tree, Pool]:
+    """EAGLE-2 dynamic draft tree: expand the top-k by cumulative confidence, prune below tau, rerank top-N
+    (N = n_nodes, or with n_min > 0 the adaptive count of tree.adaptive_count between n_min and n_nodes)."""
     ln_tau = np.float32(np.log(tau))
     fhat_root, logp_root = draft_catchup(m, st)
     pool = Pool()
@@ -188,7 +190,8 @@ def draft_dynamic(m: Model, st: SeqState, k: int, depth: int, n_nodes: int, tau:
             cidx, cval = topk(lp[fr], k)
             for r in range(k):
                 pool.add(np.float32(pool.score[i] + cval[r]), cidx[r], i, t, (t, fr, r))
-    tree, _ = rerank(pool, n_nodes, st.root)
+    n = adaptive_count(pool, n_min, n_nodes, ln_tau) if n_min > 0 else n_nodes
+    tree, _ = rerank(pool, n, st.root)
     return tree, pool
 
 
@@ -258,7 +261,7 @@ def accept_commit(st: SeqState, tree: Tree, amax: np.ndarray, feats: np.ndarray)
 def draft_tree(m: Model, st: SeqState, w: FX.Workload) -> Tree:
     if w.tree == "static":
         return draft_static(m, st, w.static_tree)
-    return draft_dynamic(m, st, w.top_k, w.depth, w.n_nodes, w.tau)[0]
+    return draft_dynamic(m, st, w.top_k, w.depth, w.n_nodes, w.tau, w.n_nodes_min)[0]
 
 
 def speculative_generate(m: Model, prompt: np.ndarray, w: FX.Workload, max_new: int | None = None,

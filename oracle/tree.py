@@ -20,6 +20,9 @@ node gets its top-k children. The verified tree is the top-N of the whole pool
 (pruned candidates stay eligible as leaves). Sort key everywhere: score desc,
 then creation id asc, where creation id = (depth, parent's frontier rank,
 child rank); parents precede children, so the top-N is ancestor-closed.
+Adaptive node count (same page: EAGLE-2 verifies 40-120 nodes instead of a
+fixed 60; the page gives no rule, read here as): N = the number of pool
+candidates whose cumulative confidence reaches tau, clamped to [N_min, N_max].
 
 Greedy acceptance ("Speculative Decoding with EAGLE", section "Deep dive":
 the target verifies all candidates in one pass and accepts the longest correct
@@ -130,6 +133,13 @@ def select_frontier(pool: Pool, depth: int, k: int, ln_tau: np.float32) -> list[
     if passing:
         return pool.order(passing)[:k]
     return pool.order(at_depth)[:1]
+
+
+def adaptive_count(pool: Pool, n_min: int, n_max: int, ln_tau: np.float32) -> int:
+    """Verified nodes of an adaptive EAGLE-2 tree: the candidates whose cumulative confidence reaches tau,
+    clamped to [n_min, n_max] and to the pool (reading of the 40-120 adaptive node count)."""
+    n = sum(1 for s in pool.score if s >= ln_tau)
+    return min(max(n, n_min), n_max, len(pool.score))
 
 
 def rerank(pool: Pool, n: int, root_token: int) -> tuple[Tree, list[int]]:

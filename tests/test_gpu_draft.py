@@ -87,7 +87,7 @@ def check_draft(m, st, w, gt: OT.Tree, tol: float):
         otree, pool = OD.draft_static(m, st, w.static_tree), None
         k = int(max(max(p) for p in OT.static_paths(w.static_tree))) + 1
     else:
-        otree, pool = OD.draft_dynamic(m, st, w.top_k, w.depth, w.n_nodes, w.tau)
+        otree, pool = OD.draft_dynamic(m, st, w.top_k, w.depth, w.n_nodes, w.tau, w.n_nodes_min)
         k = w.top_k
     same = (gt.n == otree.n and np.array_equal(gt.tokens, otree.tokens) and np.array_equal(gt.parent, otree.parent)
             and np.array_equal(gt.depth, otree.depth))
@@ -145,11 +145,18 @@ def _check_eagle2_rules(gt, lp, w, tol):
         best = max(s for s, _ in cand[t])
         for p in ps:   # an expanded node passed the threshold, or is the best of its depth (the guard)
             assert sc[p] >= ln_tau - tol or sc[p] >= best - tol, (p, sc[p], best)
-    if gt.n == n_max:   # top-N: no known candidate left out scores above the lowest kept node
-        lowest = min(sc[1:])
-        for t, cs in cand.items():
-            for s, kept in cs:
-                assert kept or s <= lowest + tol * (t + 1), (t, s, lowest, sorted(sc[1:])[:5], gt.depth.tolist())
+    # top-N: no known candidate left out scores above the lowest kept node
+    lowest = min(sc[1:])
+    for t, cs in cand.items():
+        for s, kept in cs:
+            assert kept or s <= lowest + tol * (t + 1), (t, s, lowest, sorted(sc[1:])[:5], gt.depth.tolist())
+    if w.n_nodes_min > 0:
+        # adaptive count: N = #(candidates reaching tau) clamped to [n_min, n_max]
+        left_out = [s for cs in cand.values() for s, kept in cs if not kept]
+        if gt.n < n_max:          # every candidate reaching tau is kept
+            assert all(s < ln_tau + tol * w.depth for s in left_out), (gt.n, max(left_out, default=None))
+        if gt.n > w.n_nodes_min:  # every kept node reaches tau
+            assert all(s >= ln_tau - tol * w.depth for s in sc[1:]), (gt.n, min(sc[1:]))
 
 
 def _run(cuda, w, shape, steps, tol, max_identical_miss=None):
@@ -192,6 +199,14 @@ def test_tiny_fp32_draft_scores(cuda, w):
 def test_gqa128_peaked_draft_tree(cuda, tree):
     w = workload("8b_static" if tree == "static" else "8b_eagle2", model=GQA128_PEAKED, prompt_len=40,
                  max_new=24)
+    ident, flagged = _run(cuda, w, GQA128_PEAKED, 6, 0.05)
+    assert ident >= 1
+
+
+def test_gqa128_peaked_adaptive_tree(cuda):
+    """EAGLE-2 with the adaptive node count (tau 0.1, between 4 and 60 nodes): trees against the oracle's, and
+    the count rule."""
+    w = workload("8b_eagle2", model=GQA128_PEAKED, prompt_len=40, max_new=24, n_nodes_min=4, tau=0.1)
     ident, flagged = _run(cuda, w, GQA128_PEAKED, 6, 0.05)
     assert ident >= 1
 

@@ -262,3 +262,36 @@ def test_invalid_trees_commit_nothing_and_are_reported(cuda, kind):
     with pytest.raises(L.EagleError) as e2:
         eng.step(1)
     assert e2.value.code == 7                      # the context is spent
+
+
+def test_adaptive_eagle2_batch2_ragged_trees(cuda):
+    """Two sequences with adaptive EAGLE-2 trees (tau 0.1, 4 to 60 nodes each, so their node counts differ)
+    verified together: each sequence's real rows match the oracle on that sequence alone, and both commit the
+    oracle's greedy tokens (up to flagged near-ties)."""
+    from tests.test_gpu_draft import GQA128_PEAKED, _gpu_tree
+    shape = GQA128_PEAKED
+    w = workload("8b_eagle2", model=shape, prompt_len=40, max_new=24, n_nodes_min=4, tau=0.1)
+    cap = FX.kv_capacity(w)
+    m = model(shape, cap)
+    prompts = FX.prompts(shape, 2, w.prompt_len)
+    eng = _engine(w, batch=2)
+    eng.prefill(torch.from_numpy(prompts).to(cuda))
+    sts = [OD.prefill(m, prompts[b], cap) for b in range(2)]
+    sizes, flagged = [], 0
+    for step in range(5):
+        gtree = eng.draft_tree()
+        am, lg = eng.verify(gtree, logits=True)
+        feats = []
+        for b in range(2):
+            gt = _gpu_tree(gtree, b)
+            sizes.append(gt.n)
+            oam, ofeats, ologits = OD.verify(m, sts[b], gt)
+            _check_logits(lg[b, : gt.n + 1].cpu().numpy(), ologits, bf16=True)
+            flagged += _check_argmax(am[b, : gt.n + 1].cpu().numpy(), ologits, bf16=True)
+            feats.append((gt, ofeats))
+        a, _ = eng.accept_commit()
+        for b in range(2):
+            gt, ofeats = feats[b]
+            assert int(a[b]) == OD.accept_commit(sts[b], gt, am[b, : gt.n + 1].cpu().numpy(), ofeats)
+    assert all(4 <= n <= 60 for n in sizes) and len(set(sizes)) > 1, sizes
+    print("node counts:", sizes, "flagged near-ties:", flagged)

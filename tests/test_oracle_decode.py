@@ -72,3 +72,24 @@ def test_planted_tree_accepts_exactly_and_compacts_kv(a):
     for l in range(s.n_layers):
         np.testing.assert_allclose(st.kv.k[l][: st.L], kv.k[l][: st.L], rtol=1e-4, atol=1e-5)
         np.testing.assert_allclose(st.kv.v[l][: st.L], kv.v[l][: st.L], rtol=1e-4, atol=1e-5)
+
+
+def test_adaptive_eagle2_is_lossless_and_varies_its_node_count():
+    """An adaptive EAGLE-2 tree (N between n_min and n_max by the confidence rule) still decodes exactly
+    like vanilla greedy decoding; with a peaked head the node count changes from step to step."""
+    shape = GQA_SMALL.reduced(lm_head_std=0.6, seed=19)
+    w = workload("8b_eagle2", model=shape, prompt_len=24, max_new=16, top_k=4, depth=4, n_nodes=24,
+                 n_nodes_min=6)
+    cap = FX.kv_capacity(w)
+    m = model(shape, cap)
+    p = FX.prompts(shape, 1, w.prompt_len)[0]
+    van = OD.vanilla_greedy(m, p, w.max_new, cap)
+    st = OD.prefill(m, p, cap)
+    sizes = []
+    while len(st.out) < w.max_new:
+        tree = OD.draft_tree(m, st, w)
+        sizes.append(tree.n)
+        amax, feats, _ = OD.verify(m, st, tree)
+        OD.accept_commit(st, tree, amax, feats)
+    assert st.out[: w.max_new] == van
+    assert all(6 <= n <= 24 for n in sizes) and len(set(sizes)) > 1, sizes

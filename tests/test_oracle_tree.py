@@ -89,3 +89,14 @@ def test_accept_matches_brute_force_over_paths():
             if all(tree.tokens[p[i + 1]] == amax[p[i]] for i in range(len(p) - 1)) and len(p) > len(best):
                 best = p
         assert path == best and bonus == amax[best[-1]]
+
+
+def test_adaptive_count_clamps_the_confident_candidates():
+    pool = OT.Pool()
+    for r, s in enumerate([-0.1, -0.5, -1.0, -2.0, -3.0, -4.0]):
+        pool.add(np.float32(s), r, -1, 1, (1, 0, r))
+    ln = np.float32(np.log(0.3))                     # -1.204: three candidates reach tau
+    assert OT.adaptive_count(pool, 1, 5, ln) == 3
+    assert OT.adaptive_count(pool, 4, 5, ln) == 4    # at least n_min
+    assert OT.adaptive_count(pool, 1, 2, ln) == 2    # at most n_max
+    assert OT.adaptive_count(pool, 8, 10, ln) == 6   # never more than the pool
