@@ -42,6 +42,7 @@ struct LayerPtrs {
 // whose features live at row hbase of the draft buffers.
 struct ProgSpec {
   int kind = 0, M = 0, hbase = 0, k = 0;
+  int row0 = 0, seq0 = 0, n_seq = 0;            // verify: its rows and sequences (a chunk of the batch)
   int n_phases = 0, n_counters = 0, first = 0;  // first: index of its first phase in the program array
   int first_attn = -1;                          // its first attention phase (set when it is built)
 };
@@ -56,6 +57,7 @@ struct Dims {
   int CL = 0;                       // prefill chunk length per sequence
   int M_tgt = 0, M_dft = 0, M_max = 0, M_lm = 0, n_groups_max = 0, ntV = 0, pool_cap = 0;
   bool bf16 = false;
+  int verify_spc = 0;               // sequences per verify launch when the batch is split (0: one launch)
   float inv_temp = 0.f;             // 1 / temperature, 0 for greedy decoding
   unsigned long long seed = 0;      // sampler seed
   // static topology (host)
@@ -95,6 +97,7 @@ struct eagle_ctx {
   // buffers
   eg::Rows rows{};
   eg::Group* groups = nullptr;
+  eg::Group* groups_local = nullptr;  // verify groups with rows counted from their verify launch's first row
   float* h_tgt = nullptr;
   float* h_dft = nullptr;
   void* hb = nullptr;
@@ -303,7 +306,26 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
       dm.stack_counters_max = std::max(dm.stack_counters_max, p.n_counters);
       dm.progs.push_back(p);
     };
-    add(0, dm.B * dm.NR, 0, 1);
+    if (stack_supported(dm.B * dm.NR, dm.hd)) {
+      add(0, dm.B * dm.NR, 0, 1);
+      if (!dm.progs.empty()) dm.progs.back().n_seq = dm.B;
+    } else if (stack_supported(dm.NR, dm.hd) &&
+               (dm.B + kStackMaxRows / dm.NR - 1) / (kStackMaxRows / dm.NR) <= 2) {
+      // more tree rows than one launch takes: two launches over halves of the
+      // batch (whole sequences), each streaming the weights once. (Measured at 61-row
+      // trees: batch 4 verify 17.1 -> 14.4 ms against the per-operation kernels; at
+      // batch 16 eight such launches, 7.2 ms each at 122 rows where the hi/lo pairs
+      // make the tensor work equal the weight stream, lose to them: 57.8 vs 54 ms.)
+      dm.verify_spc = kStackMaxRows / dm.NR;
+      for (int s0 = 0; s0 < dm.B; s0 += dm.verify_spc) {
+        const int ns = std::min(dm.verify_spc, dm.B - s0);
+        add(0, ns * dm.NR, 0, 1);
+        ProgSpec& p = dm.progs.back();
+        p.row0 = s0 * dm.NR;
+        p.seq0 = s0;
+        p.n_seq = ns;
+      }
+    }
     add(1, dm.B * dm.D1, 0, dm.k);
     for (int t = 1; t < dm.D; ++t)
       if (dm.level_rows[t] > 0) add(1, dm.B * dm.level_rows[t], dm.level_base[t], dm.k);
@@ -312,7 +334,7 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
 }
 
 struct Offsets {
-  size_t rows_seq, rows_pos, rows_slot, rows_grp, rows_tok, rows_fsrc, rows_mask, groups;
+  size_t rows_seq, rows_pos, rows_slot, rows_grp, rows_tok, rows_fsrc, rows_mask, groups, groups_local;
   size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, qg, attn, act, xfc, lm_hb, lm_ssq, lm_src;
   size_t hb_lo, act_lo, attn_lo, xfc_lo, lm_hb_lo;
   size_t rec_val, rec_idx, rec_max, rec_sum, dtopk_idx, dtopk_val, dlse, vargmax, root_idx;
@@ -334,6 +356,7 @@ Offsets plan(const Dims& dm) {
   o.rows_seq = L.take(M * 4); o.rows_pos = L.take(M * 4); o.rows_slot = L.take(M * 4);
   o.rows_grp = L.take(M * 4); o.rows_tok = L.take(M * 4); o.rows_fsrc = L.take(M * 4);
   o.rows_mask = L.take(M * 16); o.groups = L.take((size_t)dm.n_groups_max * sizeof(Group));
+  o.groups_local = L.take((size_t)dm.B * sizeof(Group));
   o.h_tgt = L.take((size_t)dm.M_tgt * dm.d * 4);
   o.h_dft = L.take((size_t)dm.M_dft * dm.d * 4);
   o.hb = L.take(M * dm.d * es);
@@ -456,21 +479,33 @@ struct Eng {
   };
 
   // One pre-norm decoder layer over M rows whose (hb, ssq_b) hold the layer input.
+  // Per-row metadata of rows [row0, ...) (a verify launch over a chunk of the batch).
+  static Rows rows_at(const Rows& r, int row0) {
+    return Rows{r.seq + row0, r.pos + row0, r.slot + row0, r.grp + row0, r.mask + 2 * row0, r.tok + row0,
+                r.fsrc + row0};
+  }
+
+  // rows of the layer: M rows from row row0 of the metadata (their residual stream
+  // at h), attention groups `groups` (NULL: c->groups); the GEMM inputs and the
+  // other intermediates are the row buffers from their first row.
   template <typename Sink>
   static eagle_status layer(eagle_ctx* c, Sink& sink, const LayerPtrs& lw, void* kc, void* vc, int cap, int M,
-                            int n_groups, float* h, const float* gain_next) {
+                            int n_groups, float* h, const float* gain_next, int row0 = 0,
+                            const Group* groups = nullptr) {
     const Dims& dm = c->dm;
+    const Rows rows = rows_at(c->rows, row0);
     EpiParams e = epi(c, kEpiQkv, M, dm.nqkv);
     e.ssq_in = c->ssq_b; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d;
     e.out = c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
     const float scale = 1.f / std::sqrt((float)dm.hd);
     e.qg = c->qg; e.qg_scale = scale * 1.4426950408889634f;
-    e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = c->rows;
+    e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = rows;
     EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e));
 
     AttnArgs a{};
-    a.q = (const float*)c->q; a.qg = c->qg; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo); a.groups = c->groups; a.n_groups = n_groups;
-    a.mask = c->rows.mask; a.row_grp = c->rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap; a.n_seq = dm.B;
+    a.q = (const float*)c->q; a.qg = c->qg; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo);
+    a.groups = groups ? groups : c->groups; a.n_groups = n_groups;
+    a.mask = rows.mask; a.row_grp = rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap; a.n_seq = dm.B;
     a.max_prefix = cap; a.scale = scale; a.part = c->attn_part; a.status = c->st.status;
     EG_TRY(sink.attention(a));
 
@@ -495,14 +530,15 @@ struct Eng {
   // and sequences are in c->rows, through idx (row -> rows entry) when not NULL.
   template <typename Sink>
   static eagle_status lm_head_gemm(eagle_ctx* c, Sink& sink, const void* X, const bf16* X_lo, const float* ssq,
-                                   int M, int k, float* logits, bool choose = false, const int* idx = nullptr) {
+                                   int M, int k, float* logits, bool choose = false, const int* idx = nullptr,
+                                   int row0 = 0) {
     const Dims& dm = c->dm;
     EpiParams e = epi(c, kEpiLmHead, M, dm.V);
     e.ssq_in = ssq; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.topk = k; e.y = logits;
     e.rec_val = c->rec_val; e.rec_idx = c->rec_idx; e.rec_max = c->rec_max; e.rec_sum = c->rec_sum;
     if (choose && dm.inv_temp > 0.f) {
       e.inv_temp = dm.inv_temp; e.seed = dm.seed;
-      e.samp_pos = c->rows.pos; e.samp_seq = c->rows.seq; e.samp_idx = idx;
+      e.samp_pos = c->rows.pos + row0; e.samp_seq = c->rows.seq + row0; e.samp_idx = idx;
     }
     return sink.gemm(X, X_lo, c->lm_head, M, dm.V, dm.d, e);
   }
@@ -521,21 +557,22 @@ struct Eng {
   }
 
   template <typename Sink>
-  static eagle_status target_layers(eagle_ctx* c, Sink& sink, int M, int n_groups) {
+  static eagle_status target_layers(eagle_ctx* c, Sink& sink, int M, int n_groups, int row0 = 0,
+                                    const Group* groups = nullptr) {
     const Dims& dm = c->dm;
     const size_t kvl = (size_t)dm.B * dm.Hkv * dm.cap * dm.hd * sizeof(T);
     for (int l = 0; l < dm.Lyr; ++l) {
       const float* gn = l + 1 < dm.Lyr ? c->layers[l + 1].attn_norm : c->final_norm;
       EG_TRY(layer(c, sink, c->layers[l], (char*)c->kc + l * kvl, (char*)c->vc + l * kvl, dm.cap, M, n_groups,
-                   c->h_tgt, gn));
+                   c->h_tgt + (size_t)row0 * dm.d, gn, row0, groups));
     }
     return EAGLE_OK;
   }
 
-  static eagle_status embed(eagle_ctx* c, int M) {
+  static eagle_status embed(eagle_ctx* c, int M, int row0 = 0) {
     const Dims& dm = c->dm;
-    EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok, M, dm.d, c->layers[0].attn_norm, c->h_tgt, (T*)c->hb,
-                        lo(c->hb_lo), c->ssq_b, c->stream));
+    EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok + row0, M, dm.d, c->layers[0].attn_norm,
+                        c->h_tgt + (size_t)row0 * dm.d, (T*)c->hb, lo(c->hb_lo), c->ssq_b, c->stream));
     return EAGLE_OK;
   }
 
@@ -566,9 +603,11 @@ struct Eng {
 
   static eagle_status run_prog(eagle_ctx* c, const ProgSpec& p, float* lm_logits = nullptr) {
     unsigned long long* trace = p.kind == 0 ? c->trace : nullptr;
+    const Group* g = p.kind == 0 ? c->groups_local + p.seq0 : c->groups;
+    const int ng = p.kind == 0 ? p.n_seq : c->dm.B;
     EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
                     c->stack_scratch, c->dm.stack_phases_max, c->dm.stack_counters_max, c->st.status, trace,
-                    lm_logits, c->groups, c->dm.B, p.first_attn, c->stream));
+                    lm_logits, g, ng, p.first_attn, c->stream));
     return EAGLE_OK;
   }
 
@@ -584,8 +623,8 @@ struct Eng {
       b.has_lo = true;
       Record r{c, &b};
       if (p.kind == 0) {
-        EG_TRY(target_layers(c, r, p.M, dm.B));
-        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c->hb_lo), c->ssq_b, p.M, 1, nullptr, true));
+        EG_TRY(target_layers(c, r, p.M, p.n_seq, p.row0, c->groups_local + p.seq0));
+        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c->hb_lo), c->ssq_b, p.M, 1, nullptr, true, nullptr, p.row0));
       } else {
         EG_TRY(draft_ops(c, r, p.M, dm.B, p.hbase, p.k));
       }
@@ -670,14 +709,19 @@ struct Eng {
   static eagle_status verify(eagle_ctx* c, const TreeOut& tree, int* d_argmax, float* d_logits) {
     const Dims& dm = c->dm;
     const int M = dm.B * tree.n_rows;
-    EG_CK(setup_verify_rows(c->st, tree, c->rows, c->groups, c->stream));
-    const ProgSpec* p = find_prog(c, 0, M, 0, 1);
-    if (p) {
-      // one persistent launch for every layer and the LM head (which also stores the logits if wanted)
-      EG_TRY(embed(c, M));
-      EG_TRY(run_prog(c, *p, d_logits));
-      EG_TRY(lm_head_merge(c, M, 1, c->vargmax, nullptr, nullptr));
-    } else {
+    EG_CK(setup_verify_rows(c->st, tree, c->rows, c->groups, c->groups_local, dm.verify_spc, c->stream));
+    bool persistent = false;
+    if (tree.n_rows == dm.NR)
+      for (const ProgSpec& p : dm.progs)
+        if (p.kind == 0) {
+          // one persistent launch for every layer and the LM head (which also stores the logits if
+          // wanted), per chunk of the batch when its rows exceed one launch
+          EG_TRY(embed(c, p.M, p.row0));
+          EG_TRY(run_prog(c, p, d_logits ? d_logits + (size_t)p.row0 * dm.V : nullptr));
+          EG_TRY(lm_head_merge(c, p.M, 1, c->vargmax + p.row0, nullptr, nullptr));
+          persistent = true;
+        }
+    if (!persistent) {
       EG_TRY(target_stack(c, M, dm.B));
       EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits, true));
     }
@@ -781,6 +825,7 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->rows = Rows{(int*)P(o.rows_seq), (int*)P(o.rows_pos), (int*)P(o.rows_slot), (int*)P(o.rows_grp),
                  (uint64_t*)P(o.rows_mask), (int*)P(o.rows_tok), (int*)P(o.rows_fsrc)};
   c->groups = (Group*)P(o.groups);
+  c->groups_local = (Group*)P(o.groups_local);
   c->h_tgt = (float*)P(o.h_tgt); c->h_dft = (float*)P(o.h_dft); c->hb = P(o.hb);
   c->ssq_a = (float*)P(o.ssq_a); c->ssq_b = (float*)P(o.ssq_b);
   c->q = P(o.q); c->qg = (__half*)P(o.qg); c->attn = P(o.attn); c->act = P(o.act); c->xfc = P(o.xfc);

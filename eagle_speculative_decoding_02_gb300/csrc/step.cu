@@ -113,7 +113,7 @@ __device__ bool tree_row_ok(const TreeOut& tree, int base, int j) {
 }
 
 // Verify rows: tree row j of sequence b at position L + depth(j), KV slot L + j.
-__global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* groups) {
+__global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* groups, Group* groups_local, int spc) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -154,6 +154,8 @@ __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* gr
     g.prefix = fits ? L : 0;
     g.block_len = fits ? s_real : 0;
     groups[b] = g;
+    g.row0 = (spc > 0 ? b % spc : b) * NR;
+    groups_local[b] = g;
   }
 }
 
@@ -635,8 +637,9 @@ cudaError_t setup_catchup_rows(State st, Rows rows, Group* groups, cudaStream_t 
   return launch_pdl(setup_catchup_kernel, dim3(st.B), dim3(32), 0, s, st, rows, groups);
 }
 
-cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, cudaStream_t s) {
-  return launch_pdl(setup_verify_kernel, dim3(st.B), dim3(128), 0, s, st, tree, rows, groups);
+cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, Group* groups_local, int spc,
+                              cudaStream_t s) {
+  return launch_pdl(setup_verify_kernel, dim3(st.B), dim3(128), 0, s, st, tree, rows, groups, groups_local, spc);
 }
 
 cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, int CL, int P, int* root_out,

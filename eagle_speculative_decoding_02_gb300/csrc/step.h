@@ -74,7 +74,10 @@ cudaError_t setup_prefill_rows(const int* prompt, int P, int c0, int CL, int B, 
 cudaError_t setup_catchup_rows(State st, Rows rows, Group* groups, cudaStream_t s);
 // Also checks the tree (BFS order, parent/depth/ancestor-mask consistency,
 // distinct sibling tokens) and records kStInvalid if it is not.
-cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, cudaStream_t s);
+// groups_local[b]: the same group with its rows counted from the first row of
+// its verify launch (launches of spc sequences each; spc = 0: one launch).
+cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, Group* groups_local, int spc,
+                              cudaStream_t s);
 cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, int CL, int P, int* root_out,
                            cudaStream_t s);
 cudaError_t set_root_tree(State st, TreeOut tree, cudaStream_t s);
