@@ -51,6 +51,7 @@ CODE_LM_HEAD = 2
 CODE_PROMPT = 500_000          # + sequence index
 CODE_LAYER = 1_000             # + 16 * layer + kind
 CODE_HEAD_NOISE = 900_000      # + kind
+CODE_HEAD_FUSE = 950_000
 KIND = {"wq": 0, "wk": 1, "wv": 2, "wo": 3, "wg": 4, "wu": 5, "wd": 6}
 
 
@@ -212,6 +213,7 @@ class Workload:
     n_nodes: int = 60          # verified draft nodes, root excluded
     n_nodes_max: int = 120
     n_nodes_min: int = 0       # > 0: adaptive EAGLE-2 node count between n_nodes_min and n_nodes
+    feature_taps: int = 1      # 1: the target's top-layer feature; 3: fused low / mid / high features
     tau: float = 0.3
     kv_cap: int = 0            # 0: prompt + max_new + margins
 
@@ -274,7 +276,10 @@ def target_tensor(m: ModelShape, name: str, layer: int = -1, rows: slice | None 
 
 
 def head_tensor(m: ModelShape, name: str) -> np.ndarray:
-    """EAGLE head tensor: "fc" ([d, 2d], exactly [I | 0]) or a projection of its decoder layer."""
+    """EAGLE head tensor: "fc" ([d, 2d], exactly [I | 0]), "fuse" ([d, 3d], N(0, init_std): the fused-feature
+    variant's matrix over three target features) or a projection of its decoder layer."""
+    if name == "fuse":
+        return normal(stream_key(m.seed, CODE_HEAD_FUSE), m.d * 3 * m.d, m.init_std, bf16=m.bf16).reshape(m.d, 3 * m.d)
     if name == "fc":
         fc = np.zeros((m.d, 2 * m.d), dtype=np.float32)
         fc[np.arange(m.d), np.arange(m.d)] = 1.0

@@ -57,6 +57,9 @@ def target_tensor(m: FX.ModelShape, name: str, layer: int = -1, device="cuda") -
 
 
 def head_tensor(m: FX.ModelShape, name: str, device="cuda") -> torch.Tensor:
+    if name == "fuse":
+        return fill_normal(torch.empty((m.d, 3 * m.d), dtype=_dt(m), device=device),
+                           FX.stream_key(m.seed, FX.CODE_HEAD_FUSE), m.init_std)
     if name == "fc":
         fc = torch.zeros((m.d, 2 * m.d), dtype=_dt(m), device=device)
         fc[:, : m.d] = torch.eye(m.d, dtype=_dt(m), device=device)

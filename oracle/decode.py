@@ -50,7 +50,7 @@ import numpy as np
 import fixtures as FX
 
 from .core import F32, topk
-from .model import KVCache, Model, causal_visible, draft_logp, draft_rows, logits_of, target_rows
+from .model import KVCache, Model, causal_visible, draft_features, draft_logp, draft_rows, logits_of, target_rows
 from .sampling import GREEDY, Sampler
 from .tree import Pool, Tree, accept, adaptive_count, rerank, select_frontier, static_layout, static_paths
 
@@ -77,8 +77,9 @@ def prefill(m: Model, prompt: np.ndarray, cap: int, sampler: Sampler = GREEDY, s
     kv = KVCache(s.n_layers, cap, s.n_kv_heads, s.head_dim)
     dkv = KVCache(1, cap, s.n_kv_heads, s.head_dim)
     pos = np.arange(P)
-    feats = target_rows(m, kv, prompt, pos, pos, causal_visible(0, P))
-    root = int(sampler.choose(logits_of(m, feats[-1:]), seq, np.array([P]))[0])
+    top, low, mid = target_rows(m, kv, prompt, pos, pos, causal_visible(0, P), taps=True)
+    root = int(sampler.choose(logits_of(m, top[-1:]), seq, np.array([P]))[0])
+    feats = draft_features(m, top, low, mid)
     if P > 1:
         draft_rows(m, dkv, feats[:P - 1], prompt[1:], pos[:P - 1], pos[:P - 1], causal_visible(0, P - 1))
     return SeqState(L=P, root=root, pend_feats=feats[P - 1:], pend_tokens=np.array([root], np.int32),
@@ -230,15 +231,16 @@ def draft_logp_on_tree(m: Model, st: SeqState, tree: Tree) -> np.ndarray:
 
 def verify(m: Model, st: SeqState, tree: Tree):
     """Target forward over every tree row in one pass; returns (the target's choice after each row [N+1]:
-    argmax, or at T > 0 its sample of the token at position L + depth + 1; features; logits)."""
+    argmax, or at T > 0 its sample of the token at position L + depth + 1; the rows' draft features (the
+    top-layer features, or fused); logits)."""
     L = st.L
     slots = L + np.arange(tree.n + 1)
     pos = L + tree.depth
     prefix = np.arange(L)
     vis = [np.concatenate([prefix, L + np.array(tree.path(j))]) for j in range(tree.n + 1)]
-    feats = target_rows(m, st.kv, tree.tokens, pos, slots, vis)
-    logits = logits_of(m, feats)
-    return st.sampler.choose(logits, st.seq, pos + 1), feats, logits
+    top, low, mid = target_rows(m, st.kv, tree.tokens, pos, slots, vis, taps=True)
+    logits = logits_of(m, top)
+    return st.sampler.choose(logits, st.seq, pos + 1), draft_features(m, top, low, mid), logits
 
 
 def accept_commit(st: SeqState, tree: Tree, amax: np.ndarray, feats: np.ndarray) -> int:

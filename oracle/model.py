@@ -13,6 +13,14 @@ the true next token (the shifted token sequence): g = [f_i ; E(t_{i+1})] @ FC^T,
 then one decoder layer with its own KV cache gives the predicted feature
 f^_{i+1}. Draft logits reuse the target's own final norm and LM head.
 
+Fused-feature variant ("yuhuili": EAGLE-3 fuses low-, mid- and high-level
+features of the target; read here as): the target exposes the hidden states
+after layers L/4, L/2 and L, and the draft takes u = fuse @ [low ; mid ; high]
+in place of the top-layer feature for committed positions (tree rows keep
+feeding the head's own predicted feature). Pinned in tests/test_oracle_draft.py:
+a fusion matrix selecting one feature reproduces the model cut after that layer,
+selecting the top feature reproduces the plain draft, and decoding stays lossless.
+
 Pins (tests/test_oracle_model.py): a decoder layer with permutation weights
 and single-key attention moves every coordinate where the permutations say; a
 layer with zero output projections is the identity; the layer agrees with a
@@ -55,14 +63,16 @@ class Model:
     head_layer: LayerWeights
     rope_cos: np.ndarray
     rope_sin: np.ndarray
+    fuse: np.ndarray | None = None   # [d, 3d] over [low ; mid ; high] features (fused-feature variant)
 
 
 def _ones(n: int) -> np.ndarray:
     return np.ones(n, dtype=F32)
 
 
-def build_model(shape: FX.ModelShape, max_pos: int) -> Model:
-    """Materialise the seeded weights of ``shape`` (norm gains are 1, no biases)."""
+def build_model(shape: FX.ModelShape, max_pos: int, taps: int = 1) -> Model:
+    """Materialise the seeded weights of ``shape`` (norm gains are 1, no biases); taps = 3 adds the
+    fused-feature matrix."""
     def layer(get) -> LayerWeights:
         return LayerWeights(**{k: get(k) for k in FX.layer_shapes(shape)},
                             attn_norm=_ones(shape.d), ffn_norm=_ones(shape.d))
@@ -73,7 +83,7 @@ def build_model(shape: FX.ModelShape, max_pos: int) -> Model:
     return Model(shape=shape, embed=FX.target_tensor(shape, "embed"),
                  lm_head=FX.target_tensor(shape, "lm_head"), final_norm=_ones(shape.d),
                  layers=layers, fc=FX.head_tensor(shape, "fc"), head_layer=head,
-                 rope_cos=cos, rope_sin=sin)
+                 rope_cos=cos, rope_sin=sin, fuse=FX.head_tensor(shape, "fuse") if taps == 3 else None)
 
 
 class KVCache:
@@ -115,13 +125,34 @@ def decoder_layer(m: Model, lw: LayerWeights, h: np.ndarray, pos: np.ndarray, sl
     return (h + a @ lw.wd.T).astype(F32)
 
 
+def tap_layers(n_layers: int) -> tuple[int, int]:
+    """Decoder layers after which the low and mid features are taken (1-based): L/4 and L/2, at least 1
+    (reading of EAGLE-3's fusion of low-, mid- and high-level features, "yuhuili" page; high = layer L)."""
+    return max(1, n_layers // 4), max(1, n_layers // 2)
+
+
 def target_rows(m: Model, kv: KVCache, tokens: np.ndarray, pos: np.ndarray, slots: np.ndarray,
-                visible: list[np.ndarray]) -> np.ndarray:
-    """Target forward of a set of rows; returns their top-layer features [rows, d]."""
+                visible: list[np.ndarray], taps: bool = False):
+    """Target forward of a set of rows; returns their top-layer features [rows, d], or with taps the
+    (top, low, mid) features (the hidden states after layers L, tap_layers(L))."""
     h = m.embed[tokens].astype(F32)
+    lo_l, mid_l = tap_layers(len(m.layers))
+    low = mid = None
     for l, lw in enumerate(m.layers):
         h = decoder_layer(m, lw, h, pos, slots, visible, kv.k[l], kv.v[l])
-    return h
+        if l + 1 == lo_l:
+            low = h
+        if l + 1 == mid_l:
+            mid = h
+    return (h, low, mid) if taps else h
+
+
+def draft_features(m: Model, top: np.ndarray, low: np.ndarray | None = None, mid: np.ndarray | None = None):
+    """The feature the draft head takes for committed positions: the top-layer feature, or in the fused
+    variant u = fuse @ [low ; mid ; top]."""
+    if m.fuse is None:
+        return top
+    return (np.concatenate([low, mid, top], axis=1).astype(F32) @ m.fuse.T).astype(F32)
 
 
 def logits_of(m: Model, features: np.ndarray) -> np.ndarray:

@@ -315,3 +315,56 @@ def test_eagle2_tree_equals_brute_force(tau, seed_b):
         assert tree.depth[j] == len(p)
         assert tree.parent[j] == where[p[:-1]]
         assert abs(float(tree.score[j]) - scores[j - 1]) < 1e-4 * len(p)
+
+
+# ------------------------------------------------------------------ fused low / mid / high features
+
+FOUR_LAYER = GQA_SMALL.reduced(n_layers=4, seed=23)
+
+
+def _fused_model(base: OM.Model, which: int) -> OM.Model:
+    """The fused-feature variant whose fusion matrix selects feature `which` (0 low, 1 mid, 2 high)."""
+    d = base.shape.d
+    fuse = np.zeros((d, 3 * d), np.float32)
+    fuse[np.arange(d), which * d + np.arange(d)] = 1.0
+    return dataclasses.replace(base, fuse=fuse)
+
+
+def test_fused_features_tap_the_layers_after_l4_and_l2():
+    """fuse = [I|0|0] ([0|I|0]) makes the draft's feature the output of layer L/4 (L/2): the top-layer
+    feature of the model cut after that many layers."""
+    base = OM.build_model(FOUR_LAYER, 128)
+    prompt = _prompt(base, 16)
+    assert OM.tap_layers(4) == (1, 2)
+    for which, n in ((0, 1), (1, 2), (2, 4)):
+        m = _fused_model(base, which)
+        st = OD.prefill(m, prompt, 128)
+        cut = dataclasses.replace(base, layers=base.layers[:n])
+        kv = OM.KVCache(n, 128, FOUR_LAYER.n_kv_heads, FOUR_LAYER.head_dim)
+        pos = np.arange(16)
+        ref = OM.target_rows(cut, kv, prompt, pos, pos, OM.causal_visible(0, 16))
+        np.testing.assert_array_equal(st.pend_feats[-1], ref[-1])
+
+
+def test_fused_with_top_selection_is_eagle():
+    """fuse = [0|0|I]: the fused variant drafts exactly the trees the top-layer feature gives."""
+    base = OM.build_model(FOUR_LAYER, 256)
+    m3 = _fused_model(base, 2)
+    w = workload("8b_static", model=FOUR_LAYER, prompt_len=20, max_new=16)
+    p = _prompt(base, 20)
+    s1, s3 = OD.prefill(base, p, 256), OD.prefill(m3, p, 256)
+    for _ in range(2):
+        t1, t3 = OD.draft_static(base, s1, "rank60"), OD.draft_static(m3, s3, "rank60")
+        assert np.array_equal(t1.tokens, t3.tokens)
+        np.testing.assert_array_equal(t1.score, t3.score)
+        for st, t, m in ((s1, t1, base), (s3, t3, m3)):
+            amax, feats, _ = OD.verify(m, st, t)
+            OD.accept_commit(st, t, amax, feats)
+
+
+def test_fused_variant_is_lossless():
+    base = OM.build_model(FOUR_LAYER, 256, taps=3)
+    assert base.fuse is not None and base.fuse.shape == (FOUR_LAYER.d, 3 * FOUR_LAYER.d)
+    w = workload("8b_eagle2", model=FOUR_LAYER, prompt_len=20, max_new=10, feature_taps=3)
+    p = _prompt(base, 20)
+    assert OD.speculative_generate(base, p, w, cap=256).out == OD.vanilla_greedy(base, p, 10, 256)
