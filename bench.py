@@ -163,7 +163,7 @@ def cpu_baseline(w, prompt_len: int, budget_s: float):
     wl = __import__("dataclasses").replace(w, prompt_len=prompt_len)
     cap = prompt_len + 64 + 2 * (w.depth + 1) + w.n_nodes_max + 1
     t0 = time.time()
-    m = OM.build_model(w.model, cap)
+    m = OM.build_model(w.model, cap, taps=w.feature_taps)
     prompt = FX.prompts(w.model, 1, prompt_len)[0]
     st = OD.prefill(m, prompt, cap)
     t_setup = time.time() - t0
@@ -195,7 +195,7 @@ def run_reference(args, w):
     P = 64
     wl = dataclasses.replace(w, prompt_len=P)
     cap = P + (args.steps + args.warmup + 2) * (w.depth + 1) + w.n_nodes_max + 8
-    m = OM.build_model(w.model, cap)
+    m = OM.build_model(w.model, cap, taps=w.feature_taps)
     prompt = FX.prompts(w.model, 1, P)[0]
     st = OD.prefill(m, prompt, cap)
     for _ in range(args.warmup):
@@ -263,6 +263,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="eagle", choices=["eagle", "reference"])
     ap.add_argument("--workload", default="8b_eagle2")
+    ap.add_argument("--feature-taps", type=int, default=0, choices=[0, 1, 3],
+                    help="3: the fused low / mid / high feature variant of the workload")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -280,6 +282,8 @@ def main():
 
     import fixtures as FX
     w = FX.WORKLOADS[args.workload]
+    if args.feature_taps == 3:
+        w = dataclasses.replace(w, name=f"{w.name}, fused low/mid/high features", feature_taps=3)
     if args.layers and args.profile_verify:
         w = dataclasses.replace(w, name=f"{w.name}-{args.layers}layers",
                                 model=dataclasses.replace(w.model, n_layers=args.layers))
@@ -393,10 +397,15 @@ def main():
     # dominant kernel: the persistent layer-stack launch of the verify pass (every layer's GEMMs with
     # their epilogues, tree attention and its merge, the LM head); the timed region is one verify
     # pass on the library's stream, which adds two small kernels (embedding rows, top-k merge)
-    persistent = w.batch * rows <= 128
-    kernel = ("stack_tc_kernel (verify program)" if persistent else
+    # one persistent launch up to 128 rows; up to two launches over halves of the batch
+    spc = 128 // rows
+    n_chunks = -(-w.batch // spc) if spc else 0
+    persistent = w.batch * rows <= 128 or 0 < n_chunks <= 2
+    kernel = (("stack_tc_kernel (verify program)" if n_chunks <= 1 else
+               f"stack_tc_kernel (verify program, {n_chunks} launches over halves of the batch)") if persistent else
               "verify pass: gemm_tc_kernel per projection + attn_tc_kernel / attn_merge_kernel per layer")
-    traffic = captured_traffic() if (persistent and args.workload == "8b_eagle2") else None
+    traffic = (captured_traffic() if (persistent and args.workload == "8b_eagle2" and w.feature_taps != 3)
+               else None)
     if tensor_bound:
         ach = vf / v_ms / 1e9
         roof = {"bound": "tensor", "achieved": ach, "peak": tflops_sus, "unit": "TFLOP/s", "frac": ach / tflops_sus,
@@ -441,6 +450,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, "
                 "uniform random prompt tokens)",
                 "config": {"workload": w.name, "batch": w.batch, "prompt": w.prompt_len,
+                           "feature": "fused low/mid/high" if w.feature_taps == 3 else "top layer",
                            "tree": f"{w.tree} top_k={w.top_k} depth={w.depth} tau={w.tau} nodes={w.n_nodes}",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "l2": "no flush: every step streams the whole target and head weights "

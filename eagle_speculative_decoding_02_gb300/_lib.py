@@ -27,7 +27,8 @@ class EagleConfig(C.Structure):
                 ("max_prompt", C.c_int32), ("max_new", C.c_int32), ("tree_mode", C.c_int32),
                 ("n_nodes", C.c_int32), ("static_parent", C.POINTER(C.c_int32)),
                 ("static_rank", C.POINTER(C.c_int32)), ("top_k", C.c_int32), ("depth", C.c_int32),
-                ("tau", C.c_float), ("temperature", C.c_float), ("seed", C.c_uint64), ("n_nodes_min", C.c_int32)]
+                ("tau", C.c_float), ("temperature", C.c_float), ("seed", C.c_uint64), ("n_nodes_min", C.c_int32),
+                ("feature_taps", C.c_int32)]
 
 
 class EagleLayerWeights(C.Structure):
@@ -37,7 +38,8 @@ class EagleLayerWeights(C.Structure):
 
 class EagleWeights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
-                ("layers", C.POINTER(EagleLayerWeights)), ("fc", C.c_void_p), ("head", EagleLayerWeights)]
+                ("layers", C.POINTER(EagleLayerWeights)), ("fc", C.c_void_p), ("head", EagleLayerWeights),
+                ("fuse", C.c_void_p)]
 
 
 class EagleTree(C.Structure):
@@ -69,6 +71,7 @@ SIGNATURES = {
     "eagle_set_trace": (C.c_int, [C.c_void_p, C.c_void_p, C.c_size_t, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "eagle_destroy": (C.c_int, [C.c_void_p]),
     "eagle_last_error": (C.c_char_p, [C.c_void_p]),
+    "eagle_struct_size": (C.c_size_t, [C.c_int32]),
     "eagle_op_gemm_scratch_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "eagle_op_gemm": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -101,6 +104,10 @@ def load() -> C.CDLL:
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
+        for which, st in enumerate((EagleConfig, EagleWeights, EagleLayerWeights, EagleTree, EagleStats)):
+            if lib.eagle_struct_size(which) != C.sizeof(st):
+                raise RuntimeError(f"{st.__name__}: {C.sizeof(st)} bytes here, "
+                                   f"{lib.eagle_struct_size(which)} in the library (stale build?)")
         _lib = lib
     return _lib
 

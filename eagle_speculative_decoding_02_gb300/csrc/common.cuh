@@ -111,6 +111,8 @@ struct EpiParams {
   void* hb = nullptr;       // [M][N] next GEMM input (h * gain_next)
   float* ssq_out = nullptr; // [N/128][M]
   const float* gain = nullptr;
+  float* h_tap = nullptr;   // kEpiResid: optional copies of the new residual h (a feature tap of this layer)
+  float* h_tap2 = nullptr;
   // kEpiLmHead
   int topk = 1;
   // sampling (inv_temp > 0): the top-k is taken of logit * inv_temp + Gumbel noise

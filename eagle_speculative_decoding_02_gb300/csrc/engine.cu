@@ -59,6 +59,9 @@ struct Dims {
   bool bf16 = false;
   int verify_spc = 0;               // sequences per verify launch when the batch is split (0: one launch)
   float inv_temp = 0.f;             // 1 / temperature, 0 for greedy decoding
+  bool taps = false;                // fused-feature variant: the draft takes fuse [f_low ; f_mid ; f_top]
+  int tap_low = 0, tap_mid = 0;     // ... with f_low, f_mid the hidden states after these target layers (1-based)
+  int M_fused = 0;                  // rows of the fused-feature buffer
   unsigned long long seed = 0;      // sampler seed
   // static topology (host)
   std::vector<int> s_parent, s_rank, s_depth, s_lrow, s_sidx, s_level_nodes, s_level_count;
@@ -91,6 +94,7 @@ struct eagle_ctx {
   const void* lm_head = nullptr;
   const float* final_norm = nullptr;
   const void* fc = nullptr;
+  const void* fuse = nullptr;  // fused-feature variant: [d, 3d]
   std::string err;
   bool failed = false;
   int phase = 0;  // 0 fresh, 1 prefilled, 2 drafted, 3 verified
@@ -100,6 +104,9 @@ struct eagle_ctx {
   eg::Group* groups_local = nullptr;  // verify groups with rows counted from their verify launch's first row
   float* h_tgt = nullptr;
   float* h_dft = nullptr;
+  float* h_low = nullptr;   // fused-feature variant: the low / mid taps of the target rows (as h_tgt)
+  float* h_mid = nullptr;
+  float* fused = nullptr;   // ... and u = fuse [f_low ; f_mid ; f_top] of the rows the draft catches up on
   void* hb = nullptr;
   eg::bf16* hb_lo = nullptr;   // bf16 models: GEMM inputs are hi/lo pairs (x = hb + hb_lo)
   eg::bf16* act_lo = nullptr;
@@ -197,6 +204,10 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
   dm.mode = cfg.tree_mode;
   dm.n_nodes = cfg.n_nodes;
   if (cfg.n_nodes < 1 || cfg.n_nodes + 1 > kMaxTreeRows) return bad("n_nodes must be in 1..120");
+  if (cfg.feature_taps != 0 && cfg.feature_taps != 1 && cfg.feature_taps != 3) return bad("feature_taps must be 0, 1 or 3");
+  dm.taps = cfg.feature_taps == 3;
+  dm.tap_low = std::max(1, dm.taps ? cfg.n_layers / 4 : 0);
+  dm.tap_mid = std::max(1, dm.taps ? cfg.n_layers / 2 : 0);
   dm.NR = cfg.n_nodes + 1;
   dm.level_rows.assign(kMaxDepth + 1, 0);
   dm.level_base.assign(kMaxDepth + 1, 0);
@@ -281,6 +292,7 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
   dm.M_tgt = std::max(dm.B * kMaxTreeRows, M_pf);
   dm.M_dft = std::max(dm.R_d, M_pf);
   dm.M_max = std::max(dm.M_tgt, dm.M_dft);
+  dm.M_fused = dm.taps ? std::max(M_pf, dm.B * dm.D1) : 0;
   int lvl_max = dm.D1;
   for (int t = 1; t < dm.D; ++t) lvl_max = std::max(lvl_max, dm.level_rows[t]);
   dm.M_lm = std::max(dm.B * kMaxTreeRows, dm.B * lvl_max);
@@ -335,11 +347,11 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
 
 struct Offsets {
   size_t rows_seq, rows_pos, rows_slot, rows_grp, rows_tok, rows_fsrc, rows_mask, groups, groups_local;
-  size_t h_tgt, h_dft, hb, ssq_a, ssq_b, q, qg, attn, act, xfc, lm_hb, lm_ssq, lm_src;
+  size_t h_tgt, h_dft, h_low, h_mid, fused, hb, ssq_a, ssq_b, q, qg, attn, act, xfc, lm_hb, lm_ssq, lm_src;
   size_t hb_lo, act_lo, attn_lo, xfc_lo, lm_hb_lo;
   size_t rec_val, rec_idx, rec_max, rec_sum, dtopk_idx, dtopk_val, dlse, vargmax, root_idx;
   size_t t_tok, t_par, t_dep, t_anc, t_score, vt_tok, vt_par, vt_dep, vt_anc;
-  size_t L, c, root, pend_tok, pend_feat, n_out, out, acc_len, acc_path, L_prev, hist, status;
+  size_t L, c, root, pend_tok, pend_feat, pend_low, pend_mid, n_out, out, acc_len, acc_path, L_prev, hist, status;
   size_t p_score, p_token, p_parent, p_depth, p_cid, p_frow, p_smask, p_count, p_front, p_nfront;
   size_t s_parent, s_rank, s_depth, s_lrow, s_sidx, s_smask, s_lnodes, s_lcount;
   size_t rope_cos, rope_sin, kc, vc, kc_d, vc_d, gemm, attn_part, stack_prog, stack_scratch, stack_part;
@@ -359,14 +371,18 @@ Offsets plan(const Dims& dm) {
   o.groups_local = L.take((size_t)dm.B * sizeof(Group));
   o.h_tgt = L.take((size_t)dm.M_tgt * dm.d * 4);
   o.h_dft = L.take((size_t)dm.M_dft * dm.d * 4);
+  const size_t tap_rows = dm.taps ? dm.M_tgt : 0;
+  o.h_low = L.take(tap_rows * dm.d * 4); o.h_mid = L.take(tap_rows * dm.d * 4);
+  o.fused = L.take((size_t)dm.M_fused * dm.d * 4);
+  const int xw = dm.taps ? 3 : 2;  // width of the FC / fuse GEMM input, in units of d
   o.hb = L.take(M * dm.d * es);
   o.ssq_a = L.take(M * nt_d * 4); o.ssq_b = L.take(M * nt_d * 4);
   o.q = L.take(M * dm.qd * 4); o.qg = L.take(M * dm.qd * 2); o.attn = L.take(M * dm.qd * es);
-  o.act = L.take(M * dm.ffn * es); o.xfc = L.take(M * 2 * dm.d * es);
+  o.act = L.take(M * dm.ffn * es); o.xfc = L.take(M * xw * dm.d * es);
   o.lm_hb = L.take((size_t)dm.B * dm.d * es); o.lm_ssq = L.take((size_t)dm.B * nt_d * 4);
   const size_t lo = dm.bf16 ? 2 : 0;  // low halves of the hi/lo GEMM inputs (bf16 models only)
   o.hb_lo = L.take(M * dm.d * lo); o.act_lo = L.take(M * dm.ffn * lo); o.attn_lo = L.take(M * dm.qd * lo);
-  o.xfc_lo = L.take(M * 2 * dm.d * lo); o.lm_hb_lo = L.take((size_t)dm.B * dm.d * lo);
+  o.xfc_lo = L.take(M * xw * dm.d * lo); o.lm_hb_lo = L.take((size_t)dm.B * dm.d * lo);
   o.lm_src = L.take((size_t)dm.B * 4);
   const size_t nrec = (size_t)dm.ntV * dm.M_lm;
   const int krec = std::max(dm.k, 1);
@@ -382,6 +398,7 @@ Offsets plan(const Dims& dm) {
   const size_t B = dm.B;
   o.L = L.take(B * 4); o.c = L.take(B * 4); o.root = L.take(B * 4);
   o.pend_tok = L.take(B * dm.D1 * 4); o.pend_feat = L.take(B * dm.D1 * dm.d * 4);
+  o.pend_low = L.take(dm.taps ? B * dm.D1 * dm.d * 4 : 0); o.pend_mid = L.take(dm.taps ? B * dm.D1 * dm.d * 4 : 0);
   o.n_out = L.take(B * 4); o.out = L.take(B * dm.out_cap * 4); o.acc_len = L.take(B * 4);
   o.acc_path = L.take(B * dm.D1 * 4); o.L_prev = L.take(B * 4);
   o.hist = L.take((kMaxDepth + 1) * 8); o.status = L.take(4);
@@ -403,7 +420,7 @@ Offsets plan(const Dims& dm) {
     const int Ns[] = {dm.nqkv, dm.d, 2 * dm.ffn, dm.d, dm.V};
     const int Ks[] = {dm.d, dm.qd, dm.d, dm.ffn, dm.d};
     for (int i = 0; i < 5; ++i) g = std::max(g, gemm_tc_scratch_bytes((int)M, Ns[i], Ks[i]));
-    g = std::max(g, gemm_tc_scratch_bytes((int)M, dm.d, 2 * dm.d));
+    g = std::max(g, gemm_tc_scratch_bytes((int)M, dm.d, xw * dm.d));
   }
   o.gemm_bytes = g;
   o.gemm = L.take(std::max<size_t>(g, 256));
@@ -491,7 +508,7 @@ struct Eng {
   template <typename Sink>
   static eagle_status layer(eagle_ctx* c, Sink& sink, const LayerPtrs& lw, void* kc, void* vc, int cap, int M,
                             int n_groups, float* h, const float* gain_next, int row0 = 0,
-                            const Group* groups = nullptr) {
+                            const Group* groups = nullptr, float* tap = nullptr, float* tap2 = nullptr) {
     const Dims& dm = c->dm;
     const Rows rows = rows_at(c->rows, row0);
     EpiParams e = epi(c, kEpiQkv, M, dm.nqkv);
@@ -520,6 +537,7 @@ struct Eng {
 
     e = epi(c, kEpiResid, M, dm.d);
     e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = gain_next;
+    e.h_tap = tap; e.h_tap2 = tap2;
     EG_TRY(sink.gemm(c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e));
     return EAGLE_OK;
   }
@@ -563,8 +581,11 @@ struct Eng {
     const size_t kvl = (size_t)dm.B * dm.Hkv * dm.cap * dm.hd * sizeof(T);
     for (int l = 0; l < dm.Lyr; ++l) {
       const float* gn = l + 1 < dm.Lyr ? c->layers[l + 1].attn_norm : c->final_norm;
+      // fused-feature variant: the hidden states after the tap layers are copied out
+      float* t1 = dm.taps && l + 1 == dm.tap_low ? c->h_low + (size_t)row0 * dm.d : nullptr;
+      float* t2 = dm.taps && l + 1 == dm.tap_mid ? c->h_mid + (size_t)row0 * dm.d : nullptr;
       EG_TRY(layer(c, sink, c->layers[l], (char*)c->kc + l * kvl, (char*)c->vc + l * kvl, dm.cap, M, n_groups,
-                   c->h_tgt + (size_t)row0 * dm.d, gn, row0, groups));
+                   c->h_tgt + (size_t)row0 * dm.d, gn, row0, groups, t1, t2));
     }
     return EAGLE_OK;
   }
@@ -639,6 +660,15 @@ struct Eng {
     return EAGLE_OK;
   }
 
+  // Fused-feature variant: fused[m] = fuse [low[m] ; mid[m] ; top[m]] for M rows (one GEMM, K = 3d).
+  static eagle_status fuse_features(eagle_ctx* c, const float* low, const float* mid, const float* top, int M) {
+    const Dims& dm = c->dm;
+    EG_CK(pack_taps<T>(low, mid, top, M, dm.d, (T*)c->xfc, lo(c->xfc_lo), c->stream));
+    EpiParams e = epi(c, kEpiStore, M, dm.d);
+    e.y = c->fused;
+    return gemm(c, c->xfc, lo(c->xfc_lo), c->fuse, M, dm.d, 3 * dm.d, e);
+  }
+
   // Draft head over the phase's rows: FC([feature ; E(token)]) then the head layer, then (k > 0) LM-head top-k.
   static eagle_status draft_forward(eagle_ctx* c, const float* feat, int M, int n_groups, int hbase, int k) {
     const Dims& dm = c->dm;
@@ -672,11 +702,12 @@ struct Eng {
                              lo(c->lm_hb_lo), c->lm_ssq, c->stream));
         EG_TRY(lm_head(c, c->lm_hb, lo(c->lm_hb_lo), c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr,
                        true, c->lm_src));
-        EG_CK(prefill_finish(c->st, c->root_idx, c->h_tgt, cl, P, root_out, c->stream));
+        EG_CK(prefill_finish(c->st, c->root_idx, c->h_tgt, c->h_low, c->h_mid, cl, P, root_out, c->stream));
         EG_CK(cudaStreamSynchronize(c->stream));  // src is a host temporary
       }
       EG_CK(setup_prefill_rows(d_tokens, P, c0, cl, dm.B, true, c->rows, c->groups, c->stream));
-      EG_TRY(draft_forward(c, c->h_tgt, M, G, 0, 0));
+      if (dm.taps) EG_TRY(fuse_features(c, c->h_low, c->h_mid, c->h_tgt, M));
+      EG_TRY(draft_forward(c, dm.taps ? c->fused : c->h_tgt, M, G, 0, 0));
     }
     return EAGLE_OK;
   }
@@ -685,7 +716,8 @@ struct Eng {
     const Dims& dm = c->dm;
     const Level catchup{0, dm.D1};
     EG_CK(setup_catchup_rows(c->st, c->rows, c->groups, c->stream));
-    EG_TRY(draft_forward(c, c->st.pend_feat, dm.B * dm.D1, dm.B, 0, dm.k));
+    if (dm.taps) EG_TRY(fuse_features(c, c->st.pend_low, c->st.pend_mid, c->st.pend_feat, dm.B * dm.D1));
+    EG_TRY(draft_forward(c, dm.taps ? c->fused : c->st.pend_feat, dm.B * dm.D1, dm.B, 0, dm.k));
     for (int t = 1; t <= dm.D; ++t) {
       const Level prev = t > 1 ? Level{dm.level_base[t - 1], dm.level_rows[t - 1]} : Level{0, 0};
       const Level next = t < dm.D ? Level{dm.level_base[t], dm.level_rows[t]} : Level{0, 0};
@@ -732,7 +764,7 @@ struct Eng {
 
   static eagle_status accept(eagle_ctx* c, int* acc_out, int* tok_out) {
     const Dims& dm = c->dm;
-    EG_CK(accept_commit(c->st, c->last_tree, c->vargmax, c->h_tgt, acc_out, tok_out, c->stream));
+    EG_CK(accept_commit(c->st, c->last_tree, c->vargmax, c->h_tgt, c->h_low, c->h_mid, acc_out, tok_out, c->stream));
     using KvT = typename KvOf<T>::type;
     EG_CK(compact_kv<KvT>(c->st, (KvT*)c->kc, (KvT*)c->vc, dm.Lyr, dm.Hkv, dm.hd, c->stream));
     return EAGLE_OK;
@@ -798,7 +830,7 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
     return s;
   }
   const Dims& dm = c->dm;
-  if (!w->embed || !w->lm_head || !w->final_norm || !w->layers || !w->fc) {
+  if (!w->embed || !w->lm_head || !w->final_norm || !w->layers || !w->fc || (dm.taps && !w->fuse)) {
     delete c;
     return EAGLE_ERR_INVALID_ARG;
   }
@@ -814,6 +846,7 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
     return EAGLE_ERR_INVALID_ARG;
   }
   c->embed = w->embed; c->lm_head = w->lm_head; c->final_norm = w->final_norm; c->fc = w->fc;
+  c->fuse = dm.taps ? w->fuse : nullptr;
   const Offsets o = plan(dm);
   if (!d_ws || ws_bytes < o.total || (reinterpret_cast<uintptr_t>(d_ws) % kAlign)) {
     delete c;
@@ -827,6 +860,9 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->groups = (Group*)P(o.groups);
   c->groups_local = (Group*)P(o.groups_local);
   c->h_tgt = (float*)P(o.h_tgt); c->h_dft = (float*)P(o.h_dft); c->hb = P(o.hb);
+  if (dm.taps) {
+    c->h_low = (float*)P(o.h_low); c->h_mid = (float*)P(o.h_mid); c->fused = (float*)P(o.fused);
+  }
   c->ssq_a = (float*)P(o.ssq_a); c->ssq_b = (float*)P(o.ssq_b);
   c->q = P(o.q); c->qg = (__half*)P(o.qg); c->attn = P(o.attn); c->act = P(o.act); c->xfc = P(o.xfc);
   c->lm_hb = P(o.lm_hb); c->lm_ssq = (float*)P(o.lm_ssq); c->lm_src = (int*)P(o.lm_src);
@@ -841,7 +877,9 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->vtree = TreeOut{1, (int*)P(o.vt_tok), (int*)P(o.vt_par), (int*)P(o.vt_dep), (uint64_t*)P(o.vt_anc), nullptr};
   State& st = c->st;
   st.L = (int*)P(o.L); st.c = (int*)P(o.c); st.root = (int*)P(o.root); st.pend_tok = (int*)P(o.pend_tok);
-  st.pend_feat = (float*)P(o.pend_feat); st.n_out = (int*)P(o.n_out); st.out = (int*)P(o.out);
+  st.pend_feat = (float*)P(o.pend_feat);
+  st.pend_low = dm.taps ? (float*)P(o.pend_low) : nullptr;
+  st.pend_mid = dm.taps ? (float*)P(o.pend_mid) : nullptr; st.n_out = (int*)P(o.n_out); st.out = (int*)P(o.out);
   st.acc_len = (int*)P(o.acc_len); st.acc_path = (int*)P(o.acc_path); st.L_prev = (int*)P(o.L_prev);
   st.hist = (unsigned long long*)P(o.hist); st.status = (int*)P(o.status);
   st.B = dm.B; st.D1 = dm.D1; st.d = dm.d; st.cap = dm.cap; st.cap_d = dm.cap_d; st.out_cap = dm.out_cap;
@@ -1159,5 +1197,16 @@ eagle_status eagle_destroy(eagle_ctx* c) {
 }
 
 const char* eagle_last_error(const eagle_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+size_t eagle_struct_size(int32_t which) {
+  switch (which) {
+    case 0: return sizeof(eagle_config);
+    case 1: return sizeof(eagle_weights);
+    case 2: return sizeof(eagle_layer_weights);
+    case 3: return sizeof(eagle_tree);
+    case 4: return sizeof(eagle_stats);
+    default: return 0;
+  }
+}
 
 }  // extern "C"

@@ -123,6 +123,8 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
   void* const hb = p.hb;
   float* const ssq_out = p.ssq_out;
   const float* const gain = p.gain;
+  float* const h_tap = p.h_tap;
+  float* const h_tap2 = p.h_tap2;
   const int topk = p.topk;
   const float inv_temp = p.inv_temp;
   const unsigned long long seed = p.seed;
@@ -225,6 +227,8 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
             const size_t at = (size_t)(m0 + m) * N + n;
             const float hn = hv[q] + tile[m * ldt + c] * rscale[m];
             h[at] = hn;
+            if (h_tap) h_tap[at] = hn;
+            if (h_tap2) h_tap2[at] = hn;
             store_hilo<T>(reinterpret_cast<T*>(hb), hb_lo, at, hn * gn);
             tile[m * ldt + c] = hn * hn;
           }

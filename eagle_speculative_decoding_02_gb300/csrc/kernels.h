@@ -60,6 +60,10 @@ cudaError_t embed_rows(const T* E, const int* tok, int M, int d, const float* ga
 template <typename T>
 cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* tok, int M, int d, T* x, bf16* x_lo,
                      cudaStream_t s);
+// x[m] = [low[m] ; mid[m] ; top[m]] for m < M (3d wide; hi/lo pair when x_lo is given).
+template <typename T>
+cudaError_t pack_taps(const float* low, const float* mid, const float* top, int M, int d, T* x, bf16* x_lo,
+                      cudaStream_t s);
 // Copy rows src[i] of (hb, hb_lo, ssq) to rows i of (hb_dst, lo_dst, ssq_dst); the lo pointers may be NULL.
 template <typename T>
 cudaError_t gather_rows(const T* hb, const bf16* hb_lo, const float* ssq, int M_src, const int* src, int n, int d,

@@ -38,6 +38,22 @@ __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ E, con
   }
 }
 
+// Input rows of the fused-feature matrix: x[m] = [low[m] ; mid[m] ; top[m]] (3d
+// wide), as a hi/lo pair for bf16 models.
+template <typename T>
+__global__ void pack_taps_kernel(const float* __restrict__ low, const float* __restrict__ mid,
+                                 const float* __restrict__ top, int d, T* x, bf16* x_lo) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t m = blockIdx.x;
+  const size_t row = m * 3 * d;
+  for (int n = threadIdx.x; n < d; n += blockDim.x) {
+    store_hilo<T>(x, x_lo, row + n, low[m * d + n]);
+    store_hilo<T>(x, x_lo, row + d + n, mid[m * d + n]);
+    store_hilo<T>(x, x_lo, row + 2 * d + n, top[m * d + n]);
+  }
+}
+
 // x[m] = [ feat[fsrc[m]] ; E[tok[m]] ] (length 2d); the float feature half is
 // stored as a hi/lo pair when x_lo is given, the embedding half is exact.
 template <typename T>
@@ -226,6 +242,13 @@ cudaError_t fc_input(const float* feat, const int* fsrc, const T* E, const int* 
 }
 
 template <typename T>
+cudaError_t pack_taps(const float* low, const float* mid, const float* top, int M, int d, T* x, bf16* x_lo,
+                      cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  return launch_pdl(pack_taps_kernel<T>, dim3(M), dim3(256), 0, s, low, mid, top, d, x, x_lo);
+}
+
+template <typename T>
 cudaError_t gather_rows(const T* hb, const bf16* hb_lo, const float* ssq, int M_src, const int* src, int n, int d,
                         T* hb_dst, bf16* lo_dst, float* ssq_dst, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
@@ -243,6 +266,7 @@ cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* re
                                      cudaStream_t);                                                         \
   template cudaError_t fc_input<T>(const float*, const int*, const T*, const int*, int, int, T*, bf16*,      \
                                    cudaStream_t);                                                           \
+  template cudaError_t pack_taps<T>(const float*, const float*, const float*, int, int, T*, bf16*, cudaStream_t); \
   template cudaError_t gather_rows<T>(const T*, const bf16*, const float*, int, const int*, int, int, T*, bf16*, \
                                       float*, cudaStream_t);
 EG_INST(float)

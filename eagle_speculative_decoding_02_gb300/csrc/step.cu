@@ -161,13 +161,20 @@ __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* gr
 
 // After the last prefill chunk: first new token per sequence and the initial state.
 __global__ void prefill_finish_kernel(State st, const int* __restrict__ root_idx, const float* __restrict__ h_tgt,
-                                      int CL, int P, int* root_out) {
+                                      const float* __restrict__ h_low, const float* __restrict__ h_mid, int CL, int P,
+                                      int* root_out) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
   const int root = root_idx[b];
-  const float* f = h_tgt + ((size_t)b * CL + CL - 1) * st.d;
-  for (int n = threadIdx.x; n < st.d; n += blockDim.x) st.pend_feat[(size_t)b * st.D1 * st.d + n] = f[n];
+  const size_t src = ((size_t)b * CL + CL - 1) * st.d, dst = (size_t)b * st.D1 * st.d;
+  for (int n = threadIdx.x; n < st.d; n += blockDim.x) {
+    st.pend_feat[dst + n] = h_tgt[src + n];
+    if (st.pend_low) {
+      st.pend_low[dst + n] = h_low[src + n];
+      st.pend_mid[dst + n] = h_mid[src + n];
+    }
+  }
   if (threadIdx.x == 0) {
     st.L[b] = P;
     st.c[b] = 1;
@@ -500,8 +507,9 @@ __global__ void __launch_bounds__(256) eagle2_final_kernel(State st, Pool pool, 
 
 // ---------------------------------------------------------------- accept / commit
 __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, const int* __restrict__ amax,
-                                                     const float* __restrict__ h_verify, int* acc_out,
-                                                     int* tok_out) {
+                                                     const float* __restrict__ h_verify,
+                                                     const float* __restrict__ h_low, const float* __restrict__ h_mid,
+                                                     int* acc_out, int* tok_out) {
   pdl_wait();
   pdl_trigger();
   __shared__ int path[kMaxDepth + 1];
@@ -563,7 +571,12 @@ __global__ void __launch_bounds__(256) accept_kernel(State st, TreeOut tree, con
   // committed features: root and accepted nodes
   for (int e = tid; e < (a + 1) * st.d; e += blockDim.x) {
     const int t = e / st.d, n = e % st.d;
-    st.pend_feat[((size_t)b * st.D1 + t) * st.d + n] = h_verify[((size_t)base + path[t]) * st.d + n];
+    const size_t dst = ((size_t)b * st.D1 + t) * st.d + n, src = ((size_t)base + path[t]) * st.d + n;
+    st.pend_feat[dst] = h_verify[src];
+    if (st.pend_low) {
+      st.pend_low[dst] = h_low[src];
+      st.pend_mid[dst] = h_mid[src];
+    }
   }
   if (tid == 0) {
     const int n0 = st.n_out[b];
@@ -642,9 +655,10 @@ cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, 
   return launch_pdl(setup_verify_kernel, dim3(st.B), dim3(128), 0, s, st, tree, rows, groups, groups_local, spc);
 }
 
-cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, int CL, int P, int* root_out,
-                           cudaStream_t s) {
-  return launch_pdl(prefill_finish_kernel, dim3(st.B), dim3(256), 0, s, st, root_idx, h_tgt, CL, P, root_out);
+cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, const float* h_low,
+                           const float* h_mid, int CL, int P, int* root_out, cudaStream_t s) {
+  return launch_pdl(prefill_finish_kernel, dim3(st.B), dim3(256), 0, s, st, root_idx, h_tgt, h_low, h_mid, CL, P,
+                    root_out);
 }
 
 cudaError_t set_root_tree(State st, TreeOut tree, cudaStream_t s) {
@@ -670,9 +684,10 @@ cudaError_t eagle2_final(State st, Pool pool, int n_nodes, int n_min, float ln_t
   return launch_pdl(eagle2_final_kernel, dim3(st.B), dim3(256), 0, s, st, pool, n_nodes, n_min, ln_tau, tree);
 }
 
-cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, int* acc_out,
-                          int* tok_out, cudaStream_t s) {
-  return launch_pdl(accept_kernel, dim3(st.B), dim3(256), 0, s, st, tree, amax, h_verify, acc_out, tok_out);
+cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, const float* h_low,
+                          const float* h_mid, int* acc_out, int* tok_out, cudaStream_t s) {
+  return launch_pdl(accept_kernel, dim3(st.B), dim3(256), 0, s, st, tree, amax, h_verify, h_low, h_mid, acc_out,
+                    tok_out);
 }
 
 template <typename T>

@@ -14,6 +14,8 @@ struct State {
   int* root;        // [B] x_L: committed, not yet in the KV cache
   int* pend_tok;    // [B][D1] t_{L-c+1} .. t_L
   float* pend_feat; // [B][D1][d] target features f_{L-c} .. f_{L-1}
+  float* pend_low;  // fused-feature variant: the low and mid taps of the same rows (NULL otherwise)
+  float* pend_mid;
   int* n_out;       // [B] committed tokens
   int* out;         // [B][out_cap]
   int* acc_len;     // [B] accepted draft length of the last commit
@@ -78,8 +80,8 @@ cudaError_t setup_catchup_rows(State st, Rows rows, Group* groups, cudaStream_t 
 // its verify launch (launches of spc sequences each; spc = 0: one launch).
 cudaError_t setup_verify_rows(State st, TreeOut tree, Rows rows, Group* groups, Group* groups_local, int spc,
                               cudaStream_t s);
-cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, int CL, int P, int* root_out,
-                           cudaStream_t s);
+cudaError_t prefill_finish(State st, const int* root_idx, const float* h_tgt, const float* h_low,
+                           const float* h_mid, int CL, int P, int* root_out, cudaStream_t s);
 cudaError_t set_root_tree(State st, TreeOut tree, cudaStream_t s);
 
 // Static tree: assign the tokens of depth-t nodes from their parents' top-k
@@ -101,8 +103,9 @@ cudaError_t eagle2_final(State st, Pool pool, int n_nodes, int n_min, float ln_t
 // Greedy accept over the verified tree; commit tokens and features, advance L.
 // A path longer than D1 - 1 nodes (only a caller-built tree can hold one) is
 // not cut short: nothing is committed and kStInvalid is recorded.
-cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, int* acc_out,
-                          int* tok_out, cudaStream_t s);
+// h_low / h_mid (used when st.pend_low is set): the verify rows' low and mid taps.
+cudaError_t accept_commit(State st, TreeOut tree, const int* amax, const float* h_verify, const float* h_low,
+                          const float* h_mid, int* acc_out, int* tok_out, cudaStream_t s);
 // Move accepted K/V rows to contiguous slots in every layer.
 template <typename T>
 cudaError_t compact_kv(State st, T* kc, T* vc, int n_layers, int n_kv, int hd, cudaStream_t s);

@@ -37,6 +37,7 @@ class ModelWeights:
     layers: list[LayerWeights]
     fc: torch.Tensor
     head: LayerWeights
+    fuse: torch.Tensor | None = None   # [d, 3d] fused-feature matrix (feature_taps = 3)
 
 
 def pack_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
@@ -80,7 +81,8 @@ class EagleEngine:
 
     def __init__(self, *, n_layers, d, n_heads, n_kv_heads, head_dim, ffn, vocab, rope_theta, rms_eps, bf16,
                  batch, kv_cap, max_prompt, max_new, tree_mode, n_nodes, static_parent=None, static_rank=None,
-                 top_k=10, depth=6, tau=0.3, temperature=0.0, seed=0, n_nodes_min=0, weights: ModelWeights,
+                 top_k=10, depth=6, tau=0.3, temperature=0.0, seed=0, n_nodes_min=0, feature_taps=1,
+                 weights: ModelWeights,
                  device="cuda", stream=None):
         self.lib = L.load()
         self.device = torch.device(device)
@@ -96,7 +98,7 @@ class EagleEngine:
                                  L.DTYPE_BF16 if bf16 else L.DTYPE_F32, batch, kv_cap, max_prompt, max_new,
                                  tree_mode, n_nodes, C.cast(sp, C.POINTER(C.c_int32)) if sp else None,
                                  C.cast(sr, C.POINTER(C.c_int32)) if sr else None, top_k, depth, tau,
-                                 float(temperature), int(seed), int(n_nodes_min))
+                                 float(temperature), int(seed), int(n_nodes_min), int(feature_taps))
         nbytes = C.c_size_t(0)
         L.check("eagle_workspace_size", self.lib.eagle_workspace_size(C.byref(self.cfg), C.byref(nbytes)))
         self.workspace = torch.empty(int(nbytes.value), dtype=torch.uint8, device=self.device)
@@ -104,7 +106,8 @@ class EagleEngine:
         layers = (L.EagleLayerWeights * n_layers)(*[lw.c() for lw in weights.layers])
         self._keep.append(layers)
         self.cw = L.EagleWeights(weights.embed.data_ptr(), weights.lm_head.data_ptr(),
-                                 weights.final_norm.data_ptr(), layers, weights.fc.data_ptr(), weights.head.c())
+                                 weights.final_norm.data_ptr(), layers, weights.fc.data_ptr(), weights.head.c(),
+                                 weights.fuse.data_ptr() if weights.fuse is not None else None)
         # a dedicated stream: the legacy default stream cannot be captured into a CUDA graph
         self.stream = stream if stream is not None else torch.cuda.Stream(self.device)
         ctx = C.c_void_p()

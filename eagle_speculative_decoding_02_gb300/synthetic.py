@@ -17,10 +17,10 @@ from .engine import EagleEngine, ModelWeights, pack_layer
 from .topology import named
 
 
-def device_weights(m: FX.ModelShape, device="cuda") -> ModelWeights:
-    g = FD.generate_model(m, pack_layer, device=device)
+def device_weights(m: FX.ModelShape, device="cuda", taps: int = 1) -> ModelWeights:
+    g = FD.generate_model(m, pack_layer, device=device, taps=taps)
     return ModelWeights(embed=g["embed"], lm_head=g["lm_head"], final_norm=g["final_norm"], layers=g["layers"],
-                        fc=g["fc"], head=g["head"])
+                        fc=g["fc"], head=g["head"], fuse=g.get("fuse"))
 
 
 def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: int | None = None,
@@ -29,7 +29,7 @@ def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: i
                 device="cuda") -> EagleEngine:
     m = w.model
     if weights is None:
-        weights = device_weights(m, device)
+        weights = device_weights(m, device, taps=w.feature_taps)
     batch = batch or w.batch
     max_new = max_new or w.max_new
     prompt_len = prompt_len or w.prompt_len
@@ -39,7 +39,7 @@ def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: i
     kw = dict(n_layers=m.n_layers, d=m.d, n_heads=m.n_heads, n_kv_heads=m.n_kv_heads, head_dim=m.head_dim,
               ffn=m.ffn, vocab=m.vocab, rope_theta=m.rope_theta, rms_eps=m.rms_eps, bf16=m.bf16, batch=batch,
               kv_cap=cap, max_prompt=prompt_len, max_new=max_new, weights=weights, device=device,
-              temperature=temperature, seed=seed)
+              temperature=temperature, seed=seed, feature_taps=w.feature_taps)
     if tree == "static":
         parent, rank = named(w.static_tree)
         return EagleEngine(tree_mode=L.TREE_STATIC, n_nodes=len(parent) - 1, static_parent=parent,

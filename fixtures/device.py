@@ -70,8 +70,9 @@ def head_tensor(m: FX.ModelShape, name: str, device="cuda") -> torch.Tensor:
                        noise_std=0.1 * m.init_std)
 
 
-def generate_model(m: FX.ModelShape, pack_layer, device="cuda"):
-    """Yield (kind, value): ("embed"|"lm_head"|"final_norm"|"fc", tensor), ("layer", l, packed), ("head", packed).
+def generate_model(m: FX.ModelShape, pack_layer, device="cuda", taps: int = 1):
+    """The model's tensors: "embed", "lm_head", "final_norm", "fc", "layers" (packed), "head" (packed) and,
+    with taps = 3, the fused-feature matrix "fuse".
 
     Layers are generated and packed one at a time, so the peak extra memory is one layer.
     """
@@ -84,6 +85,8 @@ def generate_model(m: FX.ModelShape, pack_layer, device="cuda"):
         del t
     h = {k: head_tensor(m, k, device=device) for k in FX.layer_shapes(m)}
     out["head"] = pack_layer(**h, attn_norm=ones.clone(), ffn_norm=ones.clone())
+    if taps == 3:
+        out["fuse"] = head_tensor(m, "fuse", device=device)
     return out
 
 

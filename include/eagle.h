@@ -119,6 +119,14 @@ typedef struct {
    * and at most n_nodes of them (its tree's remaining rows are padding rows with
    * token -1); 0 = every sequence verifies n_nodes. */
   int32_t n_nodes_min;
+  /* The feature the draft head takes for committed positions ([LPD], the
+   * EAGLE-3 entry: the draft fuses low-, mid- and high-level target features;
+   * the page gives no layer choice, read here as): 0 or 1 = the target's top-layer
+   * feature (EAGLE, EAGLE-2); 3 = u = fuse [f_low ; f_mid ; f_top], the hidden
+   * states after target layers max(1, n_layers/4), max(1, n_layers/2) and
+   * n_layers (eagle_weights.fuse is then required). The target's own logits
+   * always come from its top-layer feature. */
+  int32_t feature_taps;
 } eagle_config;
 
 /* Device pointers of one decoder layer. Matrices are row-major [out, in]
@@ -141,6 +149,7 @@ typedef struct {
   const eagle_layer_weights* layers;   /* host array of n_layers entries */
   const void* fc;                      /* draft head FC [d, 2d] over [feature ; E(next token)] */
   eagle_layer_weights head;            /* draft head decoder layer */
+  const void* fuse;                    /* feature_taps = 3: [d, 3d] over [f_low ; f_mid ; f_top]; else unused */
 } eagle_weights;
 
 /* A draft tree per sequence, BFS order, row 0 = root. Device arrays.
@@ -265,6 +274,11 @@ eagle_status eagle_committed_counts(eagle_ctx* ctx, int32_t* d_counts);
 
 eagle_status eagle_destroy(eagle_ctx* ctx);
 const char* eagle_last_error(const eagle_ctx* ctx);
+
+/* sizeof of the ABI structs, for bindings to check their own layouts against:
+ * which = 0 eagle_config, 1 eagle_weights, 2 eagle_layer_weights, 3 eagle_tree,
+ * 4 eagle_stats; 0 for any other value. Host-only. */
+size_t eagle_struct_size(int32_t which);
 
 /* ---------------------------------------------------------------------------
  * Kernel-level entry points: one hot-path kernel on caller buffers, for unit

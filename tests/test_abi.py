@@ -121,6 +121,35 @@ def test_init_rejects_small_or_misaligned_workspace_before_any_cuda_call(lib):
     assert not ctx.value
 
 
+def test_binding_structs_match_the_library(lib):
+    for which, st in enumerate((L.EagleConfig, L.EagleWeights, L.EagleLayerWeights, L.EagleTree, L.EagleStats)):
+        assert lib.eagle_struct_size(which) == C.sizeof(st), st.__name__
+    assert lib.eagle_struct_size(5) == 0
+
+
+def test_fused_features_config(lib):
+    """feature_taps: 0/1 = top-layer feature, 3 = fused low / mid / high features (needs eagle_weights.fuse)."""
+    w = FX.WORKLOADS["tiny_static"]
+    sizes = {}
+    for taps in (0, 1, 3):
+        cfg, keep = _cfg(w, feature_taps=taps)
+        n = C.c_size_t(0)
+        assert lib.eagle_workspace_size(C.byref(cfg), C.byref(n)) == 0
+        sizes[taps] = n.value
+    assert sizes[0] == sizes[1] < sizes[3]
+    for bad in (2, 4, -1):
+        cfg, keep = _cfg(w, feature_taps=bad)
+        assert lib.eagle_workspace_size(C.byref(cfg), C.byref(C.c_size_t(0))) == 1
+    # no fusion matrix: refused before any CUDA call
+    cfg, keep = _cfg(w, feature_taps=3)
+    lw = L.EagleLayerWeights(*([256] * 6))
+    layers = (L.EagleLayerWeights * 2)(lw, lw)
+    wts = L.EagleWeights(256, 256, 256, layers, 256, lw, None)
+    ctx = C.c_void_p()
+    assert lib.eagle_init(C.byref(cfg), C.byref(wts), C.c_void_p(1 << 20), sizes[3], None, C.byref(ctx)) == 1
+    assert not ctx.value
+
+
 def test_no_alloc_and_selftest_symbols_reject_null_arguments_on_the_host(lib):
     assert lib.eagle_op_gemm_noalloc(0, 128, 64, None, None, None, None) == 1
     assert lib.eagle_selftest_bounded_wait(None, None) == 1
