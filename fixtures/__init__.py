@@ -26,6 +26,16 @@ Generator definition (identical on both sides):
   noise: ``float32(s * z_target + 0.1 * s * z_noise)`` computed in float64,
   with ``s`` the init std of that tensor (0.02).
 * Token j of prompt b: ``(word(key(seed, PROMPT + b), j) >> 32) * V >> 32``.
+* Weight-only int4 projections (models with ``weight_bits = 4``; the target's
+  decoder layers only): a projection [N, K] is stored as codes, two 4-bit codes
+  per byte (byte (n, i) holds code (n, 2i) in its low and (n, 2i + 1) in its
+  high nibble), and a scale per row and group of 64 inputs. Code (n, k) is
+  ``1 + ((word(key(seed, INT4 + 16 l + kind), n K + k) >> 32) * 15 >> 32)``,
+  uniform in [1, 15]; scale (n, g) is ``bf16(float32(b (0.75 + 0.5 r)))`` with
+  ``r = (word(key(seed, INT4_SCALE + 16 l + kind), n K/64 + g) >> 11) 2^-53`` and
+  ``b = init_std / sqrt(56/3)`` (the codes minus 8 have variance 56/3), so that
+  the weights have about the init std. (What a code and a scale mean is the
+  weight format's definition, not part of this recipe.)
 
 Shapes follow the workloads: a tiny fp32 2-layer model and Llama-3-8B /
 Llama-3-70B shaped bf16 models with a one-layer EAGLE head (FC over
@@ -52,6 +62,9 @@ CODE_PROMPT = 500_000          # + sequence index
 CODE_LAYER = 1_000             # + 16 * layer + kind
 CODE_HEAD_NOISE = 900_000      # + kind
 CODE_HEAD_FUSE = 950_000
+CODE_INT4 = 2_000_000          # + 16 * layer + kind: 4-bit codes
+CODE_INT4_SCALE = 3_000_000    # + 16 * layer + kind: group scales
+INT4_GROUP = 64
 KIND = {"wq": 0, "wk": 1, "wv": 2, "wo": 3, "wg": 4, "wu": 5, "wd": 6}
 
 
@@ -186,6 +199,7 @@ class ModelShape:
     lm_head_std: float = 0.02
     init_std: float = 0.02
     seed: int = 1
+    weight_bits: int = 16      # 4: the target's decoder-layer projections are int4 codes + group scales
 
     @property
     def q_dim(self) -> int:
@@ -288,6 +302,44 @@ def head_tensor(m: ModelShape, name: str) -> np.ndarray:
     flat = normal(layer_key(m, m.n_layers - 1, name), shape[0] * shape[1], m.init_std, bf16=m.bf16,
                   noise_key=stream_key(m.seed, CODE_HEAD_NOISE + KIND[name]), noise_std=0.1 * m.init_std)
     return flat.reshape(shape)
+
+
+def int4_scale_base(m: ModelShape) -> float:
+    return m.init_std / float(np.sqrt(56.0 / 3.0))
+
+
+def int4_codes(m: ModelShape, layer: int, name: str) -> np.ndarray:
+    """Packed 4-bit codes of a target projection: uint8 [N, K/2], low nibble = even input index."""
+    n, k = layer_shapes(m)[name]
+    key = stream_key(m.seed, CODE_INT4 + 16 * layer + KIND[name])
+    out = np.empty((n, k // 2), dtype=np.uint8)
+    rows = max(1, _CHUNK // k)
+
+    def job(r0: int) -> None:
+        r1 = min(n, r0 + rows)
+        w = words(key, r0 * k, (r1 - r0) * k)
+        with np.errstate(over="ignore"):
+            c = (np.uint64(1) + (((w >> np.uint64(32)) * np.uint64(15)) >> np.uint64(32))).astype(np.uint8)
+        c = c.reshape(r1 - r0, k)
+        out[r0:r1] = c[:, 0::2] | (c[:, 1::2] << np.uint8(4))
+
+    starts = range(0, n, rows)
+    if n > rows:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(job, starts))
+    else:
+        for r0 in starts:
+            job(r0)
+    return out
+
+
+def int4_scales(m: ModelShape, layer: int, name: str) -> np.ndarray:
+    """Group scales of a target projection: float32 [N, K/64], each a bfloat16 value."""
+    n, k = layer_shapes(m)[name]
+    g = k // INT4_GROUP
+    w = words(stream_key(m.seed, CODE_INT4_SCALE + 16 * layer + KIND[name]), 0, n * g)
+    r = (w >> np.uint64(11)).astype(np.float64) * TWO_M53
+    return round_bf16((int4_scale_base(m) * (0.75 + 0.5 * r)).astype(np.float32)).reshape(n, g)
 
 
 def prompts(m: ModelShape, batch: int, length: int) -> np.ndarray:

@@ -36,6 +36,7 @@ import numpy as np
 
 import fixtures as FX
 
+from . import quant
 from .core import F32, apply_rope, attention_rows, log_softmax, rmsnorm, rope_tables, silu
 
 
@@ -72,12 +73,18 @@ def _ones(n: int) -> np.ndarray:
 
 def build_model(shape: FX.ModelShape, max_pos: int, taps: int = 1) -> Model:
     """Materialise the seeded weights of ``shape`` (norm gains are 1, no biases); taps = 3 adds the
-    fused-feature matrix."""
+    fused-feature matrix. With shape.weight_bits = 4 the target's decoder-layer projections are the
+    dequantised int4 codes and scales (oracle/quant.py)."""
     def layer(get) -> LayerWeights:
         return LayerWeights(**{k: get(k) for k in FX.layer_shapes(shape)},
                             attn_norm=_ones(shape.d), ffn_norm=_ones(shape.d))
 
-    layers = [layer(lambda k, l=l: FX.target_tensor(shape, k, l)) for l in range(shape.n_layers)]
+    def target(k: str, l: int) -> np.ndarray:
+        if shape.weight_bits == 4:
+            return quant.dequantize(FX.int4_codes(shape, l, k), FX.int4_scales(shape, l, k))
+        return FX.target_tensor(shape, k, l)
+
+    layers = [layer(lambda k, l=l: target(k, l)) for l in range(shape.n_layers)]
     head = layer(lambda k: FX.head_tensor(shape, k))
     cos, sin = rope_tables(shape.rope_theta, shape.head_dim, max_pos)
     return Model(shape=shape, embed=FX.target_tensor(shape, "embed"),
