@@ -112,10 +112,11 @@ def verify_flops(m, batch: int, L: int, rows: int) -> int:
 
 
 def verify_bytes(m, batch: int, L: int, rows: int) -> int:
-    """Algorithmic HBM bytes of one verify pass: every weight once, the KV prefix read once per layer,
-    the new K/V rows written (bf16)."""
+    """Algorithmic HBM bytes of one verify pass: every weight once (int4 layers: half a byte per weight
+    plus a bf16 scale per 64), the KV prefix read once per layer, the new K/V rows written (16-bit)."""
     per_layer = (m.q_dim + 2 * m.kv_dim) * m.d + m.d * m.q_dim + 2 * m.ffn * m.d + m.d * m.ffn
-    weights = m.n_layers * per_layer * 2 + m.vocab * m.d * 2
+    layer_bytes = per_layer // 2 + per_layer // 64 * 2 if m.weight_bits == 4 else per_layer * 2
+    weights = m.n_layers * layer_bytes + m.vocab * m.d * 2
     kv_read = m.n_layers * batch * L * 2 * m.kv_dim * 2
     kv_write = m.n_layers * batch * rows * 2 * m.kv_dim * 2
     return weights + kv_read + kv_write
@@ -124,7 +125,7 @@ def verify_bytes(m, batch: int, L: int, rows: int) -> int:
 # Sources of the persistent verify kernel: a DRAM-traffic figure in profiles/ counts
 # only while these are unchanged since its capture.
 KERNEL_SOURCES = ["stack_tc.cu", "stack.h", "attention_umma.cuh", "attention_tc.cuh", "epilogue.cuh", "tc_ptx.cuh",
-                  "common.cuh", "kernels.h", "engine.cu"]
+                  "common.cuh", "kernels.h", "engine.cu", "int4.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "stack_tc_kernel_8b_eagle2_verify_traffic.txt")
 
 
@@ -265,6 +266,8 @@ def main():
     ap.add_argument("--workload", default="8b_eagle2")
     ap.add_argument("--feature-taps", type=int, default=0, choices=[0, 1, 3],
                     help="3: the fused low / mid / high feature variant of the workload")
+    ap.add_argument("--weight-bits", type=int, default=16, choices=[4, 16],
+                    help="4: the workload with weight-only int4 target projections")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -284,6 +287,9 @@ def main():
     w = FX.WORKLOADS[args.workload]
     if args.feature_taps == 3:
         w = dataclasses.replace(w, name=f"{w.name}, fused low/mid/high features", feature_taps=3)
+    if args.weight_bits == 4:
+        w = dataclasses.replace(w, name=f"{w.name}, int4 target weights",
+                                model=dataclasses.replace(w.model, weight_bits=4))
     if args.layers and args.profile_verify:
         w = dataclasses.replace(w, name=f"{w.name}-{args.layers}layers",
                                 model=dataclasses.replace(w.model, n_layers=args.layers))
@@ -401,11 +407,12 @@ def main():
     spc = 128 // rows
     n_chunks = -(-w.batch // spc) if spc else 0
     persistent = w.batch * rows <= 128 or 0 < n_chunks <= 2
-    kernel = (("stack_tc_kernel (verify program)" if n_chunks <= 1 else
+    variant = ", int4 variant: packed blocks expanded in shared memory" if m.weight_bits == 4 else ""
+    kernel = ((f"stack_tc_kernel (verify program{variant})" if n_chunks <= 1 else
                f"stack_tc_kernel (verify program, {n_chunks} launches over halves of the batch)") if persistent else
               "verify pass: gemm_tc_kernel per projection + attn_tc_kernel / attn_merge_kernel per layer")
-    traffic = (captured_traffic() if (persistent and args.workload == "8b_eagle2" and w.feature_taps != 3)
-               else None)
+    traffic = (captured_traffic() if (persistent and args.workload == "8b_eagle2" and w.feature_taps != 3
+                                       and m.weight_bits == 16) else None)
     if tensor_bound:
         ach = vf / v_ms / 1e9
         roof = {"bound": "tensor", "achieved": ach, "peak": tflops_sus, "unit": "TFLOP/s", "frac": ach / tflops_sus,
@@ -451,6 +458,7 @@ def main():
                 "uniform random prompt tokens)",
                 "config": {"workload": w.name, "batch": w.batch, "prompt": w.prompt_len,
                            "feature": "fused low/mid/high" if w.feature_taps == 3 else "top layer",
+                           "target_weights": "int4 (bf16 scale per 64)" if m.weight_bits == 4 else "bf16",
                            "tree": f"{w.tree} top_k={w.top_k} depth={w.depth} tau={w.tau} nodes={w.n_nodes}",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "l2": "no flush: every step streams the whole target and head weights "

@@ -28,7 +28,7 @@ class EagleConfig(C.Structure):
                 ("n_nodes", C.c_int32), ("static_parent", C.POINTER(C.c_int32)),
                 ("static_rank", C.POINTER(C.c_int32)), ("top_k", C.c_int32), ("depth", C.c_int32),
                 ("tau", C.c_float), ("temperature", C.c_float), ("seed", C.c_uint64), ("n_nodes_min", C.c_int32),
-                ("feature_taps", C.c_int32)]
+                ("feature_taps", C.c_int32), ("weight_bits", C.c_int32)]
 
 
 class EagleLayerWeights(C.Structure):
@@ -72,6 +72,9 @@ SIGNATURES = {
     "eagle_destroy": (C.c_int, [C.c_void_p]),
     "eagle_last_error": (C.c_char_p, [C.c_void_p]),
     "eagle_struct_size": (C.c_size_t, [C.c_int32]),
+    "eagle_int4_packed_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "eagle_int4_pack": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
+    "eagle_op_int4_dequant": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "eagle_op_gemm_scratch_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "eagle_op_gemm": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),

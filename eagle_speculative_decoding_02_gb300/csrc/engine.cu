@@ -34,6 +34,7 @@ struct LayerPtrs {
   const void* wd;
   const float* attn_norm;
   const float* ffn_norm;
+  bool w4 = false;  // the four projections are packed int4 blocks (int4.cuh)
 };
 
 // Host-derived sizes of a configuration.
@@ -45,6 +46,7 @@ struct ProgSpec {
   int row0 = 0, seq0 = 0, n_seq = 0;            // verify: its rows and sequences (a chunk of the batch)
   int n_phases = 0, n_counters = 0, first = 0;  // first: index of its first phase in the program array
   int first_attn = -1;                          // its first attention phase (set when it is built)
+  bool w4 = false;                              // has int4 phases (set when it is built)
 };
 
 struct Dims {
@@ -62,6 +64,7 @@ struct Dims {
   bool taps = false;                // fused-feature variant: the draft takes fuse [f_low ; f_mid ; f_top]
   int tap_low = 0, tap_mid = 0;     // ... with f_low, f_mid the hidden states after these target layers (1-based)
   int M_fused = 0;                  // rows of the fused-feature buffer
+  bool w4 = false;                  // weight-only int4 target projections
   unsigned long long seed = 0;      // sampler seed
   // static topology (host)
   std::vector<int> s_parent, s_rank, s_depth, s_lrow, s_sidx, s_level_nodes, s_level_count;
@@ -146,6 +149,7 @@ struct eagle_ctx {
   void* vc_d = nullptr;
   void* gemm_scratch = nullptr;
   size_t gemm_scratch_bytes = 0;
+  void* w4_dense = nullptr;  // int4 targets, per-operation path: the current projection expanded to dtype
   float* attn_part = nullptr;
   eg::StackPhase* stack_prog = nullptr;  // every program's phases, back to back
   void* stack_scratch = nullptr;
@@ -206,6 +210,13 @@ eagle_status derive(const eagle_config& cfg, Dims& dm, std::string& why) {
   if (cfg.n_nodes < 1 || cfg.n_nodes + 1 > kMaxTreeRows) return bad("n_nodes must be in 1..120");
   if (cfg.feature_taps != 0 && cfg.feature_taps != 1 && cfg.feature_taps != 3) return bad("feature_taps must be 0, 1 or 3");
   dm.taps = cfg.feature_taps == 3;
+  if (cfg.weight_bits != 0 && cfg.weight_bits != 16 && cfg.weight_bits != 4) return bad("weight_bits must be 0, 16 or 4");
+  dm.w4 = cfg.weight_bits == 4;
+  if (dm.w4 && (cfg.d % 64 || (cfg.n_heads * cfg.head_dim) % 64 || cfg.ffn % 64 ||
+                ((cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim) % 128)) {
+    why = "int4 weights need d, n_heads * head_dim and ffn to be multiples of 64";
+    return EAGLE_ERR_UNSUPPORTED;
+  }
   dm.tap_low = std::max(1, dm.taps ? cfg.n_layers / 4 : 0);
   dm.tap_mid = std::max(1, dm.taps ? cfg.n_layers / 2 : 0);
   dm.NR = cfg.n_nodes + 1;
@@ -354,7 +365,7 @@ struct Offsets {
   size_t L, c, root, pend_tok, pend_feat, pend_low, pend_mid, n_out, out, acc_len, acc_path, L_prev, hist, status;
   size_t p_score, p_token, p_parent, p_depth, p_cid, p_frow, p_smask, p_count, p_front, p_nfront;
   size_t s_parent, s_rank, s_depth, s_lrow, s_sidx, s_smask, s_lnodes, s_lcount;
-  size_t rope_cos, rope_sin, kc, vc, kc_d, vc_d, gemm, attn_part, stack_prog, stack_scratch, stack_part;
+  size_t rope_cos, rope_sin, kc, vc, kc_d, vc_d, gemm, attn_part, stack_prog, stack_scratch, stack_part, w4_dense;
   size_t gemm_bytes;
   size_t total;
 };
@@ -424,6 +435,13 @@ Offsets plan(const Dims& dm) {
   }
   o.gemm_bytes = g;
   o.gemm = L.take(std::max<size_t>(g, 256));
+  size_t wmax = 0;  // largest target projection, expanded (int4 targets)
+  if (dm.w4) {
+    const size_t Ns[] = {(size_t)dm.nqkv, (size_t)dm.d, 2 * (size_t)dm.ffn, (size_t)dm.d};
+    const size_t Ks[] = {(size_t)dm.d, (size_t)dm.qd, (size_t)dm.d, (size_t)dm.ffn};
+    for (int i = 0; i < 4; ++i) wmax = std::max(wmax, Ns[i] * Ks[i] * es);
+  }
+  o.w4_dense = L.take(wmax);
   o.attn_part = L.take(std::max<size_t>(dm.bf16 ? attention_tc_scratch_bytes((int)M, dm.Hq, dm.hd, dm.cap_d) : 0, 256));
   o.stack_prog = L.take((size_t)dm.stack_phases_total * sizeof(StackPhase));
   o.stack_scratch = L.take(dm.progs.empty() ? 0 : stack_scratch_bytes(dm.stack_M, dm.stack_phases_max,
@@ -436,11 +454,12 @@ Offsets plan(const Dims& dm) {
 template <typename T>
 struct Eng {
   static eagle_status gemm(eagle_ctx* c, const void* X, const bf16* X_lo, const void* W, int M, int N, int K,
-                           const EpiParams& ep) {
+                           const EpiParams& ep, bool w_dep = false) {
     if (M <= 0) return EAGLE_OK;
     if constexpr (sizeof(T) == 2) {
       if (gemm_tc_ok(c->dm, N, K)) {
-        EG_CK(gemm_tc((const bf16*)X, X_lo, (const bf16*)W, M, N, K, ep, c->gemm_scratch, c->st.status, c->stream));
+        EG_CK(gemm_tc((const bf16*)X, X_lo, (const bf16*)W, M, N, K, ep, c->gemm_scratch, c->st.status, c->stream,
+                      w_dep));
         return EAGLE_OK;
       }
     }
@@ -473,7 +492,13 @@ struct Eng {
   // kernel(s); Record appends it to a persistent-kernel program.
   struct Direct {
     eagle_ctx* c;
-    eagle_status gemm(const void* X, const bf16* X_lo, const void* W, int M, int N, int K, const EpiParams& e) {
+    eagle_status gemm(const void* X, const bf16* X_lo, const void* W, int M, int N, int K, const EpiParams& e,
+                      bool w4 = false) {
+      if (w4) {  // expand the int4 projection, then the dense GEMM (which must wait for it before its weights)
+        if (M <= 0) return EAGLE_OK;
+        EG_CK(int4_dequant<T>(W, N, K, (T*)c->w4_dense, c->stream));
+        return Eng::gemm(c, X, X_lo, c->w4_dense, M, N, K, e, true);
+      }
       return Eng::gemm(c, X, X_lo, W, M, N, K, e);
     }
     eagle_status attention(const AttnArgs& a) { return Eng::attention(c, a); }
@@ -481,9 +506,10 @@ struct Eng {
   struct Record {
     eagle_ctx* c;
     StackProgramBuilder* b;
-    eagle_status gemm(const void* X, const bf16* X_lo, const void* W, int M, int N, int K, const EpiParams& e) {
+    eagle_status gemm(const void* X, const bf16* X_lo, const void* W, int M, int N, int K, const EpiParams& e,
+                      bool w4 = false) {
       (void)M;
-      StackGemmDesc g{(const bf16*)W, (const bf16*)X, X_lo, c->dm.M_max, N, K, e};
+      StackGemmDesc g{(const bf16*)W, (const bf16*)X, X_lo, c->dm.M_max, N, K, e, w4};
       b->gemm(g);
       return b->ok ? EAGLE_OK : fail(c, EAGLE_ERR_UNSUPPORTED, "persistent program: GEMM shape");
     }
@@ -517,7 +543,7 @@ struct Eng {
     const float scale = 1.f / std::sqrt((float)dm.hd);
     e.qg = c->qg; e.qg_scale = scale * 1.4426950408889634f;
     e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = rows;
-    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e));
+    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e, lw.w4));
 
     AttnArgs a{};
     a.q = (const float*)c->q; a.qg = c->qg; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo);
@@ -528,17 +554,17 @@ struct Eng {
 
     e = epi(c, kEpiResid, M, dm.d);
     e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
-    EG_TRY(sink.gemm(c->attn, lo(c->attn_lo), lw.wo, M, dm.d, dm.qd, e));
+    EG_TRY(sink.gemm(c->attn, lo(c->attn_lo), lw.wo, M, dm.d, dm.qd, e, lw.w4));
 
     e = epi(c, kEpiSwiglu, M, 2 * dm.ffn);
     e.ssq_in = c->ssq_a; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.out = c->act; e.ffn = dm.ffn;
     e.out_lo = lo(c->act_lo);
-    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e));
+    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e, lw.w4));
 
     e = epi(c, kEpiResid, M, dm.d);
     e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = gain_next;
     e.h_tap = tap; e.h_tap2 = tap2;
-    EG_TRY(sink.gemm(c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e));
+    EG_TRY(sink.gemm(c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e, lw.w4));
     return EAGLE_OK;
   }
 
@@ -628,7 +654,7 @@ struct Eng {
     const int ng = p.kind == 0 ? p.n_seq : c->dm.B;
     EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
                     c->stack_scratch, c->dm.stack_phases_max, c->dm.stack_counters_max, c->st.status, trace,
-                    lm_logits, g, ng, p.first_attn, c->stream));
+                    lm_logits, g, ng, p.first_attn, c->stream, p.w4));
     return EAGLE_OK;
   }
 
@@ -652,6 +678,7 @@ struct Eng {
       if ((int)b.phases.size() != p.n_phases || b.n_counters != p.n_counters)
         return fail(c, EAGLE_ERR_UNSUPPORTED, "persistent program: phase count");
       p.first_attn = b.first_attn;
+      p.w4 = b.has_w4;
       all.insert(all.end(), b.phases.begin(), b.phases.end());
     }
     EG_CK(cudaMemcpyAsync(c->stack_prog, all.data(), all.size() * sizeof(StackPhase), cudaMemcpyHostToDevice,
@@ -834,11 +861,18 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
     delete c;
     return EAGLE_ERR_INVALID_ARG;
   }
-  auto lp = [](const eagle_layer_weights& l) {
-    return LayerPtrs{l.wqkv, l.wo, l.wgu, l.wd, l.attn_norm, l.ffn_norm};
+  auto lp = [](const eagle_layer_weights& l, bool w4) {
+    return LayerPtrs{l.wqkv, l.wo, l.wgu, l.wd, l.attn_norm, l.ffn_norm, w4};
   };
-  for (int l = 0; l < dm.Lyr; ++l) c->layers.push_back(lp(w->layers[l]));
-  c->head = lp(w->head);
+  for (int l = 0; l < dm.Lyr; ++l) c->layers.push_back(lp(w->layers[l], dm.w4));
+  c->head = lp(w->head, false);
+  if (dm.w4)
+    for (const LayerPtrs& l : c->layers)
+      if ((reinterpret_cast<uintptr_t>(l.wqkv) | reinterpret_cast<uintptr_t>(l.wo) |
+           reinterpret_cast<uintptr_t>(l.wgu) | reinterpret_cast<uintptr_t>(l.wd)) & 15) {
+        delete c;
+        return EAGLE_ERR_INVALID_ARG;
+      }
   for (const LayerPtrs& l : c->layers)
     if (!l.wqkv || !l.wo || !l.wgu || !l.wd || !l.attn_norm || !l.ffn_norm) { delete c; return EAGLE_ERR_INVALID_ARG; }
   if (!c->head.wqkv || !c->head.wo || !c->head.wgu || !c->head.wd || !c->head.attn_norm || !c->head.ffn_norm) {
@@ -899,6 +933,7 @@ eagle_status eagle_init(const eagle_config* cfg, const eagle_weights* w, void* d
   c->gemm_scratch = P(o.gemm); c->gemm_scratch_bytes = o.gemm_bytes; c->attn_part = (float*)P(o.attn_part);
   c->stack_prog = (StackPhase*)P(o.stack_prog); c->stack_scratch = P(o.stack_scratch);
   c->stack_part = (float*)P(o.stack_part);
+  c->w4_dense = dm.w4 ? P(o.w4_dense) : nullptr;
 
   // Zero the workspace (tile counters, status, caches), then upload the tables.
   cudaError_t e = cudaMemsetAsync(d_ws, 0, o.total, c->stream);

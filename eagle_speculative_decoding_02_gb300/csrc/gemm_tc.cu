@@ -58,6 +58,7 @@ struct TcArgs {
                    // accumulator holds the hi products in columns [0, MT) and the lo ones in [MT, 2 MT)
   long long T;
   uint32_t tmem_cols;
+  int w_dep;       // the weights were written by the previous kernel: wait for it before loading them
   int* counters;   // [m_chunks][n_tiles], zero on entry and on exit
   float* partial;  // [m_chunks][G][2][MT][128]
   int* status;
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (programmatic dependent launch), the activation boxes after it.
       int pre_kb[kMaxStages];
       int npre = 0;
+      if (a.w_dep) griddep_wait();
       for (long long u = u0; u < u1 && npre < S; ++u, ++npre) {
         const int t = (int)(u / kbt);
         const int kb = (int)(u - (long long)t * kbt);
@@ -460,7 +462,7 @@ size_t gemm_tc_scratch_bytes(int M, int N, int K) {
 }
 
 cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N, int K, const EpiParams& ep,
-                    void* scratch, int* status, cudaStream_t s) {
+                    void* scratch, int* status, cudaStream_t s, bool w_dep) {
   if (M <= 0) return cudaSuccess;
   if (N % kTileN || K % kBK || !scratch) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(X_lo) | reinterpret_cast<uintptr_t>(W)) & 15)
@@ -484,6 +486,7 @@ cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N
   a.tmem_cols = p.tmem_cols;
   a.has_lo = X_lo != nullptr;
   a.wide = p.wide;
+  a.w_dep = w_dep ? 1 : 0;
   a.counters = reinterpret_cast<int*>(scratch);
   a.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + p.counters_bytes);
   a.status = status;

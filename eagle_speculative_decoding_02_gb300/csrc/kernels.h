@@ -16,8 +16,11 @@ cudaError_t gemm_simt(const T* X, const T* W, int M, int N, int K, const EpiPara
 // leaves them at zero). Returns cudaErrorInvalidValue for unsupported shapes.
 // X_lo (may be NULL): low halves of a hi/lo activation pair, Y = (X + X_lo) W^T.
 size_t gemm_tc_scratch_bytes(int M, int N, int K);
+// w_dep: W was written by the previous kernel on the stream (for example an
+// expanded int4 weight); otherwise the weight boxes of the first stages are
+// requested before the programmatic-dependent-launch wait.
 cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N, int K, const EpiParams& ep,
-                    void* scratch, int* status, cudaStream_t s);
+                    void* scratch, int* status, cudaStream_t s, bool w_dep = false);
 
 // 2D bf16 tensor map of a row-major [rows][cols] matrix, box [box_rows][64],
 // 128-byte swizzle (the operand format of the tcgen05 kernels).
@@ -28,6 +31,12 @@ bool make_tmap_f16(CUtensorMap* m, const void* base, int rows, int cols, int box
 int num_sms();
 // Raise a kernel's dynamic shared-memory limit on the current device (once per device).
 bool raise_smem_limit(const void* kernel, int bytes);
+
+// ---- weight-only int4 (int4.cuh: format and block layout) --------------------------------------
+bool int4_shape_ok(int N, int K);
+// Dense [N][K] weights of T from a packed int4 weight (the per-operation GEMMs' input).
+template <typename T>
+cudaError_t int4_dequant(const void* w4, int N, int K, T* out, cudaStream_t s);
 
 // ---- attention ---------------------------------------------------------------------------------
 struct AttnArgs {

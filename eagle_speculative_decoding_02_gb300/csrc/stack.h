@@ -25,6 +25,7 @@ struct StackPhase {   // 128-byte aligned (CUtensorMap)
   int N = 0, K = 0, n_tiles = 0, kbt = 0;
   long long T = 0;    // units (128-row tile, 64-wide k-block): n_tiles * kbt
   int cnt_off = 0;    // first split-K arrival counter of this phase
+  const uint8_t* w4 = nullptr;  // GEMM: packed int4 weight (int4.cuh blocks) instead of tmW
   EpiParams ep;       // GEMM epilogue
   AttnArgs at;        // attention / merge
 };
@@ -37,6 +38,7 @@ struct StackGemmDesc {
   int rows_cap;       // rows of the X buffers (>= M)
   int N, K;
   EpiParams ep;
+  bool w4 = false;    // W is a packed int4 weight (int4.cuh block layout), expanded in shared memory
 };
 
 // Host-side builder of a program (tensor maps are encoded here).
@@ -46,6 +48,7 @@ struct StackProgramBuilder {
   std::vector<StackPhase> phases;
   int n_counters = 0;
   int first_attn = -1;  // index of the first attention phase
+  bool has_w4 = false;  // some GEMM phase has an int4 weight: run with stack_run(..., w4 = true)
   bool ok = true;
   void gemm(const StackGemmDesc& g);
   void attention(const AttnArgs& a);  // adds the attention phase and its merge phase
@@ -76,8 +79,10 @@ size_t stack_attention_part_bytes(int M, int Hq, int Hkv, int hd, int max_prefix
 // reads (each CTA keeps a copy in shared memory); NULL / 0 without attention.
 // first_attn: index of the program's first attention phase (-1 if none); every
 // attention phase of a program has the same rows, heads and groups.
+// w4: the program has int4 phases (the 352-thread variant with converter warps).
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
                       void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
-                      float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s);
+                      float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s,
+                      bool w4 = false);
 
 }  // namespace eg

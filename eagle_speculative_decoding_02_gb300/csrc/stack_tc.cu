@@ -33,6 +33,16 @@
 // Unit i uses ring slot i % S in both halves; one full barrier per slot takes
 // both producers' arrivals and bytes, one empty barrier (the MMA's commit)
 // frees the slot for both, as in a single-producer pipeline.
+// Weight-only int4 programs (a GEMM phase whose weight is a packed int4 block
+// array, int4.cuh) run a variant with 352 threads: warp 0 streams the packed
+// blocks (4352 bytes per 128 x 64 unit) through a deeper ring of their own, and
+// converter warps 7-10 (32 weight rows each) expand each block to the bf16 slot
+// layout above (the TMA's 128-byte swizzle) once the MMA has freed the slot;
+// they also issue the bf16 boxes of the program's 16-bit phases. A slot's full
+// barrier then takes the activation producer's and the unit's converter warp's
+// arrivals. (A separate, deeper activation ring was measured: no gain; the
+// MMA issue loop, one thread at ~900 cycles per unit, is what limits this
+// variant at 61 rows.)
 // Every wait is bounded (2 s); on a timeout the CTA records kStTimeout, stops
 // issuing work, drains its copies and returns; other CTAs then time out on
 // their own waits.
@@ -42,6 +52,7 @@
 #include "attention_tc.cuh"
 #include "attention_umma.cuh"
 #include "epilogue.cuh"
+#include "int4.cuh"
 #include "stack.h"
 #include "tc_ptx.cuh"
 
@@ -51,6 +62,9 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 224;
+constexpr int kThreadsW4 = 352;            // int4 variant: + converter warps 7-10
+constexpr int kConvWarp = 7;
+constexpr int kMaxRaw = 32;                // int4 variant: packed-block ring stages (upper bound)
 constexpr int kXWarp = 6;                  // activation producer warp
 constexpr int kBK = 64;
 constexpr int kWBytes = kTileN * kBK * 2;  // 16 KB weight box
@@ -69,6 +83,7 @@ struct StackArgs {
   const StackPhase* ph;
   int n_phases;
   int M, MT, has_lo, sw, sx;
+  int rw;            // int4 variant: packed-block ring stages
   int apad;          // bytes after the epilogue tile that complete the attention staging region
   uint32_t tmem_cols;
   unsigned* done;    // [n_phases] phase counters, then the exit counter
@@ -265,8 +280,9 @@ struct AttnItems {
   }
 };
 
-template <int HD>
-__global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
+template <int HD, bool W4>
+__global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel(StackArgs a) {
+  constexpr int NT = W4 ? kThreadsW4 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.sw, MT = a.MT;
@@ -295,15 +311,25 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   volatile int* last_flag = abort_flag + 1;
   volatile int* exit_last = abort_flag + 2;
   Group* sgroups = reinterpret_cast<Group*>(tmem_slot + 4);  // kMaxGroups entries
+  // int4 variant: the packed-block ring and its barriers after the groups
+  uint64_t* rfull = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sgroups + kMaxGroups) + 15) &
+                                                ~uintptr_t(15));
+  uint64_t* rempty = rfull + a.rw;
+  uint8_t* rraw = reinterpret_cast<uint8_t*>(rempty + a.rw);  // 16-byte aligned (2 rw barriers of 8 bytes)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, G = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);  // the weight and the activation producer
+      mbar_init(&full[s], 2);  // the activation producer, and the weight producer or the unit's converter warp
       mbar_init(&empty[s], 1);
     }
+    if (W4)
+      for (int j = 0; j < a.rw; ++j) {
+        mbar_init(&rfull[j], 1);   // the packed-block producer (transaction bytes)
+        mbar_init(&rempty[j], 1);  // the unit's converter warp, once read
+      }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&afull[b], 1);
       mbar_init(&aempty[b], 4);
@@ -317,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // the groups of the attention phases, read once (the item loops decode them often)
-  for (int i = threadIdx.x; i < a.n_groups; i += kThreads) sgroups[i] = a.groups[i];
+  for (int i = threadIdx.x; i < a.n_groups; i += NT) sgroups[i] = a.groups[i];
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(a.tmem_cols)
@@ -330,7 +356,130 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   const uint32_t tmem = *tmem_slot;
   if (a.trace && threadIdx.x == 0) a.trace[(size_t)a.n_phases * G + c] = globaltimer();
 
-  if (warp == 0) {
+  if (W4 && warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ packed-block producer (int4 variant)
+      // The int4 phases' blocks stream into their own ring, ahead of the
+      // conversions; units of 16-bit phases are left to the converter warps.
+      uint64_t pol_w;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+      Cursor W;
+      bool more = W.next(a, c, G);
+      RingPos rq;
+      long long ir = 0;
+      bool ok = true;
+      while (more && ok) {
+        const StackPhase& P = a.ph[W.p];
+        if (P.w4) {
+          const int j = rq.s;
+          if (rq.r > 0 && !mbar_wait(&rempty[j], (rq.r - 1) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&rfull[j], (uint32_t)kInt4BlockBytes);
+          bulk_load_hint(rraw + (size_t)j * kInt4BlockBytes,
+                         P.w4 + ((size_t)W.sl * P.kbt + W.kb) * kInt4BlockBytes, (uint32_t)kInt4BlockBytes,
+                         &rfull[j], pol_w);
+          ++ir;
+          rq.step(a.rw);
+        }
+        more = W.advance(a, c, G);
+      }
+      if (!ok) {
+        for (long long j = (ir > a.rw ? ir - a.rw : 0); j < ir; ++j) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(&rfull[j % a.rw], (uint32_t)(j / a.rw) & 1) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+  } else if (W4 && warp >= kConvWarp) {
+    // ------------------------------------------------------------ converter warps (int4 variant)
+    // The units are dealt round-robin over nc = min(4, S) warps: warp cw expands
+    // units cw, cw + nc, ... (all 128 weight rows, four per lane) into the unit's
+    // slot once the MMA has released it, so nc units are in conversion at once.
+    // Row r's 16-byte chunk ch goes to chunk ch ^ (r & 7) of the row: the layout
+    // TMA's 128-byte swizzle writes. A unit of a 16-bit phase gets its bf16 box by
+    // TMA instead, issued by the same warp.
+    // nc <= S keeps the parity waits exact: a warp waits for the release of unit
+    // i - S only after its previous unit i - nc waited for unit i - nc - S, so the
+    // slot's barrier is never two phases behind the one it tests (a parity test
+    // against a barrier two phases behind would pass at once).
+    const int cw = warp - kConvWarp;
+    const int nc = S < 4 ? S : 4;
+    uint64_t pol_w;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+    Cursor K;
+    bool more = K.next(a, c, G);
+    RingPos sp, rq;   // slots (every unit), packed blocks (int4 units)
+    long long iu = 0, nb = 0;  // units passed, bf16 boxes issued by this warp
+    int cur_p = -1;
+    const uint8_t* cur_w4 = nullptr;  // the current phase's packed weight (read once per phase)
+    bool ok = cw < nc;
+    while (more && ok) {
+      if (K.p != cur_p) {
+        cur_p = K.p;
+        cur_w4 = a.ph[K.p].w4;
+      }
+      const int s = sp.s;
+      if ((int)(iu % nc) == cw) {
+        if (sp.r > 0) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(&empty[s], (sp.r - 1) & 1, abort_flag, a.status);
+          if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (cur_w4) {
+          const int j = rq.s;
+          bool w = true;
+          if (lane == 0) w = mbar_wait(&rfull[j], rq.r & 1, abort_flag, a.status);
+          if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* raw = rraw + (size_t)j * kInt4BlockBytes;
+          uint8_t* slot = wring + (size_t)s * wslot;
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int r = rr * 32 + lane;
+            const uint4 q0 = *reinterpret_cast<const uint4*>(raw + r * 32);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(raw + r * 32 + 16);
+            const __nv_bfloat16 sc = reinterpret_cast<const __nv_bfloat16*>(raw + kInt4CodeBytes)[r];
+            const __nv_bfloat162 s2 = __halves2bfloat162(sc, sc);
+            uint8_t* dst = slot + r * 128;
+            const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = int4_dequant8(wd[ch], s2);
+          }
+          // the MMA reads the slot through the async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&rempty[j]);
+            mbar_arrive(&full[s]);
+          }
+        } else if (lane == 0) {  // a 16-bit phase: its bf16 box, as the plain variant's weight producer loads it
+          mbar_expect_tx(&full[s], (uint32_t)kWBytes);
+          tma_load_2d_hint(wring + (size_t)s * wslot, &a.ph[K.p].tmW, &full[s], K.kb * kBK, K.sl * kTileN, pol_w);
+          ++nb;
+        }
+      }
+      if (cur_w4) rq.step(a.rw);
+      ++iu;
+      sp.step(S);
+      more = K.advance(a, c, G);
+    }
+    if (!ok && nb > 0 && lane == 0) {
+      for (long long j = (iu > S ? iu - S : 0); j < iu; ++j) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(&full[j % S], (uint32_t)(j / S) & 1) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ weight producer
       // Weight boxes depend on no phase: stream them through the ring as fast as
@@ -666,8 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
   __syncthreads();
   if (*exit_last) {
     __threadfence();
-    for (int i = threadIdx.x; i <= a.n_phases; i += kThreads) a.done[i] = 0u;
-    for (int i = threadIdx.x; i < a.n_counters; i += kThreads) a.tile_cnt[i] = 0;
+    for (int i = threadIdx.x; i <= a.n_phases; i += NT) a.done[i] = 0u;
+    for (int i = threadIdx.x; i < a.n_counters; i += NT) a.tile_cnt[i] = 0;
   }
   if (warp == 1) {
     tc_fence_after();
@@ -676,18 +825,40 @@ __global__ void __launch_bounds__(kThreads, 1) stack_tc_kernel(StackArgs a) {
 }
 
 struct Layout {
-  int sw, sx, apad;
+  int sw, sx, apad, rw;
   size_t smem;
 };
 
 // Ring stages: as many as fit once the attention tiles (aliasing the activation
 // halves and the epilogue tile, padded where those are smaller) are accounted for.
-Layout layout(int MT, bool has_lo, int hd) {
+Layout layout(int MT, bool has_lo, int hd, bool w4) {
   Layout l{};
   const size_t xbytes = (size_t)MT * kBK * 2 * (has_lo ? 2 : 1);
   const size_t wslot = kWBytes;
   const size_t attn = hd == 128 ? attn::um_smem_bytes<128>() : attn::um_smem_bytes<64>();
   const size_t fixed = kTileBytes + (size_t)(2 * kMaxW + 7) * 8 + 16 + kMaxGroups * sizeof(Group) + 1024;
+  if (w4) {
+    // int4 variant: as many slots (up to 6) as leave room for at least 10
+    // packed-block stages (4352 bytes + two barriers each; else 4), then as many
+    // stages as fit. At least as many stages as slots: a converter tests a stage's
+    // barrier only after the unit R stages back was consumed, which keeps that
+    // parity test exact too.
+    for (int pass = 0; pass < 2; ++pass)
+    for (int s = 6; s >= 2; --s) {
+      const size_t alias = (size_t)s * xbytes + kTileBytes;
+      const size_t pad = alias >= attn ? 0 : (attn - alias + 15) / 16 * 16;
+      const size_t smem = (size_t)s * (wslot + xbytes) + fixed + pad + 16;
+      if (smem >= (size_t)kSmemBudget) continue;
+      const int r = (int)std::min<size_t>(kMaxRaw, ((size_t)kSmemBudget - smem) / (kInt4BlockBytes + 16));
+      if (r < std::max(s, pass == 0 ? 10 : 4)) continue;
+      l.sw = l.sx = s;
+      l.rw = r;
+      l.apad = (int)pad;
+      l.smem = smem + (size_t)r * (kInt4BlockBytes + 16);
+      return l;
+    }
+    return l;
+  }
   for (int s = kMaxW; s >= 2; --s) {
     const size_t alias = (size_t)s * xbytes + kTileBytes;
     const size_t pad = alias >= attn ? 0 : (attn - alias + 15) / 16 * 16;
@@ -745,7 +916,12 @@ void StackProgramBuilder::gemm(const StackGemmDesc& g) {
   n_counters += ph.n_tiles;  // one arrival counter per tile
   ph.ep = g.ep;
   ph.ep.M = M;
-  if (!make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN) || !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
+  if (g.w4) {
+    ph.w4 = reinterpret_cast<const uint8_t*>(g.W);  // blocks of 128 x 64, 16-byte aligned (checked above)
+    has_w4 = true;
+  }
+  if ((!g.w4 && !make_tmap_bf16(&ph.tmW, g.W, g.N, g.K, kTileN)) ||
+      !make_tmap_bf16(&ph.tmX, g.X, g.rows_cap, g.K, MT) ||
       (g.X_lo && !make_tmap_bf16(&ph.tmXlo, g.X_lo, g.rows_cap, g.K, MT))) {
     ok = false;
     return;
@@ -777,12 +953,13 @@ void StackProgramBuilder::attention(const AttnArgs& a) {
 
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
                       void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
-                      float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s) {
+                      float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s,
+                      bool w4) {
   if (!stack_supported(M, hd) || n_phases <= 0 || !scratch || n_phases > max_phases || n_counters > max_counters)
     return cudaErrorInvalidValue;
   if (n_groups < 0 || n_groups > kMaxGroups || (n_groups > 0 && !groups)) return cudaErrorInvalidValue;
   const int MT = round_mt(M);
-  const Layout l = layout(MT, has_lo, hd);
+  const Layout l = layout(MT, has_lo, hd, w4);
   if (l.sw < 2) return cudaErrorInvalidValue;
   StackArgs a{};
   a.ph = d_phases;
@@ -792,6 +969,7 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.has_lo = has_lo;
   a.sw = l.sw;
   a.sx = l.sx;
+  a.rw = l.rw;
   a.apad = l.apad;
   uint32_t cols = attn::kUmTmemCols;  // attention S and O
   while (cols < (uint32_t)(2 * (has_lo ? 2 * MT : MT))) cols <<= 1;  // two accumulator buffers
@@ -811,13 +989,14 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.groups = groups;
   a.n_groups = n_groups;
   a.first_attn = first_attn < n_phases ? first_attn : -1;
-  auto kernel = hd == 128 ? stack_tc_kernel<128> : stack_tc_kernel<64>;
+  auto kernel = w4 ? (hd == 128 ? stack_tc_kernel<128, true> : stack_tc_kernel<64, true>)
+                   : (hd == 128 ? stack_tc_kernel<128, false> : stack_tc_kernel<64, false>);
   if (!raise_smem_limit(reinterpret_cast<const void*>(kernel), kSmemBudget)) return cudaErrorInvalidValue;
   const int G = num_sms();
   if (G > kMaxCtas) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(w4 ? kThreadsW4 : kThreads);
   cfg.dynamicSmemBytes = l.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

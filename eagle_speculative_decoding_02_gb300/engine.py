@@ -62,6 +62,30 @@ def pack_layer(wq, wk, wv, wo, wg, wu, wd, attn_norm, ffn_norm) -> LayerWeights:
                         ffn_norm=ffn_norm.float().contiguous())
 
 
+def pack_layer_int4(codes: dict, scales: dict, attn_norm, ffn_norm) -> LayerWeights:
+    """A layer of int4 projections: codes (uint8 [N, K/2], two 4-bit codes per byte, low nibble = even input)
+    and bf16 scales ([N, K/64]) per projection name, rows ordered like the bf16 layout (q, k, v; gate / up
+    interleaved in blocks of 64), then repacked by the library (eagle_int4_pack) into its block layout."""
+    lib = L.load()
+
+    def pack(c: torch.Tensor, s: torch.Tensor) -> torch.Tensor:
+        c, s = c.contiguous(), s.contiguous()
+        n, k = c.shape[0], 2 * c.shape[1]
+        nbytes = lib.eagle_int4_packed_bytes(n, k)
+        if nbytes == 0:
+            raise ValueError(f"int4 weight [{n}, {k}]: N % 128 and K % 64 must be 0")
+        out = torch.empty(nbytes, dtype=torch.uint8, device=c.device)
+        L.check("eagle_int4_pack", lib.eagle_int4_pack(c.data_ptr(), s.data_ptr(), n, k, out.data_ptr(),
+                                                       torch.cuda.current_stream(c.device).cuda_stream))
+        return out
+
+    wqkv = pack(torch.cat([codes["wq"], codes["wk"], codes["wv"]], 0), torch.cat([scales["wq"], scales["wk"],
+                                                                                scales["wv"]], 0))
+    wgu = pack(pack_gate_up(codes["wg"], codes["wu"]), pack_gate_up(scales["wg"], scales["wu"]))
+    return LayerWeights(wqkv=wqkv, wo=pack(codes["wo"], scales["wo"]), wgu=wgu, wd=pack(codes["wd"], scales["wd"]),
+                        attn_norm=attn_norm.float().contiguous(), ffn_norm=ffn_norm.float().contiguous())
+
+
 @dataclasses.dataclass
 class Tree:
     n_rows: int
@@ -82,7 +106,7 @@ class EagleEngine:
     def __init__(self, *, n_layers, d, n_heads, n_kv_heads, head_dim, ffn, vocab, rope_theta, rms_eps, bf16,
                  batch, kv_cap, max_prompt, max_new, tree_mode, n_nodes, static_parent=None, static_rank=None,
                  top_k=10, depth=6, tau=0.3, temperature=0.0, seed=0, n_nodes_min=0, feature_taps=1,
-                 weights: ModelWeights,
+                 weight_bits=16, weights: ModelWeights,
                  device="cuda", stream=None):
         self.lib = L.load()
         self.device = torch.device(device)
@@ -98,7 +122,8 @@ class EagleEngine:
                                  L.DTYPE_BF16 if bf16 else L.DTYPE_F32, batch, kv_cap, max_prompt, max_new,
                                  tree_mode, n_nodes, C.cast(sp, C.POINTER(C.c_int32)) if sp else None,
                                  C.cast(sr, C.POINTER(C.c_int32)) if sr else None, top_k, depth, tau,
-                                 float(temperature), int(seed), int(n_nodes_min), int(feature_taps))
+                                 float(temperature), int(seed), int(n_nodes_min), int(feature_taps),
+                                 int(weight_bits))
         nbytes = C.c_size_t(0)
         L.check("eagle_workspace_size", self.lib.eagle_workspace_size(C.byref(self.cfg), C.byref(nbytes)))
         self.workspace = torch.empty(int(nbytes.value), dtype=torch.uint8, device=self.device)

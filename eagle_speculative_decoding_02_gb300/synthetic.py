@@ -13,12 +13,12 @@ import fixtures as FX
 from fixtures import device as FD
 
 from . import _lib as L
-from .engine import EagleEngine, ModelWeights, pack_layer
+from .engine import EagleEngine, ModelWeights, pack_layer, pack_layer_int4
 from .topology import named
 
 
 def device_weights(m: FX.ModelShape, device="cuda", taps: int = 1) -> ModelWeights:
-    g = FD.generate_model(m, pack_layer, device=device, taps=taps)
+    g = FD.generate_model(m, pack_layer, device=device, taps=taps, pack_layer_int4=pack_layer_int4)
     return ModelWeights(embed=g["embed"], lm_head=g["lm_head"], final_norm=g["final_norm"], layers=g["layers"],
                         fc=g["fc"], head=g["head"], fuse=g.get("fuse"))
 
@@ -39,7 +39,7 @@ def make_engine(w: FX.Workload, weights: ModelWeights | None = None, *, batch: i
     kw = dict(n_layers=m.n_layers, d=m.d, n_heads=m.n_heads, n_kv_heads=m.n_kv_heads, head_dim=m.head_dim,
               ffn=m.ffn, vocab=m.vocab, rope_theta=m.rope_theta, rms_eps=m.rms_eps, bf16=m.bf16, batch=batch,
               kv_cap=cap, max_prompt=prompt_len, max_new=max_new, weights=weights, device=device,
-              temperature=temperature, seed=seed, feature_taps=w.feature_taps)
+              temperature=temperature, seed=seed, feature_taps=w.feature_taps, weight_bits=m.weight_bits)
     if tree == "static":
         parent, rank = named(w.static_tree)
         return EagleEngine(tree_mode=L.TREE_STATIC, n_nodes=len(parent) - 1, static_parent=parent,

@@ -27,6 +27,9 @@ def lib() -> C.CDLL:
         _lib.fx_fill_normal.restype = C.c_int
         _lib.fx_fill_normal.argtypes = [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_uint64, C.c_double,
                                         C.c_uint64, C.c_double, C.c_int, C.c_void_p]
+        _lib.fx_fill_int4.restype = C.c_int
+        _lib.fx_fill_int4.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_uint64, C.c_uint64,
+                                      C.c_double, C.c_void_p]
     return _lib
 
 
@@ -56,6 +59,21 @@ def target_tensor(m: FX.ModelShape, name: str, layer: int = -1, device="cuda") -
     return fill_normal(torch.empty(shape, dtype=_dt(m), device=device), key, std)
 
 
+def int4_tensor(m: FX.ModelShape, name: str, layer: int, device="cuda") -> tuple[torch.Tensor, torch.Tensor]:
+    """Packed 4-bit codes (uint8 [N, K/2]) and group scales (bf16 [N, K/64]) of a target projection."""
+    n, k = FX.layer_shapes(m)[name]
+    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty((n, k // FX.INT4_GROUP), dtype=torch.bfloat16, device=device)
+    s = torch.cuda.current_stream(codes.device).cuda_stream
+    kind = FX.KIND[name]
+    rc = lib().fx_fill_int4(codes.data_ptr(), scales.data_ptr(), n, k,
+                            FX.stream_key(m.seed, FX.CODE_INT4 + 16 * layer + kind),
+                            FX.stream_key(m.seed, FX.CODE_INT4_SCALE + 16 * layer + kind), FX.int4_scale_base(m), s)
+    if rc != 0:
+        raise RuntimeError(f"fx_fill_int4 failed: {rc}")
+    return codes, scales
+
+
 def head_tensor(m: FX.ModelShape, name: str, device="cuda") -> torch.Tensor:
     if name == "fuse":
         return fill_normal(torch.empty((m.d, 3 * m.d), dtype=_dt(m), device=device),
@@ -70,9 +88,10 @@ def head_tensor(m: FX.ModelShape, name: str, device="cuda") -> torch.Tensor:
                        noise_std=0.1 * m.init_std)
 
 
-def generate_model(m: FX.ModelShape, pack_layer, device="cuda", taps: int = 1):
+def generate_model(m: FX.ModelShape, pack_layer, device="cuda", taps: int = 1, pack_layer_int4=None):
     """The model's tensors: "embed", "lm_head", "final_norm", "fc", "layers" (packed), "head" (packed) and,
-    with taps = 3, the fused-feature matrix "fuse".
+    with taps = 3, the fused-feature matrix "fuse". Models with weight_bits = 4 pack their target layers
+    with pack_layer_int4(codes={name: uint8 [N, K/2]}, scales={name: bf16 [N, K/64]}, attn_norm, ffn_norm).
 
     Layers are generated and packed one at a time, so the peak extra memory is one layer.
     """
@@ -80,6 +99,13 @@ def generate_model(m: FX.ModelShape, pack_layer, device="cuda", taps: int = 1):
     out = {"embed": target_tensor(m, "embed", device=device), "lm_head": target_tensor(m, "lm_head", device=device),
            "final_norm": ones.clone(), "fc": head_tensor(m, "fc", device=device), "layers": []}
     for l in range(m.n_layers):
+        if m.weight_bits == 4:
+            q = {k: int4_tensor(m, k, l, device=device) for k in FX.layer_shapes(m)}
+            out["layers"].append(pack_layer_int4(codes={k: v[0] for k, v in q.items()},
+                                                 scales={k: v[1] for k, v in q.items()},
+                                                 attn_norm=ones.clone(), ffn_norm=ones.clone()))
+            del q
+            continue
         t = {k: target_tensor(m, k, l, device=device) for k in FX.layer_shapes(m)}
         out["layers"].append(pack_layer(**t, attn_norm=ones.clone(), ffn_norm=ones.clone()))
         del t

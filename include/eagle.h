@@ -127,6 +127,14 @@ typedef struct {
    * n_layers (eagle_weights.fuse is then required). The target's own logits
    * always come from its top-layer feature. */
   int32_t feature_taps;
+  /* Weights of the target's decoder-layer projections ([LPD] operational notes:
+   * EAGLE combines with GPTQ / AWQ 4-bit weight-quantised targets): 0 or 16 =
+   * `dtype` elements; 4 = weight-only int4 (each of wqkv, wo, wgu, wd points to
+   * eagle_int4_pack's block layout; symmetric, a bf16 scale per row and group of
+   * 64 inputs, W = bf16(scale * (code - 8))). Activations keep `dtype`; the
+   * embedding, LM head, norms and the draft head are not quantised. Needs d, the
+   * query width and ffn to be multiples of 64. */
+  int32_t weight_bits;
 } eagle_config;
 
 /* Device pointers of one decoder layer. Matrices are row-major [out, in]
@@ -280,6 +288,24 @@ const char* eagle_last_error(const eagle_ctx* ctx);
  * 4 eagle_stats; 0 for any other value. Host-only. */
 size_t eagle_struct_size(int32_t which);
 
+/* Weight-only int4 projections (config.weight_bits = 4). Input: a weight [N, K]
+ * as 4-bit codes, row-major, two per byte (byte (n, i) holds code (n, 2i) in its
+ * low and code (n, 2i + 1) in its high nibble; d_codes [N][K/2]) and bf16 scales
+ * (d_scales [N][K/64], scale of row n and inputs 64g .. 64g+63); the weight is
+ * W(n, k) = bf16(s(n, k/64) * (u(n, k) - 8)). eagle_int4_pack writes the layout
+ * the kernels stream: blocks of 128 rows x 64 inputs, block (t, g) at byte
+ * ((t K/64) + g) 4352, each 128 rows of 32 code bytes (word c of a row: input
+ * 8c + 2i in bits 4i..4i+3 and 8c + 2i + 1 in bits 16+4i..19+4i) followed by the
+ * 128 rows' scales. Needs N % 128 == 0 and K % 64 == 0 (else
+ * EAGLE_ERR_UNSUPPORTED, and eagle_int4_packed_bytes returns 0); d_out (16-byte
+ * aligned, eagle_int4_packed_bytes(N, K) bytes) is caller-owned. Asynchronous on
+ * `stream`; the inputs may be freed once the stream has passed the call. For a
+ * wqkv or wgu weight, pack the rows in the order of the bf16 layout (q, k, v rows;
+ * gate / up rows interleaved in blocks of 64). */
+size_t eagle_int4_packed_bytes(int32_t N, int32_t K);
+eagle_status eagle_int4_pack(const uint8_t* d_codes, const uint16_t* d_scales, int32_t N, int32_t K, void* d_out,
+                             void* stream);
+
 /* ---------------------------------------------------------------------------
  * Kernel-level entry points: one hot-path kernel on caller buffers, for unit
  * parity tests and roofline timing. They run on `stream`, allocate nothing,
@@ -317,6 +343,13 @@ eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const
  *   - There is no status word: if one of the kernel's bounded waits gives up
  *     (2 s), the call has still returned EAGLE_OK and d_y is incomplete. */
 eagle_status eagle_op_gemm_noalloc(int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_w, float* d_y,
+                                   void* stream);
+
+/* Dense weights from eagle_int4_pack's layout: d_out [N][K] of `dtype` (f32 or
+ * bf16) = bf16(scale * (code - 8)), the values every int4 GEMM of the library
+ * multiplies with (the per-operation path expands them like this; the persistent
+ * kernel expands each block in shared memory). Asynchronous on `stream`. */
+eagle_status eagle_op_int4_dequant(const void* d_w4, int32_t N, int32_t K, int32_t dtype, void* d_out,
                                    void* stream);
 
 /* The same products run by the persistent layer-stack kernel (the kernel of the

@@ -153,3 +153,21 @@ def test_fused_features_config(lib):
 def test_no_alloc_and_selftest_symbols_reject_null_arguments_on_the_host(lib):
     assert lib.eagle_op_gemm_noalloc(0, 128, 64, None, None, None, None) == 1
     assert lib.eagle_selftest_bounded_wait(None, None) == 1
+
+
+def test_int4_config(lib):
+    """weight_bits: 0/16 = dtype weights, 4 = int4 target projections (widths must be multiples of 64)."""
+    w = FX.WORKLOADS["8b_eagle2"]
+    n16, n4 = C.c_size_t(0), C.c_size_t(0)
+    cfg, keep = _cfg(w)
+    assert lib.eagle_workspace_size(C.byref(cfg), C.byref(n16)) == 0
+    cfg, keep = _cfg(w, weight_bits=4)
+    assert lib.eagle_workspace_size(C.byref(cfg), C.byref(n4)) == 0
+    assert n4.value > n16.value          # + the per-operation path's expanded projection
+    for bad, code in ((8, 1), (3, 1)):
+        cfg, keep = _cfg(w, weight_bits=bad)
+        assert lib.eagle_workspace_size(C.byref(cfg), C.byref(C.c_size_t(0))) == code
+    cfg, keep = _cfg(FX.WORKLOADS["tiny_static"], weight_bits=4)   # ffn 688
+    assert lib.eagle_workspace_size(C.byref(cfg), C.byref(C.c_size_t(0))) == 2
+    assert lib.eagle_int4_packed_bytes(256, 128) == 2 * 2 * 4352
+    assert lib.eagle_int4_packed_bytes(100, 64) == 0
