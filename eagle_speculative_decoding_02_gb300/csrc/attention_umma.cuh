@@ -344,7 +344,7 @@ __device__ bool attn_item_um(const AttnArgs& a, const CUtensorMap* tmQ, const CU
 __device__ __forceinline__ int um_group_of(const Group* groups, int n_groups, int row) {
   for (int z = 0; z < n_groups; ++z)
     if (row >= groups[z].row0 && row < groups[z].row0 + groups[z].nrows) return z;
-  return 0;
+  return -1;  // a padding row: in no group, no item wrote its partials
 }
 
 // Merge of the persistent kernel over this CTA's (row, query head) pairs
@@ -410,7 +410,9 @@ __device__ bool um_merge_staged(const AttnArgs& a, const Group* groups, int n0, 
     const float* os = reinterpret_cast<const float*>(stage);
     for (int t = ew; t < nw; t += 4) {
       const int w = w0 + t, row = w / Hq, qh = w - row * Hq;
-      const int nck = um_parts(groups[um_group_of(groups, n_groups, row)], n0);
+      // a padding row (in no group) has no parts: its output is zero, not a mix of stale partials
+      const int z = um_group_of(groups, n_groups, row);
+      const int nck = z >= 0 ? um_parts(groups[z], n0) : 0;
       float M = -INFINITY, L = 0.f, acc[NB];
       if (s0 == 0) {
 #pragma unroll

@@ -126,9 +126,9 @@ __global__ void setup_verify_kernel(State st, TreeOut tree, Rows rows, Group* gr
   for (int j = threadIdx.x; j < NR; j += blockDim.x) {
     const int m = b * NR + j;
     rows.seq[m] = b;
-    rows.pos[m] = fits ? L + tree.depth[m] : 0;
-    rows.slot[m] = fits ? L + j : -1;
     const int tok = tree.tokens[m];
+    rows.pos[m] = fits ? L + tree.depth[m] : 0;
+    rows.slot[m] = fits && tok >= 0 ? L + j : -1;  // padding rows write no K / V
     rows.tok[m] = (tok >= 0 && tok < st.V) ? tok : 0;  // padding nodes carry -1
     rows.fsrc[m] = m;
     rows.grp[m] = b;
