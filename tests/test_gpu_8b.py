@@ -170,16 +170,24 @@ def test_70b_full_lossless(cuda):
     torch.cuda.empty_cache()
 
 
-def test_8b_full_depth_eagle2_against_oracle(cuda):
-    """The 32-layer 8B-shaped model with its EAGLE-2 tree against the oracle at full depth (64-token prompt,
+@pytest.fixture(scope="module")
+def oracle_8b_full():
+    w = dataclasses.replace(FX.WORKLOADS["8b_eagle2"], prompt_len=64, max_new=64)
+    return OM.build_model(FX.LLAMA3_8B, FX.kv_capacity(w))
+
+
+@pytest.mark.parametrize("name", ["8b_eagle2", "8b_static"])
+def test_8b_full_depth_against_oracle(cuda, oracle_8b_full, name):
+    """The 32-layer 8B-shaped model with its EAGLE-2 (or static 60-node) tree against the oracle at full depth (64-token prompt,
     6 steps): the draft trees (identical, or parted only at a flagged near-tie with every node's draft
     log-probability within 0.05 of the oracle's on the GPU's tree), the verify logits (max-abs and cosine),
     the greedy tokens (equal except at flagged near-ties) and the accepted lengths."""
     from eagle_speculative_decoding_02_gb300 import synthetic as S
     from tests.test_gpu_draft import _gpu_tree, check_draft
-    w = dataclasses.replace(FX.WORKLOADS["8b_eagle2"], prompt_len=64, max_new=64)
-    cap = FX.kv_capacity(w)
-    m = OM.build_model(FX.LLAMA3_8B, cap)
+    w = dataclasses.replace(FX.WORKLOADS[name], prompt_len=64, max_new=64)
+    cap = FX.kv_capacity(dataclasses.replace(FX.WORKLOADS["8b_eagle2"], prompt_len=64, max_new=64))
+    w = dataclasses.replace(w, kv_cap=cap)
+    m = oracle_8b_full
     prompt = FX.prompts(FX.LLAMA3_8B, 1, w.prompt_len)
     eng = S.make_engine(w)
     root = eng.prefill(torch.from_numpy(prompt).to(cuda)).cpu().numpy()
@@ -203,5 +211,5 @@ def test_8b_full_depth_eagle2_against_oracle(cuda):
         flagged += int((g_am != oam).sum())
         a, _ = eng.accept_commit()
         assert int(a[0]) == OD.accept_commit(st, gt, g_am, ofeats)
-    print(f"full depth: {same}/6 draft trees identical, max |logit err| {worst:.4f}, {flagged} flagged near-ties, "
+    print(f"{name} full depth: {same}/6 draft trees identical, max |logit err| {worst:.4f}, {flagged} flagged near-ties, "
           f"committed {st.out[:12]}...")
