@@ -124,7 +124,7 @@ def verify_bytes(m, batch: int, L: int, rows: int) -> int:
 
 # Sources of the persistent verify kernel: a DRAM-traffic figure in profiles/ counts
 # only while these are unchanged since its capture.
-KERNEL_SOURCES = ["stack_tc.cu", "stack.h", "attention_umma.cuh", "attention_tc.cuh", "epilogue.cuh", "tc_ptx.cuh",
+KERNEL_SOURCES = ["stack_tc.cu", "stack.h", "attention_umma.cuh", "attention_common.cuh", "epilogue.cuh", "tc_ptx.cuh",
                   "common.cuh", "kernels.h", "engine.cu", "int4.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "stack_tc_kernel_8b_eagle2_verify_traffic.txt")
 
@@ -410,7 +410,7 @@ def main():
     variant = ", int4 variant: packed blocks expanded in shared memory" if m.weight_bits == 4 else ""
     kernel = ((f"stack_tc_kernel (verify program{variant})" if n_chunks <= 1 else
                f"stack_tc_kernel (verify program, {n_chunks} launches over halves of the batch)") if persistent else
-              "verify pass: gemm_tc_kernel per projection + attn_tc_kernel / attn_merge_kernel per layer")
+              "verify pass: gemm_tc_kernel per projection + attn_um_items_kernel / attn_um_merge_kernel per layer")
     traffic = (captured_traffic() if (persistent and args.workload == "8b_eagle2" and w.feature_taps != 3
                                        and m.weight_bits == 16) else None)
     if tensor_bound:

@@ -1,6 +1,7 @@
 // Tree-masked attention work item on the 5th-generation tensor cores
 // (tcgen05.mma, operands in shared memory, scores and output in tensor memory),
-// run by the four epilogue warps of the persistent layer-stack kernel.
+// run by the four epilogue warps of the persistent layer-stack kernel, and by
+// the standalone items / merge launches of attention_umma.cu.
 //
 // "EAGLE (LLM decoding)", section "How EAGLE works": tree attention verifies
 // every draft node in one forward pass; a query row (node j, query head h) sees
@@ -22,15 +23,14 @@
 //      the buffer holds 128 x max(HD, 128) halves).
 //   4. O = P V: 8 MMAs (N = HD), V read in place as an MN-major operand (its rows
 //      are keys, contiguous in head dimension); fp32 in TMEM columns [128, 256).
-//   5. The row's unnormalised partial (O, max, sum) goes out for
-//      attn_merge_warp, in the layout the mma.sync path writes too. The next
-//      item's copies are issued as soon as the MMAs are done, so they overlap
-//      this step.
+//   5. The row's unnormalised partial (O, max, sum) goes out for the merge
+//      (PartLayout). The next item's copies are issued as soon as the MMAs are
+//      done, so they overlap this step.
 //
-// Precision matches the mma.sync path: half q, K, P and V, fp32 accumulation.
+// Precision: half q, K, P and V, fp32 accumulation.
 #pragma once
 
-#include "attention_tc.cuh"
+#include "attention_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace eg {
@@ -169,6 +169,47 @@ __device__ void um_issue(const AttnArgs& a, const CUtensorMap* tmQ, const CUtens
     tma_load_2d(sV + h * kUmAtom, tmV, st.kv_bar, h * 64, ykv);
   }
 }
+
+// The attention work items that have keys and rows, in order (group, KV head,
+// 128-row tile, part of the keys): count() counts them, item() decodes one. The
+// keys of every group are split into parts by the balanced rule of
+// um_part_keys, with n0 = the CTAs per (KV head, row tile) pair.
+struct UmItems {
+  const Group* groups;  // the phase's groups (shared-memory copy)
+  int n_groups, Hkv, G;  // (copied: the arguments live in global memory)
+  int n0 = 1;
+  __device__ UmItems(const AttnArgs& a, const Group* g, int n_ctas)
+      : groups(g), n_groups(a.n_groups), Hkv(a.Hkv), G(a.Hq / a.Hkv) {
+    int pairs = 0;
+    for (int z = 0; z < n_groups; ++z) pairs += Hkv * rts(groups[z]);
+    n0 = pairs > 0 ? max(1, n_ctas / pairs) : 1;
+  }
+  __device__ int rts(const Group& g) const { return um_row_tiles(g.nrows, G); }
+  __device__ int chunks(const Group& g) const { return um_parts(g, n0); }
+  __device__ int count() const {
+    int n = 0;
+    for (int z = 0; z < n_groups; ++z) {
+      const Group g = groups[z];
+      n += chunks(g) * Hkv * rts(g);
+    }
+    return n;
+  }
+  __device__ void item(int i, int& chunk, int& kvh, int& rt, int& z) const {
+    for (z = 0; z < n_groups; ++z) {
+      const Group g = groups[z];
+      const int nc = chunks(g), nr = rts(g), n = nc * Hkv * nr;
+      if (i < n) {
+        chunk = i % nc;
+        const int rest = i / nc;
+        kvh = rest / nr;
+        rt = rest % nr;
+        return;
+      }
+      i -= n;
+    }
+    chunk = kvh = rt = z = 0;
+  }
+};
 
 // One item, run by 128 threads: tid 0..127 (tid 0 issues the copies and MMAs),
 // row = the TMEM lane this thread may read (its warp's lane quarter x 32 + lane)
@@ -349,7 +390,7 @@ __device__ __forceinline__ int um_group_of(const Group* groups, int n_groups, in
 
 // Merge of the persistent kernel over this CTA's (row, query head) pairs
 // w in [w0, w1): the combination of each pair's part partials (max, sum,
-// unnormalised output) in part order, as attn_merge_warp computes it, with the
+// unnormalised output) in part order (a running maximum, the flash-decoding combination), with the
 // partials staged in shared memory first. For every part s and 32-column block,
 // the partials of consecutive pairs are contiguous in the partial buffer, so a
 // few bulk copies bring all of them in one round trip (instead of dozens of

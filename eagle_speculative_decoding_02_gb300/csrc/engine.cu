@@ -442,7 +442,9 @@ Offsets plan(const Dims& dm) {
     for (int i = 0; i < 4; ++i) wmax = std::max(wmax, Ns[i] * Ks[i] * es);
   }
   o.w4_dense = L.take(wmax);
-  o.attn_part = L.take(std::max<size_t>(dm.bf16 ? attention_tc_scratch_bytes((int)M, dm.Hq, dm.hd, dm.cap_d) : 0, 256));
+  o.attn_part = L.take(std::max<size_t>(
+      dm.bf16 ? attention_umma_part_bytes((int)M, dm.Hq, dm.Hkv, dm.hd, dm.cap_d) : 0,
+      256));
   o.stack_prog = L.take((size_t)dm.stack_phases_total * sizeof(StackPhase));
   o.stack_scratch = L.take(dm.progs.empty() ? 0 : stack_scratch_bytes(dm.stack_M, dm.stack_phases_max,
                                                                           dm.stack_counters_max));
@@ -469,7 +471,7 @@ struct Eng {
 
   static eagle_status attention(eagle_ctx* c, const AttnArgs& a) {
     if constexpr (sizeof(T) == 2) {
-      EG_CK(attention_tc(a, c->stream));
+      EG_CK(attention_umma(a, c->stream));
     } else {
       EG_CK(attention_simt<T>(a, c->stream));
     }

@@ -59,8 +59,14 @@ struct AttnArgs {
 };
 template <typename T>
 cudaError_t attention_simt(const AttnArgs& a, cudaStream_t s);
-size_t attention_tc_scratch_bytes(int M, int Hq, int hd, int max_prefix);
-cudaError_t attention_tc(const AttnArgs& a, cudaStream_t s);
+// The tcgen05 tree attention (bf16 models: half KV cache) as two launches
+// (items, then merge) of the persistent kernel's attention code; needs
+// a.qg and a.part of attention_umma_part_bytes(M, Hq, Hkv, hd, max_prefix) bytes.
+size_t attention_umma_part_bytes(int M, int Hq, int Hkv, int hd, int max_prefix);
+cudaError_t attention_umma(const AttnArgs& a, cudaStream_t s);
+// The grouped half queries a.qg from float32 queries q [M][Hq][hd].
+cudaError_t attention_umma_qg(const float* q, int M, int Hq, int Hkv, int hd, float scale, __half* qg,
+                              cudaStream_t s);
 
 // ---- rows, embeddings, FC input ----------------------------------------------------------------
 template <typename T>

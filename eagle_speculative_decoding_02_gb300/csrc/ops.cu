@@ -91,7 +91,9 @@ eagle_status eagle_op_lmhead_topk(int32_t dtype, int32_t M, int32_t N, int32_t K
 }
 
 size_t eagle_op_attention_scratch_bytes(int32_t rows, int32_t n_heads, int32_t hd, int32_t prefix) {
-  return al(sizeof(Group)) + al(attention_tc_scratch_bytes(rows, n_heads, hd, prefix + 128));
+  // the group, then the partials (the larger of the two layouts), then the grouped half queries
+  const size_t part = attention_umma_part_bytes(rows, n_heads, 1, hd, prefix + 128);
+  return al(sizeof(Group)) + al(part) + al((size_t)rows * n_heads * hd * 2);
 }
 
 eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
@@ -112,7 +114,15 @@ eagle_status eagle_op_tree_attention(int32_t dtype, int32_t rows, int32_t n_head
   a.part = (float*)((char*)scratch + al(sizeof(Group)));
   a.status = nullptr;
   cudaError_t err;
-  if (dtype == EAGLE_DTYPE_BF16) err = attention_tc(a, s);
+  if (dtype == EAGLE_DTYPE_BF16) {
+    // the tcgen05 items and merge, on grouped half queries made from q
+    const size_t part = attention_umma_part_bytes(rows, n_heads, 1, hd, prefix + 128);
+    __half* qg = (__half*)((char*)scratch + al(sizeof(Group)) + al(part));
+    a.qg = qg;
+    a.n_seq = 1;
+    err = attention_umma_qg((const float*)q, rows, n_heads, n_kv_heads, hd, a.scale, qg, s);
+    if (err == cudaSuccess) err = attention_umma(a, s);
+  }
   else if (dtype == EAGLE_DTYPE_F32) err = attention_simt<float>(a, s);
   else return EAGLE_ERR_INVALID_ARG;
   return err == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;

@@ -49,7 +49,7 @@
 #include <cuda.h>
 
 #include "../../include/eagle.h"
-#include "attention_tc.cuh"
+#include "attention_common.cuh"
 #include "attention_umma.cuh"
 #include "epilogue.cuh"
 #include "int4.cuh"
@@ -238,47 +238,6 @@ __device__ bool wait_count(const StackArgs& a, int i, unsigned n, volatile int* 
     }
   }
 }
-
-// The attention work items that have keys and rows, in order (group, KV head,
-// 128-row tile, part of the keys): count() counts them, item() decodes one. The
-// keys of every group are split into parts by the balanced rule of
-// attn::um_part_keys, with n0 = the CTAs per (KV head, row tile) pair.
-struct AttnItems {
-  const Group* groups;  // the phase's groups (shared-memory copy)
-  int n_groups, Hkv, G;  // (copied: the arguments live in global memory)
-  int n0 = 1;
-  __device__ AttnItems(const AttnArgs& a, const Group* g, int n_ctas)
-      : groups(g), n_groups(a.n_groups), Hkv(a.Hkv), G(a.Hq / a.Hkv) {
-    int pairs = 0;
-    for (int z = 0; z < n_groups; ++z) pairs += Hkv * rts(groups[z]);
-    n0 = pairs > 0 ? max(1, n_ctas / pairs) : 1;
-  }
-  __device__ int rts(const Group& g) const { return attn::um_row_tiles(g.nrows, G); }
-  __device__ int chunks(const Group& g) const { return attn::um_parts(g, n0); }
-  __device__ int count() const {
-    int n = 0;
-    for (int z = 0; z < n_groups; ++z) {
-      const Group g = groups[z];
-      n += chunks(g) * Hkv * rts(g);
-    }
-    return n;
-  }
-  __device__ void item(int i, int& chunk, int& kvh, int& rt, int& z) const {
-    for (z = 0; z < n_groups; ++z) {
-      const Group g = groups[z];
-      const int nc = chunks(g), nr = rts(g), n = nc * Hkv * nr;
-      if (i < n) {
-        chunk = i % nc;
-        const int rest = i / nc;
-        kvh = rest / nr;
-        rt = rest % nr;
-        return;
-      }
-      i -= n;
-    }
-    chunk = kvh = rt = z = 0;
-  }
-};
 
 template <int HD, bool W4>
 __global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel(StackArgs a) {
@@ -624,7 +583,7 @@ __global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel
     } plan;
     if (a.first_attn >= 0) {
       const AttnArgs& at = a.ph[a.first_attn].at;
-      const AttnItems items(at, sgroups, G);
+      const attn::UmItems items(at, sgroups, G);
       const int n = items.count(), nm = at.M * at.Hq;
       plan.n0 = items.n0;
       plan.slots = attn::um_part_slots(at.max_prefix, at.Hkv, kMaxCtas);
@@ -780,7 +739,7 @@ __global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel
         }
         for (int i = plan.i0; i < plan.i1 && alive; ++i) {
           const bool has_next = i + 1 < plan.i1;
-          if (has_next) AttnItems(at, sgroups, G).item(i + 1, nxt.chunk, nxt.kvh, nxt.rt, nxt.z);
+          if (has_next) attn::UmItems(at, sgroups, G).item(i + 1, nxt.chunk, nxt.kvh, nxt.rt, nxt.z);
           alive = attn::attn_item_um<HD>(at, &P.tmXlo, &P.tmW, &P.tmX, cur, has_next, nxt, plan.n0, plan.slots, ust,
                                          etid, col, abort_flag, EpilogueSync{});
           cur = nxt;
