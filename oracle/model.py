@@ -71,10 +71,34 @@ def _ones(n: int) -> np.ndarray:
     return np.ones(n, dtype=F32)
 
 
-def build_model(shape: FX.ModelShape, max_pos: int, taps: int = 1) -> Model:
+class LazyLayers:
+    """The target's decoder layers generated on each access (the same seeded values every time): a
+    sequence of n layers that never holds more than one, for models whose float32 weights exceed the
+    host's memory (the 70B shape is 280 GB in float32)."""
+
+    def __init__(self, n: int, make):
+        self.n, self.make = n, make
+
+    def __len__(self) -> int:
+        return self.n
+
+    def __getitem__(self, l: int) -> LayerWeights:
+        if not -self.n <= l < self.n:
+            raise IndexError(l)
+        return self.make(l % self.n)
+
+    def __iter__(self):
+        for l in range(self.n):
+            yield self.make(l)
+
+
+def build_model(shape: FX.ModelShape, max_pos: int, taps: int = 1, lazy: bool = False, source=None) -> Model:
     """Materialise the seeded weights of ``shape`` (norm gains are 1, no biases); taps = 3 adds the
     fused-feature matrix. With shape.weight_bits = 4 the target's decoder-layer projections are the
-    dequantised int4 codes and scales (oracle/quant.py)."""
+    dequantised int4 codes and scales (oracle/quant.py). lazy: the target layers are regenerated on every
+    use instead of held (LazyLayers). source(name, layer) (optional) supplies a target projection as float32
+    in place of fixtures.target_tensor: another implementation of the same seeded recipe (a faster one for
+    very large shapes); it must give the same values."""
     def layer(get) -> LayerWeights:
         return LayerWeights(**{k: get(k) for k in FX.layer_shapes(shape)},
                             attn_norm=_ones(shape.d), ffn_norm=_ones(shape.d))
@@ -82,9 +106,12 @@ def build_model(shape: FX.ModelShape, max_pos: int, taps: int = 1) -> Model:
     def target(k: str, l: int) -> np.ndarray:
         if shape.weight_bits == 4:
             return quant.dequantize(FX.int4_codes(shape, l, k), FX.int4_scales(shape, l, k))
-        return FX.target_tensor(shape, k, l)
+        return source(k, l) if source is not None else FX.target_tensor(shape, k, l)
 
-    layers = [layer(lambda k, l=l: target(k, l)) for l in range(shape.n_layers)]
+    if lazy:
+        layers = LazyLayers(shape.n_layers, lambda l: layer(lambda k: target(k, l)))
+    else:
+        layers = [layer(lambda k, l=l: target(k, l)) for l in range(shape.n_layers)]
     head = layer(lambda k: FX.head_tensor(shape, k))
     cos, sin = rope_tables(shape.rope_theta, shape.head_dim, max_pos)
     return Model(shape=shape, embed=FX.target_tensor(shape, "embed"),

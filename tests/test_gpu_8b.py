@@ -213,3 +213,52 @@ def test_8b_full_depth_against_oracle(cuda, oracle_8b_full, name):
         assert int(a[0]) == OD.accept_commit(st, gt, g_am, ofeats)
     print(f"{name} full depth: {same}/6 draft trees identical, max |logit err| {worst:.4f}, {flagged} flagged near-ties, "
           f"committed {st.out[:12]}...")
+
+
+def test_70b_full_depth_against_oracle(cuda):
+    """The 80-layer 70B-shaped model against the oracle at full depth (the oracle regenerates each layer on
+    use: 280 GB of float32 weights do not fit the host): 48-token prompt, 2 EAGLE-2 steps; draft trees
+    (or flagged near-ties), verify logits, greedy tokens except at flagged near-ties, accepted lengths.
+
+    Logit bound: the 0.05 max-abs of the bf16 configs holds at 2 layers of this width and for the 32-layer
+    8B (0.026), but over 80 layers the half-precision rounding of K, V, q and P in attention adds up: the
+    GPU measured 0.109 max-abs at cosine 0.99995. This test bounds it at 0.15 (cosine >= 0.999) and flags
+    argmax differences where the oracle's top-2 margin is below 0.3 (twice the bound)."""
+    from eagle_speculative_decoding_02_gb300 import synthetic as S
+    from tests.test_gpu_draft import _gpu_tree, check_draft
+    from fixtures import device as FD
+    w = dataclasses.replace(FX.WORKLOADS["70b_eagle2"], prompt_len=48, max_new=16)
+    cap = FX.kv_capacity(w)
+    # the layers come from the device implementation of the fixture recipe, one at a time (80 layers on the
+    # host cores would take minutes per pass); spot-checked here against the host implementation
+    src = lambda k, l: FD.target_tensor(FX.LLAMA3_70B, k, l, device=cuda).float().cpu().numpy()
+    for k in ("wq", "wd"):
+        np.testing.assert_array_equal(src(k, 79)[:64], FX.target_tensor(FX.LLAMA3_70B, k, 79, rows=slice(0, 64)))
+    m = OM.build_model(FX.LLAMA3_70B, cap, lazy=True, source=src)
+    prompt = FX.prompts(FX.LLAMA3_70B, 1, w.prompt_len)
+    eng = S.make_engine(w)
+    root = eng.prefill(torch.from_numpy(prompt).to(cuda)).cpu().numpy()
+    st = OD.prefill(m, prompt[0], cap)
+    assert root[0] == st.root or _margins(OM.logits_of(m, st.pend_feats[-1:]))[0] < 0.3
+    worst, flagged = 0.0, 0
+    for step in range(2):
+        gtree = eng.draft_tree()
+        gt = _gpu_tree(gtree)
+        # at the 70B width a deep node's draft log-probability carries the differences of the head passes
+        # behind it (features of width 8192 through up to 5 head passes): tolerance 0.05 per pass
+        check_draft(m, st, w, gt, 0.05, per_depth=True)
+        am, lg = eng.verify(gtree, logits=True)
+        oam, ofeats, ologits = OD.verify(m, st, gt)
+        got = lg[0, : gt.n + 1].cpu().numpy()
+        err = float(np.abs(got - ologits).max())
+        cos = float((got.ravel() @ ologits.ravel()) / (np.linalg.norm(got) * np.linalg.norm(ologits)))
+        worst = max(worst, err)
+        assert err < 0.15 and cos >= 0.999, (step, err, cos)
+        g_am = am[0, : gt.n + 1].cpu().numpy()
+        assert not ((g_am != oam) & (_margins(ologits) >= 0.3)).any(), step
+        flagged += int((g_am != oam).sum())
+        a, _ = eng.accept_commit()
+        assert int(a[0]) == OD.accept_commit(st, gt, g_am, ofeats)
+    print(f"70B full depth: max |logit err| {worst:.4f}, {flagged} flagged near-ties")
+    del eng
+    torch.cuda.empty_cache()

@@ -114,3 +114,20 @@ def test_tree_attention_equals_causal_attention_on_each_path():
         n = len(path)
         f = OM.target_rows(m, kvp, tree.tokens[path], L + np.arange(n), L + np.arange(n), OM.causal_visible(L, n))
         np.testing.assert_allclose(feats[j], f[-1], rtol=1e-4, atol=1e-5)
+
+
+def test_lazy_layers_equal_materialised_layers():
+    """The lazily generated target layers (used for models larger than host memory) are the same weights."""
+    import dataclasses
+    import fixtures as FX
+    from oracle import decode as OD
+    from oracle import model as OM
+    shape = FX.TINY.reduced(n_layers=2)
+    m, z = OM.build_model(shape, 128), OM.build_model(shape, 128, lazy=True)
+    assert len(z.layers) == 2
+    for l in range(2):
+        for k in ("wq", "wo", "wd"):
+            np.testing.assert_array_equal(getattr(m.layers[l], k), getattr(z.layers[l], k))
+    p = FX.prompts(shape, 1, 16)[0]
+    w = dataclasses.replace(FX.WORKLOADS["tiny_static"], max_new=6)
+    assert OD.speculative_generate(z, p, w, cap=128).out == OD.speculative_generate(m, p, w, cap=128).out
