@@ -71,7 +71,7 @@ struct Group {
 
 enum EpiKind : int {
   kEpiStore = 0,   // y_f32[m][n] = acc * r_m
-  kEpiQkv = 1,     // RoPE on q/k, q -> out, k/v -> KV cache slots
+  kEpiQkv = 1,     // RoPE on q/k, q -> out (when set) and qg, k/v -> KV cache slots
   kEpiSwiglu = 2,  // silu(gate) * up over interleaved 64-row blocks -> out
   kEpiResid = 3,   // h += acc; hb = h * gain_next; per-tile sum of squares of h
   kEpiFc = 4,      // h = acc; hb = h * gain_next; per-tile sum of squares

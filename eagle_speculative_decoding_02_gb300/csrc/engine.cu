@@ -541,7 +541,9 @@ struct Eng {
     const Rows rows = rows_at(c->rows, row0);
     EpiParams e = epi(c, kEpiQkv, M, dm.nqkv);
     e.ssq_in = c->ssq_b; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d;
-    e.out = c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
+    // float32 queries only for the SIMT attention of float32 models; the tcgen05
+    // attention of bf16 models reads the grouped half queries
+    e.out = sizeof(T) == 2 ? nullptr : c->q; e.q_dim = dm.qd; e.kv_dim = dm.kvd; e.head_dim = dm.hd; e.n_kv = dm.Hkv; e.cap = cap;
     const float scale = 1.f / std::sqrt((float)dm.hd);
     e.qg = c->qg; e.qg_scale = scale * 1.4426950408889634f;
     e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = rows;

@@ -183,7 +183,7 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
               v = i < half ? v * cs[q] - pv * sn[q] : v * cs[q] + pv * sn[q];
             }
             if (region == 0) {
-              reinterpret_cast<float*>(out)[(size_t)(m0 + m) * q_dim + n] = v;
+              if (out) reinterpret_cast<float*>(out)[(size_t)(m0 + m) * q_dim + n] = v;
               if (qgc) qgc[(size_t)(m0 + m) * qg_row] = __float2half_rn(v * qg_scale);
             } else if (rslot[m] >= 0) {
               const size_t at = (((size_t)rseq[m] * n_kv + kvh) * cap + rslot[m]) * hd + i;

@@ -254,7 +254,11 @@ template <int HD, bool W4>
 __global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel(StackArgs a) {
   constexpr int NT = W4 ? kThreadsW4 : kThreads;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned (128-byte swizzled TMA boxes) by an offset from the shared
+  // array itself: a pointer rebuilt from an integer loses its address space, and
+  // every access through it is then a generic one (measured: the merge phase 10.5
+  // -> 8.7 us, the verify 4.16 -> 4.10 ms with shared-space accesses)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = a.sw, MT = a.MT;
   const int accw = a.has_lo ? 2 * MT : MT;  // accumulator columns of one tile
   const int abufw = accw;                   // accumulator columns of one buffer
@@ -282,8 +286,8 @@ __global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel
   volatile int* exit_last = abort_flag + 2;
   Group* sgroups = reinterpret_cast<Group*>(tmem_slot + 4);  // kMaxGroups entries
   // int4 variant: the packed-block ring and its barriers after the groups
-  uint64_t* rfull = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sgroups + kMaxGroups) + 15) &
-                                                ~uintptr_t(15));
+  uint8_t* const rbase = reinterpret_cast<uint8_t*>(sgroups + kMaxGroups);
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(rbase + ((16u - (smem_u32(rbase) & 15u)) & 15u));
   uint64_t* rempty = rfull + a.rw;
   uint8_t* rraw = reinterpret_cast<uint8_t*>(rempty + a.rw);  // 16-byte aligned (2 rw barriers of 8 bytes)
 
