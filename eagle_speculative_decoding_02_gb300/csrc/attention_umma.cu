@@ -35,7 +35,8 @@ constexpr size_t um_launch_smem() {
 template <int HD>
 __device__ __forceinline__ void um_launch_layout(uint8_t* raw, uint8_t*& sm, uint64_t*& bars, uint32_t*& tmem_slot,
                                                  volatile int*& abort_flag, Group*& sg) {
-  sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  // an offset from the shared array keeps the pointers in the shared address space
+  sm = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
   bars = reinterpret_cast<uint64_t*>(sm + attn::um_smem_bytes<HD>());
   tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
   abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);

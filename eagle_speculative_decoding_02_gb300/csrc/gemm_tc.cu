@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, TcArgs a, EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // an offset from the shared array keeps the pointers in the shared address space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = a.stages, MT = a.MT;
   const int xbytes = MT * kBK * 2;
   const int stage_bytes = kWBytes + xbytes * (a.has_lo ? 2 : 1);
