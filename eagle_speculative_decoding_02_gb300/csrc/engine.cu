@@ -652,13 +652,22 @@ struct Eng {
     return nullptr;
   }
 
-  static eagle_status run_prog(eagle_ctx* c, const ProgSpec& p, float* lm_logits = nullptr) {
+  // Runs a recorded program; a program ending in the LM head merges its top-k
+  // records in the same launch into idx / val / lse (k per row, as lm_head_merge).
+  static eagle_status run_prog(eagle_ctx* c, const ProgSpec& p, float* lm_logits, int k, int* idx, float* val,
+                               float* lse) {
     unsigned long long* trace = p.kind == 0 ? c->trace : nullptr;
     const Group* g = p.kind == 0 ? c->groups_local + p.seq0 : c->groups;
     const int ng = p.kind == 0 ? p.n_seq : c->dm.B;
+    TopkMerge mg;
+    if (k > 0) {
+      mg.val = c->rec_val; mg.idx = c->rec_idx; mg.mx = c->rec_max; mg.sum = c->rec_sum;
+      mg.ntiles = c->dm.ntV; mg.M = p.M; mg.k = k;
+      mg.out_idx = idx; mg.out_val = val; mg.out_lse = lse;
+    }
     EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
                     c->stack_scratch, c->dm.stack_phases_max, c->dm.stack_counters_max, c->st.status, trace,
-                    lm_logits, g, ng, p.first_attn, c->stream, p.w4));
+                    lm_logits, g, ng, p.first_attn, c->stream, p.w4, &mg));
     return EAGLE_OK;
   }
 
@@ -707,11 +716,14 @@ struct Eng {
                       c->stream));
     const ProgSpec* p = n_groups == dm.B ? find_prog(c, 1, M, hbase, k) : nullptr;
     if (p) {
-      EG_TRY(run_prog(c, *p));
+      EG_TRY(run_prog(c, *p, nullptr, 0, nullptr, nullptr, nullptr));
     } else {
       Direct d{c};
       EG_TRY(draft_ops(c, d, M, n_groups, hbase, k));
     }
+    // (the draft's top-10 merge stays a kernel of its own: merged inside the
+    // persistent launch by one CTA per row, the 10 rows' merges made every draft
+    // program tens of microseconds longer than the 512-thread merge kernel)
     if (k > 0)
       EG_TRY(lm_head_merge(c, M, k, c->dtopk_idx + (size_t)hbase * k, c->dtopk_val + (size_t)hbase * k,
                            c->dlse + hbase));
@@ -780,8 +792,8 @@ struct Eng {
           // one persistent launch for every layer and the LM head (which also stores the logits if
           // wanted), per chunk of the batch when its rows exceed one launch
           EG_TRY(embed(c, p.M, p.row0));
-          EG_TRY(run_prog(c, p, d_logits ? d_logits + (size_t)p.row0 * dm.V : nullptr));
-          EG_TRY(lm_head_merge(c, p.M, 1, c->vargmax + p.row0, nullptr, nullptr));
+          EG_TRY(run_prog(c, p, d_logits ? d_logits + (size_t)p.row0 * dm.V : nullptr, 1, c->vargmax + p.row0,
+                          nullptr, nullptr));  // merge included
           persistent = true;
         }
     if (!persistent) {

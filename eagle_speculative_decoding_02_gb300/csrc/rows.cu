@@ -1,6 +1,7 @@
 // Row-wise kernels: embedding gather, draft-head FC input, row gather and the
 // LM-head top-k merge across vocab tiles.
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace eg {
 namespace {
@@ -95,134 +96,14 @@ __global__ void gather_rows_kernel(const T* __restrict__ hb, const bf16* __restr
 // combines the pairs in fixed order and merges the lists.
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
-__global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const float* __restrict__ rec_val,
-                                                                   const int* __restrict__ rec_idx,
-                                                                   const float* __restrict__ rec_max,
-                                                                   const float* __restrict__ rec_sum, int ntiles,
-                                                                   int M, int k, int* out_idx, float* out_val,
-                                                                   float* out_lse) {
+__global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(TopkMerge g) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red_m[kMergeWarps], red_s[kMergeWarps];
-  __shared__ float sv[kMergeWarps];
-  __shared__ int si[kMergeWarps];
-  const int m = blockIdx.x, tid = threadIdx.x;
-  // (max, sum of exp(x - max)) pairs: combining keeps the larger max
-  auto combine = [](float& am, float& as, float bm, float bs) {
-    if (bm == -INFINITY) return;
-    if (am == -INFINITY) {
-      am = bm;
-      as = bs;
-    } else if (bm > am) {
-      as = as * __expf(am - bm) + bs;
-      am = bm;
-    } else {
-      as += bs * __expf(bm - am);
-    }
+  __shared__ float red[4 * kMergeWarps];
+  struct Sync {
+    __device__ void operator()() const { __syncthreads(); }
   };
-  float rm = -INFINITY, rs = 0.f;
-  // Each thread keeps the k best of its candidates (value desc, index asc), sorted, in registers.
-  float lv[kMaxTopK];
-  int li[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    lv[j] = -INFINITY;
-    li[j] = 0x7fffffff;
-  }
-  constexpr int kU = 2;
-  for (int t0 = tid; t0 < ntiles; t0 += kU * kMergeThreads) {
-    float tm[kU], ts[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int t = t0 + u * kMergeThreads;
-      const size_t r = (size_t)t * M + m;
-      tm[u] = t < ntiles ? rec_max[r] : -INFINITY;
-      ts[u] = t < ntiles ? rec_sum[r] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) combine(rm, rs, tm[u], ts[u]);
-    for (int u = 0; u < kU; ++u) {
-      const int t = t0 + u * kMergeThreads;
-      if (t >= ntiles) break;
-      // the tile's best is its max: nothing of the tile enters unless that does
-      if (!(tm[u] >= lv[k - 1])) continue;
-      const size_t base = ((size_t)t * M + m) * k;
-      float cv[kMaxTopK];
-      int cx[kMaxTopK];
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {  // the tile's candidates, all loads in flight
-        cv[j] = j < k ? rec_val[base + j] : -INFINITY;
-        cx[j] = j < k ? rec_idx[base + j] : -1;
-      }
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        // candidates of one tile arrive sorted: once one misses the list, the rest of the tile does too
-        if (j >= k || cx[j] < 0 || !(cv[j] > lv[k - 1] || (cv[j] == lv[k - 1] && cx[j] < li[k - 1]))) break;
-        float c = cv[j];
-        int ci = cx[j];
-#pragma unroll
-        for (int q = 0; q < kMaxTopK; ++q) {
-          if (q < k && (c > lv[q] || (c == lv[q] && ci < li[q]))) {
-            const float tv = lv[q];
-            const int ti = li[q];
-            lv[q] = c;
-            li[q] = ci;
-            c = tv;
-            ci = ti;
-          }
-        }
-      }
-    }
-  }
-  // (max, sum) over the block: warps by shuffles, then the warps in order
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, rm, o), os = __shfl_xor_sync(0xffffffffu, rs, o);
-    combine(rm, rs, om, os);
-  }
-  if ((tid & 31) == 0) {
-    red_m[tid >> 5] = rm;
-    red_s[tid >> 5] = rs;
-  }
-  __syncthreads();
-  if (tid == 0 && out_lse) {
-    float gm = red_m[0], gs = red_s[0];
-    for (int w = 1; w < kMergeWarps; ++w) combine(gm, gs, red_m[w], red_s[w]);
-    out_lse[m] = gm + __logf(gs);
-  }
-
-  // k rounds of a block arg-max over the heads of the sorted lists
-  int head = 0;
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int q = 0; q < kMaxTopK; ++q)
-      if (q == head) {
-        bv = lv[q];
-        bi = li[q];
-      }
-    const int mine = bi;
-    warp_argmax(bv, bi);
-    __syncthreads();
-    if ((tid & 31) == 0) {
-      sv[tid >> 5] = bv;
-      si[tid >> 5] = bi;
-    }
-    __syncthreads();
-    bv = sv[0];
-    bi = si[0];
-    for (int w = 1; w < kMergeWarps; ++w)
-      if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) {
-        bv = sv[w];
-        bi = si[w];
-      }
-    if (mine == bi && head < k) ++head;  // indices are unique: exactly one list owns the winner
-    if (tid == 0) {
-      out_idx[(size_t)m * k + r] = bi == 0x7fffffff ? -1 : bi;
-      if (out_val) out_val[(size_t)m * k + r] = bv;
-    }
-  }
+  topk_merge_row<kMergeThreads>(g, blockIdx.x, threadIdx.x, red, Sync{});
 }
 
 }  // namespace
@@ -258,7 +139,18 @@ cudaError_t gather_rows(const T* hb, const bf16* hb_lo, const float* ssq, int M_
 cudaError_t topk_merge(const float* rec_val, const int* rec_idx, const float* rec_max, const float* rec_sum,
                        int ntiles, int M, int k, int* idx, float* val, float* lse, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  return launch_pdl(topk_merge_kernel, dim3(M), dim3(kMergeThreads), 0, s, rec_val, rec_idx, rec_max, rec_sum, ntiles, M, k, idx, val, lse);
+  TopkMerge g;
+  g.val = rec_val;
+  g.idx = rec_idx;
+  g.mx = rec_max;
+  g.sum = rec_sum;
+  g.ntiles = ntiles;
+  g.M = M;
+  g.k = k;
+  g.out_idx = idx;
+  g.out_val = val;
+  g.out_lse = lse;
+  return launch_pdl(topk_merge_kernel, dim3(M), dim3(kMergeThreads), 0, s, g);
 }
 
 #define EG_INST(T)                                                                                          \

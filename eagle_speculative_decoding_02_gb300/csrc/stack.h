@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace eg {
 
@@ -80,9 +81,12 @@ size_t stack_attention_part_bytes(int M, int Hq, int Hkv, int hd, int max_prefix
 // first_attn: index of the program's first attention phase (-1 if none); every
 // attention phase of a program has the same rows, heads and groups.
 // w4: the program has int4 phases (the 352-thread variant with converter warps).
+// merge (may be NULL; merge->k == 0: none): the last phase is an LM head whose
+// top-k records are merged in the same launch (merge->M <= M rows, CTA c taking
+// row c once every CTA has finished that phase) instead of by topk_merge.
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
                       void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
                       float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s,
-                      bool w4 = false);
+                      bool w4 = false, const TopkMerge* merge = nullptr);
 
 }  // namespace eg

@@ -55,6 +55,7 @@
 #include "int4.cuh"
 #include "stack.h"
 #include "tc_ptx.cuh"
+#include "topk.cuh"
 
 namespace eg {
 namespace {
@@ -96,6 +97,7 @@ struct StackArgs {
   const Group* groups;        // attention groups of every attention phase (NULL if none)
   int n_groups;               // <= kMaxGroups
   int first_attn;             // index of the first attention phase, -1 if none (all share rows and groups)
+  TopkMerge mg;               // mg.k > 0: merge of the last (LM-head) phase's records, CTA c taking row c
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -774,6 +776,13 @@ __global__ void __launch_bounds__(W4 ? kThreadsW4 : kThreads, 1) stack_tc_kernel
         if (a.trace) a.trace[(size_t)p * G + c] = globaltimer();
       }
     }
+    // The LM head's top-k records merged in the same launch (instead of a kernel
+    // of its own after it): once every CTA has finished the last phase, CTA c
+    // merges row c (M <= 128 rows, fewer than CTAs) with its epilogue threads.
+    if (alive && a.mg.k > 0 && c < a.mg.M) {
+      alive = epi_all(etid != 0 || wait_phase(a, a.n_phases - 1, (unsigned)G, abort_flag));
+      if (alive) topk_merge_row<kEpiThreads>(a.mg, c, etid, tile, EpilogueSync{});
+    }
   }
   // the producer and MMA roles ran on lane 0 only: reconverge each warp before the
   // block barrier and the warp-wide (.sync.aligned) TMEM dealloc
@@ -928,7 +937,7 @@ void StackProgramBuilder::attention(const AttnArgs& a) {
 cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_lo, int hd, int n_counters,
                       void* scratch, int max_phases, int max_counters, int* status, unsigned long long* trace,
                       float* y_last, const Group* groups, int n_groups, int first_attn, cudaStream_t s,
-                      bool w4) {
+                      bool w4, const TopkMerge* merge) {
   if (!stack_supported(M, hd) || n_phases <= 0 || !scratch || n_phases > max_phases || n_counters > max_counters)
     return cudaErrorInvalidValue;
   if (n_groups < 0 || n_groups > kMaxGroups || (n_groups > 0 && !groups)) return cudaErrorInvalidValue;
@@ -963,6 +972,12 @@ cudaError_t stack_run(const StackPhase* d_phases, int n_phases, int M, bool has_
   a.groups = groups;
   a.n_groups = n_groups;
   a.first_attn = first_attn < n_phases ? first_attn : -1;
+  if (merge && merge->k > 0) {
+    if (merge->k > kMaxTopK || merge->M > M || merge->M > num_sms() || !merge->out_idx || !merge->val ||
+        !merge->idx || !merge->mx || !merge->sum || merge->ntiles < 1)
+      return cudaErrorInvalidValue;
+    a.mg = *merge;
+  }
   auto kernel = w4 ? (hd == 128 ? stack_tc_kernel<128, true> : stack_tc_kernel<64, true>)
                    : (hd == 128 ? stack_tc_kernel<128, false> : stack_tc_kernel<64, false>);
   if (!raise_smem_limit(reinterpret_cast<const void*>(kernel), kSmemBudget)) return cudaErrorInvalidValue;
@@ -1043,11 +1058,21 @@ eagle_status eagle_op_gemm_persistent(int32_t M, int32_t N, int32_t K, int32_t n
   if (cudaMemcpyAsync(d_prog, b.phases.data(), b.phases.size() * sizeof(StackPhase), cudaMemcpyHostToDevice, s) !=
       cudaSuccess)
     return EAGLE_ERR_CUDA;
+  TopkMerge mg;  // the top-k merge runs inside the launch, after the LM-head phase
+  if (k > 0) {
+    mg.val = lm.rec_val;
+    mg.idx = lm.rec_idx;
+    mg.mx = lm.rec_max;
+    mg.sum = lm.rec_sum;
+    mg.ntiles = (N + kTileN - 1) / kTileN;
+    mg.M = M;
+    mg.k = k;
+    mg.out_idx = idx;
+    mg.out_val = val;
+    mg.out_lse = lse;
+  }
   cudaError_t err = stack_run(d_prog, n_phases, M, x_lo != nullptr, 128, b.n_counters, p, n_phases, b.n_counters,
-                              nullptr, nullptr, nullptr, nullptr, 0, -1, s);
-  if (err == cudaSuccess && k > 0)
-    err = topk_merge(lm.rec_val, lm.rec_idx, lm.rec_max, lm.rec_sum, (N + kTileN - 1) / kTileN, M, k, idx, val, lse,
-                     s);
+                              nullptr, nullptr, nullptr, nullptr, 0, -1, s, false, &mg);
   if (err == cudaSuccess) err = cudaStreamSynchronize(s);  // b.phases is a host temporary
   return err == cudaSuccess ? EAGLE_OK : (err == cudaErrorInvalidValue ? EAGLE_ERR_UNSUPPORTED : EAGLE_ERR_CUDA);
 }
