@@ -478,8 +478,14 @@ struct Eng {
     return EAGLE_OK;
   }
 
-  // low halves of the hi/lo activation pairs (bf16 models only)
-  static bf16* lo(bf16* p) { return sizeof(T) == 2 ? p : nullptr; }
+  // Low halves of the hi/lo activation pairs: bf16 models carry every GEMM and
+  // attention activation as a hi/lo bf16 pair (about float32 precision at no
+  // HBM cost: the weights set the bytes). Weight-only int4 models do not
+  // (W4A16: bf16 activations): their 4-bit weights err far more than a bf16
+  // activation does, so the pairs' second operand bought no accuracy there and
+  // cost MMA work and ring space (8B int4 verify 5.78 -> 5.53 ms without it).
+  static bool pairs(const eagle_ctx* c) { return sizeof(T) == 2 && !c->dm.w4; }
+  static bf16* lo(const eagle_ctx* c, bf16* p) { return pairs(c) ? p : nullptr; }
 
   static EpiParams epi(eagle_ctx* c, int kind, int M, int N) {
     EpiParams e;
@@ -547,28 +553,28 @@ struct Eng {
     const float scale = 1.f / std::sqrt((float)dm.hd);
     e.qg = c->qg; e.qg_scale = scale * 1.4426950408889634f;
     e.rope_cos = c->rope_cos; e.rope_sin = c->rope_sin; e.kc = kc; e.vc = vc; e.rows = rows;
-    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e, lw.w4));
+    EG_TRY(sink.gemm(c->hb, lo(c, c->hb_lo), lw.wqkv, M, dm.nqkv, dm.d, e, lw.w4));
 
     AttnArgs a{};
-    a.q = (const float*)c->q; a.qg = c->qg; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c->attn_lo);
+    a.q = (const float*)c->q; a.qg = c->qg; a.kc = kc; a.vc = vc; a.o = c->attn; a.o_lo = lo(c, c->attn_lo);
     a.groups = groups ? groups : c->groups; a.n_groups = n_groups;
     a.mask = rows.mask; a.row_grp = rows.grp; a.M = M; a.Hq = dm.Hq; a.Hkv = dm.Hkv; a.hd = dm.hd; a.cap = cap; a.n_seq = dm.B;
     a.max_prefix = cap; a.scale = scale; a.part = c->attn_part; a.status = c->st.status;
     EG_TRY(sink.attention(a));
 
     e = epi(c, kEpiResid, M, dm.d);
-    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
-    EG_TRY(sink.gemm(c->attn, lo(c->attn_lo), lw.wo, M, dm.d, dm.qd, e, lw.w4));
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c, c->hb_lo); e.ssq_out = c->ssq_a; e.gain = lw.ffn_norm;
+    EG_TRY(sink.gemm(c->attn, lo(c, c->attn_lo), lw.wo, M, dm.d, dm.qd, e, lw.w4));
 
     e = epi(c, kEpiSwiglu, M, 2 * dm.ffn);
     e.ssq_in = c->ssq_a; e.n_ssq_in = dm.d / kTileN; e.inv_d_in = 1.f / dm.d; e.out = c->act; e.ffn = dm.ffn;
-    e.out_lo = lo(c->act_lo);
-    EG_TRY(sink.gemm(c->hb, lo(c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e, lw.w4));
+    e.out_lo = lo(c, c->act_lo);
+    EG_TRY(sink.gemm(c->hb, lo(c, c->hb_lo), lw.wgu, M, 2 * dm.ffn, dm.d, e, lw.w4));
 
     e = epi(c, kEpiResid, M, dm.d);
-    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = gain_next;
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c, c->hb_lo); e.ssq_out = c->ssq_b; e.gain = gain_next;
     e.h_tap = tap; e.h_tap2 = tap2;
-    EG_TRY(sink.gemm(c->act, lo(c->act_lo), lw.wd, M, dm.d, dm.ffn, e, lw.w4));
+    EG_TRY(sink.gemm(c->act, lo(c, c->act_lo), lw.wd, M, dm.d, dm.ffn, e, lw.w4));
     return EAGLE_OK;
   }
 
@@ -623,7 +629,7 @@ struct Eng {
   static eagle_status embed(eagle_ctx* c, int M, int row0 = 0) {
     const Dims& dm = c->dm;
     EG_CK(embed_rows<T>((const T*)c->embed, c->rows.tok + row0, M, dm.d, c->layers[0].attn_norm,
-                        c->h_tgt + (size_t)row0 * dm.d, (T*)c->hb, lo(c->hb_lo), c->ssq_b, c->stream));
+                        c->h_tgt + (size_t)row0 * dm.d, (T*)c->hb, lo(c, c->hb_lo), c->ssq_b, c->stream));
     return EAGLE_OK;
   }
 
@@ -639,10 +645,10 @@ struct Eng {
     const Dims& dm = c->dm;
     float* h = c->h_dft + (size_t)hbase * dm.d;
     EpiParams e = epi(c, kEpiFc, M, dm.d);
-    e.h = h; e.hb = c->hb; e.hb_lo = lo(c->hb_lo); e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
-    EG_TRY(sink.gemm(c->xfc, lo(c->xfc_lo), c->fc, M, dm.d, 2 * dm.d, e));
+    e.h = h; e.hb = c->hb; e.hb_lo = lo(c, c->hb_lo); e.ssq_out = c->ssq_b; e.gain = c->head.attn_norm;
+    EG_TRY(sink.gemm(c->xfc, lo(c, c->xfc_lo), c->fc, M, dm.d, 2 * dm.d, e));
     EG_TRY(layer(c, sink, c->head, c->kc_d, c->vc_d, dm.cap_d, M, n_groups, h, c->final_norm));
-    if (k > 0) EG_TRY(lm_head_gemm(c, sink, c->hb, lo(c->hb_lo), c->ssq_b, M, k, nullptr));
+    if (k > 0) EG_TRY(lm_head_gemm(c, sink, c->hb, lo(c, c->hb_lo), c->ssq_b, M, k, nullptr));
     return EAGLE_OK;
   }
 
@@ -665,7 +671,7 @@ struct Eng {
       mg.ntiles = c->dm.ntV; mg.M = p.M; mg.k = k;
       mg.out_idx = idx; mg.out_val = val; mg.out_lse = lse;
     }
-    EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, sizeof(T) == 2, c->dm.hd, p.n_counters,
+    EG_CK(stack_run(c->stack_prog + p.first, p.n_phases, p.M, pairs(c), c->dm.hd, p.n_counters,
                     c->stack_scratch, c->dm.stack_phases_max, c->dm.stack_counters_max, c->st.status, trace,
                     lm_logits, g, ng, p.first_attn, c->stream, p.w4, &mg));
     return EAGLE_OK;
@@ -680,11 +686,11 @@ struct Eng {
       StackProgramBuilder b;
       b.M = p.M;
       b.MT = stack_mt(p.M);
-      b.has_lo = true;
+      b.has_lo = pairs(c);
       Record r{c, &b};
       if (p.kind == 0) {
         EG_TRY(target_layers(c, r, p.M, p.n_seq, p.row0, c->groups_local + p.seq0));
-        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c->hb_lo), c->ssq_b, p.M, 1, nullptr, true, nullptr, p.row0));
+        EG_TRY(lm_head_gemm(c, r, c->hb, lo(c, c->hb_lo), c->ssq_b, p.M, 1, nullptr, true, nullptr, p.row0));
       } else {
         EG_TRY(draft_ops(c, r, p.M, dm.B, p.hbase, p.k));
       }
@@ -703,16 +709,16 @@ struct Eng {
   // Fused-feature variant: fused[m] = fuse [low[m] ; mid[m] ; top[m]] for M rows (one GEMM, K = 3d).
   static eagle_status fuse_features(eagle_ctx* c, const float* low, const float* mid, const float* top, int M) {
     const Dims& dm = c->dm;
-    EG_CK(pack_taps<T>(low, mid, top, M, dm.d, (T*)c->xfc, lo(c->xfc_lo), c->stream));
+    EG_CK(pack_taps<T>(low, mid, top, M, dm.d, (T*)c->xfc, lo(c, c->xfc_lo), c->stream));
     EpiParams e = epi(c, kEpiStore, M, dm.d);
     e.y = c->fused;
-    return gemm(c, c->xfc, lo(c->xfc_lo), c->fuse, M, dm.d, 3 * dm.d, e);
+    return gemm(c, c->xfc, lo(c, c->xfc_lo), c->fuse, M, dm.d, 3 * dm.d, e);
   }
 
   // Draft head over the phase's rows: FC([feature ; E(token)]) then the head layer, then (k > 0) LM-head top-k.
   static eagle_status draft_forward(eagle_ctx* c, const float* feat, int M, int n_groups, int hbase, int k) {
     const Dims& dm = c->dm;
-    EG_CK(fc_input<T>(feat, c->rows.fsrc, (const T*)c->embed, c->rows.tok, M, dm.d, (T*)c->xfc, lo(c->xfc_lo),
+    EG_CK(fc_input<T>(feat, c->rows.fsrc, (const T*)c->embed, c->rows.tok, M, dm.d, (T*)c->xfc, lo(c, c->xfc_lo),
                       c->stream));
     const ProgSpec* p = n_groups == dm.B ? find_prog(c, 1, M, hbase, k) : nullptr;
     if (p) {
@@ -741,9 +747,9 @@ struct Eng {
         std::vector<int> src(dm.B);
         for (int b = 0; b < dm.B; ++b) src[b] = b * cl + cl - 1;
         EG_CK(cudaMemcpyAsync(c->lm_src, src.data(), dm.B * sizeof(int), cudaMemcpyHostToDevice, c->stream));
-        EG_CK(gather_rows<T>((const T*)c->hb, lo(c->hb_lo), c->ssq_b, M, c->lm_src, dm.B, dm.d, (T*)c->lm_hb,
-                             lo(c->lm_hb_lo), c->lm_ssq, c->stream));
-        EG_TRY(lm_head(c, c->lm_hb, lo(c->lm_hb_lo), c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr,
+        EG_CK(gather_rows<T>((const T*)c->hb, lo(c, c->hb_lo), c->ssq_b, M, c->lm_src, dm.B, dm.d, (T*)c->lm_hb,
+                             lo(c, c->lm_hb_lo), c->lm_ssq, c->stream));
+        EG_TRY(lm_head(c, c->lm_hb, lo(c, c->lm_hb_lo), c->lm_ssq, dm.B, 1, c->root_idx, nullptr, nullptr, nullptr,
                        true, c->lm_src));
         EG_CK(prefill_finish(c->st, c->root_idx, c->h_tgt, c->h_low, c->h_mid, cl, P, root_out, c->stream));
         EG_CK(cudaStreamSynchronize(c->stream));  // src is a host temporary
@@ -798,7 +804,7 @@ struct Eng {
         }
     if (!persistent) {
       EG_TRY(target_stack(c, M, dm.B));
-      EG_TRY(lm_head(c, c->hb, lo(c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits, true));
+      EG_TRY(lm_head(c, c->hb, lo(c, c->hb_lo), c->ssq_b, M, 1, c->vargmax, nullptr, nullptr, d_logits, true));
     }
     if (d_argmax)
       EG_CK(cudaMemcpyAsync(d_argmax, c->vargmax, (size_t)M * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
