@@ -38,8 +38,9 @@
  * softmax statistics in float32, and feed every GEMM with activations split
  * into hi/lo bfloat16 pairs (x = hi + lo, two tensor-core products accumulated
  * in float32), so GEMM inputs carry ~16 significant bits (tcgen05 tensor-core
- * GEMMs). Attention products are half x half with float32 accumulation (mma
- * tensor-core attention).
+ * GEMMs); models with int4 target projections (weight_bits = 4) feed their
+ * GEMMs plain bfloat16 activations instead (W4A16). Attention products are
+ * half x half with float32 accumulation (tcgen05 tensor-core attention).
  */
 #ifndef EAGLE_H
 #define EAGLE_H
@@ -131,7 +132,8 @@ typedef struct {
    * EAGLE combines with GPTQ / AWQ 4-bit weight-quantised targets): 0 or 16 =
    * `dtype` elements; 4 = weight-only int4 (each of wqkv, wo, wgu, wd points to
    * eagle_int4_pack's block layout; symmetric, a bf16 scale per row and group of
-   * 64 inputs, W = bf16(scale * (code - 8))). Activations keep `dtype`; the
+   * 64 inputs, W = bf16(scale * (code - 8))). Activations are plain bf16 (no
+   * hi/lo pairs: W4A16); the
    * embedding, LM head, norms and the draft head are not quantised. Needs d, the
    * query width and ffn to be multiples of 64. */
   int32_t weight_bits;
