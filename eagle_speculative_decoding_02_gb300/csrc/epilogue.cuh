@@ -97,6 +97,45 @@ __device__ inline void load_epi_rows(const EpiParams& p, int m0, int msub, EpiRo
   }
 }
 
+// Four neighbouring elements of a staged tile row (one 16-byte access when the
+// leading dimension keeps them aligned).
+__device__ __forceinline__ float4 ld_tile4(const float* p, int ldt) {
+  if ((ldt & 3) == 0) return *reinterpret_cast<const float4*>(p);
+  return make_float4(p[0], p[1], p[2], p[3]);
+}
+__device__ __forceinline__ void st_tile4(float* p, int ldt, float4 v) {
+  if ((ldt & 3) == 0) {
+    *reinterpret_cast<float4*>(p) = v;
+  } else {
+    p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
+  }
+}
+// store_hilo of four neighbouring elements (at a multiple of 4).
+template <typename T>
+__device__ __forceinline__ void store_hilo4(T* hi, bf16* lo, size_t at, float4 v) {
+  if constexpr (sizeof(T) == 2) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&h0);
+    u.y = *reinterpret_cast<const uint32_t*>(&h1);
+    *reinterpret_cast<uint2*>(hi + at) = u;
+    if (lo) {
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+      const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&l0);
+      w.y = *reinterpret_cast<const uint32_t*>(&l1);
+      *reinterpret_cast<uint2*>(lo + at) = w;
+    }
+  } else {
+    store_hilo<T>(hi, lo, at, v.x);
+    store_hilo<T>(hi, lo, at + 1, v.y);
+    store_hilo<T>(hi, lo, at + 2, v.z);
+    store_hilo<T>(hi, lo, at + 3, v.w);
+  }
+}
+
 // The epilogue proper, with the row inputs already in r (visible to all 128
 // threads); msub <= kEpiRows. Run by 128 threads with ranks tid = 0..127; sync()
 // must be a barrier over exactly those threads.
@@ -143,13 +182,14 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
       break;
     }
     case kEpiQkv: {
-      // thread: columns c, c + 1 (c = 2 (tid % 64)) of rows tid / 64, tid / 64 + 2, ...:
-      // every store carries two neighbouring elements (a tile of 128 columns holds
-      // whole head halves, so both columns share their head, region and half).
-      // Half as many store instructions as one column a thread: QKV phase 19.0 ->
-      // 17.5 us per layer of the 8B verify (the epilogue of a split tile's ~20-row
-      // slice is on the phase's critical path).
-      const int c = 2 * (tid & 63), rg = tid >> 6;
+      // thread: columns c .. c + 3 (c = 4 (tid % 32)) of rows tid / 32, tid / 32 + 4, ...:
+      // every access carries four neighbouring elements (a tile of 128 columns
+      // holds whole head halves, so the four share their head, region and half).
+      // The epilogue of a split tile's ~20-row slice is on the phase's critical
+      // path: QKV phase 19.0 us per layer of the 8B verify with one column a
+      // thread, 17.5 with two, 16.5 with four (fewer store instructions; the staged
+      // tile's rows are 16-byte aligned for one shared-memory access per four).
+      const int c = 4 * (tid & 31), rg = tid >> 5;
       if (c < ncols) {
         const int n = n0 + c;
         const int hd = head_dim, half = hd >> 1;
@@ -166,47 +206,52 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
           qgc = qg + ((size_t)(qh / G) * M * G + qh % G) * hd + i;
           qg_row = G * hd;
         }
-        constexpr int kB = kEpiLoadBatch / 2;  // rows of one batch for this thread
-        for (int mb = rg; mb < msub; mb += 2 * kB) {
-          float2 cs[kB], sn[kB];
+        constexpr int kB = kEpiLoadBatch / 4;  // rows of one batch for this thread
+        for (int mb = rg; mb < msub; mb += 4 * kB) {
+          float4 cs[kB], sn[kB];
 #pragma unroll
           for (int q = 0; q < kB; ++q) {  // the batch's table loads, all in flight together
-            cs[q] = make_float2(1.f, 1.f);
-            sn[q] = make_float2(0.f, 0.f);
-            if (region < 2 && mb + 2 * q < msub) {
-              const size_t at = (size_t)rpos[mb + 2 * q] * half + fi;
-              cs[q] = *reinterpret_cast<const float2*>(rope_cos + at);
-              sn[q] = *reinterpret_cast<const float2*>(rope_sin + at);
+            cs[q] = make_float4(1.f, 1.f, 1.f, 1.f);
+            sn[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (region < 2 && mb + 4 * q < msub) {
+              const size_t at = (size_t)rpos[mb + 4 * q] * half + fi;
+              cs[q] = *reinterpret_cast<const float4*>(rope_cos + at);
+              sn[q] = *reinterpret_cast<const float4*>(rope_sin + at);
             }
           }
 #pragma unroll
           for (int q = 0; q < kB; ++q) {
-            const int m = mb + 2 * q;
+            const int m = mb + 4 * q;
             if (m >= msub) break;
             const float rs = rscale[m];
-            float v0 = tile[m * ldt + c] * rs, v1 = tile[m * ldt + c + 1] * rs;
+            float4 v = ld_tile4(tile + m * ldt + c, ldt);
+            v.x *= rs; v.y *= rs; v.z *= rs; v.w *= rs;
             if (region < 2) {
-              const float p0 = tile[m * ldt + partner] * rs, p1 = tile[m * ldt + partner + 1] * rs;
-              if (i < half) {
-                v0 = v0 * cs[q].x - p0 * sn[q].x;
-                v1 = v1 * cs[q].y - p1 * sn[q].y;
-              } else {
-                v0 = v0 * cs[q].x + p0 * sn[q].x;
-                v1 = v1 * cs[q].y + p1 * sn[q].y;
-              }
+              float4 pv = ld_tile4(tile + m * ldt + partner, ldt);
+              const float sg = i < half ? -1.f : 1.f;
+              v.x = v.x * cs[q].x + sg * (pv.x * rs) * sn[q].x;
+              v.y = v.y * cs[q].y + sg * (pv.y * rs) * sn[q].y;
+              v.z = v.z * cs[q].z + sg * (pv.z * rs) * sn[q].z;
+              v.w = v.w * cs[q].w + sg * (pv.w * rs) * sn[q].w;
             }
             if (region == 0) {
-              if (out) *reinterpret_cast<float2*>(reinterpret_cast<float*>(out) + (size_t)(m0 + m) * q_dim + n) =
-                           make_float2(v0, v1);
-              if (qgc)
-                *reinterpret_cast<__half2*>(qgc + (size_t)(m0 + m) * qg_row) =
-                    __floats2half2_rn(v0 * qg_scale, v1 * qg_scale);
+              if (out) *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)(m0 + m) * q_dim + n) = v;
+              if (qgc) {
+                __half2 a = __floats2half2_rn(v.x * qg_scale, v.y * qg_scale);
+                __half2 b = __floats2half2_rn(v.z * qg_scale, v.w * qg_scale);
+                uint2 u;
+                u.x = *reinterpret_cast<uint32_t*>(&a);
+                u.y = *reinterpret_cast<uint32_t*>(&b);
+                *reinterpret_cast<uint2*>(qgc + (size_t)(m0 + m) * qg_row) = u;
+              }
             } else if (rslot[m] >= 0) {
               const size_t at = (((size_t)rseq[m] * n_kv + kvh) * cap + rslot[m]) * hd + i;
               using KvT = typename KvOf<T>::type;
               KvT* const dst = reinterpret_cast<KvT*>(region == 1 ? kc : vc) + at;
-              dst[0] = kv_from_f<T>(v0);
-              dst[1] = kv_from_f<T>(v1);
+              dst[0] = kv_from_f<T>(v.x);
+              dst[1] = kv_from_f<T>(v.y);
+              dst[2] = kv_from_f<T>(v.z);
+              dst[3] = kv_from_f<T>(v.w);
             }
           }
         }
@@ -229,38 +274,38 @@ __device__ void epilogue_body(const EpiParams& p, float* tile, int ldt, int m0, 
     }
     case kEpiResid:
     case kEpiFc: {
-      // thread: columns c, c + 1 of rows tid / 64, tid / 64 + 2, ... (paired stores,
-      // as in the QKV case: O phase 14.7 -> 14.0 us per layer)
-      const int c = 2 * (tid & 63), rg = tid >> 6;
+      // thread: columns c .. c + 3 of rows tid / 32, tid / 32 + 4, ... (as in the QKV case)
+      const int c = 4 * (tid & 31), rg = tid >> 5;
       if (c < ncols) {
         const int n = n0 + c;
-        const float2 gn = *reinterpret_cast<const float2*>(gain + n);
-        constexpr int kB = kEpiLoadBatch / 2;
-        for (int mb = rg; mb < msub; mb += 2 * kB) {
-          float2 hv[kB];
+        const float4 gn = *reinterpret_cast<const float4*>(gain + n);
+        constexpr int kB = kEpiLoadBatch / 4;
+        for (int mb = rg; mb < msub; mb += 4 * kB) {
+          float4 hv[kB];
 #pragma unroll
           for (int q = 0; q < kB; ++q)  // residual loads of the batch, ahead of its stores
-            hv[q] = (kind == kEpiResid && mb + 2 * q < msub)
-                        ? __ldcg(reinterpret_cast<const float2*>(h + (size_t)(m0 + mb + 2 * q) * N + n))
-                        : make_float2(0.f, 0.f);
+            hv[q] = (kind == kEpiResid && mb + 4 * q < msub)
+                        ? __ldcg(reinterpret_cast<const float4*>(h + (size_t)(m0 + mb + 4 * q) * N + n))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < kB; ++q) {
-            const int m = mb + 2 * q;
+            const int m = mb + 4 * q;
             if (m >= msub) break;
             const size_t at = (size_t)(m0 + m) * N + n;
             const float rs = rscale[m];
-            const float h0 = hv[q].x + tile[m * ldt + c] * rs, h1 = hv[q].y + tile[m * ldt + c + 1] * rs;
-            *reinterpret_cast<float2*>(h + at) = make_float2(h0, h1);
-            if (h_tap) *reinterpret_cast<float2*>(h_tap + at) = make_float2(h0, h1);
-            if (h_tap2) *reinterpret_cast<float2*>(h_tap2 + at) = make_float2(h0, h1);
-            store_hilo<T>(reinterpret_cast<T*>(hb), hb_lo, at, h0 * gn.x);
-            store_hilo<T>(reinterpret_cast<T*>(hb), hb_lo, at + 1, h1 * gn.y);
-            tile[m * ldt + c] = h0 * h0;
-            tile[m * ldt + c + 1] = h1 * h1;
+            const float4 t4 = ld_tile4(tile + m * ldt + c, ldt);
+            const float4 hn = make_float4(hv[q].x + t4.x * rs, hv[q].y + t4.y * rs, hv[q].z + t4.z * rs,
+                                          hv[q].w + t4.w * rs);
+            *reinterpret_cast<float4*>(h + at) = hn;
+            if (h_tap) *reinterpret_cast<float4*>(h_tap + at) = hn;
+            if (h_tap2) *reinterpret_cast<float4*>(h_tap2 + at) = hn;
+            store_hilo4<T>(reinterpret_cast<T*>(hb), hb_lo, at,
+                           make_float4(hn.x * gn.x, hn.y * gn.y, hn.z * gn.z, hn.w * gn.w));
+            st_tile4(tile + m * ldt + c, ldt, make_float4(hn.x * hn.x, hn.y * hn.y, hn.z * hn.z, hn.w * hn.w));
           }
         }
       } else {
-        for (int m = rg; m < msub; m += 2) tile[m * ldt + c] = tile[m * ldt + c + 1] = 0.f;
+        for (int m = rg; m < msub; m += 4) st_tile4(tile + m * ldt + c, ldt, make_float4(0.f, 0.f, 0.f, 0.f));
       }
       sync();
       const int warp = tid >> 5, lane = tid & 31;

@@ -70,7 +70,7 @@ constexpr int kXWarp = 6;                  // activation producer warp
 constexpr int kBK = 64;
 constexpr int kWBytes = kTileN * kBK * 2;  // 16 KB weight box
 constexpr int kSub = 32;                   // epilogue rows per sub-tile
-constexpr int kLdt = kTileN + 1;
+constexpr int kLdt = kTileN + 4;  // rows 16-byte aligned for the epilogues' vector accesses
 constexpr int kMaxW = 12;                  // weight ring stages (upper bound)
 constexpr int kAttnCKI = attn::kUmKeys;    // keys per attention work item
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in per block
