@@ -36,6 +36,32 @@ __device__ __forceinline__ void store_hilo(T* hi, bf16* lo, size_t at, float v) 
   if (lo) lo[at] = __float2bfloat16_rn(v - to_f(h));
 }
 
+// store_hilo of four neighbouring elements (at a multiple of 4).
+template <typename T>
+__device__ __forceinline__ void store_hilo4(T* hi, bf16* lo, size_t at, float4 v) {
+  if constexpr (sizeof(T) == 2) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&h0);
+    u.y = *reinterpret_cast<const uint32_t*>(&h1);
+    *reinterpret_cast<uint2*>(hi + at) = u;
+    if (lo) {
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+      const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&l0);
+      w.y = *reinterpret_cast<const uint32_t*>(&l1);
+      *reinterpret_cast<uint2*>(lo + at) = w;
+    }
+  } else {
+    store_hilo<T>(hi, lo, at, v.x);
+    store_hilo<T>(hi, lo, at + 1, v.y);
+    store_hilo<T>(hi, lo, at + 2, v.z);
+    store_hilo<T>(hi, lo, at + 3, v.w);
+  }
+}
+
 // KV-cache element type: the model dtype for float32 models; IEEE half for bf16
 // models (11-bit significand, 8x finer than bf16, at the same two bytes; the
 // attention products then run as f16 MMAs). Stores saturate at the half range;

@@ -110,32 +110,6 @@ __device__ __forceinline__ void st_tile4(float* p, int ldt, float4 v) {
     p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
   }
 }
-// store_hilo of four neighbouring elements (at a multiple of 4).
-template <typename T>
-__device__ __forceinline__ void store_hilo4(T* hi, bf16* lo, size_t at, float4 v) {
-  if constexpr (sizeof(T) == 2) {
-    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&h0);
-    u.y = *reinterpret_cast<const uint32_t*>(&h1);
-    *reinterpret_cast<uint2*>(hi + at) = u;
-    if (lo) {
-      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-      const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
-      const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
-      uint2 w;
-      w.x = *reinterpret_cast<const uint32_t*>(&l0);
-      w.y = *reinterpret_cast<const uint32_t*>(&l1);
-      *reinterpret_cast<uint2*>(lo + at) = w;
-    }
-  } else {
-    store_hilo<T>(hi, lo, at, v.x);
-    store_hilo<T>(hi, lo, at + 1, v.y);
-    store_hilo<T>(hi, lo, at + 2, v.z);
-    store_hilo<T>(hi, lo, at + 3, v.w);
-  }
-}
-
 // The epilogue proper, with the row inputs already in r (visible to all 128
 // threads); msub <= kEpiRows. Run by 128 threads with ranks tid = 0..127; sync()
 // must be a barrier over exactly those threads.
