@@ -508,10 +508,10 @@ cudaError_t gemm_tc(const bf16* X, const bf16* X_lo, const bf16* W, int M, int N
 
 // ------------------------------------------------------------------ allocation-free entry point
 //
-// Some callers of the GEMM cannot allocate device memory: code running inside
-// a CUDA graph that is being captured by someone else, plugins of a runtime
-// that owns the device allocator, and callers that must not touch the memory
-// budget at all. eagle_op_gemm_noalloc gives them the same tcgen05 kernel with
+// Some callers of the GEMM cannot allocate device memory: plugins of a host
+// framework that owns the device allocator and does not let them call
+// cudaMalloc, and code whose device-memory budget is fixed by someone else with
+// no room for a scratch buffer. eagle_op_gemm_noalloc gives them the same tcgen05 kernel with
 // its split-K scratch (arrival counters, then partial sums) in the static
 // device array below instead of a caller buffer. The array is
 // g_noalloc_scratch_bytes = 512 KiB of counters + 10 MiB of partials (160 SMs

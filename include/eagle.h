@@ -328,9 +328,11 @@ size_t eagle_op_gemm_scratch_bytes(int32_t M, int32_t N, int32_t K, int32_t dtyp
 eagle_status eagle_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* d_x, const void* d_x_lo,
                            const void* d_w, float* d_y, void* d_scratch, size_t scratch_bytes, void* stream);
 
-/* The same bf16 GEMM for callers that cannot allocate device memory (for
- * example code running while someone else captures a CUDA graph, or a plugin
- * whose host owns the allocator): the split-K scratch lives in a static device
+/* The same bf16 GEMM for callers that cannot allocate device memory: a plugin
+ * inside a host framework that owns the device allocator and does not let its
+ * plugins call cudaMalloc, or code whose device-memory budget is fixed by
+ * someone else and has no room for a scratch buffer of its own. For them the
+ * split-K scratch lives in a static device
  * array inside this library (10.5 MiB, reserved on every GPU that loads the
  * library until the process exits), so the caller passes only X, W and Y.
  * The pages have no counterpart; this is an interface convenience.

@@ -1,7 +1,9 @@
 """The allocation-free GEMM entry point (eagle_op_gemm_noalloc), called through the C ABI.
 
-Some callers cannot allocate device memory; this entry point keeps the GEMM's
-split-K scratch in a static device array of the library. It must give the same
+Some callers cannot allocate device memory: a plugin inside a host framework
+that owns the device allocator and does not let it call cudaMalloc, or code
+whose device-memory budget is fixed by someone else. For them this entry point
+keeps the GEMM's split-K scratch in a static device array of the library. It must give the same
 result as eagle_op_gemm with a caller-owned scratch buffer, call after call
 (the array keeps the previous call's contents), and reject shapes beyond its
 fixed maximum. The file is collected last so that a failure here leaves every
